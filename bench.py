@@ -1,0 +1,423 @@
+"""Benchmark of the routed MoE expert FFN layer (MXFP4 weights, online FP8
+activations) on GB300.
+
+One step = one moe_forward over one batch of synthetic tokens (route, histogram +
+scan + permute, FP8 quantisation, W13 grouped GEMM, SwiGLU + FP8 requantisation, W2
+grouped GEMM, weighted top-k combine + shared-expert add).  Inputs are resident in
+HBM when the timed region starts; L2 is flushed (a 512 MiB write) before every timed
+step, outside its CUDA-event pair.  Prints one JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|decode256|prefill|tiny]
+  python bench.py --impl reference ...   (the CPU oracle on a bounded sample)
+
+Multi-GPU: one independent replica per GPU (the layer is not sharded; no
+collective); value = tokens processed by all ranks / max-over-ranks time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from gen import inputs as gi  # noqa: E402
+
+METRIC = "MoE-layer tokens/s"
+WEIGHT_BYTES_PER_ELEM = 0.5 + 1.0 / 32.0  # E2M1 code + E8M0 scale per 32
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode", choices=list(gi.WORKLOADS))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-flush", action="store_true")
+    return ap.parse_args()
+
+
+def dist_init(args):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                return json.load(f), "measured"
+        except Exception:
+            pass
+    return None, "fallback"
+
+
+def hbm_peak_gbs():
+    peaks, src = measured_peaks()
+    if peaks:
+        for key in ("hbm_gbs", "hbm_GBs", "hbm"):
+            if key in peaks:
+                v = peaks[key]
+                if isinstance(v, dict):
+                    v = v.get("burst", v.get("value"))
+                try:
+                    return float(v), "measured"
+                except (TypeError, ValueError):
+                    pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def fp8_tensor_peak_tflops():
+    """Dense FP8 tensor peak: the measured bf16 cuBLAS peak x the nominal 2x FP8/bf16
+    ratio, else the fallback bf16 figure x 2."""
+    peaks, _ = measured_peaks()
+    if peaks:
+        for key in ("bf16_tflops", "bf16"):
+            if key in peaks:
+                try:
+                    return 2.0 * float(peaks[key]), "measured bf16 x2 (nominal fp8/bf16 ratio)"
+                except (TypeError, ValueError):
+                    pass
+    return 2.0 * FALLBACK_BF16_TFLOPS, "fallback bf16 x2 (nominal fp8/bf16 ratio)"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"moe_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in open(self.path):
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                smax.append(float(p[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def active_groups(counts, has_shared):
+    return int((counts > 0).sum()) + (1 if has_shared else 0)
+
+
+# ------------------------------------------------------------------ CPU oracle ------
+
+def oracle_sample(d, t_host_fn, tokens, seed):
+    """Times the oracle on `tokens` tokens of the workload (their experts only)."""
+    from oracle import moe_oracle as o
+    x, lg, w_get = t_host_fn()
+    rng = np.random.default_rng(seed)
+    toks = np.sort(rng.choice(d.T, size=min(tokens, d.T), replace=False))
+    t0 = time.perf_counter()
+    ridx, _ = o.route(lg[toks], d.k)
+    experts = sorted(set(ridx.ravel().tolist()) | ({d.E} if d.has_shared else set()))
+    w13, w13s, w2, w2s = w_get(experts)
+    o.moe_forward_tokens(x, lg, d.k, w13, w13s, w2, w2s, d.has_shared, toks)
+    dt = time.perf_counter() - t0
+    return len(toks), dt
+
+
+def host_view(d, t):
+    """Callables giving the oracle numpy views of the layer inputs (weights copied to
+    the host only for the experts a sample touches)."""
+    x = t["x"].cpu().view(torch.int16).numpy().view(np.uint16)
+    lg = t["logits"].cpu().numpy()
+
+    def w_get(experts):
+        shp = lambda n: (d.G,) + tuple(t[n].shape[1:])
+        out = [np.zeros(shp(n), np.uint8) for n in ("w13", "w13_s", "w2", "w2_s")]
+        for e in experts:
+            for a, n in zip(out, ("w13", "w13_s", "w2", "w2_s")):
+                a[e] = t[n][e].cpu().numpy()
+        return out
+
+    return lambda: (x, lg, w_get)
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+# ------------------------------------------------------------------ arms ------------
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    d, t = gi.make_layer(args.workload, seed=args.seed, device=dev)
+    hv = host_view(d, t)
+    tokens = 1
+    times = []
+    n_done = 0
+    for i in range(args.warmup + args.steps):
+        n, dt = oracle_sample(d, hv, tokens, args.seed + i)
+        if i >= args.warmup:
+            times.append(dt)
+            n_done += n
+    total = sum(times)
+    value = n_done / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / len(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "T": d.T, "H": d.H, "I": d.I, "E": d.E,
+                   "k": d.k, "shared_experts": d.has_shared},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": blas_threads(),
+                         "kind": "oracle",
+                         "sample": f"{tokens} token(s) per step, its top-{d.k} experts and "
+                                   "the shared expert, full layer in float64 numpy"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local):
+    import moe_expert_ffn_scan_gb300 as moe
+    moe.lib()
+    dev = torch.device("cuda", local)
+    d, t = gi.make_layer(args.workload, seed=args.seed + rank, device=dev)
+    md = moe.dims(d.T, d.H, d.I, d.E, d.k, d.has_shared)
+    layer = moe.MoELayer(d.H, d.I, d.E, d.k, d.has_shared, t["w13"], t["w13_s"], t["w2"],
+                         t["w2_s"])
+    x, lg = t["x"], t["logits"]
+    out = torch.empty(d.T, d.H, dtype=torch.bfloat16, device=dev)
+    ws = layer.workspace(d.T)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    # routing statistics (for the algorithmic byte / flop counts)
+    dbg = {"counts": torch.empty(d.E, dtype=torch.int32, device=dev)}
+    moe.moe_forward(md, x, lg, t["w13"], t["w13_s"], t["w2"], t["w2_s"], out, ws, debug=dbg)
+    bits = moe.moe_check_status(ws)
+    if bits:
+        raise RuntimeError(f"device status bits {bits:#x}")
+    counts = dbg["counts"].cpu().numpy()
+    groups = active_groups(counts, d.has_shared)
+    Rs = d.R + (d.T if d.has_shared else 0)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)]
+           for _ in range(args.steps)]
+    for row in evs:
+        for e in row:
+            e.record(stream)  # creates the event handles
+    for _ in range(args.warmup):
+        layer.forward(x, lg, out=out)
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    with clocks:
+        barrier(world)
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            if not args.no_flush:
+                flush.fill_(i & 0xFF)
+            moe.moe_forward_timed(md, x, lg, t["w13"], t["w13_s"], t["w2"], t["w2_s"], out, ws,
+                                  evs[i])
+        torch.cuda.synchronize()
+        barrier(world)
+    bits = moe.moe_check_status(ws)
+    if bits:
+        raise RuntimeError(f"device status bits {bits:#x}")
+    stage_ms = {s: [] for s in moe.STAGES}
+    step_ms = []
+    for row in evs:
+        for j, s in enumerate(moe.STAGES):
+            stage_ms[s].append(row[j].elapsed_time(row[j + 1]))
+        step_ms.append(row[0].elapsed_time(row[7]))
+    ms = statistics.mean(step_ms)
+    ms_max = max_over_ranks(ms, world)
+    value = world * d.T / (ms_max * 1e-3)
+    stage_mean = {s: statistics.mean(v) for s, v in stage_ms.items()}
+
+    # roofline of the dominant kernel (the W13 grouped GEMM)
+    w13_bytes = groups * (2 * d.I) * d.H * WEIGHT_BYTES_PER_ELEM
+    w2_bytes = groups * d.H * d.I * WEIGHT_BYTES_PER_ELEM
+    act13 = Rs * (d.H + d.H / 128) + Rs * 2 * d.I * 2
+    act2 = Rs * (d.I + d.I / 128) + Rs * d.H * 2
+    flops13 = 2.0 * Rs * 2 * d.I * d.H
+    flops2 = 2.0 * Rs * d.H * d.I
+    hbm, hbm_src = hbm_peak_gbs()
+    tpk, tpk_src = fp8_tensor_peak_tflops()
+    t13 = stage_mean["gemm_w13"] * 1e-3
+    decode_like = (flops13 / (w13_bytes + act13)) < (tpk * 1e12) / (hbm * 1e9)
+    if decode_like:
+        ach = (w13_bytes + act13) / t13 / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
+                "frac": ach / hbm, "traffic": None,
+                "kernel": "k_gemm_mx (W13 grouped GEMM)",
+                "peak_source": f"{hbm_src} HBM copy bandwidth"}
+    else:
+        ach = flops13 / t13 / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": tpk, "unit": "TFLOP/s",
+                "frac": ach / tpk, "traffic": None,
+                "kernel": "k_gemm_mx (W13 grouped GEMM)", "peak_source": tpk_src}
+
+    # end to end through the public API, host buffers, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        xh = x.cpu().pin_memory()
+        lgh = lg.cpu().pin_memory()
+        oh = torch.empty(d.T, d.H, dtype=torch.bfloat16).pin_memory()
+        xd, lgd = torch.empty_like(x), torch.empty_like(lg)
+        for _ in range(3):
+            xd.copy_(xh, non_blocking=True)
+            lgd.copy_(lgh, non_blocking=True)
+            layer.forward(xd, lgd, out=out)
+            oh.copy_(out, non_blocking=True)
+        torch.cuda.synchronize()
+        e_ms = []
+        for i in range(args.steps):
+            if not args.no_flush:
+                flush.fill_(i & 0xFF)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            xd.copy_(xh, non_blocking=True)
+            lgd.copy_(lgh, non_blocking=True)
+            layer.forward(xd, lgd, out=out)
+            oh.copy_(out, non_blocking=True)
+            torch.cuda.synchronize()
+            e_ms.append((time.perf_counter() - t0) * 1e3)
+        em = max_over_ranks(statistics.mean(e_ms), world)
+        e2e = {"value": world * d.T / (em * 1e-3), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(xh.numel() * 2 + lgh.numel() * 4),
+               "d2h_bytes_per_step": int(oh.numel() * 2), "ms_per_step": em}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        hv = host_view(d, t)
+        n, dt = oracle_sample(d, hv, 1, args.seed)
+        cpu = {"value": n / dt, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+               "sample": f"{n} token of the {args.workload} workload (its top-{d.k} experts + "
+                         f"shared expert), full layer in float64 numpy, {dt:.2f} s"}
+
+    launches_per_step = 14
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "mxfp4xfp8->f32", "data": "synthetic",
+            "config": {"workload": args.workload, "T": d.T, "H": d.H, "I": d.I, "E": d.E,
+                       "k": d.k, "shared_experts": d.has_shared, "active_groups": groups,
+                       "routed_rows": d.R, "l2": "flushed (512 MiB write) before each step",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": roof,
+            "stage_ms": stage_mean,
+            "weight_gbs": (w13_bytes + w2_bytes) / ((stage_mean["gemm_w13"] +
+                                                     stage_mean["gemm_w2"]) * 1e-3) / 1e9,
+            "gemm_tflops": (flops13 + flops2) / ((stage_mean["gemm_w13"] +
+                                                  stage_mean["gemm_w2"]) * 1e-3) / 1e12,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks.summary(),
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_init(args)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_ours(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -99,7 +99,7 @@ def activations(T, H, seed, device, name="x"):
 
 
 def zipf_logits(T, E, seed, device, s=1.1):
-    perm = torch.randperm(E, generator=_gen(seed, "perm", device), device="cpu")
+    perm = torch.randperm(E, generator=_gen(seed, "perm", "cpu"), device="cpu")
     rank = torch.empty(E, dtype=torch.float64)
     rank[perm] = torch.arange(1, E + 1, dtype=torch.float64)
     bias = (-s * torch.log(rank)).to(device)

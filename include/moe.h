@@ -1,0 +1,185 @@
+/*
+ * moe.h -- C interface of the GB300 (sm_103a) routed Mixture-of-Experts expert FFN
+ * with MXFP4 expert weights and online FP8 activations.
+ *
+ * The method is the MoE expert path of "Pushing the Limits of Serving
+ * DeepSeek-V4-Pro" (LMSYS, H20): MXFP4 expert weights with FP8 activations
+ * quantised online (§2.2), W13 and W2 as two grouped GEMMs shaped by the routing
+ * histogram (§3.3), SwiGLU fused with the FP8 quantisation that emits W2's operand
+ * and scales (§4.3), and the top-k reduction merged with the shared-expert add
+ * (§3.2); plus the GB10 "Optimization progress report", Optimization 14 (tokens
+ * packed by expert before the MoE launch) and Optimization 06 (small-M expert GEMM
+ * without padding the few tokens to large tiles).
+ *
+ * Conventions for every entry point
+ *   - All tensors are caller-owned, row-major, contiguous DEVICE pointers, unless
+ *     stated otherwise.  Pointers must be 16-byte aligned (the weight code tensors
+ *     32-byte aligned).  bf16 tensors are passed as uint16_t storage.
+ *   - Nothing allocates.  Scratch comes from the caller's workspace, sized by the
+ *     matching *_workspace_size() query.  Workspace must be 256-byte aligned.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t, NULL = legacy default
+ *     stream) and never synchronises the host, except moe_check_status.
+ *   - Return value: MOE_OK or an MOE_ERR_* code.  Shapes and pointers are checked
+ *     on the host before any launch; nothing is launched when a check fails.
+ *     Launch failures return MOE_ERR_CUDA.  Data-dependent device checks (an index
+ *     out of range, an expired wait inside a kernel) never trap: they set bits of
+ *     a status word in the workspace, read back by moe_check_status.
+ *
+ * Formats (the pages do not define them; these are the OCP MX v1.0 / OFP8 formats)
+ *   - MXFP4 weights: E2M1 codes, two per byte, the even K index in the low nibble,
+ *     shape [G][N][K/2]; one E8M0 scale byte (2^(b-127)) per 32 consecutive K
+ *     elements, shape [G][N][K/32].
+ *   - FP8 activations: E4M3 ("FN": bias 7, max 448) codes [rows][cols]; one scale
+ *     byte per row per 128 columns [rows][cols/128] holding e + 127, where e is the
+ *     smallest integer with amax <= 448 * 2^e; codes = round-to-nearest-even of
+ *     x * 2^-e.  A block of zeros gets scale byte 127 and zero codes.
+ *
+ * Shapes supported (else MOE_ERR_UNSUPPORTED_SHAPE): H % 128 == 0, I % 128 == 0,
+ * 1 <= k <= min(E, 16), 1 <= E <= 1024, T >= 1, T * k < 2^31.
+ */
+#ifndef MOE_GB300_MOE_H_
+#define MOE_GB300_MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,        /* null / misaligned pointer, bad enum value        */
+  MOE_ERR_UNSUPPORTED_SHAPE = 2,  /* dims outside the supported set above             */
+  MOE_ERR_WORKSPACE_TOO_SMALL = 3,
+  MOE_ERR_CUDA = 4,               /* a CUDA runtime call or launch failed             */
+  MOE_ERR_DEVICE_CHECK = 5        /* moe_check_status found a device status bit set   */
+};
+
+/* T tokens, hidden size H, per-expert intermediate size I, E routed experts, top-k,
+ * has_shared = 1 adds one always-on shared expert stored as group E of the weight
+ * tensors.  G = E + has_shared groups; R = T*k routed rows; Rs = R + T*has_shared
+ * packed rows (routed rows grouped by expert, then one shared row per token). */
+typedef struct moe_dims {
+  int32_t T, H, I, E, k, has_shared;
+} moe_dims;
+
+/* MXFP4 expert weights, G groups each: w13 [G][2I][H/2] + w13_s [G][2I][H/32]
+ * (rows 0..I-1 gate projection, rows I..2I-1 up projection), w2 [G][H][I/2] +
+ * w2_s [G][H][I/32]. */
+typedef struct moe_weights {
+  const uint8_t* w13;
+  const uint8_t* w13_s;
+  const uint8_t* w2;
+  const uint8_t* w2_s;
+} moe_weights;
+
+/* Optional outputs of moe_forward's intermediates (any member may be NULL). */
+typedef struct moe_debug_out {
+  int32_t* idx;      /* [T][k]              */
+  float* w;          /* [T][k]              */
+  int32_t* counts;   /* [E]                 */
+  int32_t* offsets;  /* [G+1]               */
+  int32_t* perm_src; /* [R]                 */
+  int32_t* inv;      /* [R]                 */
+  uint8_t* xq;       /* [T][H]              */
+  uint8_t* xs;       /* [T][H/128]          */
+  uint16_t* y13;     /* [Rs][2I] bf16       */
+  uint8_t* hq;       /* [Rs][I]             */
+  uint8_t* hs;       /* [Rs][I/128]         */
+  uint16_t* y2;      /* [Rs][H] bf16        */
+} moe_debug_out;
+
+/* Text of a status code (static storage). */
+const char* moe_error_string(int status);
+
+/* Workspace bytes needed by moe_forward / moe_route / the two grouped GEMMs at
+ * these dims (0 for unsupported dims). */
+size_t moe_workspace_size(const moe_dims* d);
+size_t moe_route_workspace_size(const moe_dims* d);
+size_t moe_gemm_workspace_size(const moe_dims* d);
+
+/* a1 + a2: top-k routing, token->expert histogram, exclusive scan and permutation.
+ * Pages: LMSYS-H20 §3.2 (TopK) and §3.3 (per-expert M from the routing histogram);
+ * GB10 report Optimization 14 (route preplan, tokens packed by expert).
+ *   logits [T][E] fp32.  Per token: the k largest logits (equal logits -> lower
+ *   expert index first), in that order -> idx [T][k]; weights softmax-renormalised
+ *   over the selected k -> w [T][k] (sum 1).
+ *   counts [E] tokens per expert; offsets [G+1] exclusive scan over groups
+ *   (offsets[E+1] = Rs when has_shared); perm_src [R]: packed row -> routed row t*k+j,
+ *   rows of a group in ascending token order; inv [R]: routed row -> packed row.
+ *   Bit-exact and deterministic (no order-dependent atomics).
+ *   ws: moe_route_workspace_size(d) bytes. */
+int moe_route(const moe_dims* d, const float* logits, int32_t* idx, float* w, int32_t* counts,
+              int32_t* offsets, int32_t* perm_src, int32_t* inv, void* ws, size_t ws_bytes,
+              void* stream);
+
+/* a3: online FP8 E4M3 quantisation of bf16 x [rows][cols] with one power-of-two
+ * scale per row per 128 columns (rule above) -> q [rows][cols], s [rows][cols/128].
+ * Pages: LMSYS-H20 §2.2 (online FP8 activations), §3.2 (fused FP8 quantisation).
+ * cols % 128 == 0, rows >= 0 (rows == 0 is a no-op). */
+int moe_quant_act(int32_t rows, int32_t cols, const uint16_t* x, uint8_t* q, uint8_t* s,
+                  void* stream);
+
+/* a4: W13 grouped GEMM (LMSYS-H20 §3.3).  For every group g and packed row r in
+ * [group_offsets[g], group_offsets[g+1]):
+ *     y13[r][n] = bf16( sum_k deq(xq)[tok(r)][k] * deq(w13[g])[n][k] ),  n < 2I,
+ * FP8 x MXFP4 products accumulated in fp32 on the tensor cores (tcgen05 block-
+ * scaled MMA).  tok(r) = perm_src[r] / k for r < R and r - R for shared rows; with
+ * perm_src == NULL the activations are already packed (xq has Rs rows, tok(r) = r).
+ * xq [T][H] (or [Rs][H]), xs [T][H/128]; group_offsets [G+1] device int32,
+ * non-decreasing, group_offsets[G] <= Rs; y13 [Rs][2I] bf16 (rows outside every
+ * group are not written).  ws: moe_gemm_workspace_size(d) bytes. */
+int moe_grouped_gemm_w13(const moe_dims* d, const uint8_t* xq, const uint8_t* xs,
+                         const int32_t* perm_src, const int32_t* group_offsets,
+                         const uint8_t* w13, const uint8_t* w13_s, uint16_t* y13, void* ws,
+                         size_t ws_bytes, void* stream);
+
+/* a5: SwiGLU fused with FP8 requantisation (LMSYS-H20 §4.3): for each row,
+ * h = silu(g) * u with g = y13[r][0:I], u = y13[r][I:2I], silu(g) = g / (1 + e^-g),
+ * in fp32, then quantised per 128 columns with the activation rule -> hq [rows][I],
+ * hs [rows][I/128] (W2's operand and scales).  I % 128 == 0. */
+int moe_swiglu_quant(int32_t rows, int32_t I, const uint16_t* y13, uint8_t* hq, uint8_t* hs,
+                     void* stream);
+
+/* a6: W2 grouped GEMM (LMSYS-H20 §3.3): y2[r][n] = bf16( sum_i deq(hq)[r][i] *
+ * deq(w2[g])[n][i] ), n < H, for r in group g.  hq [Rs][I], hs [Rs][I/128],
+ * y2 [Rs][H].  ws: moe_gemm_workspace_size(d) bytes. */
+int moe_grouped_gemm_w2(const moe_dims* d, const uint8_t* hq, const uint8_t* hs,
+                        const int32_t* group_offsets, const uint8_t* w2, const uint8_t* w2_s,
+                        uint16_t* y2, void* ws, size_t ws_bytes, void* stream);
+
+/* a7: weighted top-k unpermute-combine plus shared-expert add (LMSYS-H20 §3.2):
+ *     out[t] = bf16( sum_{j<k} w[t][j] * y2[inv[t*k+j]]  (+ y2[R+t] if has_shared) ),
+ * summed in fp32 in j order, the shared row last.  y2 [Rs][H], inv [R], w [T][k],
+ * out [T][H] bf16. */
+int moe_combine(const moe_dims* d, const uint16_t* y2, const int32_t* inv, const float* w,
+                uint16_t* out, void* stream);
+
+/* The whole layer a1..a7 on one stream, no host synchronisation: x [T][H] bf16,
+ * logits [T][E] fp32, weights W (G groups), out [T][H] bf16.  dbg may be NULL.
+ * ws: moe_workspace_size(d) bytes. */
+int moe_forward(const moe_dims* d, const uint16_t* x, const float* logits,
+                const moe_weights* W, uint16_t* out, const moe_debug_out* dbg, void* ws,
+                size_t ws_bytes, void* stream);
+
+/* moe_forward with per-stage timing.  events points to 8 cudaEvent_t handles created
+ * by the caller (cudaEventCreate); the call records events[0] before the first stage
+ * and events[i] after stage i: 1 route + histogram/scan/permute, 2 activation
+ * quantisation, 3 tile plan + packed-row gather, 4 W13 grouped GEMM, 5 SwiGLU +
+ * quantisation, 6 W2 grouped GEMM, 7 combine.  Same results as moe_forward. */
+int moe_forward_timed(const moe_dims* d, const uint16_t* x, const float* logits,
+                      const moe_weights* W, uint16_t* out, const moe_debug_out* dbg,
+                      void* const* events, void* ws, size_t ws_bytes, void* stream);
+
+/* Debug helper (synchronises `stream`): reads the device status word at the start of
+ * a workspace used by the calls above.  Returns MOE_OK if no bit is set, else
+ * MOE_ERR_DEVICE_CHECK and the bits in *bits_out (if not NULL).  The word is
+ * cleared by moe_forward / moe_route / the GEMMs at their start. */
+int moe_check_status(const void* ws, void* stream, uint32_t* bits_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_MOE_H_ */

@@ -1,0 +1,254 @@
+"""Python binding of libmoe.so, the GB300 routed-MoE expert FFN (MXFP4 weights,
+online FP8 activations).
+
+Argument marshalling only: every step runs in the library's CUDA kernels.  PyTorch
+provides device memory and the current stream.  The functions carry the C names
+(see include/moe.h for argument meaning, layouts and errors); each raises
+MoeError when the C call returns a non-zero status.  Importing this package does
+not need a GPU; calling into the library does, and fails loudly if libmoe.so has
+not been built (python -m moe_expert_ffn_scan_gb300.build).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe.so")
+
+MOE_OK = 0
+STATUS_WAIT_TIMEOUT = 1
+STATUS_BAD_INDEX = 2
+STATUS_BAD_PLAN = 4
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn, code):
+        msg = lib().moe_error_string(code).decode() if _LIB is not None else str(code)
+        super().__init__(f"{fn}: status {code} ({msg})")
+        self.code = code
+
+
+class moe_dims(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("T", "H", "I", "E", "k", "has_shared")]
+
+
+class moe_weights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("w13", "w13_s", "w2", "w2_s")]
+
+
+DEBUG_FIELDS = ("idx", "w", "counts", "offsets", "perm_src", "inv", "xq", "xs", "y13", "hq",
+                "hs", "y2")
+
+
+class moe_debug_out(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in DEBUG_FIELDS]
+
+
+_LIB = None
+_P = ctypes.c_void_p
+_I = ctypes.c_int32
+_SZ = ctypes.c_size_t
+_DP = ctypes.POINTER(moe_dims)
+
+
+def lib():
+    """Load libmoe.so (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m moe_expert_ffn_scan_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        L.moe_error_string.argtypes = [ctypes.c_int]
+        L.moe_error_string.restype = ctypes.c_char_p
+        for fn in ("moe_workspace_size", "moe_route_workspace_size", "moe_gemm_workspace_size"):
+            getattr(L, fn).argtypes = [_DP]
+            getattr(L, fn).restype = _SZ
+        L.moe_route.argtypes = [_DP, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]
+        L.moe_quant_act.argtypes = [_I, _I, _P, _P, _P, _P]
+        L.moe_grouped_gemm_w13.argtypes = [_DP, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]
+        L.moe_swiglu_quant.argtypes = [_I, _I, _P, _P, _P, _P]
+        L.moe_grouped_gemm_w2.argtypes = [_DP, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]
+        L.moe_combine.argtypes = [_DP, _P, _P, _P, _P, _P]
+        L.moe_forward.argtypes = [_DP, _P, _P, ctypes.POINTER(moe_weights), _P,
+                                  ctypes.POINTER(moe_debug_out), _P, _SZ, _P]
+        L.moe_forward_timed.argtypes = [_DP, _P, _P, ctypes.POINTER(moe_weights), _P,
+                                        ctypes.POINTER(moe_debug_out), ctypes.POINTER(_P), _P,
+                                        _SZ, _P]
+        L.moe_check_status.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_uint32)]
+        for fn in ("moe_route", "moe_quant_act", "moe_grouped_gemm_w13", "moe_swiglu_quant",
+                   "moe_grouped_gemm_w2", "moe_combine", "moe_forward", "moe_forward_timed",
+                   "moe_check_status"):
+            getattr(L, fn).restype = ctypes.c_int
+        _LIB = L
+    return _LIB
+
+
+def _p(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if t.device.type != "cuda":
+        raise ValueError("tensor must live on the GPU")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _check(fn, rc):
+    if rc != MOE_OK:
+        raise MoeError(fn, rc)
+
+
+def dims(T, H, I, E, k, has_shared):
+    return moe_dims(int(T), int(H), int(I), int(E), int(k), int(has_shared))
+
+
+def _d(d):
+    if not isinstance(d, moe_dims):
+        d = dims(d.T, d.H, d.I, d.E, d.k, d.has_shared)
+    return ctypes.byref(d)
+
+
+def workspace_size(d) -> int:
+    return lib().moe_workspace_size(_d(d))
+
+
+def route_workspace_size(d) -> int:
+    return lib().moe_route_workspace_size(_d(d))
+
+
+def gemm_workspace_size(d) -> int:
+    return lib().moe_gemm_workspace_size(_d(d))
+
+
+def alloc_workspace(nbytes, device="cuda"):
+    """A workspace tensor (torch allocations are 256-byte aligned or better)."""
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def moe_route(d, logits, idx, w, counts, offsets, perm_src, inv, ws, stream=None):
+    _check("moe_route", lib().moe_route(_d(d), _p(logits), _p(idx), _p(w), _p(counts),
+                                        _p(offsets), _p(perm_src), _p(inv), _p(ws),
+                                        ws.numel(), _stream(stream)))
+
+
+def moe_quant_act(x, q, s, stream=None):
+    rows, cols = x.shape
+    _check("moe_quant_act", lib().moe_quant_act(rows, cols, _p(x), _p(q), _p(s),
+                                                _stream(stream)))
+
+
+def moe_grouped_gemm_w13(d, xq, xs, perm_src, group_offsets, w13, w13_s, y13, ws, stream=None):
+    _check("moe_grouped_gemm_w13", lib().moe_grouped_gemm_w13(
+        _d(d), _p(xq), _p(xs), _p(perm_src), _p(group_offsets), _p(w13), _p(w13_s), _p(y13),
+        _p(ws), ws.numel(), _stream(stream)))
+
+
+def moe_swiglu_quant(y13, hq, hs, stream=None):
+    rows, two_i = y13.shape
+    _check("moe_swiglu_quant", lib().moe_swiglu_quant(rows, two_i // 2, _p(y13), _p(hq), _p(hs),
+                                                      _stream(stream)))
+
+
+def moe_grouped_gemm_w2(d, hq, hs, group_offsets, w2, w2_s, y2, ws, stream=None):
+    _check("moe_grouped_gemm_w2", lib().moe_grouped_gemm_w2(
+        _d(d), _p(hq), _p(hs), _p(group_offsets), _p(w2), _p(w2_s), _p(y2), _p(ws),
+        ws.numel(), _stream(stream)))
+
+
+def moe_combine(d, y2, inv, w, out, stream=None):
+    _check("moe_combine", lib().moe_combine(_d(d), _p(y2), _p(inv), _p(w), _p(out),
+                                            _stream(stream)))
+
+
+def moe_forward(d, x, logits, w13, w13_s, w2, w2_s, out, ws, debug=None, stream=None):
+    W = moe_weights(_p(w13), _p(w13_s), _p(w2), _p(w2_s))
+    dbg = None
+    if debug:
+        dbg = moe_debug_out(*[_p(debug.get(n)) for n in DEBUG_FIELDS])
+    _check("moe_forward", lib().moe_forward(
+        _d(d), _p(x), _p(logits), ctypes.byref(W), _p(out),
+        ctypes.byref(dbg) if dbg is not None else None, _p(ws), ws.numel(), _stream(stream)))
+
+
+STAGES = ("route", "quant", "plan_gather", "gemm_w13", "swiglu_quant", "gemm_w2", "combine")
+
+
+def moe_forward_timed(d, x, logits, w13, w13_s, w2, w2_s, out, ws, events, debug=None,
+                      stream=None):
+    """moe_forward recording 8 torch.cuda.Event objects at the stage boundaries (see
+    STAGES); the events must already exist (recorded once)."""
+    W = moe_weights(_p(w13), _p(w13_s), _p(w2), _p(w2_s))
+    dbg = None
+    if debug:
+        dbg = moe_debug_out(*[_p(debug.get(n)) for n in DEBUG_FIELDS])
+    ev = (_P * 8)(*[e.cuda_event for e in events])
+    _check("moe_forward_timed", lib().moe_forward_timed(
+        _d(d), _p(x), _p(logits), ctypes.byref(W), _p(out),
+        ctypes.byref(dbg) if dbg is not None else None, ev, _p(ws), ws.numel(),
+        _stream(stream)))
+
+
+def moe_check_status(ws, stream=None) -> int:
+    """Synchronises the stream and returns the device status bits of a workspace."""
+    bits = ctypes.c_uint32(0)
+    rc = lib().moe_check_status(_p(ws), _stream(stream), ctypes.byref(bits))
+    if rc not in (MOE_OK, 5):
+        raise MoeError("moe_check_status", rc)
+    return bits.value
+
+
+def debug_buffers(d, device="cuda"):
+    """Device buffers for every intermediate moe_forward can expose."""
+    T, H, I, E, k, sh = d.T, d.H, d.I, d.E, d.k, d.has_shared
+    R = T * k
+    Rs = R + (T if sh else 0)
+    G = E + sh
+    z = lambda *s, dt: torch.empty(*s, dtype=dt, device=device)
+    return dict(idx=z(T, k, dt=torch.int32), w=z(T, k, dt=torch.float32),
+                counts=z(E, dt=torch.int32), offsets=z(G + 1, dt=torch.int32),
+                perm_src=z(max(R, 1), dt=torch.int32), inv=z(max(R, 1), dt=torch.int32),
+                xq=z(T, H, dt=torch.uint8), xs=z(T, H // 128, dt=torch.uint8),
+                y13=z(Rs, 2 * I, dt=torch.bfloat16), hq=z(Rs, I, dt=torch.uint8),
+                hs=z(Rs, I // 128, dt=torch.uint8), y2=z(Rs, H, dt=torch.bfloat16))
+
+
+class MoELayer:
+    """The user-facing layer: resident MXFP4 weights plus a reusable workspace.
+
+    `forward(x, logits)` runs moe_forward on the current stream and returns the
+    bf16 output [T, H]."""
+
+    def __init__(self, H, I, E, k, has_shared, w13, w13_s, w2, w2_s):
+        self.H, self.I, self.E, self.k, self.has_shared = H, I, E, k, has_shared
+        self.w13, self.w13_s, self.w2, self.w2_s = w13, w13_s, w2, w2_s
+        self._ws = None
+        self._T = -1
+
+    def dims(self, T):
+        return dims(T, self.H, self.I, self.E, self.k, self.has_shared)
+
+    def workspace(self, T):
+        if self._ws is None or self._T < T:
+            self._ws = alloc_workspace(workspace_size(self.dims(T)), self.w13.device)
+            self._T = T
+        return self._ws
+
+    def forward(self, x, logits, out=None, debug=None, stream=None):
+        T = x.shape[0]
+        if out is None:
+            out = torch.empty(T, self.H, dtype=torch.bfloat16, device=x.device)
+        moe_forward(self.dims(T), x, logits, self.w13, self.w13_s, self.w2, self.w2_s, out,
+                    self.workspace(T), debug=debug, stream=stream)
+        return out

@@ -1,0 +1,362 @@
+// C interface (include/moe.h): argument checks, workspace carving and launches.
+// No allocation, no host synchronisation (except moe_check_status).
+#include <stdio.h>
+
+#include "kernels.cuh"
+
+using namespace moe;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+// Bump allocator over a caller-provided workspace (or a size counter when base is null).
+struct Carver {
+  uint8_t* base;
+  size_t used = 0;
+  explicit Carver(void* b) : base(static_cast<uint8_t*>(b)) {}
+  template <typename T>
+  T* take(size_t count) {
+    size_t off = used;
+    used = align_up(used + count * sizeof(T));
+    return base ? reinterpret_cast<T*>(base + off) : nullptr;
+  }
+};
+
+bool dims_ok(const moe_dims* d) {
+  if (!d) return false;
+  if (d->T < 1 || d->H < 128 || d->I < 128 || d->E < 1 || d->E > 1024 || d->k < 1) return false;
+  if (d->k > 16 || d->k > d->E) return false;
+  if (d->H % 128 || d->I % 128) return false;
+  if (d->has_shared != 0 && d->has_shared != 1) return false;
+  long long R = static_cast<long long>(d->T) * d->k;
+  if (R + d->T >= (1LL << 31)) return false;
+  if (static_cast<long long>(2) * d->I * d->H >= (1LL << 40)) return false;
+  return true;
+}
+
+long long rows_R(const moe_dims* d) { return static_cast<long long>(d->T) * d->k; }
+long long rows_Rs(const moe_dims* d) { return rows_R(d) + (d->has_shared ? d->T : 0); }
+int groups_G(const moe_dims* d) { return d->E + d->has_shared; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+struct RouteWs {
+  uint32_t* status;
+  int32_t* blockcnt;
+  int32_t* blockbase;
+};
+
+RouteWs carve_route(Carver& c, const moe_dims* d) {
+  RouteWs w;
+  w.status = c.take<uint32_t>(64);
+  const size_t nb = static_cast<size_t>(perm_blocks(d->T)) * d->E;
+  w.blockcnt = c.take<int32_t>(nb);
+  w.blockbase = c.take<int32_t>(nb);
+  return w;
+}
+
+struct PlanWs {
+  int4* small_items;
+  int4* large_items;
+  int32_t* counts;
+  int max_small, max_large;
+};
+
+PlanWs carve_plan(Carver& c, const moe_dims* d) {
+  PlanWs p;
+  const int G = groups_G(d);
+  p.max_small = G;
+  p.max_large = static_cast<int>(rows_Rs(d) / kLargeBN + G + 1);
+  p.small_items = c.take<int4>(p.max_small);
+  p.large_items = c.take<int4>(p.max_large);
+  p.counts = c.take<int32_t>(4);
+  return p;
+}
+
+struct GemmWs {
+  uint32_t* status;
+  PlanWs plan;
+  uint8_t* xg;   // packed FP8 rows for W13 [Rs][H]
+  uint8_t* xsg;  // their scales [Rs][H/128]
+};
+
+GemmWs carve_gemm(Carver& c, const moe_dims* d) {
+  GemmWs g;
+  g.status = c.take<uint32_t>(64);
+  g.plan = carve_plan(c, d);
+  const size_t Rs = static_cast<size_t>(rows_Rs(d));
+  g.xg = c.take<uint8_t>(Rs * d->H);
+  g.xsg = c.take<uint8_t>(Rs * (d->H / 128));
+  return g;
+}
+
+struct ForwardWs {
+  RouteWs route;
+  GemmWs gemm;
+  int32_t *idx, *counts, *offsets, *perm_src, *inv;
+  float* w;
+  uint8_t *xq, *xs, *hq, *hs;
+  uint16_t *y13, *y2;
+};
+
+ForwardWs carve_forward(Carver& c, const moe_dims* d) {
+  ForwardWs f;
+  f.route = carve_route(c, d);  // status word first
+  f.gemm = carve_gemm(c, d);
+  f.gemm.status = f.route.status;
+  const size_t T = d->T, R = rows_R(d), Rs = rows_Rs(d), H = d->H, I = d->I;
+  f.idx = c.take<int32_t>(R);
+  f.w = c.take<float>(R);
+  f.counts = c.take<int32_t>(d->E);
+  f.offsets = c.take<int32_t>(groups_G(d) + 1);
+  f.perm_src = c.take<int32_t>(R);
+  f.inv = c.take<int32_t>(R);
+  f.xq = c.take<uint8_t>(T * H);
+  f.xs = c.take<uint8_t>(T * (H / 128));
+  f.y13 = c.take<uint16_t>(Rs * 2 * I);
+  f.hq = c.take<uint8_t>(Rs * I);
+  f.hs = c.take<uint8_t>(Rs * (I / 128));
+  f.y2 = c.take<uint16_t>(Rs * H);
+  return f;
+}
+
+int run_gemm(const moe_dims* d, const uint8_t* act, const uint8_t* act_s, const int32_t* offsets,
+             const uint8_t* w, const uint8_t* w_s, int N, int K, uint16_t* y, const PlanWs& plan,
+             uint32_t* status, cudaStream_t st) {
+  GemmLaunch a{};
+  a.w_codes = w;
+  a.w_scales = w_s;
+  a.act = act;
+  a.act_scales = act_s;
+  a.y = y;
+  a.G = groups_G(d);
+  a.N = N;
+  a.K = K;
+  a.rows_total = static_cast<int>(rows_Rs(d));
+  a.small_items = plan.small_items;
+  a.large_items = plan.large_items;
+  a.item_counts = plan.counts;
+  a.max_small = plan.max_small;
+  a.max_large = plan.max_large;
+  a.status = status;
+  return cuda_rc(launch_grouped_gemm(a, st));
+}
+
+bool weights_ok(const uint8_t* c, const uint8_t* s) {
+  return c && s && aligned(c, 32) && aligned(s, 16);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_error_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument (null or misaligned pointer)";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE_CHECK: return "device-side check failed (see status bits)";
+    default: return "unknown status";
+  }
+}
+
+size_t moe_route_workspace_size(const moe_dims* d) {
+  if (!dims_ok(d)) return 0;
+  Carver c(nullptr);
+  carve_route(c, d);
+  return c.used;
+}
+
+size_t moe_gemm_workspace_size(const moe_dims* d) {
+  if (!dims_ok(d)) return 0;
+  Carver c(nullptr);
+  carve_gemm(c, d);
+  return c.used;
+}
+
+size_t moe_workspace_size(const moe_dims* d) {
+  if (!dims_ok(d)) return 0;
+  Carver c(nullptr);
+  carve_forward(c, d);
+  return c.used;
+}
+
+int moe_route(const moe_dims* d, const float* logits, int32_t* idx, float* w, int32_t* counts,
+              int32_t* offsets, int32_t* perm_src, int32_t* inv, void* ws, size_t ws_bytes,
+              void* stream) {
+  if (!dims_ok(d)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!logits || !idx || !w || !counts || !offsets || !perm_src || !inv || !ws)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned(ws, kAlign) || !aligned(logits, 4)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < moe_route_workspace_size(d)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Carver c(ws);
+  RouteWs rw = carve_route(c, d);
+  if (cudaMemsetAsync(rw.status, 0, sizeof(uint32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
+  cudaError_t e = launch_route(logits, d->T, d->E, d->k, idx, w, st);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  e = launch_permute(idx, d->T, d->E, d->k, d->has_shared, rw.blockcnt, rw.blockbase, counts,
+                     offsets, perm_src, inv, rw.status, st);
+  return cuda_rc(e);
+}
+
+int moe_quant_act(int32_t rows, int32_t cols, const uint16_t* x, uint8_t* q, uint8_t* s,
+                  void* stream) {
+  if (rows < 0 || cols <= 0 || cols % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (rows == 0) return MOE_OK;
+  if (!x || !q || !s || !aligned(x, 16) || !aligned(q, 16)) return MOE_ERR_INVALID_ARG;
+  return cuda_rc(launch_quant_act(x, rows, cols, q, s, static_cast<cudaStream_t>(stream)));
+}
+
+int moe_grouped_gemm_w13(const moe_dims* d, const uint8_t* xq, const uint8_t* xs,
+                         const int32_t* perm_src, const int32_t* group_offsets,
+                         const uint8_t* w13, const uint8_t* w13_s, uint16_t* y13, void* ws,
+                         size_t ws_bytes, void* stream) {
+  if (!dims_ok(d)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!xq || !xs || !group_offsets || !y13 || !ws || !weights_ok(w13, w13_s))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned(xq, 16) || !aligned(ws, kAlign) || !aligned(y13, 16)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < moe_gemm_workspace_size(d)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Carver c(ws);
+  GemmWs g = carve_gemm(c, d);
+  if (cudaMemsetAsync(g.status, 0, sizeof(uint32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
+  cudaError_t e = launch_plan(group_offsets, groups_G(d), kSmallBN, kLargeBN,
+                              g.plan.small_items, g.plan.large_items, g.plan.counts, g.status, st);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  const uint8_t* act = xq;
+  const uint8_t* act_s = xs;
+  if (perm_src) {
+    e = launch_gather_rows(xq, xs, perm_src, d->T, d->k, static_cast<int>(rows_R(d)),
+                           static_cast<int>(rows_Rs(d)), d->H, g.xg, g.xsg, g.status, st);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    act = g.xg;
+    act_s = g.xsg;
+  }
+  return run_gemm(d, act, act_s, group_offsets, w13, w13_s, 2 * d->I, d->H, y13, g.plan,
+                  g.status, st);
+}
+
+int moe_swiglu_quant(int32_t rows, int32_t I, const uint16_t* y13, uint8_t* hq, uint8_t* hs,
+                     void* stream) {
+  if (rows < 0 || I <= 0 || I % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (rows == 0) return MOE_OK;
+  if (!y13 || !hq || !hs || !aligned(y13, 16) || !aligned(hq, 16)) return MOE_ERR_INVALID_ARG;
+  return cuda_rc(launch_swiglu_quant(y13, rows, I, hq, hs, static_cast<cudaStream_t>(stream)));
+}
+
+int moe_grouped_gemm_w2(const moe_dims* d, const uint8_t* hq, const uint8_t* hs,
+                        const int32_t* group_offsets, const uint8_t* w2, const uint8_t* w2_s,
+                        uint16_t* y2, void* ws, size_t ws_bytes, void* stream) {
+  if (!dims_ok(d)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!hq || !hs || !group_offsets || !y2 || !ws || !weights_ok(w2, w2_s))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned(hq, 16) || !aligned(ws, kAlign) || !aligned(y2, 16)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < moe_gemm_workspace_size(d)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Carver c(ws);
+  GemmWs g = carve_gemm(c, d);
+  if (cudaMemsetAsync(g.status, 0, sizeof(uint32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
+  cudaError_t e = launch_plan(group_offsets, groups_G(d), kSmallBN, kLargeBN,
+                              g.plan.small_items, g.plan.large_items, g.plan.counts, g.status, st);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  return run_gemm(d, hq, hs, group_offsets, w2, w2_s, d->H, d->I, y2, g.plan, g.status, st);
+}
+
+int moe_combine(const moe_dims* d, const uint16_t* y2, const int32_t* inv, const float* w,
+                uint16_t* out, void* stream) {
+  if (!dims_ok(d)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!y2 || !inv || !w || !out || !aligned(y2, 16) || !aligned(out, 16))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_rc(launch_combine(y2, inv, w, d->T, d->k, d->H, d->has_shared, out, nullptr,
+                                static_cast<cudaStream_t>(stream)));
+}
+
+int moe_forward(const moe_dims* d, const uint16_t* x, const float* logits,
+                const moe_weights* W, uint16_t* out, const moe_debug_out* dbg, void* ws,
+                size_t ws_bytes, void* stream) {
+  return moe_forward_timed(d, x, logits, W, out, dbg, nullptr, ws, ws_bytes, stream);
+}
+
+int moe_forward_timed(const moe_dims* d, const uint16_t* x, const float* logits,
+                      const moe_weights* W, uint16_t* out, const moe_debug_out* dbg,
+                      void* const* events, void* ws, size_t ws_bytes, void* stream) {
+  if (!dims_ok(d)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!x || !logits || !W || !out || !ws) return MOE_ERR_INVALID_ARG;
+  if (!weights_ok(W->w13, W->w13_s) || !weights_ok(W->w2, W->w2_s)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(out, 16) || !aligned(ws, kAlign) || !aligned(logits, 4))
+    return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < moe_workspace_size(d)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Carver c(ws);
+  ForwardWs f = carve_forward(c, d);
+  // caller-visible intermediates replace the workspace buffers
+  if (dbg) {
+#define MOE_DBG(field) \
+  if (dbg->field) f.field = dbg->field;
+    MOE_DBG(idx) MOE_DBG(w) MOE_DBG(counts) MOE_DBG(offsets) MOE_DBG(perm_src) MOE_DBG(inv)
+    MOE_DBG(xq) MOE_DBG(xs) MOE_DBG(y13) MOE_DBG(hq) MOE_DBG(hs) MOE_DBG(y2)
+#undef MOE_DBG
+    if (!aligned(f.xq, 16) || !aligned(f.y13, 16) || !aligned(f.hq, 16) || !aligned(f.y2, 16))
+      return MOE_ERR_INVALID_ARG;
+  }
+  const int T = d->T, H = d->H, I = d->I, E = d->E, k = d->k;
+  const int R = static_cast<int>(rows_R(d)), Rs = static_cast<int>(rows_Rs(d));
+  uint32_t* status = f.route.status;
+  if (cudaMemsetAsync(status, 0, sizeof(uint32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
+  auto mark = [&](int i) -> bool {
+    return !events || cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st) == cudaSuccess;
+  };
+  cudaError_t e;
+#define MOE_TRY(call)                     \
+  e = (call);                             \
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+#define MOE_MARK(i) \
+  if (!mark(i)) return MOE_ERR_CUDA;
+  MOE_MARK(0)
+  MOE_TRY(launch_route(logits, T, E, k, f.idx, f.w, st))
+  MOE_TRY(launch_permute(f.idx, T, E, k, d->has_shared, f.route.blockcnt, f.route.blockbase,
+                         f.counts, f.offsets, f.perm_src, f.inv, status, st))
+  MOE_MARK(1)
+  MOE_TRY(launch_quant_act(x, T, H, f.xq, f.xs, st))
+  MOE_MARK(2)
+  MOE_TRY(launch_plan(f.offsets, groups_G(d), kSmallBN, kLargeBN, f.gemm.plan.small_items,
+                      f.gemm.plan.large_items, f.gemm.plan.counts, status, st))
+  MOE_TRY(launch_gather_rows(f.xq, f.xs, f.perm_src, T, k, R, Rs, H, f.gemm.xg, f.gemm.xsg,
+                             status, st))
+  MOE_MARK(3)
+  int rc = run_gemm(d, f.gemm.xg, f.gemm.xsg, f.offsets, W->w13, W->w13_s, 2 * I, H, f.y13,
+                    f.gemm.plan, status, st);
+  if (rc != MOE_OK) return rc;
+  MOE_MARK(4)
+  MOE_TRY(launch_swiglu_quant(f.y13, Rs, I, f.hq, f.hs, st))
+  MOE_MARK(5)
+  rc = run_gemm(d, f.hq, f.hs, f.offsets, W->w2, W->w2_s, H, I, f.y2, f.gemm.plan, status, st);
+  if (rc != MOE_OK) return rc;
+  MOE_MARK(6)
+  MOE_TRY(launch_combine(f.y2, f.inv, f.w, T, k, H, d->has_shared, out, status, st))
+  MOE_MARK(7)
+#undef MOE_TRY
+#undef MOE_MARK
+  return MOE_OK;
+}
+
+int moe_check_status(const void* ws, void* stream, uint32_t* bits_out) {
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  uint32_t bits = 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&bits, ws, sizeof(uint32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (bits_out) *bits_out = bits;
+  return bits ? MOE_ERR_DEVICE_CHECK : MOE_OK;
+}
+
+}  // extern "C"

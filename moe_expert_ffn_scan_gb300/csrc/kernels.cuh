@@ -1,0 +1,58 @@
+// Launch interfaces between the C-ABI layer (capi.cu) and the kernels.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+// Token-tile limits of the two GEMM variants: groups with M <= kSmallBN rows run in
+// the small-M kernel (deep pipeline, N padded to a multiple of 16 only); larger
+// groups are split into chunks of <= kLargeBN rows.
+constexpr int kSmallBN = 32;
+constexpr int kSmallStages = 8;
+constexpr int kLargeBN = 128;
+constexpr int kLargeStages = 6;
+
+cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* idx, float* w,
+                         cudaStream_t st);
+int perm_blocks(int T);
+cudaError_t launch_permute(const int32_t* idx, int T, int E, int k, int has_shared,
+                           int32_t* blockcnt, int32_t* blockbase, int32_t* counts,
+                           int32_t* offsets, int32_t* perm_src, int32_t* inv, uint32_t* status,
+                           cudaStream_t st);
+cudaError_t launch_plan(const int32_t* offsets, int G, int small_bn, int large_bn,
+                        int4* small_items, int4* large_items, int32_t* item_counts,
+                        uint32_t* status, cudaStream_t st);
+
+cudaError_t launch_quant_act(const uint16_t* x, int rows, int cols, uint8_t* q, uint8_t* s,
+                             cudaStream_t st);
+cudaError_t launch_swiglu_quant(const uint16_t* y13, int rows, int I, uint8_t* hq, uint8_t* hs,
+                                cudaStream_t st);
+cudaError_t launch_gather_rows(const uint8_t* xq, const uint8_t* xs, const int32_t* perm_src,
+                               int T, int k, int R, int Rs, int H, uint8_t* xg, uint8_t* xsg,
+                               uint32_t* status, cudaStream_t st);
+cudaError_t launch_combine(const uint16_t* y2, const int32_t* inv, const float* w, int T, int k,
+                           int H, int has_shared, uint16_t* out, uint32_t* status,
+                           cudaStream_t st);
+
+struct GemmLaunch {
+  const uint8_t* w_codes;     // [G][N][K/2]
+  const uint8_t* w_scales;    // [G][N][K/32]
+  const uint8_t* act;         // [rows_total][K] packed FP8 rows
+  const uint8_t* act_scales;  // [rows_total][K/128]
+  uint16_t* y;                // [rows_total][N]
+  int G, N, K, rows_total;
+  const int4* small_items;
+  const int4* large_items;
+  const int32_t* item_counts;  // [2]: small, large
+  int max_small, max_large;
+  uint32_t* status;
+};
+cudaError_t launch_grouped_gemm(const GemmLaunch& a, cudaStream_t st);
+
+// Transaction bytes one 128 x 128 weight-tile TMA load reports to its mbarrier: the
+// packed global size (128 rows x 64 bytes), not the 16-byte-aligned shared-memory
+// footprint (which is twice that).
+constexpr uint32_t kWeightTileTxBytes = 128 * 64;
+
+}  // namespace moe

@@ -1,0 +1,338 @@
+// a1 top-k routing, a2 histogram / exclusive scan / permutation, a8 tile plan.
+//
+// Routing follows the TopK step of "Pushing the Limits of Serving DeepSeek-V4-Pro"
+// (LMSYS, H20), §3.2; the per-expert M that shapes the grouped GEMMs comes from the
+// routing histogram (§3.3); packing tokens by expert ahead of the expert GEMMs is
+// Optimization 14 ("direct route preplan") of the GB10 optimisation report.
+//
+// Everything here is integer-exact and deterministic: ranks inside an expert's
+// segment come from per-warp bit masks and prefix sums, never from the order in
+// which atomics happen to land.
+#include "kernels.cuh"
+
+namespace moe {
+
+// ---------------------------------------------------------------- a1: route -------
+//
+// One warp per token.  Lane l holds logits l, l+32, ... (coalesced loads).  k rounds
+// of warp-wide argmax over the not-yet-taken experts, ties to the lower index.
+template <int EPL>
+__global__ void __launch_bounds__(256) k_route(const float* __restrict__ logits, int T, int E,
+                                               int k, int32_t* __restrict__ idx,
+                                               float* __restrict__ w) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const float* row = logits + static_cast<size_t>(t) * E;
+  float v[EPL];
+  uint32_t taken = 0;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    int e = lane + 32 * i;
+    v[i] = e < E ? row[e] : 0.f;
+    if (e >= E) taken |= 1u << i;
+  }
+  float my_v = 0.f;
+  int my_e = 0;
+  for (int j = 0; j < k; ++j) {
+    float bv = 0.f;
+    int be = 0x7FFFFFFF;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      int e = lane + 32 * i;
+      bool ok = !((taken >> i) & 1u);
+      if (ok && (be == 0x7FFFFFFF || v[i] > bv)) {  // ascending e: strict > keeps lower index
+        bv = v[i];
+        be = e;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
+      int oe = __shfl_xor_sync(0xFFFFFFFFu, be, off);
+      bool better = (oe != 0x7FFFFFFF) &&
+                    (be == 0x7FFFFFFF || ov > bv || (ov == bv && oe < be));
+      if (better) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    if (lane == j) {
+      my_v = bv;
+      my_e = be;
+    }
+  }
+  // weights: exp(l_j - l_0) / sum over the selected
+  float l0 = __shfl_sync(0xFFFFFFFFu, my_v, 0);
+  float ex = lane < k ? expf(my_v - l0) : 0.f;
+  float s = ex;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
+  if (lane < k) {
+    idx[static_cast<size_t>(t) * k + lane] = my_e;
+    w[static_cast<size_t>(t) * k + lane] = ex / s;
+  }
+}
+
+// ---------------------------------------------------------------- a2: histogram ---
+//
+// Tokens are processed in blocks of kPermTokens (one per thread).  Pass 1 counts
+// per (block, expert); pass 2 scans those counts per expert and over experts;
+// pass 3 recomputes each warp's masks and writes every routed row's position.
+constexpr int kPermTokens = 256;
+
+__global__ void __launch_bounds__(kPermTokens) k_hist_block(const int32_t* __restrict__ idx,
+                                                            int T, int E, int k,
+                                                            int32_t* __restrict__ blockcnt,
+                                                            uint32_t* status) {
+  extern __shared__ int32_t s_cnt[];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
+  __syncthreads();
+  const int t = blockIdx.x * kPermTokens + threadIdx.x;
+  if (t < T) {
+    for (int j = 0; j < k; ++j) {
+      int e = idx[static_cast<size_t>(t) * k + j];
+      if (e < 0 || e >= E) {
+        set_status(status, STATUS_BAD_INDEX);
+        continue;
+      }
+      atomicAdd(&s_cnt[e], 1);  // integer count: order-independent result
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    blockcnt[static_cast<size_t>(blockIdx.x) * E + e] = s_cnt[e];
+}
+
+// One CTA.  blockbase[b][e] = sum of blockcnt[b'][e] for b' < b; counts; offsets
+// over G = E + has_shared groups (the shared group holds T rows).
+__global__ void __launch_bounds__(1024) k_scan(const int32_t* __restrict__ blockcnt, int nblk,
+                                               int T, int E, int has_shared,
+                                               int32_t* __restrict__ blockbase,
+                                               int32_t* __restrict__ counts,
+                                               int32_t* __restrict__ offsets) {
+  __shared__ int32_t s_part[1024];
+  __shared__ int32_t s_warp[32];
+  const int tid = threadIdx.x;
+  const int G = E + has_shared;
+  // per-expert totals over blocks (thread per expert, E <= 1024)
+  int32_t total = 0;
+  if (tid < E) {
+    for (int b = 0; b < nblk; ++b) {
+      int32_t c = blockcnt[static_cast<size_t>(b) * E + tid];
+      blockbase[static_cast<size_t>(b) * E + tid] = total;
+      total += c;
+    }
+    counts[tid] = total;
+  }
+  int32_t gsize = tid < E ? total : (tid == E && has_shared ? T : 0);
+  // exclusive scan of gsize over threads 0..1023 (G <= 1025: group 1024 handled below)
+  int32_t x = gsize;
+  const int lane = tid & 31, wid = tid >> 5;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    int32_t y = __shfl_up_sync(0xFFFFFFFFu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) s_warp[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    int32_t y = s_warp[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      int32_t z = __shfl_up_sync(0xFFFFFFFFu, y, off);
+      if (lane >= off) y += z;
+    }
+    s_warp[lane] = y;  // inclusive over warps
+  }
+  __syncthreads();
+  int32_t incl = x + (wid > 0 ? s_warp[wid - 1] : 0);
+  s_part[tid] = incl;
+  if (tid < G) offsets[tid] = incl - gsize;
+  __syncthreads();
+  if (tid == 0) {
+    int32_t end = s_part[1023];
+    if (G == 1025) {  // E == 1024 with a shared expert: group 1024 = the shared rows
+      offsets[1024] = end;
+      offsets[1025] = end + T;
+    } else {
+      offsets[G] = end;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kPermTokens) k_permute_block(
+    const int32_t* __restrict__ idx, int T, int E, int k, const int32_t* __restrict__ blockbase,
+    const int32_t* __restrict__ offsets, int32_t* __restrict__ perm_src,
+    int32_t* __restrict__ inv) {
+  extern __shared__ uint32_t s_bits[];  // [8 warps][E] masks, then [8][E] warp bases
+  constexpr int kWarps = kPermTokens / 32;
+  int32_t* s_wbase = reinterpret_cast<int32_t*>(s_bits + kWarps * E);
+  for (int i = threadIdx.x; i < kWarps * E; i += blockDim.x) s_bits[i] = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int t = blockIdx.x * kPermTokens + threadIdx.x;
+  const bool live = t < T;
+  if (live) {
+    for (int j = 0; j < k; ++j) {
+      int e = idx[static_cast<size_t>(t) * k + j];
+      if (e >= 0 && e < E) atomicOr(&s_bits[wid * E + e], 1u << lane);
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int32_t run = 0;
+    for (int w = 0; w < kWarps; ++w) {
+      s_wbase[w * E + e] = run;
+      run += __popc(s_bits[w * E + e]);
+    }
+  }
+  __syncthreads();
+  if (live) {
+    const uint32_t lt = (1u << lane) - 1u;
+    for (int j = 0; j < k; ++j) {
+      int e = idx[static_cast<size_t>(t) * k + j];
+      if (e < 0 || e >= E) continue;
+      int32_t pos = offsets[e] + blockbase[static_cast<size_t>(blockIdx.x) * E + e] +
+                    s_wbase[wid * E + e] + __popc(s_bits[wid * E + e] & lt);
+      int32_t src = t * k + j;
+      perm_src[pos] = src;
+      inv[src] = pos;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- a8: tile plan ---
+//
+// Per group g with M = offsets[g+1] - offsets[g] rows: groups with M <= small_bn go
+// to the small-M list as one item (the GEMM pads M only to the next multiple of 16,
+// never to a large tile); larger groups are split into ceil(M / large_bn) chunks of
+// near-equal size for the large-M list.  Items are {group, row0, rows, 0}.
+// One CTA of 1024 threads; each thread owns a contiguous run of groups.
+__global__ void __launch_bounds__(1024) k_plan(const int32_t* __restrict__ offsets, int G,
+                                               int small_bn, int large_bn,
+                                               int4* __restrict__ small_items,
+                                               int4* __restrict__ large_items,
+                                               int32_t* __restrict__ item_counts,
+                                               uint32_t* status) {
+  __shared__ int32_t s_ws[32], s_wl[32];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int per = (G + 1023) / 1024;
+  const int g0 = tid * per, g1 = min(G, g0 + per);
+  int32_t ns = 0, nl = 0;
+  for (int g = g0; g < g1; ++g) {
+    int32_t m = offsets[g + 1] - offsets[g];
+    if (m < 0) set_status(status, STATUS_BAD_PLAN);
+    if (m <= 0) continue;
+    if (m <= small_bn) ++ns;
+    else nl += (m + large_bn - 1) / large_bn;
+  }
+  // exclusive scans of ns and nl over threads
+  int32_t xs = ns, xl = nl;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    int32_t a = __shfl_up_sync(0xFFFFFFFFu, xs, off);
+    int32_t b = __shfl_up_sync(0xFFFFFFFFu, xl, off);
+    if (lane >= off) {
+      xs += a;
+      xl += b;
+    }
+  }
+  if (lane == 31) {
+    s_ws[wid] = xs;
+    s_wl[wid] = xl;
+  }
+  __syncthreads();
+  if (wid == 0) {
+    int32_t a = s_ws[lane], b = s_wl[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      int32_t c = __shfl_up_sync(0xFFFFFFFFu, a, off);
+      int32_t d = __shfl_up_sync(0xFFFFFFFFu, b, off);
+      if (lane >= off) {
+        a += c;
+        b += d;
+      }
+    }
+    s_ws[lane] = a;
+    s_wl[lane] = b;
+  }
+  __syncthreads();
+  int32_t ps = xs - ns + (wid > 0 ? s_ws[wid - 1] : 0);
+  int32_t pl = xl - nl + (wid > 0 ? s_wl[wid - 1] : 0);
+  for (int g = g0; g < g1; ++g) {
+    int32_t r0 = offsets[g], m = offsets[g + 1] - r0;
+    if (m <= 0) continue;
+    if (m <= small_bn) {
+      small_items[ps++] = make_int4(g, r0, m, 0);
+    } else {
+      int32_t nch = (m + large_bn - 1) / large_bn;
+      // near-equal chunks, each a multiple of 16 rows except the last
+      int32_t base = ((m + nch - 1) / nch + 15) / 16 * 16;
+      for (int c = 0; c < nch; ++c) {
+        int32_t a = c * base, b = min(m, a + base);
+        if (a >= m) break;
+        large_items[pl++] = make_int4(g, r0 + a, b - a, 0);
+      }
+    }
+  }
+  if (tid == 1023) {
+    item_counts[0] = s_ws[31];
+    item_counts[1] = s_wl[31];
+  }
+}
+
+// ---------------------------------------------------------------- launchers -------
+
+cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* idx, float* w,
+                         cudaStream_t st) {
+  const int warps = 8;
+  dim3 grid((T + warps - 1) / warps), block(32 * warps);
+  const int epl = (E + 31) / 32;
+#define MOE_ROUTE_CASE(N) \
+  if (epl <= N) {         \
+    k_route<N><<<grid, block, 0, st>>>(logits, T, E, k, idx, w); \
+    return cudaGetLastError(); \
+  }
+  MOE_ROUTE_CASE(1)
+  MOE_ROUTE_CASE(2)
+  MOE_ROUTE_CASE(4)
+  MOE_ROUTE_CASE(8)
+  MOE_ROUTE_CASE(12)
+  MOE_ROUTE_CASE(16)
+  MOE_ROUTE_CASE(32)
+#undef MOE_ROUTE_CASE
+  return cudaErrorInvalidValue;
+}
+
+int perm_blocks(int T) { return (T + kPermTokens - 1) / kPermTokens; }
+
+cudaError_t launch_permute(const int32_t* idx, int T, int E, int k, int has_shared,
+                           int32_t* blockcnt, int32_t* blockbase, int32_t* counts,
+                           int32_t* offsets, int32_t* perm_src, int32_t* inv, uint32_t* status,
+                           cudaStream_t st) {
+  const int nblk = perm_blocks(T);
+  k_hist_block<<<nblk, kPermTokens, E * sizeof(int32_t), st>>>(idx, T, E, k, blockcnt, status);
+  k_scan<<<1, 1024, 0, st>>>(blockcnt, nblk, T, E, has_shared, blockbase, counts, offsets);
+  size_t smem = 2 * (kPermTokens / 32) * E * sizeof(uint32_t);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(k_permute_block,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  k_permute_block<<<nblk, kPermTokens, smem, st>>>(idx, T, E, k, blockbase, offsets, perm_src,
+                                                   inv);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_plan(const int32_t* offsets, int G, int small_bn, int large_bn,
+                        int4* small_items, int4* large_items, int32_t* item_counts,
+                        uint32_t* status, cudaStream_t st) {
+  k_plan<<<1, 1024, 0, st>>>(offsets, G, small_bn, large_bn, small_items, large_items,
+                             item_counts, status);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,94 @@
+"""Host-side checks of the C interface (no GPU needed): every symbol declared in
+include/moe.h is exported by libmoe.so, and argument / shape validation rejects bad
+calls before anything is launched."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import moe_expert_ffn_scan_gb300 as moe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(moe.LIB_PATH):
+        from moe_expert_ffn_scan_gb300 import build
+        build.build()
+    return moe.lib()
+
+
+def test_header_declares_the_hot_path(lib):
+    names = _declared_functions()
+    for n in ("moe_route", "moe_quant_act", "moe_grouped_gemm_w13", "moe_swiglu_quant",
+              "moe_grouped_gemm_w2", "moe_combine", "moe_forward"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in _declared_functions():
+        assert hasattr(lib, n), f"libmoe.so does not export {n}"
+
+
+def test_error_strings(lib):
+    for code in range(6):
+        assert lib.moe_error_string(code)
+    assert b"unknown" in lib.moe_error_string(99)
+
+
+def test_workspace_sizes_and_unsupported_shapes(lib):
+    ok = moe.dims(7, 7168, 3072, 384, 8, 1)
+    assert moe.workspace_size(ok) > moe.gemm_workspace_size(ok) > 0
+    assert moe.route_workspace_size(ok) > 0
+    for bad in (moe.dims(7, 7100, 3072, 384, 8, 1),   # H % 128
+                moe.dims(7, 7168, 3000, 384, 8, 1),   # I % 128
+                moe.dims(0, 512, 256, 8, 2, 0),       # T
+                moe.dims(4, 512, 256, 8, 9, 0),       # k > E
+                moe.dims(4, 512, 256, 2000, 8, 0),    # E > 1024
+                moe.dims(4, 512, 256, 64, 17, 0),     # k > 16
+                moe.dims(4, 512, 256, 8, 2, 2)):      # has_shared not 0/1
+        assert moe.workspace_size(bad) == 0
+
+
+def test_validation_happens_before_any_launch(lib):
+    d = moe.dims(7, 512, 256, 8, 2, 0)
+    P = ctypes.c_void_p
+    # null pointers -> invalid argument, unsupported dims -> unsupported shape
+    assert lib.moe_route(ctypes.byref(d), None, None, None, None, None, None, None, None, 0,
+                         None) == 1
+    bad = moe.dims(7, 500, 256, 8, 2, 0)
+    assert lib.moe_forward(ctypes.byref(bad), None, None, None, None, None, None, 0, None) == 2
+    assert lib.moe_quant_act(4, 100, None, None, None, None) == 2
+    assert lib.moe_quant_act(0, 128, None, None, None, None) == 0
+    assert lib.moe_swiglu_quant(4, 100, None, None, None, None) == 2
+    # misaligned workspace -> invalid argument
+    fake = P(0x1000 + 8)
+    assert lib.moe_route(ctypes.byref(d), P(0x1000), P(0x1000), P(0x1000), P(0x1000),
+                         P(0x1000), P(0x1000), P(0x1000), fake, 1 << 20, None) == 1
+    # workspace too small
+    assert lib.moe_route(ctypes.byref(d), P(0x1000), P(0x1000), P(0x1000), P(0x1000),
+                         P(0x1000), P(0x1000), P(0x1000), P(0x10000), 16, None) == 3
+    w = moe.moe_weights(0x10000, 0x10000, 0x10008, 0x10000)  # w2 misaligned (needs 32 B)
+    assert lib.moe_forward(ctypes.byref(d), P(0x1000), P(0x1000), ctypes.byref(w),
+                           P(0x1000), None, P(0x10000), 1 << 30, None) == 1
+
+
+def test_python_binding_rejects_host_tensors(lib):
+    import torch
+    x = torch.zeros(4, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        moe.moe_quant_act(x, torch.zeros(4, 128, dtype=torch.uint8),
+                          torch.zeros(4, 1, dtype=torch.uint8))

@@ -1,0 +1,145 @@
+"""GPU parity of the whole layer (moe_forward) against the oracle.
+
+Small shapes are checked in full, stage by stage, on identical seeded inputs.  The
+full-size decode and prefill workloads are checked on every integer output in full
+and on sampled floating-point outputs that the oracle computes one by one."""
+
+import numpy as np
+import pytest
+import torch
+
+import moe_expert_ffn_scan_gb300 as moe
+from gen import inputs as gi
+from oracle import moe_oracle as o
+from tests._parity import (assert_float_close, assert_fp8_codes_close, bf16_np, bits_np)
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def _forward(d, t):
+    dbg = moe.debug_buffers(d)
+    out = torch.empty(d.T, d.H, dtype=torch.bfloat16, device=DEV)
+    ws = moe.alloc_workspace(moe.workspace_size(d))
+    moe.moe_forward(d, t["x"], t["logits"], t["w13"], t["w13_s"], t["w2"], t["w2_s"], out, ws,
+                    debug=dbg)
+    bits = moe.moe_check_status(ws)
+    assert bits == 0, f"device status {bits:#x}"
+    return out, dbg
+
+
+def _np(t):
+    return {k: (v.cpu().numpy() if v.dtype != torch.bfloat16 else bits_np(v))
+            for k, v in t.items()}
+
+
+def _check_full(d, t):
+    out, dbg = _forward(d, {k: v.to(DEV) for k, v in t.items()})
+    n = _np(t)
+    ref = o.moe_forward(n["x"], n["logits"], d.k, n["w13"], n["w13_s"], n["w2"], n["w2_s"],
+                        d.has_shared)
+    g = {k: v.cpu() for k, v in dbg.items()}
+    R = d.T * d.k
+    for name in ("idx", "counts", "offsets", "xq", "xs"):
+        assert np.array_equal(g[name].numpy(), ref[name]), name
+    assert np.array_equal(g["perm_src"].numpy()[:R], ref["perm_src"])
+    assert np.array_equal(g["inv"].numpy()[:R], ref["inv"])
+    np.testing.assert_allclose(g["w"].numpy(), ref["w"], rtol=2e-6, atol=1e-7)
+    stats = {}
+    stats["y13"] = assert_float_close(bf16_np(g["y13"]), ref["y13"], "y13")
+    stats["hq_agree"] = assert_fp8_codes_close(g["hq"].numpy(), g["hs"].numpy(), ref["hq"],
+                                               ref["hs"], "hq")
+    stats["y2"] = assert_float_close(bf16_np(g["y2"]), ref["y2"], "y2")
+    stats["out"] = assert_float_close(bf16_np(out), ref["out"], "out")
+    return stats
+
+
+def test_forward_tiny_workload():
+    d, t = gi.make_layer("tiny")
+    _check_full(moe.dims(d.T, d.H, d.I, d.E, d.k, d.has_shared), t)
+
+
+@pytest.mark.parametrize("T,H,I,E,k,sh,kind", [
+    (13, 256, 128, 5, 3, 1, "normal"),      # ragged, shared expert
+    (1, 512, 256, 8, 2, 1, "normal"),       # a single token
+    (200, 384, 256, 16, 4, 1, "zipf"),      # skewed: large and empty groups
+    (40, 1024, 512, 64, 8, 0, "zipf"),
+    (90, 256, 256, 3, 3, 0, "normal"),      # k == E: every token to every expert
+])
+def test_forward_ragged_shapes(T, H, I, E, k, sh, kind):
+    d = gi.Dims(T=T, H=H, I=I, E=E, k=k, has_shared=sh)
+    t = gi.custom_layer(d, seed=T + E, logits_kind=kind)
+    _check_full(moe.dims(T, H, I, E, k, sh), t)
+
+
+def test_forward_zero_input():
+    d, t = gi.make_layer("tiny")
+    t["x"] = torch.zeros_like(t["x"])
+    out, dbg = _forward(moe.dims(d.T, d.H, d.I, d.E, d.k, d.has_shared),
+                        {k: v.to(DEV) for k, v in t.items()})
+    assert torch.all(out.float() == 0)
+
+
+# ---------------------------------------------------------------- full size ---------
+
+def _sampled_check(workload, n_tokens, n_cols, seed=0):
+    d, t = gi.make_layer(workload, seed=seed, device=DEV)
+    md = moe.dims(d.T, d.H, d.I, d.E, d.k, d.has_shared)
+    out, dbg = _forward(md, t)
+    # integer stages in full
+    lg = t["logits"].cpu().numpy()
+    ridx, rw = o.route(lg, d.k)
+    rc, roff, rperm, rinv = o.permute(ridx, d.E, d.has_shared)
+    g = {k: v.cpu().numpy() for k, v in dbg.items() if v.dtype != torch.bfloat16}
+    R = d.T * d.k
+    assert np.array_equal(g["idx"], ridx)
+    assert np.array_equal(g["counts"], rc)
+    assert np.array_equal(g["offsets"], roff)
+    assert np.array_equal(g["perm_src"][:R], rperm)
+    assert np.array_equal(g["inv"][:R], rinv)
+    np.testing.assert_allclose(g["w"], rw, rtol=2e-6, atol=1e-7)
+    xbits = bits_np(t["x"])
+    qrows = np.arange(d.T) if d.T <= 4096 else np.sort(
+        np.random.default_rng(seed + 1).choice(d.T, 512, replace=False))
+    xq, xs = o.quant_act(xbits[qrows])
+    assert np.array_equal(g["xq"][qrows], xq) and np.array_equal(g["xs"][qrows], xs)
+    # sampled floating-point outputs: whole tokens through the oracle
+    rng = np.random.default_rng(seed)
+    toks = np.sort(rng.choice(d.T, size=min(n_tokens, d.T), replace=False))
+    experts = sorted(set(ridx[toks].ravel().tolist()) | ({d.E} if d.has_shared else set()))
+    # the oracle sees the sampled tokens' rows and only the experts they use
+    w13 = np.zeros((d.G,) + tuple(t["w13"].shape[1:]), np.uint8)
+    w13s = np.zeros((d.G,) + tuple(t["w13_s"].shape[1:]), np.uint8)
+    w2 = np.zeros((d.G,) + tuple(t["w2"].shape[1:]), np.uint8)
+    w2s = np.zeros((d.G,) + tuple(t["w2_s"].shape[1:]), np.uint8)
+    for e in experts:
+        w13[e] = t["w13"][e].cpu().numpy()
+        w13s[e] = t["w13_s"][e].cpu().numpy()
+        w2[e] = t["w2"][e].cpu().numpy()
+        w2s[e] = t["w2_s"][e].cpu().numpy()
+    ref = o.moe_forward_tokens(xbits, lg, d.k, w13, w13s, w2, w2s, d.has_shared, toks)
+    assert_float_close(bf16_np(out[torch.from_numpy(toks).to(DEV)]), ref["out"], "out")
+    # y13 / y2 rows of the sampled tokens, sampled columns
+    inv = g["inv"][:R].reshape(d.T, d.k)
+    rows = np.concatenate([inv[toks].ravel()] + ([R + toks] if d.has_shared else []))
+    ref_rows = np.concatenate([ref["inv"].reshape(len(toks), d.k).ravel()] +
+                              ([len(toks) * d.k + np.arange(len(toks))] if d.has_shared else []))
+    y13 = bf16_np(dbg["y13"][torch.from_numpy(rows).to(DEV)])
+    assert_float_close(y13, ref["y13"][ref_rows], "y13 rows")
+    y2 = bf16_np(dbg["y2"][torch.from_numpy(rows).to(DEV)])
+    assert_float_close(y2, ref["y2"][ref_rows], "y2 rows")
+    del t, dbg
+    torch.cuda.empty_cache()
+
+
+def test_forward_decode_full_size_sampled():
+    _sampled_check("decode", n_tokens=2, n_cols=0)
+
+
+def test_forward_decode256_full_size_sampled():
+    _sampled_check("decode256", n_tokens=2, n_cols=0)
+
+
+def test_forward_prefill_full_size_sampled():
+    _sampled_check("prefill", n_tokens=1, n_cols=0)
