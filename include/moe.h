@@ -114,6 +114,24 @@ int moe_route(const moe_dims* d, const float* logits, int32_t* idx, float* w, in
               int32_t* offsets, int32_t* perm_src, int32_t* inv, void* ws, size_t ws_bytes,
               void* stream);
 
+/* moe_route without a workspace argument, for callers that cannot allocate device
+ * memory (a host framework whose pool owns every device byte, or a latency-critical
+ * loop that cannot afford cudaMalloc/cudaFree and their implicit synchronisation).
+ * The pages have no counterpart: this is an interface convenience, not a step of
+ * the method.  Same arguments and results as moe_route minus ws / ws_bytes.
+ *   - Scratch lives in a fixed device array of 256 KiB + 256 bytes inside the
+ *     library, held on every GPU that loads it until the process exits.  Limit:
+ *     ceil(T/256) * E <= 32768 (T <= 8192 at E = 1024, T <= 21760 at E = 384);
+ *     larger inputs return MOE_ERR_UNSUPPORTED_SHAPE.
+ *   - The first call on each device looks up the array's device address (with that
+ *     device current); make that first call before any stream capture.
+ *   - All calls share the array and it keeps the last call's contents; calls that
+ *     overlap on the GPU (other streams, other host threads) race on it and must be
+ *     serialised by the caller.  Nothing is allocated. */
+int moe_route_static(const moe_dims* d, const float* logits, int32_t* idx, float* w,
+                     int32_t* counts, int32_t* offsets, int32_t* perm_src, int32_t* inv,
+                     void* stream);
+
 /* a3: online FP8 E4M3 quantisation of bf16 x [rows][cols] with one power-of-two
  * scale per row per 128 columns (rule above) -> q [rows][cols], s [rows][cols/128].
  * Pages: LMSYS-H20 §2.2 (online FP8 activations), §3.2 (fused FP8 quantisation).
