@@ -49,6 +49,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-flush", action="store_true")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="override E (a smaller layer of the same shape, for ncu captures)")
+    ap.add_argument("--tokens", type=int, default=None, help="override T")
     return ap.parse_args()
 
 
@@ -177,6 +180,15 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def make_layer(args, seed, dev):
+    if args.experts is None and args.tokens is None:
+        return gi.make_layer(args.workload, seed=seed, device=dev)
+    import dataclasses
+    d = gi.WORKLOADS[args.workload]
+    d = dataclasses.replace(d, E=args.experts or d.E, T=args.tokens or d.T)
+    return d, gi.custom_layer(d, seed=seed, device=dev, logits_kind=gi.LOGITS_KIND[args.workload])
+
+
 def active_groups(counts, has_shared):
     return int((counts > 0).sum()) + (1 if has_shared else 0)
 
@@ -232,7 +244,7 @@ def run_reference(args, rank, world):
     if rank != 0:
         return
     dev = "cuda" if torch.cuda.is_available() else "cpu"
-    d, t = gi.make_layer(args.workload, seed=args.seed, device=dev)
+    d, t = make_layer(args, args.seed, dev)
     hv = host_view(d, t)
     tokens = 1
     times = []
@@ -265,7 +277,7 @@ def run_ours(args, rank, world, local):
     import moe_expert_ffn_scan_gb300 as moe
     moe.lib()
     dev = torch.device("cuda", local)
-    d, t = gi.make_layer(args.workload, seed=args.seed + rank, device=dev)
+    d, t = make_layer(args, args.seed + rank, dev)
     md = moe.dims(d.T, d.H, d.I, d.E, d.k, d.has_shared)
     layer = moe.MoELayer(d.H, d.I, d.E, d.k, d.has_shared, t["w13"], t["w13_s"], t["w2"],
                          t["w2_s"])

@@ -222,7 +222,8 @@ int moe_grouped_gemm_w13(const moe_dims* d, const uint8_t* xq, const uint8_t* xs
   if (!dims_ok(d)) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (!xq || !xs || !group_offsets || !y13 || !ws || !weights_ok(w13, w13_s))
     return MOE_ERR_INVALID_ARG;
-  if (!aligned(xq, 16) || !aligned(ws, kAlign) || !aligned(y13, 16)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(xq, 16) || !aligned(xs, 4) || !aligned(ws, kAlign) || !aligned(y13, 16))
+    return MOE_ERR_INVALID_ARG;
   if (ws_bytes < moe_gemm_workspace_size(d)) return MOE_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   Carver c(ws);
@@ -258,7 +259,8 @@ int moe_grouped_gemm_w2(const moe_dims* d, const uint8_t* hq, const uint8_t* hs,
   if (!dims_ok(d)) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (!hq || !hs || !group_offsets || !y2 || !ws || !weights_ok(w2, w2_s))
     return MOE_ERR_INVALID_ARG;
-  if (!aligned(hq, 16) || !aligned(ws, kAlign) || !aligned(y2, 16)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(hq, 16) || !aligned(hs, 4) || !aligned(ws, kAlign) || !aligned(y2, 16))
+    return MOE_ERR_INVALID_ARG;
   if (ws_bytes < moe_gemm_workspace_size(d)) return MOE_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   Carver c(ws);
@@ -304,7 +306,8 @@ int moe_forward_timed(const moe_dims* d, const uint16_t* x, const float* logits,
     MOE_DBG(idx) MOE_DBG(w) MOE_DBG(counts) MOE_DBG(offsets) MOE_DBG(perm_src) MOE_DBG(inv)
     MOE_DBG(xq) MOE_DBG(xs) MOE_DBG(y13) MOE_DBG(hq) MOE_DBG(hs) MOE_DBG(y2)
 #undef MOE_DBG
-    if (!aligned(f.xq, 16) || !aligned(f.y13, 16) || !aligned(f.hq, 16) || !aligned(f.y2, 16))
+    if (!aligned(f.xq, 16) || !aligned(f.y13, 16) || !aligned(f.hq, 16) || !aligned(f.y2, 16) ||
+        !aligned(f.hs, 4) || !aligned(f.xs, 4))
       return MOE_ERR_INVALID_ARG;
   }
   const int T = d->T, H = d->H, I = d->I, E = d->E, k = d->k;

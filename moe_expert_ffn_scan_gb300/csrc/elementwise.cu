@@ -122,9 +122,9 @@ __global__ void __launch_bounds__(256) k_gather_rows(const uint8_t* __restrict__
   for (int i = lane; i < ns; i += 32) xsg[r * ns + i] = xs[static_cast<long long>(tok) * ns + i];
 }
 
-// a7.  One CTA per token; each thread owns 8 consecutive columns.  fp32 sum in j
-// order, shared row last, one rounding to bf16.
-__global__ void __launch_bounds__(256) k_combine(const uint16_t* __restrict__ y2,
+// a7.  CTA (token t, 1024-column chunk); each thread owns 8 consecutive columns.
+// fp32 sum in j order, shared row last, one rounding to bf16.
+__global__ void __launch_bounds__(128) k_combine(const uint16_t* __restrict__ y2,
                                                  const int32_t* __restrict__ inv,
                                                  const float* __restrict__ w, int T, int k,
                                                  int H, int has_shared, int R, int Rs,
@@ -143,7 +143,8 @@ __global__ void __launch_bounds__(256) k_combine(const uint16_t* __restrict__ y2
     s_w[threadIdx.x] = w[static_cast<long long>(t) * k + threadIdx.x];
   }
   __syncthreads();
-  for (int c = threadIdx.x * 8; c < H; c += blockDim.x * 8) {
+  const int c = blockIdx.y * (blockDim.x * 8) + threadIdx.x * 8;
+  if (c < H) {
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.f;
@@ -212,8 +213,9 @@ cudaError_t launch_combine(const uint16_t* y2, const int32_t* inv, const float* 
                            cudaStream_t st) {
   if (T == 0) return cudaSuccess;
   const int R = T * k, Rs = R + (has_shared ? T : 0);
-  int threads = H / 8 < 256 ? ((H / 8 + 31) / 32) * 32 : 256;
-  k_combine<<<T, threads, 0, st>>>(y2, inv, w, T, k, H, has_shared, R, Rs, out, status);
+  const int threads = 128;
+  dim3 grid(T, (H + threads * 8 - 1) / (threads * 8));
+  k_combine<<<grid, threads, 0, st>>>(y2, inv, w, T, k, H, has_shared, R, Rs, out, status);
   return cudaGetLastError();
 }
 

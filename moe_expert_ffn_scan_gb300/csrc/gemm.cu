@@ -37,27 +37,42 @@ struct GemmParams {
   int max_items;
   uint16_t* y;                // [rows_total][N]
   int N, K, G, rows_total;
-  uint32_t a_tx_bytes;        // transaction bytes of one weight-tile TMA load (packed size)
   uint32_t* status;
 };
 
-template <int BN_MAX, int STAGES>
+// Quads (4 sub-tiles = 512 K elements) of scale bytes the scale-factor warp keeps in
+// flight ahead of the stage it is staging.
+constexpr int kSfQuads = 4;
+
+// Weight stages prefetched into L2 ahead of the TMA loads into shared memory.
+constexpr int kL2PrefetchStages = 8;
+
+// Shared-memory layout of one pipeline configuration.  A stage holds KO sub-tiles of
+// 128 K elements: weights [KO][128 rows][128 B] (FP4 in its 16-byte-aligned form),
+// tokens [KO][BN_MAX rows][128 B] (FP8), KO weight scale atoms and one token scale
+// atom (512 B each).
+template <int BN_MAX, int STAGES, int KO>
 struct GemmCfg {
-  static constexpr int kABytes = 128 * 128;       // 128 rows x 128 FP4 (16B-aligned form)
-  static constexpr int kBBytes = BN_MAX * 128;    // BN_MAX rows x 128 FP8
-  static constexpr int kSfBytes = 512;            // one 128-row scale atom
+  static constexpr int kASub = 128 * 128;
+  static constexpr int kBSub = BN_MAX * 128;
+  static constexpr int kABytes = KO * kASub;
+  static constexpr int kBBytes = KO * kBSub;
+  static constexpr int kSfBytes = 512;
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + STAGES * kABytes;
   static constexpr int kOffSfa = kOffB + STAGES * kBBytes;
-  static constexpr int kOffSfb = kOffSfa + STAGES * kSfBytes;
+  static constexpr int kOffSfb = kOffSfa + STAGES * KO * kSfBytes;
   static constexpr int kOffBar = kOffSfb + STAGES * kSfBytes;
   static constexpr int kNumBars = 2 * STAGES + 4;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
-  static constexpr int kTmemNeed = 2 * BN_MAX + 8 * STAGES;
+  static constexpr int kSfCols = 4 * (KO + 1);              // TMEM columns per stage
+  static constexpr int kTmemNeed = 2 * BN_MAX + STAGES * kSfCols;
   static constexpr int kTmemCols =
       kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128 : kTmemNeed <= 256 ? 256 : 512;
   static_assert(BN_MAX % 16 == 0 && BN_MAX <= 128, "token tile");
+  static_assert(KO == 1 || BN_MAX == 16, "multi-sub-tile stages load 16-row token boxes");
+  static_assert(KO == 1 || KO == 2 || KO == 4, "sub-tiles per stage");
   static_assert(kTmemNeed <= 512, "TMEM");
 };
 
@@ -73,11 +88,15 @@ __device__ __forceinline__ uint32_t idesc_mxf4_e4m3(int n) {
   return d;
 }
 
-template <int BN_MAX, int STAGES>
-__global__ void __launch_bounds__(256, 1)
+__device__ __forceinline__ uint32_t u4_comp(const uint4& v, int t) {
+  return t == 0 ? v.x : t == 1 ? v.y : t == 2 ? v.z : v.w;
+}
+
+template <int BN_MAX, int STAGES, int KO, int OCC>
+__global__ void __launch_bounds__(256, OCC)
     k_gemm_mx(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
               const GemmParams p) {
-  using C = GemmCfg<BN_MAX, STAGES>;
+  using C = GemmCfg<BN_MAX, STAGES, KO>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -112,7 +131,7 @@ __global__ void __launch_bounds__(256, 1)
   const uint32_t tmem = *tmem_slot;
 
   const int n_tiles = p.N / 128;
-  const int nk = p.K / 128;
+  const int nk = p.K / (128 * KO);  // pipeline stages per tile
   int count = *p.item_count;
   if (count > p.max_items) {
     if (threadIdx.x == 0) set_status(p.status, STATUS_BAD_PLAN);
@@ -138,20 +157,56 @@ __global__ void __launch_bounds__(256, 1)
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
+      // Weight stages are also prefetched into L2 kL2PrefetchStages stages ahead of
+      // the shared-memory ring, so more HBM bytes are in flight than the ring holds.
+      struct SPos {
+        long long L;
+        int kb, g, nt;
+      };
+      auto seek = [&](long long L, SPos& P) -> bool {
+        int row0, rows;
+        for (; L < total; L += gridDim.x) {
+          if (load_item(L, P.g, row0, rows, P.nt)) {
+            P.L = L;
+            P.kb = 0;
+            return true;
+          }
+        }
+        return false;
+      };
+      auto adv = [&](SPos& P) -> bool {
+        if (++P.kb < nk) return true;
+        return seek(P.L + gridDim.x, P);
+      };
+      SPos pf{};
+      bool pf_ok = seek(blockIdx.x, pf);
+      for (int i = 0; i < kL2PrefetchStages && pf_ok; ++i) {
+        tma_prefetch_l2_4d(&tmW, 0, pf.nt * 128, pf.kb * KO, pf.g);
+        pf_ok = adv(pf);
+      }
       uint32_t it = 0;
       for (long long L = blockIdx.x; L < total && !*abort_flag; L += gridDim.x) {
         int g, row0, rows, nt;
         if (!load_item(L, g, row0, rows, nt)) continue;
         const int bn = (rows + 15) & ~15;
+        const uint32_t tx = KO * kWeightTileTxBytes + (KO == 1 ? bn : 16 * KO) * 128;
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1u;
           if (it >= STAGES && !mbar_wait(&empty[s], ph ^ 1u, p.status, abort_flag)) break;
-          mbar_arrive_expect_tx(&full[s], p.a_tx_bytes + bn * 128);
-          tma_load_3d(smem + C::kOffA + s * C::kABytes, &tmW, &full[s], kb * 128, nt * 128, g);
-          for (int i = 0; i < bn; i += 16)
-            tma_load_2d(smem + C::kOffB + s * C::kBBytes + i * 128, &tmX, &full[s], kb * 128,
-                        row0 + i);
+          mbar_arrive_expect_tx(&full[s], tx);
+          tma_load_4d(smem + C::kOffA + s * C::kABytes, &tmW, &full[s], 0, nt * 128, kb * KO, g);
+          if (KO == 1) {
+            for (int i = 0; i < bn; i += 16)
+              tma_load_3d(smem + C::kOffB + s * C::kBBytes + i * 128, &tmX, &full[s], 0,
+                          row0 + i, kb);
+          } else {
+            tma_load_3d(smem + C::kOffB + s * C::kBBytes, &tmX, &full[s], 0, row0, kb * KO);
+          }
+          if (pf_ok) {
+            tma_prefetch_l2_4d(&tmW, 0, pf.nt * 128, pf.kb * KO, pf.g);
+            pf_ok = adv(pf);
+          }
         }
       }
     }
@@ -177,21 +232,28 @@ __global__ void __launch_bounds__(256, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t sfa_t = tmem + 2 * BN_MAX + s * 8;
-          const uint32_t sfb_t = sfa_t + 4;
-          tc_cp_32x128b_x4(sfa_t, smem_desc(smem_u32(smem + C::kOffSfa + s * C::kSfBytes), 0,
-                                            128, kLayoutNone));
+          const uint32_t sf_t = tmem + 2 * BN_MAX + s * C::kSfCols;
+          const uint32_t sfb_t = sf_t + 4 * KO;
+#pragma unroll
+          for (int ko = 0; ko < KO; ++ko)
+            tc_cp_32x128b_x4(sf_t + 4 * ko,
+                             smem_desc(smem_u32(smem + C::kOffSfa + (s * KO + ko) * C::kSfBytes),
+                                       0, 128, kLayoutNone));
           tc_cp_32x128b_x4(sfb_t, smem_desc(smem_u32(smem + C::kOffSfb + s * C::kSfBytes), 0,
                                             128, kLayoutNone));
           const uint32_t a0 = smem_u32(smem + C::kOffA + s * C::kABytes);
           const uint32_t b0 = smem_u32(smem + C::kOffB + s * C::kBBytes);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = smem_desc(a0 + kk * 32, 0, 1024, kLayoutSw128);
-            const uint64_t bd = smem_desc(b0 + kk * 32, 0, 1024, kLayoutSw128);
-            const uint32_t id = idesc | (static_cast<uint32_t>(kk) << 29) |
-                                (static_cast<uint32_t>(kk) << 4);
-            mma_mxf8f6f4(d_tmem, ad, bd, id, sfa_t, sfb_t, (kb | kk) != 0);
+          for (int ko = 0; ko < KO; ++ko) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = smem_desc(a0 + ko * C::kASub + kk * 32, 0, 1024, kLayoutSw128);
+              const uint64_t bd = smem_desc(b0 + ko * C::kBSub + kk * 32, 0, 1024, kLayoutSw128);
+              // A scale: byte kk (32-K block) of the sub-tile's atom; B scale: byte ko.
+              const uint32_t id = idesc | (static_cast<uint32_t>(kk) << 29) |
+                                  (static_cast<uint32_t>(ko) << 4);
+              mma_mxf8f6f4(d_tmem, ad, bd, id, sf_t + 4 * ko, sfb_t, (kb | ko | kk) != 0);
+            }
           }
           tc_commit(&empty[s]);
         }
@@ -202,42 +264,143 @@ __global__ void __launch_bounds__(256, 1)
     }
   } else if (warp == 2) {
     // ---------------------------------------------------------------- scale factors
-    uint32_t it = 0;
+    // Per stage: KO weight atoms (row r at byte (r % 32) * 16 + (r / 32) * 4 + kblock)
+    // and one token atom whose byte ko holds the token's scale for sub-tile ko.
     const int kw = p.K / 32, kx = p.K / 128;
-    for (long long L = blockIdx.x; L < total && !*abort_flag; L += gridDim.x) {
-      int g, row0, rows, nt;
-      if (!load_item(L, g, row0, rows, nt)) continue;
-      const uint8_t* ws = p.w_scales + (static_cast<size_t>(g) * p.N + nt * 128) * kw;
+    auto put_stage = [&](int s, const uint32_t (&wa)[KO][4], const uint32_t (&xb)[4]) {
+#pragma unroll
+      for (int ko = 0; ko < KO; ++ko)
+        *reinterpret_cast<uint4*>(smem + C::kOffSfa + (s * KO + ko) * C::kSfBytes + lane * 16) =
+            make_uint4(wa[ko][0], wa[ko][1], wa[ko][2], wa[ko][3]);
+      *reinterpret_cast<uint4*>(smem + C::kOffSfb + s * C::kSfBytes + lane * 16) =
+          make_uint4(xb[0], xb[1], xb[2], xb[3]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&full[s]);
+    };
+    auto wait_slot = [&](uint32_t it) -> bool {
+      if (it < STAGES) return true;
+      int w_ok = 1;
+      if (lane == 0)
+        w_ok = mbar_wait(&empty[it % STAGES], ((it / STAGES) & 1u) ^ 1u, p.status, abort_flag);
+      return __shfl_sync(0xFFFFFFFFu, w_ok, 0) != 0;
+    };
+    if ((p.K & 511) == 0) {
+      // Pipelined path.  Scale bytes are fetched a quad (4 sub-tiles) at a time -- one
+      // 16-byte load per weight row, one 4-byte load per token -- kSfQuads quads ahead
+      // of the stage being staged, so their latency overlaps the MMAs.
+      constexpr int Q = kSfQuads;
+      constexpr int J = (BN_MAX + 31) / 32;
+      constexpr int SPQ = 4 / KO;  // stages per quad
+      const int nq = p.K / 512;
+      struct Pos {
+        long long L;
+        int kq, g, row0, rows, nt;
+      };
+      auto seek = [&](long long L, Pos& P) -> bool {
+        for (; L < total; L += gridDim.x) {
+          if (load_item(L, P.g, P.row0, P.rows, P.nt)) {
+            P.L = L;
+            P.kq = 0;
+            return true;
+          }
+        }
+        return false;
+      };
+      auto step = [&](Pos& P) -> bool {
+        if (++P.kq < nq) return true;
+        return seek(P.L + gridDim.x, P);
+      };
+      uint4 wv[Q][4];
+      uint32_t av[Q][J];
+      Pos ld{}, cs{};
+      bool ld_ok = seek(blockIdx.x, ld);
+      bool cs_ok = seek(blockIdx.x, cs);
+      auto fetch = [&](uint4 (&w4)[4], uint32_t (&a)[J]) {
+        const uint8_t* wsp =
+            p.w_scales + (static_cast<size_t>(ld.g) * p.N + ld.nt * 128) * kw + ld.kq * 16;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          w4[j] = __ldg(reinterpret_cast<const uint4*>(wsp + static_cast<size_t>(j * 32 + lane) * kw));
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+          const int r = j * 32 + lane;
+          a[j] = r < ld.rows ? __ldg(reinterpret_cast<const uint32_t*>(
+                                   p.x_scales + static_cast<size_t>(ld.row0 + r) * kx + ld.kq * 4))
+                             : 0x7F7F7F7Fu;
+        }
+        ld_ok = step(ld);
+      };
+#pragma unroll
+      for (int i = 0; i < Q; ++i)
+        if (ld_ok) fetch(wv[i], av[i]);
+      uint32_t it = 0;
       bool ok = true;
-      for (int kb = 0; kb < nk; ++kb, ++it) {
-        const int s = it % STAGES;
-        const uint32_t ph = (it / STAGES) & 1u;
-        if (it >= STAGES) {
-          int w_ok = 1;
-          if (lane == 0) w_ok = mbar_wait(&empty[s], ph ^ 1u, p.status, abort_flag);
-          if (!__shfl_sync(0xFFFFFFFFu, w_ok, 0)) {
+      while (cs_ok && ok) {
+#pragma unroll
+        for (int i = 0; i < Q; ++i) {
+          if (!cs_ok || !ok) break;
+#pragma unroll
+          for (int b = 0; b < SPQ; ++b) {
+            if (!wait_slot(it)) {
+              ok = false;
+              break;
+            }
+            uint32_t wa[KO][4], xb[4];
+#pragma unroll
+            for (int ko = 0; ko < KO; ++ko)
+#pragma unroll
+              for (int j = 0; j < 4; ++j) wa[ko][j] = u4_comp(wv[i][j], b * KO + ko);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              if (j < J) {
+                const uint32_t a = av[i][j < J ? j : 0] >> (8 * b * KO);
+                xb[j] = KO == 4 ? a : (KO == 2 ? (a & 0xFFFFu) : (a & 0xFFu));
+              } else {
+                xb[j] = 0x7F7F7F7Fu;
+              }
+            }
+            put_stage(it % STAGES, wa, xb);
+            ++it;
+          }
+          if (!ok) break;
+          cs_ok = step(cs);
+          if (ld_ok) fetch(wv[i], av[i]);  // refill slot i with the quad Q ahead
+        }
+      }
+    } else {
+      // General path (K not a multiple of 512): one stage at a time.
+      uint32_t it = 0;
+      for (long long L = blockIdx.x; L < total && !*abort_flag; L += gridDim.x) {
+        int g, row0, rows, nt;
+        if (!load_item(L, g, row0, rows, nt)) continue;
+        const uint8_t* wsp = p.w_scales + (static_cast<size_t>(g) * p.N + nt * 128) * kw;
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          if (!wait_slot(it)) {
             ok = false;
             break;
           }
-        }
-        uint32_t va[4], vb[4];
+          uint32_t wa[KO][4], xb[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int r = j * 32 + lane;
-          va[j] = __ldg(reinterpret_cast<const uint32_t*>(ws + static_cast<size_t>(r) * kw + kb * 4));
-          uint32_t sb = 127u;
-          if (r < rows) sb = __ldg(p.x_scales + static_cast<size_t>(row0 + r) * kx + kb);
-          vb[j] = sb * 0x01010101u;
+          for (int j = 0; j < 4; ++j) {
+            const int r = j * 32 + lane;
+            uint32_t packed = 0;
+#pragma unroll
+            for (int ko = 0; ko < KO; ++ko) {
+              const int sub = kb * KO + ko;
+              wa[ko][j] = __ldg(reinterpret_cast<const uint32_t*>(
+                  wsp + static_cast<size_t>(r) * kw + sub * 4));
+              uint32_t sb = 127u;
+              if (r < rows) sb = __ldg(p.x_scales + static_cast<size_t>(row0 + r) * kx + sub);
+              packed |= sb << (8 * ko);
+            }
+            xb[j] = packed;
+          }
+          put_stage(it % STAGES, wa, xb);
         }
-        *reinterpret_cast<uint4*>(smem + C::kOffSfa + s * C::kSfBytes + lane * 16) =
-            make_uint4(va[0], va[1], va[2], va[3]);
-        *reinterpret_cast<uint4*>(smem + C::kOffSfb + s * C::kSfBytes + lane * 16) =
-            make_uint4(vb[0], vb[1], vb[2], vb[3]);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&full[s]);
+        if (!ok) break;
       }
-      if (!ok) break;
     }
   } else if (warp >= 4) {
     // ---------------------------------------------------------------- epilogue
@@ -316,55 +479,58 @@ DevInfo& dev_info() {
   return info[dev];
 }
 
-template <int BN_MAX, int STAGES>
+template <int BN_MAX, int STAGES, int KO, int OCC>
 cudaError_t launch_one(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmParams& p,
                        int max_items, cudaStream_t st) {
-  using C = GemmCfg<BN_MAX, STAGES>;
+  using C = GemmCfg<BN_MAX, STAGES, KO>;
+  auto kern = k_gemm_mx<BN_MAX, STAGES, KO, OCC>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (!attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_mx<BN_MAX, STAGES>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   const long long tiles = static_cast<long long>(max_items) * (p.N / 128);
   if (tiles == 0) return cudaSuccess;
-  const int sms = dev_info().sms;
-  const int grid = static_cast<int>(tiles < sms ? tiles : sms);
+  const int slots = dev_info().sms * OCC;
+  const int grid = static_cast<int>(tiles < slots ? tiles : slots);
   GemmParams q = p;
   q.max_items = max_items;
-  k_gemm_mx<BN_MAX, STAGES><<<grid, 256, C::kSmemBytes, st>>>(tmW, tmX, q);
+  kern<<<grid, 256, C::kSmemBytes, st>>>(tmW, tmX, q);
   return cudaGetLastError();
 }
 
 }  // namespace
 
+// Tensor maps for one launch: weights as a 4D view {128 K elements, N rows, K/128
+// sub-tiles, G} (box {128, 128, ko, 1}, FP4 unpacked to the 16-byte-aligned form),
+// packed activation rows as a 3D view {128 bytes, rows, K/128} (box {128, 16, ko}).
 int gemm_encode_maps(const uint8_t* w_codes, int G, int N, int K, const uint8_t* act,
-                     int rows_total, CUtensorMap* tmW, CUtensorMap* tmX) {
+                     int rows_total, int ko, CUtensorMap* tmW, CUtensorMap* tmX) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return MOE_ERR_CUDA;
   {
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N),
+    cuuint64_t dims[4] = {128, static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(K / 128),
                           static_cast<cuuint64_t>(G)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(K / 2),
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(K / 2), 64,
                              static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(K / 2)};
-    cuuint32_t box[3] = {128, 128, 1};
-    cuuint32_t es[3] = {1, 1, 1};
-    if (enc(tmW, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<uint8_t*>(w_codes), dims,
+    cuuint32_t box[4] = {128, 128, static_cast<cuuint32_t>(ko), 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    if (enc(tmW, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 4, const_cast<uint8_t*>(w_codes), dims,
             strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return MOE_ERR_CUDA;
   }
   {
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K),
-                          static_cast<cuuint64_t>(rows_total > 0 ? rows_total : 1)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
-    cuuint32_t box[2] = {128, 16};
-    cuuint32_t es[2] = {1, 1};
-    if (enc(tmX, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(act), dims, strides, box,
+    cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(rows_total > 0 ? rows_total : 1),
+                          static_cast<cuuint64_t>(K / 128)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(K), 128};
+    cuuint32_t box[3] = {128, 16, static_cast<cuuint32_t>(ko)};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (enc(tmX, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(act), dims, strides, box,
             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return MOE_ERR_CUDA;
@@ -372,11 +538,7 @@ int gemm_encode_maps(const uint8_t* w_codes, int G, int N, int K, const uint8_t*
   return MOE_OK;
 }
 
-
 cudaError_t launch_grouped_gemm(const GemmLaunch& a, cudaStream_t st) {
-  CUtensorMap tmW, tmX;
-  int rc = gemm_encode_maps(a.w_codes, a.G, a.N, a.K, a.act, a.rows_total, &tmW, &tmX);
-  if (rc != MOE_OK) return cudaErrorInvalidValue;
   GemmParams p{};
   p.w_scales = a.w_scales;
   p.x_scales = a.act_scales;
@@ -385,16 +547,25 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& a, cudaStream_t st) {
   p.K = a.K;
   p.G = a.G;
   p.rows_total = a.rows_total;
-  p.a_tx_bytes = kWeightTileTxBytes;
   p.status = a.status;
+  CUtensorMap tmW, tmX;
   // small-M list
+  const bool multi = (a.K / 128) % kSmallKO == 0;
+  if (gemm_encode_maps(a.w_codes, a.G, a.N, a.K, a.act, a.rows_total, multi ? kSmallKO : 1,
+                       &tmW, &tmX) != MOE_OK)
+    return cudaErrorInvalidValue;
   p.items = a.small_items;
   p.item_count = a.item_counts;
-  cudaError_t e = launch_one<kSmallBN, kSmallStages>(tmW, tmX, p, a.max_small, st);
+  cudaError_t e =
+      multi ? launch_one<kSmallBN, kSmallStages, kSmallKO, kSmallOcc>(tmW, tmX, p, a.max_small, st)
+            : launch_one<kSmallBN, 2 * kSmallStages, 1, kSmallOcc>(tmW, tmX, p, a.max_small, st);
   if (e != cudaSuccess) return e;
+  // large-M list
+  if (gemm_encode_maps(a.w_codes, a.G, a.N, a.K, a.act, a.rows_total, 1, &tmW, &tmX) != MOE_OK)
+    return cudaErrorInvalidValue;
   p.items = a.large_items;
   p.item_count = a.item_counts + 1;
-  return launch_one<kLargeBN, kLargeStages>(tmW, tmX, p, a.max_large, st);
+  return launch_one<kLargeBN, kLargeStages, 1, 1>(tmW, tmX, p, a.max_large, st);
 }
 
 }  // namespace moe

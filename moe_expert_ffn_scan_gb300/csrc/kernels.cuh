@@ -5,11 +5,14 @@
 
 namespace moe {
 
-// Token-tile limits of the two GEMM variants: groups with M <= kSmallBN rows run in
-// the small-M kernel (deep pipeline, N padded to a multiple of 16 only); larger
-// groups are split into chunks of <= kLargeBN rows.
-constexpr int kSmallBN = 32;
-constexpr int kSmallStages = 8;
+// GEMM variants.  Groups with M <= kSmallBN rows run in the small-M kernel: N = 16
+// tokens, two 128-K sub-tiles per pipeline stage (one 4D TMA load each for weights
+// and tokens) and two CTAs per SM, so twice the TMA / MMA issue rate per SM.  Larger
+// groups are split into chunks of <= kLargeBN rows for the large-M kernel.
+constexpr int kSmallBN = 16;
+constexpr int kSmallStages = 2;
+constexpr int kSmallKO = 2;
+constexpr int kSmallOcc = 2;
 constexpr int kLargeBN = 128;
 constexpr int kLargeStages = 6;
 
