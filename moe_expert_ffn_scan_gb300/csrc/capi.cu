@@ -62,17 +62,20 @@ RouteWs carve_route(Carver& c, const moe_dims* d) {
 
 struct PlanWs {
   int4* small_items;
+  int4* medium_items;
   int4* large_items;
   int32_t* counts;
-  int max_small, max_large;
+  int max_small, max_medium, max_large;
 };
 
 PlanWs carve_plan(Carver& c, const moe_dims* d) {
   PlanWs p;
   const int G = groups_G(d);
   p.max_small = G;
+  p.max_medium = G;
   p.max_large = static_cast<int>(rows_Rs(d) / kLargeBN + G + 1);
   p.small_items = c.take<int4>(p.max_small);
+  p.medium_items = c.take<int4>(p.max_medium);
   p.large_items = c.take<int4>(p.max_large);
   p.counts = c.take<int32_t>(4);
   return p;
@@ -127,7 +130,7 @@ ForwardWs carve_forward(Carver& c, const moe_dims* d) {
 
 int run_gemm(const moe_dims* d, const uint8_t* act, const uint8_t* act_s, const int32_t* offsets,
              const uint8_t* w, const uint8_t* w_s, int N, int K, uint16_t* y, const PlanWs& plan,
-             uint32_t* status, cudaStream_t st) {
+             int max_group_rows, uint32_t* status, cudaStream_t st) {
   GemmLaunch a{};
   a.w_codes = w;
   a.w_scales = w_s;
@@ -139,10 +142,13 @@ int run_gemm(const moe_dims* d, const uint8_t* act, const uint8_t* act_s, const 
   a.K = K;
   a.rows_total = static_cast<int>(rows_Rs(d));
   a.small_items = plan.small_items;
+  a.medium_items = plan.medium_items;
   a.large_items = plan.large_items;
   a.item_counts = plan.counts;
   a.max_small = plan.max_small;
+  a.max_medium = plan.max_medium;
   a.max_large = plan.max_large;
+  a.max_group_rows = max_group_rows;
   a.status = status;
   return cuda_rc(launch_grouped_gemm(a, st));
 }
@@ -229,8 +235,9 @@ int moe_grouped_gemm_w13(const moe_dims* d, const uint8_t* xq, const uint8_t* xs
   Carver c(ws);
   GemmWs g = carve_gemm(c, d);
   if (cudaMemsetAsync(g.status, 0, sizeof(uint32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
-  cudaError_t e = launch_plan(group_offsets, groups_G(d), kSmallBN, kLargeBN,
-                              g.plan.small_items, g.plan.large_items, g.plan.counts, g.status, st);
+  cudaError_t e = launch_plan(group_offsets, groups_G(d), g.plan.small_items,
+                              g.plan.medium_items, g.plan.large_items, g.plan.counts, g.status,
+                              st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   const uint8_t* act = xq;
   const uint8_t* act_s = xs;
@@ -242,7 +249,7 @@ int moe_grouped_gemm_w13(const moe_dims* d, const uint8_t* xq, const uint8_t* xs
     act_s = g.xsg;
   }
   return run_gemm(d, act, act_s, group_offsets, w13, w13_s, 2 * d->I, d->H, y13, g.plan,
-                  g.status, st);
+                  static_cast<int>(rows_Rs(d)), g.status, st);
 }
 
 int moe_swiglu_quant(int32_t rows, int32_t I, const uint16_t* y13, uint8_t* hq, uint8_t* hs,
@@ -266,10 +273,12 @@ int moe_grouped_gemm_w2(const moe_dims* d, const uint8_t* hq, const uint8_t* hs,
   Carver c(ws);
   GemmWs g = carve_gemm(c, d);
   if (cudaMemsetAsync(g.status, 0, sizeof(uint32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
-  cudaError_t e = launch_plan(group_offsets, groups_G(d), kSmallBN, kLargeBN,
-                              g.plan.small_items, g.plan.large_items, g.plan.counts, g.status, st);
+  cudaError_t e = launch_plan(group_offsets, groups_G(d), g.plan.small_items,
+                              g.plan.medium_items, g.plan.large_items, g.plan.counts, g.status,
+                              st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  return run_gemm(d, hq, hs, group_offsets, w2, w2_s, d->H, d->I, y2, g.plan, g.status, st);
+  return run_gemm(d, hq, hs, group_offsets, w2, w2_s, d->H, d->I, y2, g.plan,
+                  static_cast<int>(rows_Rs(d)), g.status, st);
 }
 
 int moe_combine(const moe_dims* d, const uint16_t* y2, const int32_t* inv, const float* w,
@@ -330,18 +339,21 @@ int moe_forward_timed(const moe_dims* d, const uint16_t* x, const float* logits,
   MOE_MARK(1)
   MOE_TRY(launch_quant_act(x, T, H, f.xq, f.xs, st))
   MOE_MARK(2)
-  MOE_TRY(launch_plan(f.offsets, groups_G(d), kSmallBN, kLargeBN, f.gemm.plan.small_items,
-                      f.gemm.plan.large_items, f.gemm.plan.counts, status, st))
+  MOE_TRY(launch_plan(f.offsets, groups_G(d), f.gemm.plan.small_items,
+                      f.gemm.plan.medium_items, f.gemm.plan.large_items, f.gemm.plan.counts,
+                      status, st))
   MOE_TRY(launch_gather_rows(f.xq, f.xs, f.perm_src, T, k, R, Rs, H, f.gemm.xg, f.gemm.xsg,
                              status, st))
   MOE_MARK(3)
+  // every group (a routed expert or the shared expert) holds at most T rows
   int rc = run_gemm(d, f.gemm.xg, f.gemm.xsg, f.offsets, W->w13, W->w13_s, 2 * I, H, f.y13,
-                    f.gemm.plan, status, st);
+                    f.gemm.plan, T, status, st);
   if (rc != MOE_OK) return rc;
   MOE_MARK(4)
   MOE_TRY(launch_swiglu_quant(f.y13, Rs, I, f.hq, f.hs, st))
   MOE_MARK(5)
-  rc = run_gemm(d, f.hq, f.hs, f.offsets, W->w2, W->w2_s, H, I, f.y2, f.gemm.plan, status, st);
+  rc = run_gemm(d, f.hq, f.hs, f.offsets, W->w2, W->w2_s, H, I, f.y2, f.gemm.plan, T, status,
+                st);
   if (rc != MOE_OK) return rc;
   MOE_MARK(6)
   MOE_TRY(launch_combine(f.y2, f.inv, f.w, T, k, H, d->has_shared, out, status, st))

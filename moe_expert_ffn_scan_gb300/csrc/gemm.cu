@@ -44,13 +44,12 @@ struct GemmParams {
 // flight ahead of the stage it is staging.
 constexpr int kSfQuads = 4;
 
-// Weight stages prefetched into L2 ahead of the TMA loads into shared memory.
-constexpr int kL2PrefetchStages = 8;
-
 // Shared-memory layout of one pipeline configuration.  A stage holds KO sub-tiles of
 // 128 K elements: weights [KO][128 rows][128 B] (FP4 in its 16-byte-aligned form),
 // tokens [KO][BN_MAX rows][128 B] (FP8), KO weight scale atoms and one token scale
-// atom (512 B each).
+// atom (512 B each).  With KO > 1 each stage is one weight TMA (box 128 x 128 x KO)
+// and one token TMA (box 128 x BN_MAX x KO); with KO == 1 the tokens come in boxes of
+// 16 rows, as many as the group needs.
 template <int BN_MAX, int STAGES, int KO>
 struct GemmCfg {
   static constexpr int kASub = 128 * 128;
@@ -65,13 +64,12 @@ struct GemmCfg {
   static constexpr int kOffBar = kOffSfb + STAGES * kSfBytes;
   static constexpr int kNumBars = 2 * STAGES + 4;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
+  static constexpr int kSmemBytes = kOffMisc + 16;
   static constexpr int kSfCols = 4 * (KO + 1);              // TMEM columns per stage
   static constexpr int kTmemNeed = 2 * BN_MAX + STAGES * kSfCols;
   static constexpr int kTmemCols =
       kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128 : kTmemNeed <= 256 ? 256 : 512;
   static_assert(BN_MAX % 16 == 0 && BN_MAX <= 128, "token tile");
-  static_assert(KO == 1 || BN_MAX == 16, "multi-sub-tile stages load 16-row token boxes");
   static_assert(KO == 1 || KO == 2 || KO == 4, "sub-tiles per stage");
   static_assert(kTmemNeed <= 512, "TMEM");
 };
@@ -97,9 +95,14 @@ __global__ void __launch_bounds__(256, OCC)
     k_gemm_mx(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
               const GemmParams p) {
   using C = GemmCfg<BN_MAX, STAGES, KO>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  // The 128B-swizzled tiles need 1024-byte alignment; the dynamic shared memory of a
+  // kernel without static shared memory starts at such a boundary.  Checked, not
+  // assumed: a misaligned base reports STATUS_BAD_PLAN and the CTA returns.
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (threadIdx.x == 0) set_status(p.status, STATUS_BAD_PLAN);
+    return;
+  }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* full = bars;
   uint64_t* empty = bars + STAGES;
@@ -157,39 +160,12 @@ __global__ void __launch_bounds__(256, OCC)
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
-      // Weight stages are also prefetched into L2 kL2PrefetchStages stages ahead of
-      // the shared-memory ring, so more HBM bytes are in flight than the ring holds.
-      struct SPos {
-        long long L;
-        int kb, g, nt;
-      };
-      auto seek = [&](long long L, SPos& P) -> bool {
-        int row0, rows;
-        for (; L < total; L += gridDim.x) {
-          if (load_item(L, P.g, row0, rows, P.nt)) {
-            P.L = L;
-            P.kb = 0;
-            return true;
-          }
-        }
-        return false;
-      };
-      auto adv = [&](SPos& P) -> bool {
-        if (++P.kb < nk) return true;
-        return seek(P.L + gridDim.x, P);
-      };
-      SPos pf{};
-      bool pf_ok = seek(blockIdx.x, pf);
-      for (int i = 0; i < kL2PrefetchStages && pf_ok; ++i) {
-        tma_prefetch_l2_4d(&tmW, 0, pf.nt * 128, pf.kb * KO, pf.g);
-        pf_ok = adv(pf);
-      }
       uint32_t it = 0;
       for (long long L = blockIdx.x; L < total && !*abort_flag; L += gridDim.x) {
         int g, row0, rows, nt;
         if (!load_item(L, g, row0, rows, nt)) continue;
         const int bn = (rows + 15) & ~15;
-        const uint32_t tx = KO * kWeightTileTxBytes + (KO == 1 ? bn : 16 * KO) * 128;
+        const uint32_t tx = KO * kWeightTileTxBytes + (KO == 1 ? bn : BN_MAX * KO) * 128;
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1u;
@@ -202,10 +178,6 @@ __global__ void __launch_bounds__(256, OCC)
                           row0 + i, kb);
           } else {
             tma_load_3d(smem + C::kOffB + s * C::kBBytes, &tmX, &full[s], 0, row0, kb * KO);
-          }
-          if (pf_ok) {
-            tma_prefetch_l2_4d(&tmW, 0, pf.nt * 128, pf.kb * KO, pf.g);
-            pf_ok = adv(pf);
           }
         }
       }
@@ -507,9 +479,9 @@ cudaError_t launch_one(const CUtensorMap& tmW, const CUtensorMap& tmX, const Gem
 
 // Tensor maps for one launch: weights as a 4D view {128 K elements, N rows, K/128
 // sub-tiles, G} (box {128, 128, ko, 1}, FP4 unpacked to the 16-byte-aligned form),
-// packed activation rows as a 3D view {128 bytes, rows, K/128} (box {128, 16, ko}).
+// packed activation rows as a 3D view {128 bytes, rows, K/128} (box {128, xr, ko}).
 int gemm_encode_maps(const uint8_t* w_codes, int G, int N, int K, const uint8_t* act,
-                     int rows_total, int ko, CUtensorMap* tmW, CUtensorMap* tmX) {
+                     int rows_total, int ko, int xr, CUtensorMap* tmW, CUtensorMap* tmX) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return MOE_ERR_CUDA;
   {
@@ -528,7 +500,7 @@ int gemm_encode_maps(const uint8_t* w_codes, int G, int N, int K, const uint8_t*
     cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(rows_total > 0 ? rows_total : 1),
                           static_cast<cuuint64_t>(K / 128)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(K), 128};
-    cuuint32_t box[3] = {128, 16, static_cast<cuuint32_t>(ko)};
+    cuuint32_t box[3] = {128, static_cast<cuuint32_t>(xr), static_cast<cuuint32_t>(ko)};
     cuuint32_t es[3] = {1, 1, 1};
     if (enc(tmX, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(act), dims, strides, box,
             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -537,6 +509,25 @@ int gemm_encode_maps(const uint8_t* w_codes, int G, int N, int K, const uint8_t*
   }
   return MOE_OK;
 }
+
+namespace {
+
+// One variant: KO = 2 sub-tiles per stage when K allows it, else the KO = 1 layout.
+template <int BN, int ST2, int ST1, int OCC>
+cudaError_t launch_variant(const GemmLaunch& a, GemmParams p, const int4* items,
+                           const int32_t* count, int max_items, cudaStream_t st) {
+  const bool two = (a.K / 128) % 2 == 0;
+  CUtensorMap tmW, tmX;
+  if (gemm_encode_maps(a.w_codes, a.G, a.N, a.K, a.act, a.rows_total, two ? 2 : 1,
+                       two ? BN : 16, &tmW, &tmX) != MOE_OK)
+    return cudaErrorInvalidValue;
+  p.items = items;
+  p.item_count = count;
+  return two ? launch_one<BN, ST2, 2, OCC>(tmW, tmX, p, max_items, st)
+             : launch_one<BN, ST1, 1, OCC>(tmW, tmX, p, max_items, st);
+}
+
+}  // namespace
 
 cudaError_t launch_grouped_gemm(const GemmLaunch& a, cudaStream_t st) {
   GemmParams p{};
@@ -548,24 +539,16 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& a, cudaStream_t st) {
   p.G = a.G;
   p.rows_total = a.rows_total;
   p.status = a.status;
-  CUtensorMap tmW, tmX;
-  // small-M list
-  const bool multi = (a.K / 128) % kSmallKO == 0;
-  if (gemm_encode_maps(a.w_codes, a.G, a.N, a.K, a.act, a.rows_total, multi ? kSmallKO : 1,
-                       &tmW, &tmX) != MOE_OK)
-    return cudaErrorInvalidValue;
-  p.items = a.small_items;
-  p.item_count = a.item_counts;
-  cudaError_t e =
-      multi ? launch_one<kSmallBN, kSmallStages, kSmallKO, kSmallOcc>(tmW, tmX, p, a.max_small, st)
-            : launch_one<kSmallBN, 2 * kSmallStages, 1, kSmallOcc>(tmW, tmX, p, a.max_small, st);
-  if (e != cudaSuccess) return e;
-  // large-M list
-  if (gemm_encode_maps(a.w_codes, a.G, a.N, a.K, a.act, a.rows_total, 1, &tmW, &tmX) != MOE_OK)
-    return cudaErrorInvalidValue;
-  p.items = a.large_items;
-  p.item_count = a.item_counts + 1;
-  return launch_one<kLargeBN, kLargeStages, 1, 1>(tmW, tmX, p, a.max_large, st);
+  // A list whose groups cannot exist (no group has more than max_group_rows rows) is
+  // provably empty and not launched.
+  cudaError_t e = launch_variant<kSmallBN, kSmallStages, kSmallStagesKO1, kSmallOcc>(
+      a, p, a.small_items, a.item_counts, a.max_small, st);
+  if (e != cudaSuccess || a.max_group_rows <= kSmallBN) return e;
+  e = launch_variant<kMediumBN, kMediumStages, kMediumStagesKO1, kMediumOcc>(
+      a, p, a.medium_items, a.item_counts + 1, a.max_medium, st);
+  if (e != cudaSuccess || a.max_group_rows <= kMediumBN) return e;
+  return launch_variant<kLargeBN, kLargeStages, kLargeStagesKO1, 1>(
+      a, p, a.large_items, a.item_counts + 2, a.max_large, st);
 }
 
 }  // namespace moe

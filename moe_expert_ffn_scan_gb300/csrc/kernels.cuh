@@ -5,16 +5,22 @@
 
 namespace moe {
 
-// GEMM variants.  Groups with M <= kSmallBN rows run in the small-M kernel: N = 16
-// tokens, two 128-K sub-tiles per pipeline stage (one 4D TMA load each for weights
-// and tokens) and two CTAs per SM, so twice the TMA / MMA issue rate per SM.  Larger
-// groups are split into chunks of <= kLargeBN rows for the large-M kernel.
+// GEMM variants, chosen per group by its row count M (the tile plan):
+//   small  M <= 16: N = 16 tokens, 2 CTAs per SM, 3 stages of two 128-K sub-tiles;
+//   medium M <= 64: N <= 64, 2 CTAs per SM, 2 stages;
+//   large  M > 64: chunks of <= 128 rows, 1 CTA per SM, 3 stages.
+// With K/128 odd the stages hold one sub-tile (the *KO1 stage counts).
 constexpr int kSmallBN = 16;
-constexpr int kSmallStages = 2;
-constexpr int kSmallKO = 2;
+constexpr int kSmallStages = 3;
+constexpr int kSmallStagesKO1 = 5;
 constexpr int kSmallOcc = 2;
+constexpr int kMediumBN = 64;
+constexpr int kMediumStages = 2;
+constexpr int kMediumStagesKO1 = 4;
+constexpr int kMediumOcc = 2;
 constexpr int kLargeBN = 128;
-constexpr int kLargeStages = 6;
+constexpr int kLargeStages = 3;
+constexpr int kLargeStagesKO1 = 6;
 
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* idx, float* w,
                          cudaStream_t st);
@@ -23,9 +29,9 @@ cudaError_t launch_permute(const int32_t* idx, int T, int E, int k, int has_shar
                            int32_t* blockcnt, int32_t* blockbase, int32_t* counts,
                            int32_t* offsets, int32_t* perm_src, int32_t* inv, uint32_t* status,
                            cudaStream_t st);
-cudaError_t launch_plan(const int32_t* offsets, int G, int small_bn, int large_bn,
-                        int4* small_items, int4* large_items, int32_t* item_counts,
-                        uint32_t* status, cudaStream_t st);
+cudaError_t launch_plan(const int32_t* offsets, int G, int4* small_items, int4* medium_items,
+                        int4* large_items, int32_t* item_counts, uint32_t* status,
+                        cudaStream_t st);
 
 cudaError_t launch_quant_act(const uint16_t* x, int rows, int cols, uint8_t* q, uint8_t* s,
                              cudaStream_t st);
@@ -46,9 +52,11 @@ struct GemmLaunch {
   uint16_t* y;                // [rows_total][N]
   int G, N, K, rows_total;
   const int4* small_items;
+  const int4* medium_items;
   const int4* large_items;
-  const int32_t* item_counts;  // [2]: small, large
-  int max_small, max_large;
+  const int32_t* item_counts;  // [3]: small, medium, large
+  int max_small, max_medium, max_large;
+  int max_group_rows;          // upper bound on any group's row count
   uint32_t* status;
 };
 cudaError_t launch_grouped_gemm(const GemmLaunch& a, cudaStream_t st);

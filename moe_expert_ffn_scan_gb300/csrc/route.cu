@@ -205,81 +205,83 @@ __global__ void __launch_bounds__(kPermTokens) k_permute_block(
 
 // ---------------------------------------------------------------- a8: tile plan ---
 //
-// Per group g with M = offsets[g+1] - offsets[g] rows: groups with M <= small_bn go
-// to the small-M list as one item (the GEMM pads M only to the next multiple of 16,
-// never to a large tile); larger groups are split into ceil(M / large_bn) chunks of
-// near-equal size for the large-M list.  Items are {group, row0, rows, 0}.
-// One CTA of 1024 threads; each thread owns a contiguous run of groups.
+// Per group g with M = offsets[g+1] - offsets[g] rows (the effective M the pages tune
+// for): M <= kSmallBN -> one small-M item (padded only to 16 tokens, never to a large
+// tile); M <= kMediumBN -> one medium item; larger groups are split into
+// ceil(M / kLargeBN) near-equal chunks (multiples of 16 rows except the last) for the
+// large-M kernel.  Items are {group, row0, rows, 0}.  One CTA of 1024 threads; each
+// thread owns a contiguous run of groups; positions come from block-wide scans, so
+// the lists are in group order and deterministic.
+__device__ __forceinline__ int32_t block_exclusive_scan(int32_t v, int32_t* s_warp,
+                                                        int32_t* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int32_t x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    int32_t y = __shfl_up_sync(0xFFFFFFFFu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) s_warp[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    int32_t y = s_warp[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      int32_t z = __shfl_up_sync(0xFFFFFFFFu, y, off);
+      if (lane >= off) y += z;
+    }
+    s_warp[lane] = y;
+  }
+  __syncthreads();
+  const int32_t excl = x - v + (wid > 0 ? s_warp[wid - 1] : 0);
+  *total = s_warp[31];
+  __syncthreads();
+  return excl;
+}
+
 __global__ void __launch_bounds__(1024) k_plan(const int32_t* __restrict__ offsets, int G,
-                                               int small_bn, int large_bn,
                                                int4* __restrict__ small_items,
+                                               int4* __restrict__ medium_items,
                                                int4* __restrict__ large_items,
                                                int32_t* __restrict__ item_counts,
                                                uint32_t* status) {
-  __shared__ int32_t s_ws[32], s_wl[32];
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  __shared__ int32_t s_warp[32];
+  const int tid = threadIdx.x;
   const int per = (G + 1023) / 1024;
   const int g0 = tid * per, g1 = min(G, g0 + per);
-  int32_t ns = 0, nl = 0;
+  int32_t ns = 0, nm = 0, nl = 0;
   for (int g = g0; g < g1; ++g) {
     int32_t m = offsets[g + 1] - offsets[g];
     if (m < 0) set_status(status, STATUS_BAD_PLAN);
     if (m <= 0) continue;
-    if (m <= small_bn) ++ns;
-    else nl += (m + large_bn - 1) / large_bn;
+    if (m <= kSmallBN) ++ns;
+    else if (m <= kMediumBN) ++nm;
+    else nl += (m + kLargeBN - 1) / kLargeBN;
   }
-  // exclusive scans of ns and nl over threads
-  int32_t xs = ns, xl = nl;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    int32_t a = __shfl_up_sync(0xFFFFFFFFu, xs, off);
-    int32_t b = __shfl_up_sync(0xFFFFFFFFu, xl, off);
-    if (lane >= off) {
-      xs += a;
-      xl += b;
-    }
-  }
-  if (lane == 31) {
-    s_ws[wid] = xs;
-    s_wl[wid] = xl;
-  }
-  __syncthreads();
-  if (wid == 0) {
-    int32_t a = s_ws[lane], b = s_wl[lane];
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      int32_t c = __shfl_up_sync(0xFFFFFFFFu, a, off);
-      int32_t d = __shfl_up_sync(0xFFFFFFFFu, b, off);
-      if (lane >= off) {
-        a += c;
-        b += d;
-      }
-    }
-    s_ws[lane] = a;
-    s_wl[lane] = b;
-  }
-  __syncthreads();
-  int32_t ps = xs - ns + (wid > 0 ? s_ws[wid - 1] : 0);
-  int32_t pl = xl - nl + (wid > 0 ? s_wl[wid - 1] : 0);
+  int32_t ts, tm, tl;
+  int32_t ps = block_exclusive_scan(ns, s_warp, &ts);
+  int32_t pm = block_exclusive_scan(nm, s_warp, &tm);
+  int32_t pl = block_exclusive_scan(nl, s_warp, &tl);
   for (int g = g0; g < g1; ++g) {
     int32_t r0 = offsets[g], m = offsets[g + 1] - r0;
     if (m <= 0) continue;
-    if (m <= small_bn) {
+    if (m <= kSmallBN) {
       small_items[ps++] = make_int4(g, r0, m, 0);
+    } else if (m <= kMediumBN) {
+      medium_items[pm++] = make_int4(g, r0, m, 0);
     } else {
-      int32_t nch = (m + large_bn - 1) / large_bn;
-      // near-equal chunks, each a multiple of 16 rows except the last
+      int32_t nch = (m + kLargeBN - 1) / kLargeBN;
       int32_t base = ((m + nch - 1) / nch + 15) / 16 * 16;
       for (int c = 0; c < nch; ++c) {
         int32_t a = c * base, b = min(m, a + base);
-        if (a >= m) break;
-        large_items[pl++] = make_int4(g, r0 + a, b - a, 0);
+        large_items[pl++] = make_int4(g, r0 + a, a < m ? b - a : 0, 0);
       }
     }
   }
-  if (tid == 1023) {
-    item_counts[0] = s_ws[31];
-    item_counts[1] = s_wl[31];
+  if (tid == 0) {
+    item_counts[0] = ts;
+    item_counts[1] = tm;
+    item_counts[2] = tl;
   }
 }
 
@@ -327,11 +329,11 @@ cudaError_t launch_permute(const int32_t* idx, int T, int E, int k, int has_shar
   return cudaGetLastError();
 }
 
-cudaError_t launch_plan(const int32_t* offsets, int G, int small_bn, int large_bn,
-                        int4* small_items, int4* large_items, int32_t* item_counts,
-                        uint32_t* status, cudaStream_t st) {
-  k_plan<<<1, 1024, 0, st>>>(offsets, G, small_bn, large_bn, small_items, large_items,
-                             item_counts, status);
+cudaError_t launch_plan(const int32_t* offsets, int G, int4* small_items, int4* medium_items,
+                        int4* large_items, int32_t* item_counts, uint32_t* status,
+                        cudaStream_t st) {
+  k_plan<<<1, 1024, 0, st>>>(offsets, G, small_items, medium_items, large_items, item_counts,
+                             status);
   return cudaGetLastError();
 }
 
