@@ -333,17 +333,28 @@ int moe_forward_timed(const moe_dims* d, const uint16_t* x, const float* logits,
 #define MOE_MARK(i) \
   if (!mark(i)) return MOE_ERR_CUDA;
   MOE_MARK(0)
-  MOE_TRY(launch_route(logits, T, E, k, f.idx, f.w, st))
-  MOE_TRY(launch_permute(f.idx, T, E, k, d->has_shared, f.route.blockcnt, f.route.blockbase,
-                         f.counts, f.offsets, f.perm_src, f.inv, status, st))
+  if (T <= kPrepMaxT) {
+    // decode: route + histogram + permute + tile plan in one CTA
+    MOE_TRY(launch_prep_small(logits, T, E, k, d->has_shared, f.idx, f.w, f.counts, f.offsets,
+                              f.perm_src, f.inv, f.gemm.plan.small_items,
+                              f.gemm.plan.medium_items, f.gemm.plan.large_items,
+                              f.gemm.plan.counts, status, st))
+  } else {
+    MOE_TRY(launch_route(logits, T, E, k, f.idx, f.w, st))
+    MOE_TRY(launch_permute(f.idx, T, E, k, d->has_shared, f.route.blockcnt, f.route.blockbase,
+                           f.counts, f.offsets, f.perm_src, f.inv, status, st))
+  }
   MOE_MARK(1)
-  MOE_TRY(launch_quant_act(x, T, H, f.xq, f.xs, st))
+  // quantise each token once, writing its codes straight into its packed rows
+  MOE_TRY(launch_quant_scatter(x, T, H, k, d->has_shared, f.inv, dbg && dbg->xq ? f.xq : nullptr,
+                               dbg && dbg->xs ? f.xs : nullptr, f.gemm.xg, f.gemm.xsg, status,
+                               st))
   MOE_MARK(2)
-  MOE_TRY(launch_plan(f.offsets, groups_G(d), f.gemm.plan.small_items,
-                      f.gemm.plan.medium_items, f.gemm.plan.large_items, f.gemm.plan.counts,
-                      status, st))
-  MOE_TRY(launch_gather_rows(f.xq, f.xs, f.perm_src, T, k, R, Rs, H, f.gemm.xg, f.gemm.xsg,
-                             status, st))
+  if (T > kPrepMaxT) {
+    MOE_TRY(launch_plan(f.offsets, groups_G(d), f.gemm.plan.small_items,
+                        f.gemm.plan.medium_items, f.gemm.plan.large_items, f.gemm.plan.counts,
+                        status, st))
+  }
   MOE_MARK(3)
   // every group (a routed expert or the shared expert) holds at most T rows
   int rc = run_gemm(d, f.gemm.xg, f.gemm.xsg, f.offsets, W->w13, W->w13_s, 2 * I, H, f.y13,

@@ -26,6 +26,7 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
 // block.  Returns the 8 codes packed little-endian; writes the scale byte via lane 0
 // of the group.
 __device__ __forceinline__ uint2 quant8(const float (&f)[8], uint8_t* scale_out, int sublane) {
+  // every lane of the 16-lane group gets the same scale; lane `sublane == 0` stores it
   float amax = 0.f;
 #pragma unroll
   for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
@@ -67,6 +68,55 @@ __global__ void __launch_bounds__(256) k_quant_act(const uint16_t* __restrict__ 
   if (live) *reinterpret_cast<uint2*>(q + r * cols + b * 128 + sub * 8) = c;
 }
 
+// a3 fused with the packed-row gather: token t's codes and scales go to xq / xs
+// (when given) and straight to its k routed rows inv[t*k + j] and its shared row R + t
+// of the packed activations, so no separate gather pass re-reads them.
+__global__ void __launch_bounds__(256) k_quant_scatter(const uint16_t* __restrict__ x, int T,
+                                                       int H, int k, int has_shared,
+                                                       const int32_t* __restrict__ inv,
+                                                       uint8_t* __restrict__ xq,
+                                                       uint8_t* __restrict__ xs,
+                                                       uint8_t* __restrict__ xg,
+                                                       uint8_t* __restrict__ xsg,
+                                                       uint32_t* status) {
+  const int nblk = H / 128;
+  const long long gw = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31, half = lane >> 4, sub = lane & 15;
+  const long long blk = gw * 2 + half;
+  const long long total = static_cast<long long>(T) * nblk;
+  const bool live = blk < total;
+  const long long t = live ? blk / nblk : 0, b = live ? blk % nblk : 0;
+  float f[8];
+  if (live) {
+    uint4 u = *reinterpret_cast<const uint4*>(x + t * H + b * 128 + sub * 8);
+    bf16x8_to_f32(u, f);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) f[i] = 0.f;
+  }
+  uint8_t scale;
+  uint2 c = quant8(f, &scale, 0);
+  if (!live) return;
+  const long long R = static_cast<long long>(T) * k;
+  if (xq) *reinterpret_cast<uint2*>(xq + t * H + b * 128 + sub * 8) = c;
+  if (xs && sub == 0) xs[t * nblk + b] = scale;
+  for (int j = 0; j <= k; ++j) {
+    long long r;
+    if (j < k) {
+      r = inv[t * k + j];
+      if (r < 0 || r >= R) {
+        if (sub == 0) set_status(status, STATUS_BAD_INDEX);
+        continue;
+      }
+    } else {
+      if (!has_shared) break;
+      r = R + t;
+    }
+    *reinterpret_cast<uint2*>(xg + r * H + b * 128 + sub * 8) = c;
+    if (sub == 0) xsg[r * nblk + b] = scale;
+  }
+}
+
 // a5.  Row r of y13 holds [gate(I) | up(I)] in bf16; h = silu(gate) * up in fp32.
 __global__ void __launch_bounds__(256) k_swiglu_quant(const uint16_t* __restrict__ y13,
                                                       int rows, int I,
@@ -88,7 +138,7 @@ __global__ void __launch_bounds__(256) k_swiglu_quant(const uint16_t* __restrict
     bf16x8_to_f32(ug, g);
     bf16x8_to_f32(uu, u);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) h[i] = g[i] / (1.0f + expf(-g[i])) * u[i];
+    for (int i = 0; i < 8; ++i) h[i] = g[i] * __frcp_rn(1.0f + expf(-g[i])) * u[i];
   } else {
 #pragma unroll
     for (int i = 0; i < 8; ++i) h[i] = 0.f;
@@ -188,6 +238,16 @@ cudaError_t launch_quant_act(const uint16_t* x, int rows, int cols, uint8_t* q, 
   long long nb = static_cast<long long>(rows) * (cols / 128);
   if (nb == 0) return cudaSuccess;
   k_quant_act<<<grid_for_blocks(nb), 256, 0, st>>>(x, rows, cols, q, s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_scatter(const uint16_t* x, int T, int H, int k, int has_shared,
+                                 const int32_t* inv, uint8_t* xq, uint8_t* xs, uint8_t* xg,
+                                 uint8_t* xsg, uint32_t* status, cudaStream_t st) {
+  long long nb = static_cast<long long>(T) * (H / 128);
+  if (nb == 0) return cudaSuccess;
+  k_quant_scatter<<<grid_for_blocks(nb), 256, 0, st>>>(x, T, H, k, has_shared, inv, xq, xs, xg,
+                                                       xsg, status);
   return cudaGetLastError();
 }
 

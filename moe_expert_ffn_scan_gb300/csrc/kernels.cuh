@@ -22,6 +22,17 @@ constexpr int kLargeBN = 128;
 constexpr int kLargeStages = 3;
 constexpr int kLargeStagesKO1 = 6;
 
+// Token count up to which route + histogram + permute + plan run as one CTA.
+constexpr int kPrepMaxT = 128;
+
+cudaError_t launch_prep_small(const float* logits, int T, int E, int k, int has_shared,
+                              int32_t* idx, float* w, int32_t* counts, int32_t* offsets,
+                              int32_t* perm_src, int32_t* inv, int4* small_items,
+                              int4* medium_items, int4* large_items, int32_t* item_counts,
+                              uint32_t* status, cudaStream_t st);
+cudaError_t launch_quant_scatter(const uint16_t* x, int T, int H, int k, int has_shared,
+                                 const int32_t* inv, uint8_t* xq, uint8_t* xs, uint8_t* xg,
+                                 uint8_t* xsg, uint32_t* status, cudaStream_t st);
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* idx, float* w,
                          cudaStream_t st);
 int perm_blocks(int T);

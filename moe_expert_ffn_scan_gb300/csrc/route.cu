@@ -15,15 +15,11 @@ namespace moe {
 // ---------------------------------------------------------------- a1: route -------
 //
 // One warp per token.  Lane l holds logits l, l+32, ... (coalesced loads).  k rounds
-// of warp-wide argmax over the not-yet-taken experts, ties to the lower index.
+// of warp-wide argmax over the not-yet-taken experts, ties to the lower index.  On
+// return lane j < k holds the j-th selection (expert, renormalised weight).
 template <int EPL>
-__global__ void __launch_bounds__(256) k_route(const float* __restrict__ logits, int T, int E,
-                                               int k, int32_t* __restrict__ idx,
-                                               float* __restrict__ w) {
-  const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (t >= T) return;
-  const float* row = logits + static_cast<size_t>(t) * E;
+__device__ __forceinline__ void route_token(const float* __restrict__ row, int E, int k,
+                                            int lane, int& my_e, float& my_w) {
   float v[EPL];
   uint32_t taken = 0;
 #pragma unroll
@@ -33,7 +29,7 @@ __global__ void __launch_bounds__(256) k_route(const float* __restrict__ logits,
     if (e >= E) taken |= 1u << i;
   }
   float my_v = 0.f;
-  int my_e = 0;
+  my_e = 0;
   for (int j = 0; j < k; ++j) {
     float bv = 0.f;
     int be = 0x7FFFFFFF;
@@ -69,9 +65,22 @@ __global__ void __launch_bounds__(256) k_route(const float* __restrict__ logits,
   float s = ex;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
+  my_w = ex / s;
+}
+
+template <int EPL>
+__global__ void __launch_bounds__(256) k_route(const float* __restrict__ logits, int T, int E,
+                                               int k, int32_t* __restrict__ idx,
+                                               float* __restrict__ w) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;
+  int e;
+  float wt;
+  route_token<EPL>(logits + static_cast<size_t>(t) * E, E, k, lane, e, wt);
   if (lane < k) {
-    idx[static_cast<size_t>(t) * k + lane] = my_e;
-    w[static_cast<size_t>(t) * k + lane] = ex / s;
+    idx[static_cast<size_t>(t) * k + lane] = e;
+    w[static_cast<size_t>(t) * k + lane] = wt;
   }
 }
 
@@ -239,13 +248,12 @@ __device__ __forceinline__ int32_t block_exclusive_scan(int32_t v, int32_t* s_wa
   return excl;
 }
 
-__global__ void __launch_bounds__(1024) k_plan(const int32_t* __restrict__ offsets, int G,
-                                               int4* __restrict__ small_items,
-                                               int4* __restrict__ medium_items,
-                                               int4* __restrict__ large_items,
-                                               int32_t* __restrict__ item_counts,
-                                               uint32_t* status) {
-  __shared__ int32_t s_warp[32];
+// Builds the three item lists from group offsets (global or shared memory).  Called
+// by all 1024 threads of one CTA.
+__device__ void plan_groups(const int32_t* offsets, int G, int4* __restrict__ small_items,
+                            int4* __restrict__ medium_items, int4* __restrict__ large_items,
+                            int32_t* __restrict__ item_counts, uint32_t* status,
+                            int32_t* s_warp) {
   const int tid = threadIdx.x;
   const int per = (G + 1023) / 1024;
   const int g0 = tid * per, g1 = min(G, g0 + per);
@@ -283,6 +291,95 @@ __global__ void __launch_bounds__(1024) k_plan(const int32_t* __restrict__ offse
     item_counts[1] = tm;
     item_counts[2] = tl;
   }
+}
+
+__global__ void __launch_bounds__(1024) k_plan(const int32_t* __restrict__ offsets, int G,
+                                               int4* __restrict__ small_items,
+                                               int4* __restrict__ medium_items,
+                                               int4* __restrict__ large_items,
+                                               int32_t* __restrict__ item_counts,
+                                               uint32_t* status) {
+  __shared__ int32_t s_warp[32];
+  plan_groups(offsets, G, small_items, medium_items, large_items, item_counts, status, s_warp);
+}
+
+// ------------------------------------------------ a1 + a2 + a8 in one CTA (small T) ---
+//
+// The decode path ("route preplan", GB10 report Optimization 14): for T <= kPrepMaxT
+// one CTA routes every token, builds per-expert token bit masks, the counts, the
+// offsets (block scan), each routed row's position (its token's rank among the
+// expert's tokens = popcount of the mask below it) and the tile plan.  One launch
+// instead of five; same results as the multi-kernel path.
+template <int EPL>
+__global__ void __launch_bounds__(1024) k_prep_small(
+    const float* __restrict__ logits, int T, int E, int k, int has_shared,
+    int32_t* __restrict__ idx, float* __restrict__ w, int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ perm_src, int32_t* __restrict__ inv,
+    int4* __restrict__ small_items, int4* __restrict__ medium_items,
+    int4* __restrict__ large_items, int32_t* __restrict__ item_counts, uint32_t* status) {
+  constexpr int kWords = kPrepMaxT / 32;
+  __shared__ uint32_t s_mask[1024 * kWords];  // [expert][token word]
+  __shared__ int32_t s_idx[kPrepMaxT * 16];
+  __shared__ int32_t s_off[1026];
+  __shared__ int32_t s_warp[32];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int G = E + has_shared;
+  for (int i = tid; i < E * kWords; i += 1024) s_mask[i] = 0;
+  __syncthreads();
+  for (int t = wid; t < T; t += 32) {
+    int e;
+    float wt;
+    route_token<EPL>(logits + static_cast<size_t>(t) * E, E, k, lane, e, wt);
+    if (lane < k) {
+      idx[t * k + lane] = e;
+      w[t * k + lane] = wt;
+      s_idx[t * k + lane] = e;
+      atomicOr(&s_mask[e * kWords + (t >> 5)], 1u << (t & 31));
+    }
+  }
+  __syncthreads();
+  // counts and offsets (thread-contiguous runs of groups, block scan)
+  const int per = (G + 1023) / 1024;
+  const int g0 = tid * per, g1 = min(G, g0 + per);
+  int32_t run = 0;
+  for (int g = g0; g < g1; ++g) {
+    int32_t c = 0;
+    if (g < E) {
+#pragma unroll
+      for (int i = 0; i < kWords; ++i) c += __popc(s_mask[g * kWords + i]);
+      counts[g] = c;
+    } else {
+      c = T;  // the shared expert: one row per token
+    }
+    run += c;
+  }
+  int32_t total;
+  int32_t pos = block_exclusive_scan(run, s_warp, &total);
+  for (int g = g0; g < g1; ++g) {
+    s_off[g] = pos;
+    offsets[g] = pos;
+    pos += g < E ? counts[g] : T;
+  }
+  if (tid == 0) {
+    s_off[G] = total;
+    offsets[G] = total;
+  }
+  __syncthreads();
+  // positions: rank of token t among expert e's tokens
+  for (int i = tid; i < T * k; i += 1024) {
+    const int t = i / k, e = s_idx[i];
+    int32_t rank = 0;
+#pragma unroll
+    for (int wd = 0; wd < kWords; ++wd) {
+      const uint32_t m = s_mask[e * kWords + wd];
+      if (wd < (t >> 5)) rank += __popc(m);
+      else if (wd == (t >> 5)) rank += __popc(m & ((1u << (t & 31)) - 1u));
+    }
+    const int32_t p = s_off[e] + rank;
+    perm_src[p] = i;
+    inv[i] = p;
+  }
+  plan_groups(s_off, G, small_items, medium_items, large_items, item_counts, status, s_warp);
 }
 
 // ---------------------------------------------------------------- launchers -------
@@ -335,6 +432,31 @@ cudaError_t launch_plan(const int32_t* offsets, int G, int4* small_items, int4* 
   k_plan<<<1, 1024, 0, st>>>(offsets, G, small_items, medium_items, large_items, item_counts,
                              status);
   return cudaGetLastError();
+}
+
+cudaError_t launch_prep_small(const float* logits, int T, int E, int k, int has_shared,
+                              int32_t* idx, float* w, int32_t* counts, int32_t* offsets,
+                              int32_t* perm_src, int32_t* inv, int4* small_items,
+                              int4* medium_items, int4* large_items, int32_t* item_counts,
+                              uint32_t* status, cudaStream_t st) {
+  if (T > kPrepMaxT) return cudaErrorInvalidValue;
+  const int epl = (E + 31) / 32;
+#define MOE_PREP_CASE(N)                                                                    \
+  if (epl <= N) {                                                                           \
+    k_prep_small<N><<<1, 1024, 0, st>>>(logits, T, E, k, has_shared, idx, w, counts,        \
+                                        offsets, perm_src, inv, small_items, medium_items,  \
+                                        large_items, item_counts, status);                  \
+    return cudaGetLastError();                                                              \
+  }
+  MOE_PREP_CASE(1)
+  MOE_PREP_CASE(2)
+  MOE_PREP_CASE(4)
+  MOE_PREP_CASE(8)
+  MOE_PREP_CASE(12)
+  MOE_PREP_CASE(16)
+  MOE_PREP_CASE(32)
+#undef MOE_PREP_CASE
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace moe

@@ -143,6 +143,8 @@ GEMM_SHAPES = [
     ("w13", 4, 512, 1024, [16, 17, 33, 130]),
     ("w2", 3, 256, 384, [300, 7, 128]),
     ("w13", 2, 256, 128, [1, 64]),
+    ("w2", 3, 1024, 3072, [1, 40, 200]),
+    ("w13", 5, 512, 512, [0, 16, 64, 65, 129]),
 ]
 
 
