@@ -80,7 +80,8 @@ def max_over_ranks(x, world):
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
@@ -123,6 +124,23 @@ def fp8_tensor_peak_tflops():
                 except (TypeError, ValueError):
                     pass
     return 2.0 * FALLBACK_BF16_TFLOPS, "fallback bf16 x2 (nominal fp8/bf16 ratio)"
+
+
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per active weight group of
+# one small-M W13 GEMM launch, from the ncu capture summarised in
+# profiles/k_gemm_mx_small_decode_T7_E64.md, keyed by the hash of the GEMM sources it
+# was taken on.  A changed kernel reports traffic null until it is captured again.
+NCU_SMALL_W13_TRAFFIC = {"src": "bc17838a14c2101f", "bytes_per_group": (966.6e6 + 3.8e6) / 41}
+
+
+def gemm_src_hash():
+    import hashlib
+    csrc = os.path.join(ROOT, "moe_expert_ffn_scan_gb300", "csrc")
+    digests = []
+    for name in ("gemm.cu", "kernels.cuh", "common.cuh"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            digests.append(hashlib.sha256(f.read()).hexdigest())
+    return hashlib.sha256(("\n".join(digests) + "\n").encode()).hexdigest()[:16]
 
 
 class ClockSampler:
@@ -344,8 +362,11 @@ def run_ours(args, rank, world, local):
     decode_like = (flops13 / (w13_bytes + act13)) < (tpk * 1e12) / (hbm * 1e9)
     if decode_like:
         ach = (w13_bytes + act13) / t13 / 1e9
+        traffic = None
+        if d.T <= 16 and gemm_src_hash() == NCU_SMALL_W13_TRAFFIC["src"]:
+            traffic = groups * NCU_SMALL_W13_TRAFFIC["bytes_per_group"]
         roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
-                "frac": ach / hbm, "traffic": None,
+                "frac": ach / hbm, "traffic": traffic,
                 "kernel": "k_gemm_mx (W13 grouped GEMM)",
                 "peak_source": f"{hbm_src} HBM copy bandwidth"}
     else:
