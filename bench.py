@@ -44,7 +44,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode", choices=list(gi.WORKLOADS))
+    ap.add_argument("--workload", default="decode", choices=list(gi.WORKLOADS) + ["sweep"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -261,6 +261,10 @@ def blas_threads():
 def run_reference(args, rank, world):
     if rank != 0:
         return
+    if args.workload == "sweep":
+        print(json.dumps({"impl": "reference", "unavailable": "the GEMM sweep has no CPU arm; "
+                          "run a layer workload"}), flush=True)
+        return
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     d, t = make_layer(args, args.seed, dev)
     hv = host_view(d, t)
@@ -438,12 +442,83 @@ def run_ours(args, rank, world, local):
         print(json.dumps(line), flush=True)
 
 
+def run_sweep(args, rank, world, local):
+    """Grouped-GEMM shape sweep: W13 (N=6144, K=7168) and W2 (N=7168, K=3072), G groups
+    of M rows each (G*M ~ 32768 for M >= 64, else G = 64).  Activations bf16 N(0,1),
+    quantised by the library's FP8 quantiser.  One JSON line with every point."""
+    import moe_expert_ffn_scan_gb300 as moe
+    moe.lib()
+    dev = torch.device("cuda", local)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    hbm, hbm_src = hbm_peak_gbs()
+    tpk, tpk_src = fp8_tensor_peak_tflops()
+    points = []
+    for which in ("w13", "w2"):
+        N, K = gi.SWEEP_SHAPES[which]
+        for M in gi.SWEEP_M:
+            x, offsets, w, ws_ = gi.sweep_point(which, M, seed=args.seed, device=dev)
+            rows, G = x.shape[0], offsets.numel() - 1
+            q = torch.empty(rows, K, dtype=torch.uint8, device=dev)
+            qs = torch.empty(rows, K // 128, dtype=torch.uint8, device=dev)
+            moe.moe_quant_act(x, q, qs)
+            del x
+            y = torch.empty(rows, N, dtype=torch.bfloat16, device=dev)
+            if which == "w13":
+                d = moe.dims(rows, K, N // 2, G, 1, 0)
+            else:
+                d = moe.dims(rows, N, K, G, 1, 0)
+            wsp = moe.alloc_workspace(moe.gemm_workspace_size(d), dev)
+
+            def call():
+                if which == "w13":
+                    moe.moe_grouped_gemm_w13(d, q, qs, None, offsets, w, ws_, y, wsp)
+                else:
+                    moe.moe_grouped_gemm_w2(d, q, qs, offsets, w, ws_, y, wsp)
+            for _ in range(args.warmup):
+                call()
+            torch.cuda.synchronize()
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.steps)]
+            for i in range(args.steps):
+                flush.fill_(i & 0xFF)
+                evs[i][0].record()
+                call()
+                evs[i][1].record()
+            torch.cuda.synchronize()
+            bits = moe.moe_check_status(wsp)
+            if bits:
+                raise RuntimeError(f"device status bits {bits:#x}")
+            ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+            wbytes = G * N * K * WEIGHT_BYTES_PER_ELEM
+            flops = 2.0 * rows * N * K
+            gbs = wbytes / (ms * 1e-3) / 1e9
+            tfl = flops / (ms * 1e-3) / 1e12
+            points.append({"gemm": which, "M": M, "G": G, "ms": ms, "weight_gbs": gbs,
+                           "tflops": tfl, "hbm_frac": gbs / hbm, "tensor_frac": tfl / tpk,
+                           "roofline_frac": max(gbs / hbm, tfl / tpk)})
+            del q, qs, y, w, ws_, wsp
+            torch.cuda.empty_cache()
+    if rank == 0:
+        line = {"metric": "grouped-GEMM sweep (weight GB/s, TFLOP/s per M)",
+                "value": statistics.mean(p["roofline_frac"] for p in points),
+                "unit": "mean roofline fraction", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "higher_is_better": True, "data": "synthetic",
+                "dtype": "mxfp4xfp8->f32",
+                "config": {"workload": "sweep", "l2": "flushed before each call",
+                           "hbm_peak_gbs": hbm, "hbm_peak_source": hbm_src,
+                           "fp8_peak_tflops": tpk, "fp8_peak_source": tpk_src},
+                "points": points}
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     rank, world, local = dist_init(args)
     try:
         if args.impl == "reference":
             run_reference(args, rank, world)
+        elif args.workload == "sweep":
+            run_sweep(args, rank, world, local)
         else:
             run_ours(args, rank, world, local)
     finally:

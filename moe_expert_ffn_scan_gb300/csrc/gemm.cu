@@ -57,19 +57,20 @@ struct GemmCfg {
   static constexpr int kABytes = KO * kASub;
   static constexpr int kBBytes = KO * kBSub;
   static constexpr int kSfBytes = 512;
+  static constexpr int kSfbAtoms = (BN_MAX + 127) / 128;  // token scale atoms per stage
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + STAGES * kABytes;
   static constexpr int kOffSfa = kOffB + STAGES * kBBytes;
   static constexpr int kOffSfb = kOffSfa + STAGES * KO * kSfBytes;
-  static constexpr int kOffBar = kOffSfb + STAGES * kSfBytes;
+  static constexpr int kOffBar = kOffSfb + STAGES * kSfbAtoms * kSfBytes;
   static constexpr int kNumBars = 2 * STAGES + 4;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16;
-  static constexpr int kSfCols = 4 * (KO + 1);              // TMEM columns per stage
+  static constexpr int kSfCols = 4 * (KO + kSfbAtoms);      // TMEM columns per stage
   static constexpr int kTmemNeed = 2 * BN_MAX + STAGES * kSfCols;
   static constexpr int kTmemCols =
       kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128 : kTmemNeed <= 256 ? 256 : 512;
-  static_assert(BN_MAX % 16 == 0 && BN_MAX <= 128, "token tile");
+  static_assert(BN_MAX % 16 == 0 && BN_MAX <= 256, "token tile");
   static_assert(KO == 1 || KO == 2 || KO == 4, "sub-tiles per stage");
   static_assert(kTmemNeed <= 512, "TMEM");
 };
@@ -211,8 +212,12 @@ __global__ void __launch_bounds__(256, OCC)
             tc_cp_32x128b_x4(sf_t + 4 * ko,
                              smem_desc(smem_u32(smem + C::kOffSfa + (s * KO + ko) * C::kSfBytes),
                                        0, 128, kLayoutNone));
-          tc_cp_32x128b_x4(sfb_t, smem_desc(smem_u32(smem + C::kOffSfb + s * C::kSfBytes), 0,
-                                            128, kLayoutNone));
+#pragma unroll
+          for (int a = 0; a < C::kSfbAtoms; ++a)  // tokens 128a .. 128a+127 at columns +4a
+            tc_cp_32x128b_x4(sfb_t + 4 * a,
+                             smem_desc(smem_u32(smem + C::kOffSfb +
+                                                (s * C::kSfbAtoms + a) * C::kSfBytes),
+                                       0, 128, kLayoutNone));
           const uint32_t a0 = smem_u32(smem + C::kOffA + s * C::kABytes);
           const uint32_t b0 = smem_u32(smem + C::kOffB + s * C::kBBytes);
 #pragma unroll
@@ -237,15 +242,19 @@ __global__ void __launch_bounds__(256, OCC)
   } else if (warp == 2) {
     // ---------------------------------------------------------------- scale factors
     // Per stage: KO weight atoms (row r at byte (r % 32) * 16 + (r / 32) * 4 + kblock)
-    // and one token atom whose byte ko holds the token's scale for sub-tile ko.
+    // and one token atom per 128 tokens whose byte ko holds the token's scale for
+    // sub-tile ko (token r of atom a at byte (r % 32) * 16 + ((r / 32) % 4) * 4 + ko).
+    constexpr int NA = C::kSfbAtoms;
     const int kw = p.K / 32, kx = p.K / 128;
-    auto put_stage = [&](int s, const uint32_t (&wa)[KO][4], const uint32_t (&xb)[4]) {
+    auto put_stage = [&](int s, const uint32_t (&wa)[KO][4], const uint32_t (&xb)[4 * NA]) {
 #pragma unroll
       for (int ko = 0; ko < KO; ++ko)
         *reinterpret_cast<uint4*>(smem + C::kOffSfa + (s * KO + ko) * C::kSfBytes + lane * 16) =
             make_uint4(wa[ko][0], wa[ko][1], wa[ko][2], wa[ko][3]);
-      *reinterpret_cast<uint4*>(smem + C::kOffSfb + s * C::kSfBytes + lane * 16) =
-          make_uint4(xb[0], xb[1], xb[2], xb[3]);
+#pragma unroll
+      for (int a = 0; a < NA; ++a)
+        *reinterpret_cast<uint4*>(smem + C::kOffSfb + (s * NA + a) * C::kSfBytes + lane * 16) =
+            make_uint4(xb[4 * a], xb[4 * a + 1], xb[4 * a + 2], xb[4 * a + 3]);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&full[s]);
@@ -318,13 +327,13 @@ __global__ void __launch_bounds__(256, OCC)
               ok = false;
               break;
             }
-            uint32_t wa[KO][4], xb[4];
+            uint32_t wa[KO][4], xb[4 * NA];
 #pragma unroll
             for (int ko = 0; ko < KO; ++ko)
 #pragma unroll
               for (int j = 0; j < 4; ++j) wa[ko][j] = u4_comp(wv[i][j], b * KO + ko);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < 4 * NA; ++j) {
               if (j < J) {
                 const uint32_t a = av[i][j < J ? j : 0] >> (8 * b * KO);
                 xb[j] = KO == 4 ? a : (KO == 2 ? (a & 0xFFFFu) : (a & 0xFFu));
@@ -353,18 +362,24 @@ __global__ void __launch_bounds__(256, OCC)
             ok = false;
             break;
           }
-          uint32_t wa[KO][4], xb[4];
+          uint32_t wa[KO][4], xb[4 * NA];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
+            const int r = j * 32 + lane;
+#pragma unroll
+            for (int ko = 0; ko < KO; ++ko)
+              wa[ko][j] = __ldg(reinterpret_cast<const uint32_t*>(
+                  wsp + static_cast<size_t>(r) * kw + (kb * KO + ko) * 4));
+          }
+#pragma unroll
+          for (int j = 0; j < 4 * NA; ++j) {
             const int r = j * 32 + lane;
             uint32_t packed = 0;
 #pragma unroll
             for (int ko = 0; ko < KO; ++ko) {
-              const int sub = kb * KO + ko;
-              wa[ko][j] = __ldg(reinterpret_cast<const uint32_t*>(
-                  wsp + static_cast<size_t>(r) * kw + sub * 4));
               uint32_t sb = 127u;
-              if (r < rows) sb = __ldg(p.x_scales + static_cast<size_t>(row0 + r) * kx + sub);
+              if (r < rows)
+                sb = __ldg(p.x_scales + static_cast<size_t>(row0 + r) * kx + kb * KO + ko);
               packed |= sb << (8 * ko);
             }
             xb[j] = packed;

@@ -145,6 +145,7 @@ GEMM_SHAPES = [
     ("w13", 2, 256, 128, [1, 64]),
     ("w2", 3, 1024, 3072, [1, 40, 200]),
     ("w13", 5, 512, 512, [0, 16, 64, 65, 129]),
+    ("w13", 2, 256, 512, [224, 150]),
 ]
 
 
@@ -221,3 +222,20 @@ def test_combine(T, H, k, sh):
     assert_float_close(bf16_np(out), ref, "out")
     # fp32 sums of k <= 8 bf16 terms round to the same bf16 in almost every element
     assert np.mean(bf16_np(out) != ref) < 1e-2
+
+
+@pytest.mark.parametrize("K", [512, 384])
+def test_grouped_gemm_token_scales_beyond_128_rows(K):
+    """One chunk of 224 token rows (two token-scale atoms): every row gets its own
+    activation scale byte, integer codes keep the result exact."""
+    G, N = 1, 256
+    sizes = [224]
+    offsets, aq, asc, wq, wsc = _gemm_case(G, N, K, sizes, seed=7, integer=True)
+    asc = (125 + (torch.arange(224).view(224, 1) * 7 + torch.arange(K // 128).view(1, -1)) % 5
+           ).to(torch.uint8)
+    wsc = (124 + torch.randint(0, 5, wsc.shape, generator=torch.Generator().manual_seed(3))
+           ).to(torch.uint8)
+    y = _run_gemm("w13", G, N, K, offsets, aq, asc, wq, wsc)
+    ref = o.grouped_gemm(aq.numpy(), asc.numpy(), offsets, wq.numpy(), wsc.numpy())
+    bad = np.argwhere(y != ref)
+    assert bad.size == 0, f"{len(bad)} mismatches, rows {np.unique(bad[:, 0])[:10]}"
