@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(256) k_swiglu_quant(const uint16_t* __restrict
     bf16x8_to_f32(ug, g);
     bf16x8_to_f32(uu, u);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) h[i] = g[i] * __frcp_rn(1.0f + expf(-g[i])) * u[i];
+    for (int i = 0; i < 8; ++i) h[i] = __fdividef(g[i], 1.0f + __expf(-g[i])) * u[i];
   } else {
 #pragma unroll
     for (int i = 0; i < 8; ++i) h[i] = 0.f;
@@ -198,14 +198,24 @@ __global__ void __launch_bounds__(128) k_combine(const uint16_t* __restrict__ y2
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-    for (int j = 0; j < k; ++j) {
-      const int32_t r = s_row[j];
-      if (r < 0) continue;
-      const float wj = s_w[j];
-      float f[8];
-      bf16x8_to_f32(*reinterpret_cast<const uint4*>(y2 + static_cast<long long>(r) * H + c), f);
+    // issue the loads of up to 8 routed rows before consuming any
+    for (int j0 = 0; j0 < k; j0 += 8) {
+      uint4 v[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, f[i], acc[i]);
+      for (int jj = 0; jj < 8; ++jj) {
+        const int32_t r = j0 + jj < k ? s_row[j0 + jj] : -1;
+        v[jj] = r >= 0 ? *reinterpret_cast<const uint4*>(y2 + static_cast<long long>(r) * H + c)
+                       : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        if (j0 + jj >= k || s_row[j0 + jj] < 0) continue;
+        const float wj = s_w[j0 + jj];
+        float f[8];
+        bf16x8_to_f32(v[jj], f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, f[i], acc[i]);
+      }
     }
     if (has_shared) {
       float f[8];

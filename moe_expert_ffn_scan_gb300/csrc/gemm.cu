@@ -47,10 +47,9 @@ constexpr int kSfQuads = 4;
 // Shared-memory layout of one pipeline configuration.  A stage holds KO sub-tiles of
 // 128 K elements: weights [KO][128 rows][128 B] (FP4 in its 16-byte-aligned form),
 // tokens [KO][BN_MAX rows][128 B] (FP8), KO weight scale atoms and one token scale
-// atom (512 B each).  With KO > 1 each stage is one weight TMA (box 128 x 128 x KO)
-// and one token TMA (box 128 x BN_MAX x KO); with KO == 1 the tokens come in boxes of
-// 16 rows, as many as the group needs.
-template <int BN_MAX, int STAGES, int KO>
+// atoms (512 B each).  Each stage is one weight TMA (box 128 x 128 x KO) and one
+// token TMA (box 128 x BN_MAX x KO; rows past the chunk are loaded and ignored).
+template <int BN_MAX, int STAGES, int KO, int OCC>
 struct GemmCfg {
   static constexpr int kASub = 128 * 128;
   static constexpr int kBSub = BN_MAX * 128;
@@ -58,11 +57,22 @@ struct GemmCfg {
   static constexpr int kBBytes = KO * kBSub;
   static constexpr int kSfBytes = 512;
   static constexpr int kSfbAtoms = (BN_MAX + 127) / 128;  // token scale atoms per stage
-  static constexpr int kOffA = 0;
+  // Wide scale staging (the 1-CTA-per-SM large variant): each 32-row atom is written
+  // four times (rows r, r+32, r+64, r+96) so that one tcgen05.cp.128x{128,256}b per
+  // operand moves every sub-tile's / token block's scales of a stage -- the same TMEM
+  // contents as one 32x128b.warpx4 copy per atom, with fewer instructions to issue.
+  static constexpr bool kWideSf = OCC == 1;
+  static constexpr int kSfaStage = kWideSf ? KO * 2048 : KO * kSfBytes;
+  static constexpr int kSfbStage = kWideSf ? kSfbAtoms * 2048 : kSfbAtoms * kSfBytes;
+  // Wide staging goes first, so reads through its (larger-stride) copy descriptors can
+  // only reach the tiles that follow, never past the CTA's shared memory; otherwise the
+  // 1024-byte-aligned tiles go first and the scale atoms after them.
+  static constexpr int kSfTotal = STAGES * (kSfaStage + kSfbStage);
+  static constexpr int kOffSfa = kWideSf ? 0 : STAGES * (kABytes + kBBytes);
+  static constexpr int kOffSfb = kOffSfa + STAGES * kSfaStage;
+  static constexpr int kOffA = kWideSf ? (kSfTotal + 1023) / 1024 * 1024 : 0;
   static constexpr int kOffB = kOffA + STAGES * kABytes;
-  static constexpr int kOffSfa = kOffB + STAGES * kBBytes;
-  static constexpr int kOffSfb = kOffSfa + STAGES * KO * kSfBytes;
-  static constexpr int kOffBar = kOffSfb + STAGES * kSfbAtoms * kSfBytes;
+  static constexpr int kOffBar = kWideSf ? kOffB + STAGES * kBBytes : kOffSfa + kSfTotal;
   static constexpr int kNumBars = 2 * STAGES + 4;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16;
@@ -72,6 +82,7 @@ struct GemmCfg {
       kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128 : kTmemNeed <= 256 ? 256 : 512;
   static_assert(BN_MAX % 16 == 0 && BN_MAX <= 256, "token tile");
   static_assert(KO == 1 || KO == 2 || KO == 4, "sub-tiles per stage");
+  static_assert(!kWideSf || (KO <= 2 && kSfbAtoms <= 2), "wide scale copies move <= 256 bits");
   static_assert(kTmemNeed <= 512, "TMEM");
 };
 
@@ -95,7 +106,7 @@ template <int BN_MAX, int STAGES, int KO, int OCC>
 __global__ void __launch_bounds__(256, OCC)
     k_gemm_mx(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
               const GemmParams p) {
-  using C = GemmCfg<BN_MAX, STAGES, KO>;
+  using C = GemmCfg<BN_MAX, STAGES, KO, OCC>;
   // The 128B-swizzled tiles need 1024-byte alignment; the dynamic shared memory of a
   // kernel without static shared memory starts at such a boundary.  Checked, not
   // assumed: a misaligned base reports STATUS_BAD_PLAN and the CTA returns.
@@ -166,20 +177,14 @@ __global__ void __launch_bounds__(256, OCC)
         int g, row0, rows, nt;
         if (!load_item(L, g, row0, rows, nt)) continue;
         const int bn = (rows + 15) & ~15;
-        const uint32_t tx = KO * kWeightTileTxBytes + (KO == 1 ? bn : BN_MAX * KO) * 128;
+        const uint32_t tx = KO * kWeightTileTxBytes + BN_MAX * KO * 128;
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1u;
           if (it >= STAGES && !mbar_wait(&empty[s], ph ^ 1u, p.status, abort_flag)) break;
           mbar_arrive_expect_tx(&full[s], tx);
           tma_load_4d(smem + C::kOffA + s * C::kABytes, &tmW, &full[s], 0, nt * 128, kb * KO, g);
-          if (KO == 1) {
-            for (int i = 0; i < bn; i += 16)
-              tma_load_3d(smem + C::kOffB + s * C::kBBytes + i * 128, &tmX, &full[s], 0,
-                          row0 + i, kb);
-          } else {
-            tma_load_3d(smem + C::kOffB + s * C::kBBytes, &tmX, &full[s], 0, row0, kb * KO);
-          }
+          tma_load_3d(smem + C::kOffB + s * C::kBBytes, &tmX, &full[s], 0, row0, kb * KO);
         }
       }
     }
@@ -207,17 +212,30 @@ __global__ void __launch_bounds__(256, OCC)
           tc_fence_after();
           const uint32_t sf_t = tmem + 2 * BN_MAX + s * C::kSfCols;
           const uint32_t sfb_t = sf_t + 4 * KO;
+          if constexpr (C::kWideSf) {
+            // [KO][128 rows][16 B] -> KO * 4 columns; [NA][128][16 B] -> NA * 4 columns
+            const uint64_t da = smem_desc(smem_u32(smem + C::kOffSfa + s * C::kSfaStage), 2048,
+                                          128, kLayoutNone);
+            const uint64_t db = smem_desc(smem_u32(smem + C::kOffSfb + s * C::kSfbStage), 2048,
+                                          128, kLayoutNone);
+            if (KO == 2) tc_cp_128x256b(sf_t, da);
+            else tc_cp_128x128b(sf_t, da);
+            if (C::kSfbAtoms == 2) tc_cp_128x256b(sfb_t, db);
+            else tc_cp_128x128b(sfb_t, db);
+          } else {
 #pragma unroll
-          for (int ko = 0; ko < KO; ++ko)
-            tc_cp_32x128b_x4(sf_t + 4 * ko,
-                             smem_desc(smem_u32(smem + C::kOffSfa + (s * KO + ko) * C::kSfBytes),
-                                       0, 128, kLayoutNone));
+            for (int ko = 0; ko < KO; ++ko)
+              tc_cp_32x128b_x4(sf_t + 4 * ko,
+                               smem_desc(smem_u32(smem + C::kOffSfa + s * C::kSfaStage +
+                                                  ko * C::kSfBytes),
+                                         0, 128, kLayoutNone));
 #pragma unroll
-          for (int a = 0; a < C::kSfbAtoms; ++a)  // tokens 128a .. 128a+127 at columns +4a
-            tc_cp_32x128b_x4(sfb_t + 4 * a,
-                             smem_desc(smem_u32(smem + C::kOffSfb +
-                                                (s * C::kSfbAtoms + a) * C::kSfBytes),
-                                       0, 128, kLayoutNone));
+            for (int a = 0; a < C::kSfbAtoms; ++a)  // tokens 128a .. 128a+127 at columns +4a
+              tc_cp_32x128b_x4(sfb_t + 4 * a,
+                               smem_desc(smem_u32(smem + C::kOffSfb + s * C::kSfbStage +
+                                                  a * C::kSfBytes),
+                                         0, 128, kLayoutNone));
+          }
           const uint32_t a0 = smem_u32(smem + C::kOffA + s * C::kABytes);
           const uint32_t b0 = smem_u32(smem + C::kOffB + s * C::kBBytes);
 #pragma unroll
@@ -246,15 +264,25 @@ __global__ void __launch_bounds__(256, OCC)
     // sub-tile ko (token r of atom a at byte (r % 32) * 16 + ((r / 32) % 4) * 4 + ko).
     constexpr int NA = C::kSfbAtoms;
     const int kw = p.K / 32, kx = p.K / 128;
+    constexpr int REP = C::kWideSf ? 4 : 1;  // copies of each atom row (see GemmCfg)
+    constexpr int ATOM = C::kWideSf ? 2048 : C::kSfBytes;
     auto put_stage = [&](int s, const uint32_t (&wa)[KO][4], const uint32_t (&xb)[4 * NA]) {
 #pragma unroll
-      for (int ko = 0; ko < KO; ++ko)
-        *reinterpret_cast<uint4*>(smem + C::kOffSfa + (s * KO + ko) * C::kSfBytes + lane * 16) =
-            make_uint4(wa[ko][0], wa[ko][1], wa[ko][2], wa[ko][3]);
+      for (int ko = 0; ko < KO; ++ko) {
+        const uint4 v = make_uint4(wa[ko][0], wa[ko][1], wa[ko][2], wa[ko][3]);
 #pragma unroll
-      for (int a = 0; a < NA; ++a)
-        *reinterpret_cast<uint4*>(smem + C::kOffSfb + (s * NA + a) * C::kSfBytes + lane * 16) =
-            make_uint4(xb[4 * a], xb[4 * a + 1], xb[4 * a + 2], xb[4 * a + 3]);
+        for (int rep = 0; rep < REP; ++rep)
+          *reinterpret_cast<uint4*>(smem + C::kOffSfa + s * C::kSfaStage + ko * ATOM +
+                                    (rep * 32 + lane) * 16) = v;
+      }
+#pragma unroll
+      for (int a = 0; a < NA; ++a) {
+        const uint4 v = make_uint4(xb[4 * a], xb[4 * a + 1], xb[4 * a + 2], xb[4 * a + 3]);
+#pragma unroll
+        for (int rep = 0; rep < REP; ++rep)
+          *reinterpret_cast<uint4*>(smem + C::kOffSfb + s * C::kSfbStage + a * ATOM +
+                                    (rep * 32 + lane) * 16) = v;
+      }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&full[s]);
@@ -469,7 +497,7 @@ DevInfo& dev_info() {
 template <int BN_MAX, int STAGES, int KO, int OCC>
 cudaError_t launch_one(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmParams& p,
                        int max_items, cudaStream_t st) {
-  using C = GemmCfg<BN_MAX, STAGES, KO>;
+  using C = GemmCfg<BN_MAX, STAGES, KO, OCC>;
   auto kern = k_gemm_mx<BN_MAX, STAGES, KO, OCC>;
   static bool attr_set[64] = {};
   int dev = 0;
@@ -531,15 +559,18 @@ namespace {
 template <int BN, int ST2, int ST1, int OCC>
 cudaError_t launch_variant(const GemmLaunch& a, GemmParams p, const int4* items,
                            const int32_t* count, int max_items, cudaStream_t st) {
-  const bool two = (a.K / 128) % 2 == 0;
+  // ST2 == 0: this variant always stages one sub-tile at a time
+  const bool two = ST2 > 0 && (a.K / 128) % 2 == 0;
   CUtensorMap tmW, tmX;
-  if (gemm_encode_maps(a.w_codes, a.G, a.N, a.K, a.act, a.rows_total, two ? 2 : 1,
-                       two ? BN : 16, &tmW, &tmX) != MOE_OK)
+  if (gemm_encode_maps(a.w_codes, a.G, a.N, a.K, a.act, a.rows_total, two ? 2 : 1, BN, &tmW,
+                       &tmX) != MOE_OK)
     return cudaErrorInvalidValue;
   p.items = items;
   p.item_count = count;
-  return two ? launch_one<BN, ST2, 2, OCC>(tmW, tmX, p, max_items, st)
-             : launch_one<BN, ST1, 1, OCC>(tmW, tmX, p, max_items, st);
+  if constexpr (ST2 > 0) {
+    if (two) return launch_one<BN, ST2, 2, OCC>(tmW, tmX, p, max_items, st);
+  }
+  return launch_one<BN, ST1, 1, OCC>(tmW, tmX, p, max_items, st);
 }
 
 }  // namespace

@@ -8,8 +8,8 @@ namespace moe {
 // GEMM variants, chosen per group by its row count M (the tile plan):
 //   small  M <= 16: N = 16 tokens, 2 CTAs per SM, 3 stages of two 128-K sub-tiles;
 //   medium M <= 64: N <= 64, 2 CTAs per SM, 2 stages;
-//   large  M > 64: chunks of <= 224 rows (N = 224 MMAs carry 3.5x the tensor work of
-//          their issue cost), 1 CTA per SM, 2 stages.
+//   large  M > 64: chunks of <= 224 rows (an N = 224 MMA carries more tensor work than
+//          its issue cost), 1 CTA per SM, 2 stages.
 // With K/128 odd the stages hold one sub-tile (the *KO1 stage counts).
 constexpr int kSmallBN = 16;
 constexpr int kSmallStages = 3;
