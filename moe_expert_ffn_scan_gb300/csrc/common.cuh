@@ -39,6 +39,16 @@ __device__ __forceinline__ void set_status(uint32_t* status, uint32_t bits) {
   if (status) atomicOr(status, bits);
 }
 
+// ------------------------------------------------------------------ PDL -----------
+// Every kernel of the path is launched with programmatic stream serialisation: it may
+// start while its predecessor finishes, runs its prologue, then waits here for the
+// predecessor's results (griddepcontrol.wait returns once the previous grid has
+// completed and its memory is visible), and lets its own successor start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ mbarrier ------
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

@@ -48,6 +48,8 @@ __device__ __forceinline__ uint2 quant8(const float (&f)[8], uint8_t* scale_out,
 __global__ void __launch_bounds__(256) k_quant_act(const uint16_t* __restrict__ x, int rows,
                                                    int cols, uint8_t* __restrict__ q,
                                                    uint8_t* __restrict__ s) {
+  pdl_wait();
+  pdl_trigger();
   const int nblk = cols / 128;
   const long long gw = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31, half = lane >> 4, sub = lane & 15;
@@ -79,6 +81,8 @@ __global__ void __launch_bounds__(256) k_quant_scatter(const uint16_t* __restric
                                                        uint8_t* __restrict__ xg,
                                                        uint8_t* __restrict__ xsg,
                                                        uint32_t* status) {
+  pdl_wait();
+  pdl_trigger();
   const int nblk = H / 128;
   const long long gw = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31, half = lane >> 4, sub = lane & 15;
@@ -122,6 +126,8 @@ __global__ void __launch_bounds__(256) k_swiglu_quant(const uint16_t* __restrict
                                                       int rows, int I,
                                                       uint8_t* __restrict__ hq,
                                                       uint8_t* __restrict__ hs) {
+  pdl_wait();
+  pdl_trigger();
   const int nblk = I / 128;
   const long long gw = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31, half = lane >> 4, sub = lane & 15;
@@ -157,6 +163,8 @@ __global__ void __launch_bounds__(256) k_gather_rows(const uint8_t* __restrict__
                                                      uint8_t* __restrict__ xg,
                                                      uint8_t* __restrict__ xsg,
                                                      uint32_t* status) {
+  pdl_wait();
+  pdl_trigger();
   const long long r = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (r >= Rs) return;
@@ -180,6 +188,8 @@ __global__ void __launch_bounds__(128) k_combine(const uint16_t* __restrict__ y2
                                                  int H, int has_shared, int R, int Rs,
                                                  uint16_t* __restrict__ out,
                                                  uint32_t* status) {
+  pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.x;
   __shared__ int32_t s_row[16];
   __shared__ float s_w[16];
@@ -247,8 +257,7 @@ cudaError_t launch_quant_act(const uint16_t* x, int rows, int cols, uint8_t* q, 
                              cudaStream_t st) {
   long long nb = static_cast<long long>(rows) * (cols / 128);
   if (nb == 0) return cudaSuccess;
-  k_quant_act<<<grid_for_blocks(nb), 256, 0, st>>>(x, rows, cols, q, s);
-  return cudaGetLastError();
+  return launch_k(k_quant_act, grid_for_blocks(nb), 256, 0, st, x, rows, cols, q, s);
 }
 
 cudaError_t launch_quant_scatter(const uint16_t* x, int T, int H, int k, int has_shared,
@@ -256,17 +265,15 @@ cudaError_t launch_quant_scatter(const uint16_t* x, int T, int H, int k, int has
                                  uint8_t* xsg, uint32_t* status, cudaStream_t st) {
   long long nb = static_cast<long long>(T) * (H / 128);
   if (nb == 0) return cudaSuccess;
-  k_quant_scatter<<<grid_for_blocks(nb), 256, 0, st>>>(x, T, H, k, has_shared, inv, xq, xs, xg,
-                                                       xsg, status);
-  return cudaGetLastError();
+  return launch_k(k_quant_scatter, grid_for_blocks(nb), 256, 0, st, x, T, H, k, has_shared, inv,
+                  xq, xs, xg, xsg, status);
 }
 
 cudaError_t launch_swiglu_quant(const uint16_t* y13, int rows, int I, uint8_t* hq, uint8_t* hs,
                                 cudaStream_t st) {
   long long nb = static_cast<long long>(rows) * (I / 128);
   if (nb == 0) return cudaSuccess;
-  k_swiglu_quant<<<grid_for_blocks(nb), 256, 0, st>>>(y13, rows, I, hq, hs);
-  return cudaGetLastError();
+  return launch_k(k_swiglu_quant, grid_for_blocks(nb), 256, 0, st, y13, rows, I, hq, hs);
 }
 
 cudaError_t launch_gather_rows(const uint8_t* xq, const uint8_t* xs, const int32_t* perm_src,
@@ -274,8 +281,8 @@ cudaError_t launch_gather_rows(const uint8_t* xq, const uint8_t* xs, const int32
                                uint32_t* status, cudaStream_t st) {
   if (Rs == 0) return cudaSuccess;
   unsigned grid = static_cast<unsigned>((static_cast<long long>(Rs) + 7) / 8);
-  k_gather_rows<<<grid, 256, 0, st>>>(xq, xs, perm_src, T, k, R, Rs, H, xg, xsg, status);
-  return cudaGetLastError();
+  return launch_k(k_gather_rows, grid, 256, 0, st, xq, xs, perm_src, T, k, R, Rs, H, xg, xsg,
+                  status);
 }
 
 cudaError_t launch_combine(const uint16_t* y2, const int32_t* inv, const float* w, int T, int k,
@@ -285,8 +292,8 @@ cudaError_t launch_combine(const uint16_t* y2, const int32_t* inv, const float* 
   const int R = T * k, Rs = R + (has_shared ? T : 0);
   const int threads = 128;
   dim3 grid(T, (H + threads * 8 - 1) / (threads * 8));
-  k_combine<<<grid, threads, 0, st>>>(y2, inv, w, T, k, H, has_shared, R, Rs, out, status);
-  return cudaGetLastError();
+  return launch_k(k_combine, grid, threads, 0, st, y2, inv, w, T, k, H, has_shared, R, Rs, out,
+                  status);
 }
 
 }  // namespace moe

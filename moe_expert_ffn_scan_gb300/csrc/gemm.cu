@@ -143,6 +143,9 @@ __global__ void __launch_bounds__(256, OCC)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // prologue done: wait for the producer of the tile plan / activations
+  pdl_wait();
+  pdl_trigger();
   const uint32_t tmem = *tmem_slot;
 
   const int n_tiles = p.N / 128;
@@ -514,8 +517,7 @@ cudaError_t launch_one(const CUtensorMap& tmW, const CUtensorMap& tmX, const Gem
   const int grid = static_cast<int>(tiles < slots ? tiles : slots);
   GemmParams q = p;
   q.max_items = max_items;
-  kern<<<grid, 256, C::kSmemBytes, st>>>(tmW, tmX, q);
-  return cudaGetLastError();
+  return launch_k(kern, grid, 256, C::kSmemBytes, st, tmW, tmX, q);
 }
 
 }  // namespace

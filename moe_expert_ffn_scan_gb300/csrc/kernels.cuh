@@ -5,6 +5,23 @@
 
 namespace moe {
 
+// Launch with programmatic dependent launch enabled (see pdl_wait in common.cuh).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                     cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // GEMM variants, chosen per group by its row count M (the tile plan):
 //   small  M <= 16: N = 16 tokens, 2 CTAs per SM, 3 stages of two 128-K sub-tiles;
 //   medium M <= 64: N <= 64, 2 CTAs per SM, 2 stages;

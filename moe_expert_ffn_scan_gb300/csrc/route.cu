@@ -72,6 +72,8 @@ template <int EPL>
 __global__ void __launch_bounds__(256) k_route(const float* __restrict__ logits, int T, int E,
                                                int k, int32_t* __restrict__ idx,
                                                float* __restrict__ w) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -95,6 +97,8 @@ __global__ void __launch_bounds__(kPermTokens) k_hist_block(const int32_t* __res
                                                             int T, int E, int k,
                                                             int32_t* __restrict__ blockcnt,
                                                             uint32_t* status) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ int32_t s_cnt[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
   __syncthreads();
@@ -121,6 +125,8 @@ __global__ void __launch_bounds__(1024) k_scan(const int32_t* __restrict__ block
                                                int32_t* __restrict__ blockbase,
                                                int32_t* __restrict__ counts,
                                                int32_t* __restrict__ offsets) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int32_t s_part[1024];
   __shared__ int32_t s_warp[32];
   const int tid = threadIdx.x;
@@ -175,6 +181,8 @@ __global__ void __launch_bounds__(kPermTokens) k_permute_block(
     const int32_t* __restrict__ idx, int T, int E, int k, const int32_t* __restrict__ blockbase,
     const int32_t* __restrict__ offsets, int32_t* __restrict__ perm_src,
     int32_t* __restrict__ inv) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ uint32_t s_bits[];  // [8 warps][E] masks, then [8][E] warp bases
   constexpr int kWarps = kPermTokens / 32;
   int32_t* s_wbase = reinterpret_cast<int32_t*>(s_bits + kWarps * E);
@@ -299,6 +307,8 @@ __global__ void __launch_bounds__(1024) k_plan(const int32_t* __restrict__ offse
                                                int4* __restrict__ large_items,
                                                int32_t* __restrict__ item_counts,
                                                uint32_t* status) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int32_t s_warp[32];
   plan_groups(offsets, G, small_items, medium_items, large_items, item_counts, status, s_warp);
 }
@@ -317,6 +327,8 @@ __global__ void __launch_bounds__(1024) k_prep_small(
     int32_t* __restrict__ offsets, int32_t* __restrict__ perm_src, int32_t* __restrict__ inv,
     int4* __restrict__ small_items, int4* __restrict__ medium_items,
     int4* __restrict__ large_items, int32_t* __restrict__ item_counts, uint32_t* status) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int kWords = kPrepMaxT / 32;
   __shared__ uint32_t s_mask[1024 * kWords];  // [expert][token word]
   __shared__ int32_t s_idx[kPrepMaxT * 16];
@@ -391,8 +403,7 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* idx,
   const int epl = (E + 31) / 32;
 #define MOE_ROUTE_CASE(N) \
   if (epl <= N) {         \
-    k_route<N><<<grid, block, 0, st>>>(logits, T, E, k, idx, w); \
-    return cudaGetLastError(); \
+    return launch_k(k_route<N>, grid, block, 0, st, logits, T, E, k, idx, w); \
   }
   MOE_ROUTE_CASE(1)
   MOE_ROUTE_CASE(2)
@@ -412,26 +423,28 @@ cudaError_t launch_permute(const int32_t* idx, int T, int E, int k, int has_shar
                            int32_t* offsets, int32_t* perm_src, int32_t* inv, uint32_t* status,
                            cudaStream_t st) {
   const int nblk = perm_blocks(T);
-  k_hist_block<<<nblk, kPermTokens, E * sizeof(int32_t), st>>>(idx, T, E, k, blockcnt, status);
-  k_scan<<<1, 1024, 0, st>>>(blockcnt, nblk, T, E, has_shared, blockbase, counts, offsets);
+  cudaError_t e = launch_k(k_hist_block, nblk, kPermTokens, E * sizeof(int32_t), st, idx, T, E,
+                           k, blockcnt, status);
+  if (e != cudaSuccess) return e;
+  e = launch_k(k_scan, 1, 1024, 0, st, blockcnt, nblk, T, E, has_shared, blockbase, counts,
+               offsets);
+  if (e != cudaSuccess) return e;
   size_t smem = 2 * (kPermTokens / 32) * E * sizeof(uint32_t);
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(k_permute_block,
+    e = cudaFuncSetAttribute(k_permute_block,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  k_permute_block<<<nblk, kPermTokens, smem, st>>>(idx, T, E, k, blockbase, offsets, perm_src,
-                                                   inv);
-  return cudaGetLastError();
+  return launch_k(k_permute_block, nblk, kPermTokens, smem, st, idx, T, E, k, blockbase, offsets,
+                  perm_src, inv);
 }
 
 cudaError_t launch_plan(const int32_t* offsets, int G, int4* small_items, int4* medium_items,
                         int4* large_items, int32_t* item_counts, uint32_t* status,
                         cudaStream_t st) {
-  k_plan<<<1, 1024, 0, st>>>(offsets, G, small_items, medium_items, large_items, item_counts,
-                             status);
-  return cudaGetLastError();
+  return launch_k(k_plan, 1, 1024, 0, st, offsets, G, small_items, medium_items, large_items,
+                  item_counts, status);
 }
 
 cudaError_t launch_prep_small(const float* logits, int T, int E, int k, int has_shared,
@@ -443,10 +456,9 @@ cudaError_t launch_prep_small(const float* logits, int T, int E, int k, int has_
   const int epl = (E + 31) / 32;
 #define MOE_PREP_CASE(N)                                                                    \
   if (epl <= N) {                                                                           \
-    k_prep_small<N><<<1, 1024, 0, st>>>(logits, T, E, k, has_shared, idx, w, counts,        \
-                                        offsets, perm_src, inv, small_items, medium_items,  \
-                                        large_items, item_counts, status);                  \
-    return cudaGetLastError();                                                              \
+    return launch_k(k_prep_small<N>, 1, 1024, 0, st, logits, T, E, k, has_shared, idx, w,   \
+                    counts, offsets, perm_src, inv, small_items, medium_items, large_items, \
+                    item_counts, status);                                                   \
   }
   MOE_PREP_CASE(1)
   MOE_PREP_CASE(2)
