@@ -205,8 +205,7 @@ int moe_route(const moe_dims* d, const float* logits, int32_t* idx, float* w, in
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   Carver c(ws);
   RouteWs rw = carve_route(c, d);
-  if (cudaMemsetAsync(rw.status, 0, sizeof(uint32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
-  cudaError_t e = launch_route(logits, d->T, d->E, d->k, idx, w, st);
+  cudaError_t e = launch_route(logits, d->T, d->E, d->k, idx, w, rw.status, st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   e = launch_permute(idx, d->T, d->E, d->k, d->has_shared, rw.blockcnt, rw.blockbase, counts,
                      offsets, perm_src, inv, rw.status, st);
@@ -321,8 +320,7 @@ int moe_forward_timed(const moe_dims* d, const uint16_t* x, const float* logits,
   }
   const int T = d->T, H = d->H, I = d->I, E = d->E, k = d->k;
   const int R = static_cast<int>(rows_R(d)), Rs = static_cast<int>(rows_Rs(d));
-  uint32_t* status = f.route.status;
-  if (cudaMemsetAsync(status, 0, sizeof(uint32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
+  uint32_t* status = f.route.status;  // cleared by the first kernel below
   auto mark = [&](int i) -> bool {
     return !events || cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st) == cudaSuccess;
   };
@@ -340,7 +338,7 @@ int moe_forward_timed(const moe_dims* d, const uint16_t* x, const float* logits,
                               f.gemm.plan.medium_items, f.gemm.plan.large_items,
                               f.gemm.plan.counts, status, st))
   } else {
-    MOE_TRY(launch_route(logits, T, E, k, f.idx, f.w, st))
+    MOE_TRY(launch_route(logits, T, E, k, f.idx, f.w, status, st))
     MOE_TRY(launch_permute(f.idx, T, E, k, d->has_shared, f.route.blockcnt, f.route.blockbase,
                            f.counts, f.offsets, f.perm_src, f.inv, status, st))
   }

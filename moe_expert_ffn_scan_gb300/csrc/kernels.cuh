@@ -52,7 +52,7 @@ cudaError_t launch_quant_scatter(const uint16_t* x, int T, int H, int k, int has
                                  const int32_t* inv, uint8_t* xq, uint8_t* xs, uint8_t* xg,
                                  uint8_t* xsg, uint32_t* status, cudaStream_t st);
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* idx, float* w,
-                         cudaStream_t st);
+                         uint32_t* clear_status, cudaStream_t st);
 int perm_blocks(int T);
 cudaError_t launch_permute(const int32_t* idx, int T, int E, int k, int has_shared,
                            int32_t* blockcnt, int32_t* blockbase, int32_t* counts,

@@ -71,9 +71,11 @@ __device__ __forceinline__ void route_token(const float* __restrict__ row, int E
 template <int EPL>
 __global__ void __launch_bounds__(256) k_route(const float* __restrict__ logits, int T, int E,
                                                int k, int32_t* __restrict__ idx,
-                                               float* __restrict__ w) {
+                                               float* __restrict__ w, uint32_t* clear_status) {
   pdl_wait();
   pdl_trigger();
+  // the first kernel of a call clears the call's status word
+  if (clear_status && blockIdx.x == 0 && threadIdx.x == 0) *clear_status = 0;
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -329,6 +331,9 @@ __global__ void __launch_bounds__(1024) k_prep_small(
     int4* __restrict__ large_items, int32_t* __restrict__ item_counts, uint32_t* status) {
   pdl_wait();
   pdl_trigger();
+  // the first kernel of a call clears the call's status word (before anything sets it)
+  if (threadIdx.x == 0) *status = 0;
+  __syncthreads();
   constexpr int kWords = kPrepMaxT / 32;
   __shared__ uint32_t s_mask[1024 * kWords];  // [expert][token word]
   __shared__ int32_t s_idx[kPrepMaxT * 16];
@@ -397,13 +402,13 @@ __global__ void __launch_bounds__(1024) k_prep_small(
 // ---------------------------------------------------------------- launchers -------
 
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* idx, float* w,
-                         cudaStream_t st) {
+                         uint32_t* clear_status, cudaStream_t st) {
   const int warps = 8;
   dim3 grid((T + warps - 1) / warps), block(32 * warps);
   const int epl = (E + 31) / 32;
 #define MOE_ROUTE_CASE(N) \
   if (epl <= N) {         \
-    return launch_k(k_route<N>, grid, block, 0, st, logits, T, E, k, idx, w); \
+    return launch_k(k_route<N>, grid, block, 0, st, logits, T, E, k, idx, w, clear_status); \
   }
   MOE_ROUTE_CASE(1)
   MOE_ROUTE_CASE(2)

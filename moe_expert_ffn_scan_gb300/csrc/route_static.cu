@@ -76,9 +76,8 @@ extern "C" int moe_route_static(const moe_dims* d, const float* logits, int32_t*
   int32_t* blockbase = reinterpret_cast<int32_t*>(b + kStatusBytes + table_al);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // blockcnt and blockbase are fully rewritten by every call; only the status word
-  // must start at zero.
-  if (cudaMemsetAsync(status, 0, sizeof(uint32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
-  if (moe::launch_route(logits, d->T, d->E, d->k, idx, w, st) != cudaSuccess)
+  // must start at zero (the routing kernel clears it).
+  if (moe::launch_route(logits, d->T, d->E, d->k, idx, w, status, st) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (moe::launch_permute(idx, d->T, d->E, d->k, d->has_shared, blockcnt, blockbase, counts,
                           offsets, perm_src, inv, status, st) != cudaSuccess)
