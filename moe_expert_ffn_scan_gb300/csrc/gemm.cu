@@ -19,9 +19,11 @@
 //   * Scale factors (weights: 4 per row per 128-K stage; activations: one per row per
 //     128-K stage, replicated over the four 32-blocks) are rearranged by one warp
 //     into the 128-row scale-factor atom and copied to TMEM with tcgen05.cp.
-//   * Warp-specialised, persistent CTAs: warp 0 issues TMA, warp 1 issues MMAs, warp
-//     2 stages scale factors, warps 4-7 drain the double-buffered TMEM accumulator
-//     (fp32 -> bf16) while the next tile's MMAs run.
+//   * Warp-specialised, persistent CTAs: warp 0 issues TMA (the weight tiles; in the
+//     large variant warp 3 issues the token tiles), warp 1 issues MMAs, warp 2 stages
+//     scale factors (own barrier, so their TMEM copies issue before the tiles land),
+//     warps 4-7 drain the double-buffered TMEM accumulator (fp32 -> bf16) while the
+//     next tile's MMAs run.
 //   * Every wait is bounded; an expired wait sets a status bit and the CTA unwinds.
 #include <mutex>
 
@@ -73,7 +75,13 @@ struct GemmCfg {
   static constexpr int kOffA = kWideSf ? (kSfTotal + 1023) / 1024 * 1024 : 0;
   static constexpr int kOffB = kOffA + STAGES * kABytes;
   static constexpr int kOffBar = kWideSf ? kOffB + STAGES * kBBytes : kOffSfa + kSfTotal;
-  static constexpr int kNumBars = 2 * STAGES + 4;
+  static constexpr int kNumBars = 3 * STAGES + 4;
+  // Large variant: token tiles (up to 56 KB a stage) get their own TMA thread, and the
+  // scale factors their own barrier, so the MMA thread issues the scale copies while
+  // the tiles are still landing (measured: -0.5 ms on the 32K-token layer; the
+  // small and medium variants measured no better and keep one barrier per stage).
+  static constexpr bool kTokenThread = BN_MAX > 64;
+  static constexpr bool kSfFirst = BN_MAX > 64;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16;
   static constexpr int kSfCols = 4 * (KO + kSfbAtoms);      // TMEM columns per stage
@@ -120,6 +128,7 @@ __global__ void __launch_bounds__(256, OCC)
   uint64_t* empty = bars + STAGES;
   uint64_t* acc_full = bars + 2 * STAGES;
   uint64_t* acc_empty = bars + 2 * STAGES + 2;
+  uint64_t* sf_full = bars + 2 * STAGES + 4;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
@@ -127,8 +136,10 @@ __global__ void __launch_bounds__(256, OCC)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 2);   // TMA arrive(+tx) and the scale-factor warp
-      mbar_init(&empty[s], 1);  // tcgen05.commit
+      // TMA arrival(s) (+tx), and the scale-factor warp unless it has its own barrier
+      mbar_init(&full[s], (C::kTokenThread ? 2 : 1) + (C::kSfFirst ? 0 : 1));
+      mbar_init(&empty[s], 1);    // tcgen05.commit
+      mbar_init(&sf_full[s], 1);  // the scale-factor warp (kSfFirst)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -145,7 +156,6 @@ __global__ void __launch_bounds__(256, OCC)
   tc_fence_after();
   // prologue done: wait for the producer of the tile plan / activations
   pdl_wait();
-  pdl_trigger();
   const uint32_t tmem = *tmem_slot;
 
   const int n_tiles = p.N / 128;
@@ -179,14 +189,36 @@ __global__ void __launch_bounds__(256, OCC)
       for (long long L = blockIdx.x; L < total && !*abort_flag; L += gridDim.x) {
         int g, row0, rows, nt;
         if (!load_item(L, g, row0, rows, nt)) continue;
-        const int bn = (rows + 15) & ~15;
-        const uint32_t tx = KO * kWeightTileTxBytes + BN_MAX * KO * 128;
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1u;
           if (it >= STAGES && !mbar_wait(&empty[s], ph ^ 1u, p.status, abort_flag)) break;
-          mbar_arrive_expect_tx(&full[s], tx);
-          tma_load_4d(smem + C::kOffA + s * C::kABytes, &tmW, &full[s], 0, nt * 128, kb * KO, g);
+          if constexpr (C::kTokenThread) {
+            mbar_arrive_expect_tx(&full[s], KO * kWeightTileTxBytes);
+            tma_load_4d(smem + C::kOffA + s * C::kABytes, &tmW, &full[s], 0, nt * 128, kb * KO,
+                        g);
+          } else {
+            mbar_arrive_expect_tx(&full[s], KO * kWeightTileTxBytes + BN_MAX * KO * 128);
+            tma_load_4d(smem + C::kOffA + s * C::kABytes, &tmW, &full[s], 0, nt * 128, kb * KO,
+                        g);
+            tma_load_3d(smem + C::kOffB + s * C::kBBytes, &tmX, &full[s], 0, row0, kb * KO);
+          }
+        }
+      }
+    }
+  } else if (warp == 3 && C::kTokenThread) {
+    // ---------------------------------------------------------------- token TMA
+    // (its own thread, so the weight stream's issue slots carry weight loads only)
+    if (lane == 0) {
+      uint32_t it = 0;
+      for (long long L = blockIdx.x; L < total && !*abort_flag; L += gridDim.x) {
+        int g, row0, rows, nt;
+        if (!load_item(L, g, row0, rows, nt)) continue;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1u;
+          if (it >= STAGES && !mbar_wait(&empty[s], ph ^ 1u, p.status, abort_flag)) break;
+          mbar_arrive_expect_tx(&full[s], BN_MAX * KO * 128);
           tma_load_3d(smem + C::kOffB + s * C::kBBytes, &tmX, &full[s], 0, row0, kb * KO);
         }
       }
@@ -208,7 +240,7 @@ __global__ void __launch_bounds__(256, OCC)
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1u;
-          if (!mbar_wait(&full[s], ph, p.status, abort_flag)) {
+          if (!mbar_wait(C::kSfFirst ? &sf_full[s] : &full[s], ph, p.status, abort_flag)) {
             ok = false;
             break;
           }
@@ -238,6 +270,13 @@ __global__ void __launch_bounds__(256, OCC)
                                smem_desc(smem_u32(smem + C::kOffSfb + s * C::kSfbStage +
                                                   a * C::kSfBytes),
                                          0, 128, kLayoutNone));
+          }
+          if (C::kSfFirst) {
+            if (!mbar_wait(&full[s], ph, p.status, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
           }
           const uint32_t a0 = smem_u32(smem + C::kOffA + s * C::kABytes);
           const uint32_t b0 = smem_u32(smem + C::kOffB + s * C::kBBytes);
@@ -288,7 +327,7 @@ __global__ void __launch_bounds__(256, OCC)
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&full[s]);
+      if (lane == 0) mbar_arrive(C::kSfFirst ? &sf_full[s] : &full[s]);
     };
     auto wait_slot = [&](uint32_t it) -> bool {
       if (it < STAGES) return true;
@@ -453,6 +492,9 @@ __global__ void __launch_bounds__(256, OCC)
     }
   }
 
+  // Let the next kernel's CTAs in only now, so that none of them sits on an SM waiting
+  // for this grid for the whole GEMM; the overlap left is this grid's drain.
+  pdl_trigger();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -517,7 +559,10 @@ cudaError_t launch_one(const CUtensorMap& tmW, const CUtensorMap& tmX, const Gem
   const int grid = static_cast<int>(tiles < slots ? tiles : slots);
   GemmParams q = p;
   q.max_items = max_items;
-  return launch_k(kern, grid, 256, C::kSmemBytes, st, tmW, tmX, q);
+  // The large variant (one CTA per SM) runs ~8% slower at 32K tokens when launched as a
+  // programmatic dependent (measured; cause not identified), so it waits for its
+  // predecessor the plain way.  The small and medium variants keep the overlap.
+  return launch_k_pdl(BN_MAX <= 64, kern, grid, 256, C::kSmemBytes, st, tmW, tmX, q);
 }
 
 }  // namespace

@@ -5,10 +5,12 @@
 
 namespace moe {
 
-// Launch with programmatic dependent launch enabled (see pdl_wait in common.cuh).
+// Launch with programmatic dependent launch enabled or not (see pdl_wait in
+// common.cuh; without it, pdl_wait returns at once because the stream has already
+// ordered the launch after its predecessor).
 template <typename... KArgs, typename... Args>
-cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                     cudaStream_t st, Args... args) {
+cudaError_t launch_k_pdl(bool pdl, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                         cudaStream_t st, Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -16,10 +18,15 @@ cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                     cudaStream_t st, Args... args) {
+  return launch_k_pdl(true, kern, grid, block, smem, st, args...);
 }
 
 // GEMM variants, chosen per group by its row count M (the tile plan):

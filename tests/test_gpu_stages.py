@@ -146,6 +146,9 @@ GEMM_SHAPES = [
     ("w2", 3, 1024, 3072, [1, 40, 200]),
     ("w13", 5, 512, 512, [0, 16, 64, 65, 129]),
     ("w13", 2, 256, 512, [224, 150]),
+    # more small-group tiles than one wave of CTAs: full waves, then a split last wave
+    ("w13", 40, 1024, 640, [(i * 7) % 17 for i in range(40)]),
+    ("w2", 24, 2048, 1536, [(i * 5) % 16 + 1 for i in range(24)]),
 ]
 
 
