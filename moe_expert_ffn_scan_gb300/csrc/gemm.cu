@@ -75,23 +75,35 @@ struct GemmCfg {
   static constexpr int kOffA = kWideSf ? (kSfTotal + 1023) / 1024 * 1024 : 0;
   static constexpr int kOffB = kOffA + STAGES * kABytes;
   static constexpr int kOffBar = kWideSf ? kOffB + STAGES * kBBytes : kOffSfa + kSfTotal;
-  static constexpr int kNumBars = 3 * STAGES + 4;
   // Large variant: token tiles (up to 56 KB a stage) get their own TMA thread, and the
   // scale factors their own barrier, so the MMA thread issues the scale copies while
   // the tiles are still landing (measured: -0.5 ms on the 32K-token layer; the
   // small and medium variants measured no better and keep one barrier per stage).
   static constexpr bool kTokenThread = BN_MAX > 64;
   static constexpr bool kSfFirst = BN_MAX > 64;
+  // Small variant: two MMA-issuing threads (warps 1 and 3) take the even and odd K
+  // stages of a tile into two accumulators that the epilogue adds, so a stage waits
+  // for half as much MMA issue before its shared memory is released.  (The medium
+  // variant's second accumulators would not fit two CTAs' TMEM.)
+  static constexpr int kIssuers = BN_MAX <= 16 ? 2 : 1;
+  static constexpr int kAccCols = kIssuers * BN_MAX;  // one accumulator buffer
+  // full[issuer][stage] (each issuer waits only on its own, so it sees every phase of
+  // every barrier it waits on), empty[stage], acc_full[2], acc_empty[2], sf_full[stage]
+  static constexpr int kNumBars = (kIssuers + 2) * STAGES + 4;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16;
   static constexpr int kSfCols = 4 * (KO + kSfbAtoms);      // TMEM columns per stage
-  static constexpr int kTmemNeed = 2 * BN_MAX + STAGES * kSfCols;
+  static constexpr int kTmemNeed = 2 * kAccCols + STAGES * kSfCols;
   static constexpr int kTmemCols =
       kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128 : kTmemNeed <= 256 ? 256 : 512;
   static_assert(BN_MAX % 16 == 0 && BN_MAX <= 256, "token tile");
   static_assert(KO == 1 || KO == 2 || KO == 4, "sub-tiles per stage");
   static_assert(!kWideSf || (KO <= 2 && kSfbAtoms <= 2), "wide scale copies move <= 256 bits");
   static_assert(kTmemNeed <= 512, "TMEM");
+  static_assert(kTmemCols * OCC <= 512, "co-resident CTAs must fit TMEM together");
+  static_assert(OCC == 1 || OCC * (kSmemBytes + 1024) <= 233472,
+                "co-resident CTAs must fit shared memory together");
+  static_assert(!(kTokenThread && kIssuers > 1), "warp 3 has one role");
 };
 
 // Instruction descriptor, kind::mxf8f6f4 block-scaled: A = E2M1 (5), B = E4M3 (0),
@@ -124,25 +136,26 @@ __global__ void __launch_bounds__(256, OCC)
     return;
   }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
-  uint64_t* full = bars;
-  uint64_t* empty = bars + STAGES;
-  uint64_t* acc_full = bars + 2 * STAGES;
-  uint64_t* acc_empty = bars + 2 * STAGES + 2;
-  uint64_t* sf_full = bars + 2 * STAGES + 4;
+  uint64_t* full = bars;  // [kIssuers][STAGES]: stage kb goes to issuer kb % kIssuers
+  uint64_t* empty = full + C::kIssuers * STAGES;
+  uint64_t* acc_full = empty + STAGES;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* sf_full = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < C::kIssuers * STAGES; ++s)
       // TMA arrival(s) (+tx), and the scale-factor warp unless it has its own barrier
       mbar_init(&full[s], (C::kTokenThread ? 2 : 1) + (C::kSfFirst ? 0 : 1));
+    for (int s = 0; s < STAGES; ++s) {
       mbar_init(&empty[s], 1);    // tcgen05.commit
       mbar_init(&sf_full[s], 1);  // the scale-factor warp (kSfFirst)
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_full[b], C::kIssuers);  // one tcgen05.commit per issuer
       mbar_init(&acc_empty[b], 4);  // four epilogue warps
     }
     *abort_flag = 0;
@@ -193,15 +206,14 @@ __global__ void __launch_bounds__(256, OCC)
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1u;
           if (it >= STAGES && !mbar_wait(&empty[s], ph ^ 1u, p.status, abort_flag)) break;
+          uint64_t* fb = &full[(kb % C::kIssuers) * STAGES + s];
           if constexpr (C::kTokenThread) {
-            mbar_arrive_expect_tx(&full[s], KO * kWeightTileTxBytes);
-            tma_load_4d(smem + C::kOffA + s * C::kABytes, &tmW, &full[s], 0, nt * 128, kb * KO,
-                        g);
+            mbar_arrive_expect_tx(fb, KO * kWeightTileTxBytes);
+            tma_load_4d(smem + C::kOffA + s * C::kABytes, &tmW, fb, 0, nt * 128, kb * KO, g);
           } else {
-            mbar_arrive_expect_tx(&full[s], KO * kWeightTileTxBytes + BN_MAX * KO * 128);
-            tma_load_4d(smem + C::kOffA + s * C::kABytes, &tmW, &full[s], 0, nt * 128, kb * KO,
-                        g);
-            tma_load_3d(smem + C::kOffB + s * C::kBBytes, &tmX, &full[s], 0, row0, kb * KO);
+            mbar_arrive_expect_tx(fb, KO * kWeightTileTxBytes + BN_MAX * KO * 128);
+            tma_load_4d(smem + C::kOffA + s * C::kABytes, &tmW, fb, 0, nt * 128, kb * KO, g);
+            tma_load_3d(smem + C::kOffB + s * C::kBBytes, &tmX, fb, 0, row0, kb * KO);
           }
         }
       }
@@ -223,10 +235,14 @@ __global__ void __launch_bounds__(256, OCC)
         }
       }
     }
-  } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
+  } else if (warp == 1 || (C::kIssuers == 2 && warp == 3)) {
+    // ---------------------------------------------------------------- MMA issuer(s)
+    // Issuer `par` takes the stages kb with kb % kIssuers == par into its own
+    // accumulator; every issuer walks every stage to keep the ring's phase.
+    const int par = warp == 1 ? 0 : 1;
     if (lane == 0) {
       uint32_t it = 0, tc = 0;
+      uint32_t phases = 0;  // bit s: parity of the next phase of full[par][s] to wait for
       for (long long L = blockIdx.x; L < total && !*abort_flag; L += gridDim.x) {
         int g, row0, rows, nt;
         if (!load_item(L, g, row0, rows, nt)) continue;
@@ -234,18 +250,21 @@ __global__ void __launch_bounds__(256, OCC)
         const uint32_t b = tc & 1u, use = tc >> 1;
         if (tc >= 2 && !mbar_wait(&acc_empty[b], (use - 1) & 1u, p.status, abort_flag)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem + b * BN_MAX;
+        const uint32_t d_tmem = tmem + b * C::kAccCols + par * BN_MAX;
         const uint32_t idesc = idesc_mxf4_e4m3(bn);
         bool ok = true;
         for (int kb = 0; kb < nk; ++kb, ++it) {
+          if (C::kIssuers == 2 && (kb & 1) != par) continue;
           const int s = it % STAGES;
-          const uint32_t ph = (it / STAGES) & 1u;
-          if (!mbar_wait(C::kSfFirst ? &sf_full[s] : &full[s], ph, p.status, abort_flag)) {
+          const uint32_t ph = (phases >> s) & 1u;
+          phases ^= 1u << s;
+          uint64_t* fb = &full[par * STAGES + s];
+          if (!mbar_wait(C::kSfFirst ? &sf_full[s] : fb, ph, p.status, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sf_t = tmem + 2 * BN_MAX + s * C::kSfCols;
+          const uint32_t sf_t = tmem + 2 * C::kAccCols + s * C::kSfCols;
           const uint32_t sfb_t = sf_t + 4 * KO;
           if constexpr (C::kWideSf) {
             // [KO][128 rows][16 B] -> KO * 4 columns; [NA][128][16 B] -> NA * 4 columns
@@ -272,7 +291,7 @@ __global__ void __launch_bounds__(256, OCC)
                                          0, 128, kLayoutNone));
           }
           if (C::kSfFirst) {
-            if (!mbar_wait(&full[s], ph, p.status, abort_flag)) {
+            if (!mbar_wait(fb, ph, p.status, abort_flag)) {
               ok = false;
               break;
             }
@@ -289,7 +308,8 @@ __global__ void __launch_bounds__(256, OCC)
               // A scale: byte kk (32-K block) of the sub-tile's atom; B scale: byte ko.
               const uint32_t id = idesc | (static_cast<uint32_t>(kk) << 29) |
                                   (static_cast<uint32_t>(ko) << 4);
-              mma_mxf8f6f4(d_tmem, ad, bd, id, sf_t + 4 * ko, sfb_t, (kb | ko | kk) != 0);
+              mma_mxf8f6f4(d_tmem, ad, bd, id, sf_t + 4 * ko, sfb_t,
+                           kb > par || ko != 0 || kk != 0);
             }
           }
           tc_commit(&empty[s]);
@@ -308,7 +328,8 @@ __global__ void __launch_bounds__(256, OCC)
     const int kw = p.K / 32, kx = p.K / 128;
     constexpr int REP = C::kWideSf ? 4 : 1;  // copies of each atom row (see GemmCfg)
     constexpr int ATOM = C::kWideSf ? 2048 : C::kSfBytes;
-    auto put_stage = [&](int s, const uint32_t (&wa)[KO][4], const uint32_t (&xb)[4 * NA]) {
+    auto put_stage = [&](int s, int kb, const uint32_t (&wa)[KO][4],
+                         const uint32_t (&xb)[4 * NA]) {
 #pragma unroll
       for (int ko = 0; ko < KO; ++ko) {
         const uint4 v = make_uint4(wa[ko][0], wa[ko][1], wa[ko][2], wa[ko][3]);
@@ -327,7 +348,8 @@ __global__ void __launch_bounds__(256, OCC)
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(C::kSfFirst ? &sf_full[s] : &full[s]);
+      if (lane == 0)
+        mbar_arrive(C::kSfFirst ? &sf_full[s] : &full[(kb % C::kIssuers) * STAGES + s]);
     };
     auto wait_slot = [&](uint32_t it) -> bool {
       if (it < STAGES) return true;
@@ -411,7 +433,7 @@ __global__ void __launch_bounds__(256, OCC)
                 xb[j] = 0x7F7F7F7Fu;
               }
             }
-            put_stage(it % STAGES, wa, xb);
+            put_stage(it % STAGES, cs.kq * SPQ + b, wa, xb);
             ++it;
           }
           if (!ok) break;
@@ -454,7 +476,7 @@ __global__ void __launch_bounds__(256, OCC)
             }
             xb[j] = packed;
           }
-          put_stage(it % STAGES, wa, xb);
+          put_stage(it % STAGES, kb, wa, xb);
         }
         if (!ok) break;
       }
@@ -473,14 +495,24 @@ __global__ void __launch_bounds__(256, OCC)
       tc_fence_after();
       const int n = nt * 128 + q * 32 + lane;
       uint16_t* ycol = p.y + static_cast<size_t>(row0) * p.N + n;
+      const uint32_t acc = tmem + (static_cast<uint32_t>(q * 32) << 16) + b * C::kAccCols;
       for (int c0 = 0; c0 < rows; c0 += 16) {
         uint32_t r[16];
-        tmem_ld_32x32b_x16(tmem + (static_cast<uint32_t>(q * 32) << 16) + b * BN_MAX + c0, r);
+        float v[16];
+        tmem_ld_32x32b_x16(acc + c0, r);
         tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+        if (C::kIssuers == 2 && nk > 1) {  // even-stage + odd-stage sums, in that order
+          tmem_ld_32x32b_x16(acc + BN_MAX + c0, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] += __uint_as_float(r[i]);
+        }
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           if (c0 + i < rows) {
-            __nv_bfloat16 h = __float2bfloat16_rn(__uint_as_float(r[i]));
+            __nv_bfloat16 h = __float2bfloat16_rn(v[i]);
             ycol[static_cast<size_t>(c0 + i) * p.N] = *reinterpret_cast<uint16_t*>(&h);
           }
         }

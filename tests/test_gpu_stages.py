@@ -149,6 +149,8 @@ GEMM_SHAPES = [
     # more small-group tiles than one wave of CTAs: full waves, then a split last wave
     ("w13", 40, 1024, 640, [(i * 7) % 17 for i in range(40)]),
     ("w2", 24, 2048, 1536, [(i * 5) % 16 + 1 for i in range(24)]),
+    # decode-like: long K (28 two-sub-tile stages), 1-7 rows per group
+    ("w13", 6, 1024, 7168, [1, 2, 7, 1, 0, 3]),
 ]
 
 
