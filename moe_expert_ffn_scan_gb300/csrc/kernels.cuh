@@ -43,9 +43,9 @@ constexpr int kMediumBN = 64;
 constexpr int kMediumStages = 2;
 constexpr int kMediumStagesKO1 = 4;
 constexpr int kMediumOcc = 2;
-constexpr int kLargeBN = 224;
+constexpr int kLargeBN = 240;
 constexpr int kLargeStages = 2;
-constexpr int kLargeStagesKO1 = 4;
+constexpr int kLargeStagesKO1 = 2;
 
 // Token count up to which route + histogram + permute + plan run as one CTA.
 constexpr int kPrepMaxT = 128;

@@ -230,13 +230,14 @@ def test_combine(T, H, k, sh):
 
 
 @pytest.mark.parametrize("K", [512, 384])
-def test_grouped_gemm_token_scales_beyond_128_rows(K):
-    """One chunk of 224 token rows (two token-scale atoms): every row gets its own
-    activation scale byte, integer codes keep the result exact."""
+@pytest.mark.parametrize("M", [224, 240])
+def test_grouped_gemm_token_scales_beyond_128_rows(K, M):
+    """One large-variant chunk of M token rows (two token-scale atoms): every row gets
+    its own activation scale byte, integer codes keep the result exact."""
     G, N = 1, 256
-    sizes = [224]
+    sizes = [M]
     offsets, aq, asc, wq, wsc = _gemm_case(G, N, K, sizes, seed=7, integer=True)
-    asc = (125 + (torch.arange(224).view(224, 1) * 7 + torch.arange(K // 128).view(1, -1)) % 5
+    asc = (125 + (torch.arange(M).view(M, 1) * 7 + torch.arange(K // 128).view(1, -1)) % 5
            ).to(torch.uint8)
     wsc = (124 + torch.randint(0, 5, wsc.shape, generator=torch.Generator().manual_seed(3))
            ).to(torch.uint8)
