@@ -130,7 +130,7 @@ def fp8_tensor_peak_tflops():
 # one small-M W13 GEMM launch, from the ncu capture summarised in
 # profiles/k_gemm_mx_small_decode_T7_E64.md, keyed by the hash of the GEMM sources it
 # was taken on.  A changed kernel reports traffic null until it is captured again.
-NCU_SMALL_W13_TRAFFIC = {"src": "ff126315dea36758", "bytes_per_group": (966.53e6 + 3.78e6) / 41}
+NCU_SMALL_W13_TRAFFIC = {"src": "3e50a81bb12b5987", "bytes_per_group": (966.91e6 + 3.87e6) / 41}
 
 
 def gemm_src_hash():
