@@ -201,6 +201,22 @@ def mxfp4_dequant(codes, scales):
 
 
 # ---------------------------------------------------------------------------
+# f4: router gate projection (the scores the TopK step ranks)
+# ---------------------------------------------------------------------------
+
+def router_logits(x_bf16_bits, wg):
+    """logits[t, e] = sum_h x[t, h] * W_g[e, h], summed in float64 and rounded once
+    to float32.  x is the bf16 hidden state [T, H], W_g the fp32 gate weight [E, H].
+
+    The TopK step of the LMSYS H20 post (§3.2) ranks per-expert router scores; the
+    pages do not print the gate, so it is read as the plain linear projection of the
+    token's hidden state, kept in fp32 (the precision its output is handed on in)."""
+    x = bf16_bits_to_f64(x_bf16_bits)
+    w = np.asarray(wg, dtype=np.float32).astype(np.float64)
+    return f32_round(x @ w.T)
+
+
+# ---------------------------------------------------------------------------
 # a1: top-k routing
 # ---------------------------------------------------------------------------
 
