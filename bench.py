@@ -232,7 +232,12 @@ def host_view(d, t):
     """Callables giving the oracle numpy views of the layer inputs (weights copied to
     the host only for the experts a sample touches)."""
     x = t["x"].cpu().view(torch.int16).numpy().view(np.uint16)
-    lg = t["logits"].cpu().numpy()
+    if t.get("wg") is not None:
+        # logits that are the gate projection of x: the oracle projects them itself
+        from oracle import moe_oracle as o
+        lg = o.router_logits(x, t["wg"].cpu().numpy()).astype(np.float32)
+    else:
+        lg = t["logits"].cpu().numpy()
 
     def w_get(experts):
         shp = lambda n: (d.G,) + tuple(t[n].shape[1:])
@@ -300,6 +305,9 @@ def run_ours(args, rank, world, local):
     moe.lib()
     dev = torch.device("cuda", local)
     d, t = make_layer(args, args.seed + rank, dev)
+    if t["logits"] is None:  # logits are the gate projection of x: the library's router
+        t["logits"] = torch.empty(d.T, d.E, dtype=torch.float32, device=dev)
+        moe.moe_router_logits(t["x"], t["wg"], t["logits"])
     md = moe.dims(d.T, d.H, d.I, d.E, d.k, d.has_shared)
     layer = moe.MoELayer(d.H, d.I, d.E, d.k, d.has_shared, t["w13"], t["w13_s"], t["w2"],
                          t["w2_s"])

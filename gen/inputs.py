@@ -19,7 +19,9 @@ uniform over the 16 codes), E8M0 scale bytes uniform over {123..127} (exponent
 uniform in [-4, 0]).  Activations are bf16 N(0, 1).
 
 Router logits:
-  tiny:            logits = fp32(x . W_g^T), W_g fp32 ~ N(0, 0.02), product in fp64;
+  tiny:            logits = the gate projection x . W_g^T with W_g fp32 ~ N(0, 0.02);
+      this module draws W_g only, the projection is a step of the method (the
+      oracle computes it in the tests, the library's router kernel in the benchmark);
   decode:          logits fp32 ~ N(0, 1);
   decode256/prefill: logits = fp32(bias_e + g), g standard Gumbel noise and
       bias_e = -1.1 * ln(rank(e)), rank from a seeded permutation of the experts;
@@ -110,12 +112,20 @@ def zipf_logits(T, E, seed, device, s=1.1):
     return (bias[None, :] + gumbel).to(torch.float32)
 
 
+def gate_weight(E, H, seed, device):
+    """Router gate weight W_g fp32 [E, H], N(0, 0.02^2) entries."""
+    return (torch.randn(E, H, generator=_gen(seed, "gate", "cpu"), dtype=torch.float32)
+            * 0.02).to(device)
+
+
 def router_logits(kind, x, E, seed, device):
+    """Router logits drawn directly ("normal", "zipf"); for "gate" the logits are the
+    gate projection of x, which is a step of the method, not of input generation: the
+    layer then carries W_g (`gate_weight`) and logits None, and the caller projects
+    (the oracle in the tests, the library's router kernel in the benchmark)."""
     T, H = x.shape
     if kind == "gate":
-        wg = torch.randn(E, H, generator=_gen(seed, "gate", "cpu"), dtype=torch.float32) * 0.02
-        lg = (x.detach().cpu().double() @ wg.double().T).float()
-        return lg.to(device)
+        return None
     if kind == "normal":
         return torch.randn(T, E, generator=_gen(seed, "logits", device), device=device,
                            dtype=torch.float32)
@@ -133,18 +143,20 @@ def make_layer(workload: str, seed: int = 0, device="cpu", T: int | None = None)
         d = dataclasses.replace(d, T=T)
     x = activations(d.T, d.H, seed, device)
     logits = router_logits(LOGITS_KIND[workload], x, d.E, seed, device)
+    wg = gate_weight(d.E, d.H, seed, device) if logits is None else None
     w13, w13_s = mxfp4_weights(d.G, 2 * d.I, d.H, seed, device, "w13")
     w2, w2_s = mxfp4_weights(d.G, d.H, d.I, seed, device, "w2")
-    return d, dict(x=x, logits=logits, w13=w13, w13_s=w13_s, w2=w2, w2_s=w2_s)
+    return d, dict(x=x, logits=logits, wg=wg, w13=w13, w13_s=w13_s, w2=w2, w2_s=w2_s)
 
 
 def custom_layer(d: Dims, seed: int = 0, device="cpu", logits_kind="normal"):
     """Same recipe at arbitrary dims (ragged / edge-case tests)."""
     x = activations(d.T, d.H, seed, device)
     logits = router_logits(logits_kind, x, d.E, seed, device)
+    wg = gate_weight(d.E, d.H, seed, device) if logits is None else None
     w13, w13_s = mxfp4_weights(d.G, 2 * d.I, d.H, seed, device, "w13")
     w2, w2_s = mxfp4_weights(d.G, d.H, d.I, seed, device, "w2")
-    return dict(x=x, logits=logits, w13=w13, w13_s=w13_s, w2=w2, w2_s=w2_s)
+    return dict(x=x, logits=logits, wg=wg, w13=w13, w13_s=w13_s, w2=w2, w2_s=w2_s)
 
 
 def sweep_point(which: str, M: int, seed: int = 0, device="cpu", G: int | None = None):

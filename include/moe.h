@@ -132,6 +132,19 @@ int moe_route_static(const moe_dims* d, const float* logits, int32_t* idx, float
                      int32_t* counts, int32_t* offsets, int32_t* perm_src, int32_t* inv,
                      void* stream);
 
+/* f4: router gate projection in front of moe_route:
+ *     logits[t][e] = sum_h x[t][h] * wg[e][h],  fp32 products and fp32 sums,
+ * for x bf16 [T][H] (the token hidden states) and wg fp32 [E][H] (the gate weight),
+ * logits fp32 [T][E].  Pages: LMSYS-H20 §3.2 (the TopK step ranks these per-expert
+ * scores; the gate itself is not printed, so it is read as this plain projection).
+ * Each logit's H products are summed in one fixed order (run-to-run identical);
+ * against an exactly rounded sum the error stays within fp32 accumulation bounds.
+ * Requires T >= 1, E >= 1, H >= 16, H % 16 == 0 (MOE_ERR_UNSUPPORTED_SHAPE), x and wg
+ * 16-byte aligned, logits 4-byte aligned (MOE_ERR_INVALID_ARG).  Caller-owned
+ * device buffers; no workspace; asynchronous on `stream`. */
+int moe_router_logits(int32_t T, int32_t H, int32_t E, const uint16_t* x, const float* wg,
+                      float* logits, void* stream);
+
 /* a3: online FP8 E4M3 quantisation of bf16 x [rows][cols] with one power-of-two
  * scale per row per 128 columns (rule above) -> q [rows][cols], s [rows][cols/128].
  * Pages: LMSYS-H20 §2.2 (online FP8 activations), §3.2 (fused FP8 quantisation).

@@ -70,6 +70,7 @@ def lib():
             getattr(L, fn).restype = _SZ
         L.moe_route.argtypes = [_DP, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]
         L.moe_quant_act.argtypes = [_I, _I, _P, _P, _P, _P]
+        L.moe_router_logits.argtypes = [_I, _I, _I, _P, _P, _P, _P]
         L.moe_grouped_gemm_w13.argtypes = [_DP, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]
         L.moe_swiglu_quant.argtypes = [_I, _I, _P, _P, _P, _P]
         L.moe_grouped_gemm_w2.argtypes = [_DP, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]
@@ -141,6 +142,14 @@ def moe_route(d, logits, idx, w, counts, offsets, perm_src, inv, ws, stream=None
     _check("moe_route", lib().moe_route(_d(d), _p(logits), _p(idx), _p(w), _p(counts),
                                         _p(offsets), _p(perm_src), _p(inv), _p(ws),
                                         ws.numel(), _stream(stream)))
+
+
+def moe_router_logits(x, wg, logits, stream=None):
+    """logits [T, E] fp32 = x [T, H] bf16 . wg [E, H] fp32 ^T (router gate projection)."""
+    T, H = x.shape
+    E = wg.shape[0]
+    _check("moe_router_logits", lib().moe_router_logits(T, H, E, _p(x), _p(wg), _p(logits),
+                                                        _stream(stream)))
 
 
 def moe_quant_act(x, q, s, stream=None):

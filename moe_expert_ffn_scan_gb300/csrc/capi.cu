@@ -212,6 +212,15 @@ int moe_route(const moe_dims* d, const float* logits, int32_t* idx, float* w, in
   return cuda_rc(e);
 }
 
+int moe_router_logits(int32_t T, int32_t H, int32_t E, const uint16_t* x, const float* wg,
+                      float* logits, void* stream) {
+  if (T < 1 || E < 1 || H < 16 || H % 16) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!x || !wg || !logits || !aligned(x, 16) || !aligned(wg, 16) || !aligned(logits, 4))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_rc(
+      launch_router_logits(x, wg, logits, T, H, E, static_cast<cudaStream_t>(stream)));
+}
+
 int moe_quant_act(int32_t rows, int32_t cols, const uint16_t* x, uint8_t* q, uint8_t* s,
                   void* stream) {
   if (rows < 0 || cols <= 0 || cols % 128) return MOE_ERR_UNSUPPORTED_SHAPE;

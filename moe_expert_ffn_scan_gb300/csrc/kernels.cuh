@@ -71,6 +71,12 @@ cudaError_t launch_plan(const int32_t* offsets, int G, int4* small_items, int4* 
 
 cudaError_t launch_quant_act(const uint16_t* x, int rows, int cols, uint8_t* q, uint8_t* s,
                              cudaStream_t st);
+
+// Router gate projection: token count up to which the W_g-streaming kernel runs (it
+// re-reads W_g once per 16 tokens); above it the register-tiled kernel.
+constexpr int kRouterGemvMaxT = 64;
+cudaError_t launch_router_logits(const uint16_t* x, const float* wg, float* logits, int T, int H,
+                                 int E, cudaStream_t st);
 cudaError_t launch_swiglu_quant(const uint16_t* y13, int rows, int I, uint8_t* hq, uint8_t* hs,
                                 cudaStream_t st);
 cudaError_t launch_gather_rows(const uint8_t* xq, const uint8_t* xs, const int32_t* perm_src,

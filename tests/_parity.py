@@ -10,6 +10,16 @@ REL_RMS = 2e-2
 MIN_COS = 0.9999
 
 
+def with_gate_logits(t):
+    """Layers whose logits are the gate projection of x come from the generator with
+    W_g and logits None; the oracle projects them here and both sides get the same
+    logits."""
+    if t.get("logits") is None:
+        lg = o.router_logits(bits_np(t["x"]), t["wg"].cpu().numpy()).astype(np.float32)
+        t["logits"] = torch.from_numpy(lg).to(t["x"].device)
+    return t
+
+
 def bf16_np(t):
     """bf16 torch tensor (any device) -> float64 numpy."""
     return t.detach().float().cpu().numpy().astype(np.float64)

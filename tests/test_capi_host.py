@@ -81,6 +81,13 @@ def test_validation_happens_before_any_launch(lib):
     # workspace too small
     assert lib.moe_route(ctypes.byref(d), P(0x1000), P(0x1000), P(0x1000), P(0x1000),
                          P(0x1000), P(0x1000), P(0x1000), P(0x10000), 16, None) == 3
+    # router projection: shape checks, then null / misaligned pointers
+    assert lib.moe_router_logits(0, 128, 8, P(0x1000), P(0x1000), P(0x1000), None) == 2
+    assert lib.moe_router_logits(4, 120, 8, P(0x1000), P(0x1000), P(0x1000), None) == 2
+    assert lib.moe_router_logits(4, 128, 0, P(0x1000), P(0x1000), P(0x1000), None) == 2
+    assert lib.moe_router_logits(4, 128, 8, None, P(0x1000), P(0x1000), None) == 1
+    assert lib.moe_router_logits(4, 128, 8, P(0x1008), P(0x1000), P(0x1000), None) == 1
+    assert lib.moe_router_logits(4, 128, 8, P(0x1000), P(0x1004), P(0x1000), None) == 1
     w = moe.moe_weights(0x10000, 0x10000, 0x10008, 0x10000)  # w2 misaligned (needs 32 B)
     assert lib.moe_forward(ctypes.byref(d), P(0x1000), P(0x1000), ctypes.byref(w),
                            P(0x1000), None, P(0x10000), 1 << 30, None) == 1

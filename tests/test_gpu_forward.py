@@ -11,7 +11,8 @@ import torch
 import moe_expert_ffn_scan_gb300 as moe
 from gen import inputs as gi
 from oracle import moe_oracle as o
-from tests._parity import (assert_float_close, assert_fp8_codes_close, bf16_np, bits_np)
+from tests._parity import (assert_float_close, assert_fp8_codes_close, bf16_np, bits_np,
+                           with_gate_logits)
 
 pytestmark = pytest.mark.gpu
 
@@ -31,11 +32,11 @@ def _forward(d, t):
 
 def _np(t):
     return {k: (v.cpu().numpy() if v.dtype != torch.bfloat16 else bits_np(v))
-            for k, v in t.items()}
+            for k, v in t.items() if v is not None}
 
 
 def _check_full(d, t):
-    out, dbg = _forward(d, {k: v.to(DEV) for k, v in t.items()})
+    out, dbg = _forward(d, {k: v.to(DEV) for k, v in t.items() if v is not None})
     n = _np(t)
     ref = o.moe_forward(n["x"], n["logits"], d.k, n["w13"], n["w13_s"], n["w2"], n["w2_s"],
                         d.has_shared)
@@ -57,6 +58,7 @@ def _check_full(d, t):
 
 def test_forward_tiny_workload():
     d, t = gi.make_layer("tiny")
+    with_gate_logits(t)
     _check_full(moe.dims(d.T, d.H, d.I, d.E, d.k, d.has_shared), t)
 
 
@@ -75,9 +77,10 @@ def test_forward_ragged_shapes(T, H, I, E, k, sh, kind):
 
 def test_forward_zero_input():
     d, t = gi.make_layer("tiny")
+    with_gate_logits(t)
     t["x"] = torch.zeros_like(t["x"])
     out, dbg = _forward(moe.dims(d.T, d.H, d.I, d.E, d.k, d.has_shared),
-                        {k: v.to(DEV) for k, v in t.items()})
+                        {k: v.to(DEV) for k, v in t.items() if v is not None})
     assert torch.all(out.float() == 0)
 
 

@@ -10,6 +10,12 @@ import torch
 
 from gen import inputs as gi
 from oracle import moe_oracle as o
+from tests._parity import with_gate_logits
+
+
+def _tiny():
+    d, t = gi.make_layer("tiny")
+    return d, with_gate_logits(t)
 
 
 def _bits(x_bf16):
@@ -208,7 +214,7 @@ def _np_layer(t):
 
 
 def test_dense_unrouted_equals_routed_tiny():
-    d, t = gi.make_layer("tiny")
+    d, t = _tiny()
     x, lg, w13, w13s, w2, w2s = _np_layer(t)
     r = o.moe_forward(x, lg, d.k, w13, w13s, w2, w2s, d.has_shared)
     dense = o.dense_unrouted_forward(x, lg, d.k, w13, w13s, w2, w2s, d.has_shared)
@@ -227,7 +233,7 @@ def test_dense_unrouted_equals_routed_with_shared_ragged():
 
 
 def test_zero_input_gives_zero_output():
-    d, t = gi.make_layer("tiny")
+    d, t = _tiny()
     t["x"] = torch.zeros_like(t["x"])
     x, lg, w13, w13s, w2, w2s = _np_layer(t)
     r = o.moe_forward(x, lg, d.k, w13, w13s, w2, w2s, d.has_shared)
@@ -235,7 +241,7 @@ def test_zero_input_gives_zero_output():
 
 
 def test_token_subset_matches_full_layer():
-    d, t = gi.make_layer("tiny")
+    d, t = _tiny()
     x, lg, w13, w13s, w2, w2s = _np_layer(t)
     full = o.moe_forward(x, lg, d.k, w13, w13s, w2, w2s, d.has_shared)
     sub = o.moe_forward_tokens(x, lg, d.k, w13, w13s, w2, w2s, d.has_shared, [3, 17, 60])
