@@ -433,6 +433,27 @@ def run_ours(args, rank, world, local):
                "h2d_bytes_per_step": int(xh.numel() * 2 + lgh.numel() * 4),
                "d2h_bytes_per_step": int(oh.numel() * 2), "ms_per_step": em}
 
+    # the router gate projection for this workload's T (outside the layer step: the
+    # layer's boundary takes logits); W_g synthetic fp32 [E, H]
+    wg = t["wg"] if t.get("wg") is not None else gi.gate_weight(d.E, d.H, args.seed, dev)
+    rlg = torch.empty(d.T, d.E, dtype=torch.float32, device=dev)
+    for _ in range(3):
+        moe.moe_router_logits(x, wg, rlg)
+    r_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(args.steps)]
+    for i in range(args.steps):
+        if not args.no_flush:
+            flush.fill_(i & 0xFF)
+        r_ev[i][0].record(stream)
+        moe.moe_router_logits(x, wg, rlg)
+        r_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    r_ms = statistics.mean(a.elapsed_time(b) for a, b in r_ev)
+    r_bytes = d.E * d.H * 4 + d.T * d.H * 2 + d.T * d.E * 4
+    router = {"ms": r_ms, "gbs": r_bytes / (r_ms * 1e-3) / 1e9,
+              "tflops": 2.0 * d.T * d.E * d.H / (r_ms * 1e-3) / 1e12,
+              "kernel": "k_router_gemv" if d.T <= 1024 else "k_router_tiled (fp32 CUDA cores)"}
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         hv = host_view(d, t)
@@ -459,6 +480,7 @@ def run_ours(args, rank, world, local):
                                                      stage_mean["gemm_w2"]) * 1e-3) / 1e9,
             "gemm_tflops": (flops13 + flops2) / ((stage_mean["gemm_w13"] +
                                                   stage_mean["gemm_w2"]) * 1e-3) / 1e12,
+            "router_gate": router,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": 2 * launches_per_step * args.steps,

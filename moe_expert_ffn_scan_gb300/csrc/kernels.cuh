@@ -73,8 +73,9 @@ cudaError_t launch_quant_act(const uint16_t* x, int rows, int cols, uint8_t* q, 
                              cudaStream_t st);
 
 // Router gate projection: token count up to which the W_g-streaming kernel runs (it
-// re-reads W_g once per 16 tokens); above it the register-tiled kernel.
-constexpr int kRouterGemvMaxT = 64;
+// re-reads W_g, from L2, once per 16 tokens); above it the register-tiled kernel,
+// which has too few tiles to fill the GPU below ~1K tokens.
+constexpr int kRouterGemvMaxT = 1024;
 cudaError_t launch_router_logits(const uint16_t* x, const float* wg, float* logits, int T, int H,
                                  int E, cudaStream_t st);
 cudaError_t launch_swiglu_quant(const uint16_t* y13, int rows, int I, uint8_t* hq, uint8_t* hs,

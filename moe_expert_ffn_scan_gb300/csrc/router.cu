@@ -4,12 +4,12 @@
 // ranks per-expert router scores; this is the projection that produces them, kept in
 // fp32 (x is the bf16 hidden state, W_g the fp32 gate weight).  A plain fp32
 // contraction on the CUDA cores: two shapes of it matter.
-//   * Decode (T <= 64): HBM-bound on W_g (E x H x 4 bytes, 11 MB at E=384,
-//     H=7168).  k_router_gemv: a CTA owns kRgExperts experts and up to kRgTokens
-//     tokens; its 8 warps split H, each lane streams 16-byte W_g loads and keeps
-//     kRgExperts x kRgTokens partial sums; warp sums, then the 8 warp partials are
-//     added in warp order (deterministic, no atomics).
-//   * Prefill (T > 64): 2*T*E*H flops, compute-bound.  k_router_tiled: classic
+//   * Decode and mid T (T <= 1024): HBM- / latency-bound on W_g (E x H x 4 bytes, 11 MB at E=384,
+//     H=7168).  k_router_gemv: a CTA owns kRgExperts experts and up to 8 or 16
+//     tokens; its 8 warps split H, each lane issues a round of W_g and x loads
+//     together and keeps experts x tokens partial sums; warp sums, then the 8 warp
+//     partials are added in warp order (deterministic, no atomics).
+//   * Prefill (T > 1024): 2*T*E*H flops, compute-bound.  k_router_tiled: classic
 //     register-tiled SGEMM, 128 tokens x 64 experts per CTA, 8 x 4 outputs per
 //     thread, K staged 16 columns at a time in shared memory (x converted to fp32).
 // Both accumulate each logit's H products in one fixed order, so results are
@@ -18,71 +18,91 @@
 
 namespace moe {
 
-constexpr int kRgTokens = 16;   // tokens per CTA (blockIdx.y walks token groups)
-constexpr int kRgExperts = 2;   // experts per CTA
+// Experts per CTA: 2 measured best (1: x re-read too often; 4: too few CTAs at mid T).
+constexpr int kRgExperts = 2;
 constexpr int kRgWarps = 8;
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
+// TT tokens per CTA (blockIdx.y walks token groups of TT); U 4-column steps per lane
+// whose W_g and x loads are all issued before any of their FMAs.  Loads past the
+// warp's slice read a valid column with W_g = 0 (adds +0, leaving sums unchanged), and
+// token rows past T read row T-1 into sums that are never written, so the loop body
+// is straight-line code.
+template <int TT, int U>
 __global__ void __launch_bounds__(256) k_router_gemv(const uint16_t* __restrict__ x,
                                                      const float* __restrict__ wg,
                                                      float* __restrict__ logits, int T, int H,
                                                      int E) {
   pdl_wait();
   pdl_trigger();
-  __shared__ float red[kRgWarps][kRgExperts][kRgTokens];
+  __shared__ float red[kRgWarps][kRgExperts][TT];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e0 = blockIdx.x * kRgExperts;
-  const int t0 = blockIdx.y * kRgTokens;
-  const int nt = min(kRgTokens, T - t0);
-  // this warp's slice of H, in 4-column steps (H % 16 == 0, so slices are whole steps)
+  const int t0 = blockIdx.y * TT;
+  const int nt = min(TT, T - t0);
+  // this warp's slice of H, in 4-column steps (H % 16 == 0: slices are whole steps)
   const int steps = H / 4;
   const int per = (steps + kRgWarps - 1) / kRgWarps;
   const int s0 = warp * per, s1 = min(steps, s0 + per);
-  float acc[kRgExperts][kRgTokens];
+  const float* wrow[kRgExperts];
+#pragma unroll
+  for (int j = 0; j < kRgExperts; ++j)
+    wrow[j] = wg + static_cast<size_t>(min(e0 + j, E - 1)) * H;  // clamped rows: unused
+  const uint16_t* xrow[TT];
+#pragma unroll
+  for (int t = 0; t < TT; ++t) xrow[t] = x + static_cast<size_t>(t0 + min(t, nt - 1)) * H;
+  float acc[kRgExperts][TT];
 #pragma unroll
   for (int j = 0; j < kRgExperts; ++j)
 #pragma unroll
-    for (int t = 0; t < kRgTokens; ++t) acc[j][t] = 0.f;
-  for (int s = s0 + lane; s < s1; s += 32) {
-    const int h = s * 4;
-    float4 w[kRgExperts];
+    for (int t = 0; t < TT; ++t) acc[j][t] = 0.f;
+  for (int sb = s0 + lane; sb < s1; sb += 32 * U) {
+    float4 w[U][kRgExperts];
+    uint2 xv[U][TT];
 #pragma unroll
-    for (int j = 0; j < kRgExperts; ++j)
-      w[j] = e0 + j < E ? __ldg(reinterpret_cast<const float4*>(wg + static_cast<size_t>(e0 + j) * H + h))
-                        : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int u = 0; u < U; ++u) {
+      const int s = sb + 32 * u;
+      const bool ok = s < s1;
+      const int sl = ok ? s : s1 - 1;
 #pragma unroll
-    for (int t = 0; t < kRgTokens; ++t) {
-      if (t < nt) {
-        const uint2 xv =
-            __ldg(reinterpret_cast<const uint2*>(x + static_cast<size_t>(t0 + t) * H + h));
-        const float x0 = bf16_lo(xv.x), x1 = bf16_hi(xv.x), x2 = bf16_lo(xv.y),
-                    x3 = bf16_hi(xv.y);
+      for (int j = 0; j < kRgExperts; ++j)
+        w[u][j] = ok ? __ldg(reinterpret_cast<const float4*>(wrow[j] + sl * 4))
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int t = 0; t < TT; ++t)
+        xv[u][t] = __ldg(reinterpret_cast<const uint2*>(xrow[t] + sl * 4));
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int t = 0; t < TT; ++t) {
+        const float x0 = bf16_lo(xv[u][t].x), x1 = bf16_hi(xv[u][t].x),
+                    x2 = bf16_lo(xv[u][t].y), x3 = bf16_hi(xv[u][t].y);
 #pragma unroll
         for (int j = 0; j < kRgExperts; ++j) {
           float a = acc[j][t];
-          a = fmaf(x0, w[j].x, a);
-          a = fmaf(x1, w[j].y, a);
-          a = fmaf(x2, w[j].z, a);
-          a = fmaf(x3, w[j].w, a);
+          a = fmaf(x0, w[u][j].x, a);
+          a = fmaf(x1, w[u][j].y, a);
+          a = fmaf(x2, w[u][j].z, a);
+          a = fmaf(x3, w[u][j].w, a);
           acc[j][t] = a;
         }
       }
-    }
   }
 #pragma unroll
   for (int j = 0; j < kRgExperts; ++j)
 #pragma unroll
-    for (int t = 0; t < kRgTokens; ++t) {
+    for (int t = 0; t < TT; ++t) {
       float v = acc[j][t];
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
       if (lane == 0) red[warp][j][t] = v;
     }
   __syncthreads();
-  if (threadIdx.x < kRgExperts * kRgTokens) {
-    const int j = threadIdx.x / kRgTokens, t = threadIdx.x % kRgTokens;
+  if (threadIdx.x < kRgExperts * TT) {
+    const int j = threadIdx.x / TT, t = threadIdx.x % TT;
     if (t < nt && e0 + j < E) {
       float v = 0.f;
 #pragma unroll
@@ -174,9 +194,13 @@ __global__ void __launch_bounds__(256) k_router_tiled(const uint16_t* __restrict
 
 cudaError_t launch_router_logits(const uint16_t* x, const float* wg, float* logits, int T, int H,
                                  int E, cudaStream_t st) {
+  if (T <= 8) {
+    dim3 grid((E + kRgExperts - 1) / kRgExperts, 1);
+    return launch_k(k_router_gemv<8, 4>, grid, 256, 0, st, x, wg, logits, T, H, E);
+  }
   if (T <= kRouterGemvMaxT) {
-    dim3 grid((E + kRgExperts - 1) / kRgExperts, (T + kRgTokens - 1) / kRgTokens);
-    return launch_k(k_router_gemv, grid, 256, 0, st, x, wg, logits, T, H, E);
+    dim3 grid((E + kRgExperts - 1) / kRgExperts, (T + 15) / 16);
+    return launch_k(k_router_gemv<16, 2>, grid, 256, 0, st, x, wg, logits, T, H, E);
   }
   dim3 grid((E + kRtBN - 1) / kRtBN, (T + kRtBM - 1) / kRtBM);
   return launch_k(k_router_tiled, grid, 256, 0, st, x, wg, logits, T, H, E);

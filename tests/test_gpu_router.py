@@ -44,10 +44,11 @@ def _run(x, wg):
 @pytest.mark.parametrize("T,H,E", [
     (7, 7168, 384),    # decode: the W_g-streaming kernel
     (1, 128, 8),
-    (64, 512, 8),      # the tiny layer's dims; largest T of the streaming kernel
-    (65, 512, 8),      # smallest T of the tiled kernel
-    (130, 1024, 40),   # ragged token and expert tiles
-    (300, 256, 1000),
+    (64, 512, 8),      # the tiny layer's dims
+    (1024, 256, 24),   # largest T of the streaming kernel
+    (1025, 512, 8),    # smallest T of the tiled kernel
+    (130, 1024, 40),   # ragged token groups
+    (1300, 256, 1000), # tiled: ragged token and expert tiles
     (16, 4096, 3),     # fewer experts than one CTA's share
     (17, 16, 7),       # H = one K stage
 ])
@@ -72,6 +73,8 @@ def test_router_logits_deterministic():
     b = _run(x, wg)
     assert torch.equal(a, b)
     x, wg = _inputs(7, 7168, 384, seed=5)
+    assert torch.equal(_run(x, wg), _run(x, wg))
+    x, wg = _inputs(2000, 512, 64, seed=5)  # the tiled kernel
     assert torch.equal(_run(x, wg), _run(x, wg))
 
 
