@@ -194,6 +194,20 @@ int moe_forward(const moe_dims* d, const uint16_t* x, const float* logits,
                 const moe_weights* W, uint16_t* out, const moe_debug_out* dbg, void* ws,
                 size_t ws_bytes, void* stream);
 
+/* The whole layer from and to host memory, for callers whose activations live on the
+ * host: copies x_host [T][H] bf16 and logits_host [T][E] fp32 to device staging in
+ * the workspace, runs moe_forward, and copies the output back to out_host [T][H] bf16
+ * -- two host->device copies, the layer's kernels and one device->host copy, all
+ * asynchronous on `stream` (host buffers should be pinned for the copies to be
+ * asynchronous; the caller synchronises before reading out_host).  The pages have no
+ * counterpart (their layers run inside a serving engine with device-resident
+ * activations); this is the end-to-end form of moe_forward.  Weights as for
+ * moe_forward (device).  ws: moe_host_workspace_size(d) bytes, 256-byte aligned. */
+size_t moe_host_workspace_size(const moe_dims* d);
+int moe_forward_host(const moe_dims* d, const uint16_t* x_host, const float* logits_host,
+                     const moe_weights* W, uint16_t* out_host, void* ws, size_t ws_bytes,
+                     void* stream);
+
 /* moe_forward with per-stage timing.  events points to 8 cudaEvent_t handles created
  * by the caller (cudaEventCreate); the call records events[0] before the first stage
  * and events[i] after stage i: 1 route + histogram/scan/permute, 2 activation

@@ -65,7 +65,8 @@ def lib():
         L = ctypes.CDLL(LIB_PATH)
         L.moe_error_string.argtypes = [ctypes.c_int]
         L.moe_error_string.restype = ctypes.c_char_p
-        for fn in ("moe_workspace_size", "moe_route_workspace_size", "moe_gemm_workspace_size"):
+        for fn in ("moe_workspace_size", "moe_route_workspace_size", "moe_gemm_workspace_size",
+                   "moe_host_workspace_size"):
             getattr(L, fn).argtypes = [_DP]
             getattr(L, fn).restype = _SZ
         L.moe_route.argtypes = [_DP, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]
@@ -77,6 +78,8 @@ def lib():
         L.moe_combine.argtypes = [_DP, _P, _P, _P, _P, _P]
         L.moe_forward.argtypes = [_DP, _P, _P, ctypes.POINTER(moe_weights), _P,
                                   ctypes.POINTER(moe_debug_out), _P, _SZ, _P]
+        L.moe_forward_host.argtypes = [_DP, _P, _P, ctypes.POINTER(moe_weights), _P, _P, _SZ,
+                                       _P]
         L.moe_forward_timed.argtypes = [_DP, _P, _P, ctypes.POINTER(moe_weights), _P,
                                         ctypes.POINTER(moe_debug_out), ctypes.POINTER(_P), _P,
                                         _SZ, _P]
@@ -123,6 +126,10 @@ def _d(d):
 
 def workspace_size(d) -> int:
     return lib().moe_workspace_size(_d(d))
+
+
+def host_workspace_size(d) -> int:
+    return lib().moe_host_workspace_size(_d(d))
 
 
 def route_workspace_size(d) -> int:
@@ -191,6 +198,23 @@ def moe_forward(d, x, logits, w13, w13_s, w2, w2_s, out, ws, debug=None, stream=
         ctypes.byref(dbg) if dbg is not None else None, _p(ws), ws.numel(), _stream(stream)))
 
 
+def _host_p(t):
+    if t.device.type != "cpu":
+        raise ValueError("tensor must live in host memory")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return t.data_ptr()
+
+
+def moe_forward_host(d, x_host, logits_host, w13, w13_s, w2, w2_s, out_host, ws, stream=None):
+    """The layer from host buffers to a host buffer (two copies in, one out, on the
+    stream; pinned buffers keep them asynchronous).  ws: host_workspace_size(d)."""
+    W = moe_weights(_p(w13), _p(w13_s), _p(w2), _p(w2_s))
+    _check("moe_forward_host", lib().moe_forward_host(
+        _d(d), _host_p(x_host), _host_p(logits_host), ctypes.byref(W), _host_p(out_host),
+        _p(ws), ws.numel(), _stream(stream)))
+
+
 STAGES = ("route", "quant", "plan_gather", "gemm_w13", "swiglu_quant", "gemm_w2", "combine")
 
 
@@ -233,6 +257,33 @@ def debug_buffers(d, device="cuda"):
                 hs=z(Rs, I // 128, dt=torch.uint8), y2=z(Rs, H, dt=torch.bfloat16))
 
 
+class HostGraph:
+    """forward_host captured once as a CUDA graph over pinned buffers x_host [T, H]
+    bf16, logits_host [T, E] fp32 and out_host [T, H] bf16.  Write a step's inputs
+    into x_host / logits_host, call replay(), synchronise, read out_host."""
+
+    def __init__(self, layer, T):
+        self.layer, self.T = layer, T
+        self.x_host = torch.zeros(T, layer.H, dtype=torch.bfloat16).pin_memory()
+        self.logits_host = torch.zeros(T, layer.E, dtype=torch.float32).pin_memory()
+        self.out_host = torch.zeros(T, layer.H, dtype=torch.bfloat16).pin_memory()
+        layer.host_workspace(T)  # allocated before capture
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            layer.forward_host(self.x_host, self.logits_host, self.out_host)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            layer.forward_host(self.x_host, self.logits_host, self.out_host)
+        torch.cuda.synchronize()
+
+    def replay(self):
+        self.graph.replay()
+        return self.out_host
+
+
 class MoELayer:
     """The user-facing layer: resident MXFP4 weights plus a reusable workspace.
 
@@ -253,6 +304,25 @@ class MoELayer:
             self._ws = alloc_workspace(workspace_size(self.dims(T)), self.w13.device)
             self._T = T
         return self._ws
+
+    def host_workspace(self, T):
+        if getattr(self, "_hws", None) is None or self._hT < T:
+            self._hws = alloc_workspace(host_workspace_size(self.dims(T)), self.w13.device)
+            self._hT = T
+        return self._hws
+
+    def forward_host(self, x_host, logits_host, out_host, stream=None):
+        """End to end from host memory: x_host [T, H] bf16 and logits_host [T, E] fp32
+        (pinned) in, out_host [T, H] bf16 (pinned) written when the stream reaches it."""
+        T = x_host.shape[0]
+        moe_forward_host(self.dims(T), x_host, logits_host, self.w13, self.w13_s, self.w2,
+                         self.w2_s, out_host, self.host_workspace(T), stream=stream)
+        return out_host
+
+    def host_graph(self, T):
+        """A CUDA graph of forward_host on layer-owned pinned buffers (see HostGraph):
+        one launch per step for the copies in, the layer's kernels and the copy out."""
+        return HostGraph(self, T)
 
     def forward(self, x, logits, out=None, debug=None, stream=None):
         T = x.shape[0]

@@ -128,6 +128,22 @@ ForwardWs carve_forward(Carver& c, const moe_dims* d) {
   return f;
 }
 
+// Device staging of the host-buffer forward, after the forward workspace.
+struct HostStagingWs {
+  uint16_t* x;
+  float* logits;
+  uint16_t* out;
+};
+
+HostStagingWs carve_host_staging(Carver& c, const moe_dims* d) {
+  HostStagingWs h;
+  const size_t T = d->T, H = d->H, E = d->E;
+  h.x = c.take<uint16_t>(T * H);
+  h.logits = c.take<float>(T * E);
+  h.out = c.take<uint16_t>(T * H);
+  return h;
+}
+
 int run_gemm(const moe_dims* d, const uint8_t* act, const uint8_t* act_s, const int32_t* offsets,
              const uint8_t* w, const uint8_t* w_s, int N, int K, uint16_t* y, const PlanWs& plan,
              int max_group_rows, uint32_t* status, cudaStream_t st) {
@@ -302,6 +318,38 @@ int moe_forward(const moe_dims* d, const uint16_t* x, const float* logits,
                 const moe_weights* W, uint16_t* out, const moe_debug_out* dbg, void* ws,
                 size_t ws_bytes, void* stream) {
   return moe_forward_timed(d, x, logits, W, out, dbg, nullptr, ws, ws_bytes, stream);
+}
+
+size_t moe_host_workspace_size(const moe_dims* d) {
+  if (!dims_ok(d)) return 0;
+  Carver c(nullptr);
+  carve_forward(c, d);
+  carve_host_staging(c, d);
+  return c.used;
+}
+
+int moe_forward_host(const moe_dims* d, const uint16_t* x_host, const float* logits_host,
+                     const moe_weights* W, uint16_t* out_host, void* ws, size_t ws_bytes,
+                     void* stream) {
+  if (!dims_ok(d)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!x_host || !logits_host || !W || !out_host || !ws) return MOE_ERR_INVALID_ARG;
+  if (!aligned(ws, kAlign)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < moe_host_workspace_size(d)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Carver c(ws);
+  carve_forward(c, d);  // the forward's own workspace comes first
+  const size_t fwd_bytes = c.used;
+  HostStagingWs h = carve_host_staging(c, d);
+  const size_t xb = static_cast<size_t>(d->T) * d->H * sizeof(uint16_t);
+  const size_t lb = static_cast<size_t>(d->T) * d->E * sizeof(float);
+  if (cudaMemcpyAsync(h.x, x_host, xb, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(h.logits, logits_host, lb, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  int rc = moe_forward_timed(d, h.x, h.logits, W, h.out, nullptr, nullptr, ws, fwd_bytes, st);
+  if (rc != MOE_OK) return rc;
+  if (cudaMemcpyAsync(out_host, h.out, xb, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
 }
 
 int moe_forward_timed(const moe_dims* d, const uint16_t* x, const float* logits,

@@ -81,6 +81,17 @@ def test_validation_happens_before_any_launch(lib):
     # workspace too small
     assert lib.moe_route(ctypes.byref(d), P(0x1000), P(0x1000), P(0x1000), P(0x1000),
                          P(0x1000), P(0x1000), P(0x1000), P(0x10000), 16, None) == 3
+    # host-buffer forward: dims, nulls, workspace size and alignment
+    w = moe.moe_weights(0x10000, 0x10000, 0x10000, 0x10000)
+    assert lib.moe_forward_host(ctypes.byref(bad), P(0x1000), P(0x1000), ctypes.byref(w),
+                                P(0x1000), P(0x10000), 1 << 30, None) == 2
+    assert lib.moe_forward_host(ctypes.byref(d), None, P(0x1000), ctypes.byref(w), P(0x1000),
+                                P(0x10000), 1 << 30, None) == 1
+    assert lib.moe_forward_host(ctypes.byref(d), P(0x1000), P(0x1000), ctypes.byref(w),
+                                P(0x1000), P(0x10000), 16, None) == 3
+    assert lib.moe_forward_host(ctypes.byref(d), P(0x1000), P(0x1000), ctypes.byref(w),
+                                P(0x1000), P(0x10008), 1 << 30, None) == 1
+    assert moe.host_workspace_size(d) > moe.workspace_size(d)
     # router projection: shape checks, then null / misaligned pointers
     assert lib.moe_router_logits(0, 128, 8, P(0x1000), P(0x1000), P(0x1000), None) == 2
     assert lib.moe_router_logits(4, 120, 8, P(0x1000), P(0x1000), P(0x1000), None) == 2

@@ -75,6 +75,32 @@ def test_forward_ragged_shapes(T, H, I, E, k, sh, kind):
     _check_full(moe.dims(T, H, I, E, k, sh), t)
 
 
+@pytest.mark.parametrize("workload", ["tiny", "decode"])
+def test_forward_host_equals_device_forward(workload):
+    """moe_forward_host (pinned host buffers in and out) gives the device forward's
+    output bit for bit."""
+    d, t = gi.make_layer(workload, seed=4, device=DEV)
+    with_gate_logits(t)
+    layer = moe.MoELayer(d.H, d.I, d.E, d.k, d.has_shared, t["w13"], t["w13_s"], t["w2"],
+                         t["w2_s"])
+    ref = layer.forward(t["x"], t["logits"])
+    xh = t["x"].cpu().pin_memory()
+    lgh = t["logits"].cpu().pin_memory()
+    oh = torch.full((d.T, d.H), float("nan"), dtype=torch.bfloat16).pin_memory()
+    layer.forward_host(xh, lgh, oh)
+    torch.cuda.synchronize()
+    assert torch.equal(oh, ref.cpu())
+    assert moe.moe_check_status(layer.host_workspace(d.T)) == 0
+    hg = layer.host_graph(d.T)
+    hg.x_host.copy_(xh)
+    hg.logits_host.copy_(lgh)
+    for _ in range(2):
+        hg.out_host.fill_(float("nan"))
+        hg.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(hg.out_host, ref.cpu())
+
+
 def test_forward_zero_input():
     d, t = gi.make_layer("tiny")
     with_gate_logits(t)
