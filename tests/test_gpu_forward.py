@@ -68,6 +68,11 @@ def test_forward_tiny_workload():
     (200, 384, 256, 16, 4, 1, "zipf"),      # skewed: large and empty groups
     (40, 1024, 512, 64, 8, 0, "zipf"),
     (90, 256, 256, 3, 3, 0, "normal"),      # k == E: every token to every expert
+    (128, 256, 128, 16, 4, 1, "zipf"),      # largest T of the one-CTA decode prep
+    (129, 256, 128, 16, 4, 1, "zipf"),      # smallest T of the multi-kernel route path
+    (5, 128, 128, 1, 1, 0, "normal"),       # one expert, k = 1, minimal H and I
+    (3, 256, 128, 1024, 16, 1, "normal"),   # largest E and k the interface accepts
+    (300, 640, 384, 12, 2, 1, "zipf"),      # H/128 and I/128 odd: one-sub-tile stages
 ])
 def test_forward_ragged_shapes(T, H, I, E, k, sh, kind):
     d = gi.Dims(T=T, H=H, I=I, E=E, k=k, has_shared=sh)
