@@ -14,49 +14,53 @@ namespace moe {
 
 // ---------------------------------------------------------------- a1: route -------
 //
-// One warp per token.  Lane l holds logits l, l+32, ... (coalesced loads).  k rounds
-// of warp-wide argmax over the not-yet-taken experts, ties to the lower index.  On
-// return lane j < k holds the j-th selection (expert, renormalised weight).
+// One warp per token.  Lane l holds logits l, l+32, ... (coalesced loads) as
+// order-preserving unsigned keys (key(a) > key(b) <=> a > b for finite floats, -0
+// folded onto +0 so that equal values have equal keys; key 0 marks a taken or absent
+// slot, which no finite logit maps to).  k rounds: each lane's best untaken key
+// (lowest slot on ties), the warp's largest key (redux.sync max), then the lowest
+// expert index among the lanes holding it (redux.sync min) -- ties to the lower
+// index.  On return lane j < k holds the j-th selection (expert, renormalised weight).
+__device__ __forceinline__ uint32_t logit_key(float f) {
+  const uint32_t u = __float_as_uint(f == 0.f ? 0.f : f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_logit(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
 template <int EPL>
 __device__ __forceinline__ void route_token(const float* __restrict__ row, int E, int k,
                                             int lane, int& my_e, float& my_w) {
-  float v[EPL];
-  uint32_t taken = 0;
+  uint32_t key[EPL];
 #pragma unroll
   for (int i = 0; i < EPL; ++i) {
-    int e = lane + 32 * i;
-    v[i] = e < E ? row[e] : 0.f;
-    if (e >= E) taken |= 1u << i;
+    const int e = lane + 32 * i;
+    key[i] = e < E ? logit_key(row[e]) : 0u;
   }
   float my_v = 0.f;
   my_e = 0;
   for (int j = 0; j < k; ++j) {
-    float bv = 0.f;
-    int be = 0x7FFFFFFF;
+    uint32_t bk = 0;
+    int bi = 0;
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
-      int e = lane + 32 * i;
-      bool ok = !((taken >> i) & 1u);
-      if (ok && (be == 0x7FFFFFFF || v[i] > bv)) {  // ascending e: strict > keeps lower index
-        bv = v[i];
-        be = e;
+      if (key[i] > bk) {  // ascending slot: strict > keeps the lower index
+        bk = key[i];
+        bi = i;
       }
     }
+    const uint32_t mk = __reduce_max_sync(0xFFFFFFFFu, bk);
+    const uint32_t cand = bk == mk ? static_cast<uint32_t>(lane + 32 * bi) : 0xFFFFFFFFu;
+    const uint32_t be = __reduce_min_sync(0xFFFFFFFFu, cand);
+    if (static_cast<int>(be & 31u) == lane) {
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
-      int oe = __shfl_xor_sync(0xFFFFFFFFu, be, off);
-      bool better = (oe != 0x7FFFFFFF) &&
-                    (be == 0x7FFFFFFF || ov > bv || (ov == bv && oe < be));
-      if (better) {
-        bv = ov;
-        be = oe;
-      }
+      for (int i = 0; i < EPL; ++i)
+        if (i == static_cast<int>(be >> 5)) key[i] = 0u;
     }
-    if ((be & 31) == lane) taken |= 1u << (be >> 5);
     if (lane == j) {
-      my_v = bv;
-      my_e = be;
+      my_v = key_logit(mk);
+      my_e = static_cast<int>(be);
     }
   }
   // weights: exp(l_j - l_0) / sum over the selected
@@ -331,9 +335,9 @@ __global__ void __launch_bounds__(1024) k_prep_small(
     int4* __restrict__ large_items, int32_t* __restrict__ item_counts, uint32_t* status) {
   pdl_wait();
   pdl_trigger();
-  // the first kernel of a call clears the call's status word (before anything sets it)
+  // the first kernel of a call clears the call's status word; every later set of a
+  // status bit in this kernel comes after the barriers below
   if (threadIdx.x == 0) *status = 0;
-  __syncthreads();
   constexpr int kWords = kPrepMaxT / 32;
   __shared__ uint32_t s_mask[1024 * kWords];  // [expert][token word]
   __shared__ int32_t s_idx[kPrepMaxT * 16];
