@@ -4,8 +4,13 @@ activations) on GB300.
 One step = one moe_forward over one batch of synthetic tokens (route, histogram +
 scan + permute, FP8 quantisation, W13 grouped GEMM, SwiGLU + FP8 requantisation, W2
 grouped GEMM, weighted top-k combine + shared-expert add).  Inputs are resident in
-HBM when the timed region starts; L2 is flushed (a 512 MiB write) before every timed
-step, outside its CUDA-event pair.  Prints one JSON line on rank 0.
+HBM when the timed region starts.  L2 between timed steps (--l2): "auto" (default)
+flushes it with a 512 MiB write before every step, outside its CUDA-event pair, unless
+one step streams at least 4x the L2 size of expert weights (decode, decode256,
+prefill: 1.8-13.5 GB per step against a 126 MB L2), where no step's weights can be
+L2-resident and the write-flush would only add its own dirty-line write-back to the
+next step; such runs also report the write-flushed step time.  Prints one JSON line
+on rank 0.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|decode256|prefill|tiny]
   python bench.py --impl reference ...   (the CPU oracle on a bounded sample)
@@ -48,7 +53,8 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-flush", action="store_true")
+    ap.add_argument("--no-flush", action="store_true", help="same as --l2 none")
+    ap.add_argument("--l2", default="auto", choices=["auto", "flush", "none"])
     ap.add_argument("--experts", type=int, default=None,
                     help="override E (a smaller layer of the same shape, for ncu captures)")
     ap.add_argument("--tokens", type=int, default=None, help="override T")
@@ -326,6 +332,15 @@ def run_ours(args, rank, world, local):
     counts = dbg["counts"].cpu().numpy()
     groups = active_groups(counts, d.has_shared)
     Rs = d.R + (d.T if d.has_shared else 0)
+    step_weight_bytes = groups * 3 * d.I * d.H * WEIGHT_BYTES_PER_ELEM
+    l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
+    policy = "none" if args.no_flush else args.l2
+    do_flush = policy == "flush" or (policy == "auto" and step_weight_bytes < 4 * l2_bytes)
+    if do_flush:
+        l2_note = "flushed (512 MiB write) before each step"
+    else:
+        l2_note = (f"not flushed: each step streams {step_weight_bytes / 1e9:.2f} GB of expert "
+                   f"weights ({step_weight_bytes / l2_bytes:.0f}x the {l2_bytes >> 20} MiB L2)")
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)]
            for _ in range(args.steps)]
@@ -352,12 +367,12 @@ def run_ours(args, rank, world, local):
         barrier(world)
         torch.cuda.synchronize()
         for i in range(args.steps):
-            if not args.no_flush:
+            if do_flush:
                 flush.fill_(i & 0xFF)
             step_evs[i][0].record(stream)
             graph.replay()
             step_evs[i][1].record(stream)
-            if not args.no_flush:
+            if do_flush:
                 flush.fill_((i + 128) & 0xFF)
             moe.moe_forward_timed(md, x, lg, t["w13"], t["w13_s"], t["w2"], t["w2_s"], out, ws,
                                   evs[i])
@@ -372,6 +387,17 @@ def run_ours(args, rank, world, local):
         for j, s in enumerate(moe.STAGES):
             stage_ms[s].append(row[j].elapsed_time(row[j + 1]))
     stream_step_ms = statistics.mean(row[0].elapsed_time(row[7]) for row in evs)
+    flushed_ms = None
+    if not do_flush:  # the same graph with the 512 MiB write-flush before each step
+        fe = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            fe[i][0].record(stream)
+            graph.replay()
+            fe[i][1].record(stream)
+        torch.cuda.synchronize()
+        flushed_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in fe), world)
     ms = statistics.mean(step_ms)
     ms_max = max_over_ranks(ms, world)
     value = world * d.T / (ms_max * 1e-3)
@@ -414,7 +440,7 @@ def run_ours(args, rank, world, local):
         torch.cuda.synchronize()
         e_ms = []
         for i in range(args.steps):
-            if not args.no_flush:
+            if do_flush:
                 flush.fill_(i & 0xFF)
             torch.cuda.synchronize()
             t0 = time.perf_counter()
@@ -442,7 +468,7 @@ def run_ours(args, rank, world, local):
     r_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
             for _ in range(args.steps)]
     for i in range(args.steps):
-        if not args.no_flush:
+        if do_flush:
             flush.fill_(i & 0xFF)
         r_ev[i][0].record(stream)
         moe.moe_router_logits(x, wg, rlg)
@@ -471,11 +497,12 @@ def run_ours(args, rank, world, local):
             "dtype": "mxfp4xfp8->f32", "data": "synthetic",
             "config": {"workload": args.workload, "T": d.T, "H": d.H, "I": d.I, "E": d.E,
                        "k": d.k, "shared_experts": d.has_shared, "active_groups": groups,
-                       "routed_rows": d.R, "l2": "flushed (512 MiB write) before each step",
+                       "routed_rows": d.R, "l2": l2_note,
                        "parallelism": f"replicas x{world}"},
             "roofline": roof,
             "stage_ms": stage_mean,
             "stream_ms_per_step": stream_step_ms,
+            "ms_per_step_l2_write_flushed": flushed_ms,
             "weight_gbs": (w13_bytes + w2_bytes) / ((stage_mean["gemm_w13"] +
                                                      stage_mean["gemm_w2"]) * 1e-3) / 1e9,
             "gemm_tflops": (flops13 + flops2) / ((stage_mean["gemm_w13"] +
