@@ -61,23 +61,23 @@ RouteWs carve_route(Carver& c, const moe_dims* d) {
 }
 
 struct PlanWs {
-  int4* small_items;
-  int4* medium_items;
-  int4* large_items;
-  int32_t* counts;
-  int max_small, max_medium, max_large;
+  PlanOut out;                    // per-variant item lists and their lengths
+  int max_items[kNumVariants];
 };
 
 PlanWs carve_plan(Carver& c, const moe_dims* d) {
   PlanWs p;
   const int G = groups_G(d);
-  p.max_small = G;
-  p.max_medium = G;
-  p.max_large = static_cast<int>(rows_Rs(d) / kLargeBN + G + 1);
-  p.small_items = c.take<int4>(p.max_small);
-  p.medium_items = c.take<int4>(p.max_medium);
-  p.large_items = c.take<int4>(p.max_large);
-  p.counts = c.take<int32_t>(4);
+  const long long Rs = rows_Rs(d);
+  p.max_items[0] = G;                                         // one item per group
+  p.max_items[1] = G;
+  p.max_items[2] = static_cast<int>(Rs / (kMediumBN + 1) + G + 1);  // chunks of > 64 rows
+  p.max_items[3] = static_cast<int>(Rs / (kMidBN + 1) + G + 1);     // chunks of > 128 rows
+  for (int v = 0; v < kNumVariants; ++v) {
+    p.out.items[v] = c.take<int4>(p.max_items[v]);
+    p.out.capacity[v] = p.max_items[v];
+  }
+  p.out.counts = c.take<int32_t>(kNumVariants);
   return p;
 }
 
@@ -157,13 +157,11 @@ int run_gemm(const moe_dims* d, const uint8_t* act, const uint8_t* act_s, const 
   a.N = N;
   a.K = K;
   a.rows_total = static_cast<int>(rows_Rs(d));
-  a.small_items = plan.small_items;
-  a.medium_items = plan.medium_items;
-  a.large_items = plan.large_items;
-  a.item_counts = plan.counts;
-  a.max_small = plan.max_small;
-  a.max_medium = plan.max_medium;
-  a.max_large = plan.max_large;
+  for (int v = 0; v < kNumVariants; ++v) {
+    a.items[v] = plan.out.items[v];
+    a.max_items[v] = plan.max_items[v];
+  }
+  a.item_counts = plan.out.counts;
   a.max_group_rows = max_group_rows;
   a.status = status;
   return cuda_rc(launch_grouped_gemm(a, st));
@@ -259,9 +257,7 @@ int moe_grouped_gemm_w13(const moe_dims* d, const uint8_t* xq, const uint8_t* xs
   Carver c(ws);
   GemmWs g = carve_gemm(c, d);
   if (cudaMemsetAsync(g.status, 0, sizeof(uint32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
-  cudaError_t e = launch_plan(group_offsets, groups_G(d), g.plan.small_items,
-                              g.plan.medium_items, g.plan.large_items, g.plan.counts, g.status,
-                              st);
+  cudaError_t e = launch_plan(group_offsets, groups_G(d), g.plan.out, g.status, st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   const uint8_t* act = xq;
   const uint8_t* act_s = xs;
@@ -297,9 +293,7 @@ int moe_grouped_gemm_w2(const moe_dims* d, const uint8_t* hq, const uint8_t* hs,
   Carver c(ws);
   GemmWs g = carve_gemm(c, d);
   if (cudaMemsetAsync(g.status, 0, sizeof(uint32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
-  cudaError_t e = launch_plan(group_offsets, groups_G(d), g.plan.small_items,
-                              g.plan.medium_items, g.plan.large_items, g.plan.counts, g.status,
-                              st);
+  cudaError_t e = launch_plan(group_offsets, groups_G(d), g.plan.out, g.status, st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   return run_gemm(d, hq, hs, group_offsets, w2, w2_s, d->H, d->I, y2, g.plan,
                   static_cast<int>(rows_Rs(d)), g.status, st);
@@ -391,9 +385,7 @@ int moe_forward_timed(const moe_dims* d, const uint16_t* x, const float* logits,
   if (T <= kPrepMaxT) {
     // decode: route + histogram + permute + tile plan in one CTA
     MOE_TRY(launch_prep_small(logits, T, E, k, d->has_shared, f.idx, f.w, f.counts, f.offsets,
-                              f.perm_src, f.inv, f.gemm.plan.small_items,
-                              f.gemm.plan.medium_items, f.gemm.plan.large_items,
-                              f.gemm.plan.counts, status, st))
+                              f.perm_src, f.inv, f.gemm.plan.out, status, st))
   } else {
     MOE_TRY(launch_route(logits, T, E, k, f.idx, f.w, status, st))
     MOE_TRY(launch_permute(f.idx, T, E, k, d->has_shared, f.route.blockcnt, f.route.blockbase,
@@ -406,9 +398,7 @@ int moe_forward_timed(const moe_dims* d, const uint16_t* x, const float* logits,
                                st))
   MOE_MARK(2)
   if (T > kPrepMaxT) {
-    MOE_TRY(launch_plan(f.offsets, groups_G(d), f.gemm.plan.small_items,
-                        f.gemm.plan.medium_items, f.gemm.plan.large_items, f.gemm.plan.counts,
-                        status, st))
+    MOE_TRY(launch_plan(f.offsets, groups_G(d), f.gemm.plan.out, status, st))
   }
   MOE_MARK(3)
   // every group (a routed expert or the shared expert) holds at most T rows

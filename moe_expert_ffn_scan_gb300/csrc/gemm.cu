@@ -104,6 +104,7 @@ struct GemmCfg {
   static_assert(OCC == 1 || OCC * (kSmemBytes + 1024) <= 233472,
                 "co-resident CTAs must fit shared memory together");
   static_assert(!(kTokenThread && kIssuers > 1), "warp 3 has one role");
+  static_assert(kSmemBytes <= 232448, "dynamic shared memory of one CTA");
 };
 
 // Instruction descriptor, kind::mxf8f6f4 block-scaled: A = E2M1 (5), B = E4M3 (0),
@@ -592,9 +593,10 @@ cudaError_t launch_one(const CUtensorMap& tmW, const CUtensorMap& tmX, const Gem
   GemmParams q = p;
   q.max_items = max_items;
   // The large variant (one CTA per SM) runs ~8% slower at 32K tokens when launched as a
-  // programmatic dependent (measured; cause not identified), so it waits for its
-  // predecessor the plain way.  The small and medium variants keep the overlap.
-  return launch_k_pdl(BN_MAX <= 64, kern, grid, 256, C::kSmemBytes, st, tmW, tmX, q);
+  // programmatic dependent (measured; cause not identified), so the one-CTA-per-SM
+  // variants wait for their predecessor the plain way.  The two-CTA-per-SM small and
+  // medium variants keep the overlap.
+  return launch_k_pdl(OCC > 1, kern, grid, 256, C::kSmemBytes, st, tmW, tmX, q);
 }
 
 }  // namespace
@@ -667,13 +669,16 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& a, cudaStream_t st) {
   // A list whose groups cannot exist (no group has more than max_group_rows rows) is
   // provably empty and not launched.
   cudaError_t e = launch_variant<kSmallBN, kSmallStages, kSmallStagesKO1, kSmallOcc>(
-      a, p, a.small_items, a.item_counts, a.max_small, st);
+      a, p, a.items[0], a.item_counts, a.max_items[0], st);
   if (e != cudaSuccess || a.max_group_rows <= kSmallBN) return e;
   e = launch_variant<kMediumBN, kMediumStages, kMediumStagesKO1, kMediumOcc>(
-      a, p, a.medium_items, a.item_counts + 1, a.max_medium, st);
+      a, p, a.items[1], a.item_counts + 1, a.max_items[1], st);
   if (e != cudaSuccess || a.max_group_rows <= kMediumBN) return e;
+  e = launch_variant<kMidBN, kMidStages, kMidStagesKO1, 1>(a, p, a.items[2],
+                                                           a.item_counts + 2, a.max_items[2], st);
+  if (e != cudaSuccess || a.max_group_rows <= kMidBN) return e;
   return launch_variant<kLargeBN, kLargeStages, kLargeStagesKO1, 1>(
-      a, p, a.large_items, a.item_counts + 2, a.max_large, st);
+      a, p, a.items[3], a.item_counts + 3, a.max_items[3], st);
 }
 
 }  // namespace moe

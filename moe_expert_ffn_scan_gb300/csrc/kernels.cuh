@@ -32,8 +32,10 @@ cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
 // GEMM variants, chosen per group by its row count M (the tile plan):
 //   small  M <= 16: N = 16 tokens, 2 CTAs per SM, 3 stages of two 128-K sub-tiles;
 //   medium M <= 64: N <= 64, 2 CTAs per SM, 2 stages;
-//   large  M > 64: chunks of <= 224 rows (an N = 224 MMA carries more tensor work than
-//          its issue cost), 1 CTA per SM, 2 stages.
+//   larger M is cut into ceil(M / 240) near-equal chunks (multiples of 16 rows):
+//   mid    chunks of <= 128 rows: N <= 128, 1 CTA per SM, 3 stages;
+//   large  chunks of 129..240 rows: N <= 240 (an N = 240 MMA carries more tensor work
+//          than its issue cost), 1 CTA per SM, 2 stages (all the shared memory).
 // With K/128 odd the stages hold one sub-tile (the *KO1 stage counts).
 constexpr int kSmallBN = 16;
 constexpr int kSmallStages = 3;
@@ -43,18 +45,29 @@ constexpr int kMediumBN = 64;
 constexpr int kMediumStages = 2;
 constexpr int kMediumStagesKO1 = 4;
 constexpr int kMediumOcc = 2;
+constexpr int kMidBN = 128;
+constexpr int kMidStages = 3;
+constexpr int kMidStagesKO1 = 5;
 constexpr int kLargeBN = 240;
 constexpr int kLargeStages = 2;
 constexpr int kLargeStagesKO1 = 2;
+
+// The tile plan's work lists, one per variant (0 small, 1 medium, 2 mid, 3 large),
+// each {group, row0, rows, 0} in group order, and their lengths.
+constexpr int kNumVariants = 4;
+struct PlanOut {
+  int4* items[kNumVariants];
+  int32_t* counts;                 // [kNumVariants]
+  int32_t capacity[kNumVariants];  // list lengths; items past them are not written
+};
 
 // Token count up to which route + histogram + permute + plan run as one CTA.
 constexpr int kPrepMaxT = 128;
 
 cudaError_t launch_prep_small(const float* logits, int T, int E, int k, int has_shared,
                               int32_t* idx, float* w, int32_t* counts, int32_t* offsets,
-                              int32_t* perm_src, int32_t* inv, int4* small_items,
-                              int4* medium_items, int4* large_items, int32_t* item_counts,
-                              uint32_t* status, cudaStream_t st);
+                              int32_t* perm_src, int32_t* inv, PlanOut plan, uint32_t* status,
+                              cudaStream_t st);
 cudaError_t launch_quant_scatter(const uint16_t* x, int T, int H, int k, int has_shared,
                                  const int32_t* inv, uint8_t* xq, uint8_t* xs, uint8_t* xg,
                                  uint8_t* xsg, uint32_t* status, cudaStream_t st);
@@ -65,8 +78,7 @@ cudaError_t launch_permute(const int32_t* idx, int T, int E, int k, int has_shar
                            int32_t* blockcnt, int32_t* blockbase, int32_t* counts,
                            int32_t* offsets, int32_t* perm_src, int32_t* inv, uint32_t* status,
                            cudaStream_t st);
-cudaError_t launch_plan(const int32_t* offsets, int G, int4* small_items, int4* medium_items,
-                        int4* large_items, int32_t* item_counts, uint32_t* status,
+cudaError_t launch_plan(const int32_t* offsets, int G, PlanOut plan, uint32_t* status,
                         cudaStream_t st);
 
 cudaError_t launch_quant_act(const uint16_t* x, int rows, int cols, uint8_t* q, uint8_t* s,
@@ -94,11 +106,9 @@ struct GemmLaunch {
   const uint8_t* act_scales;  // [rows_total][K/128]
   uint16_t* y;                // [rows_total][N]
   int G, N, K, rows_total;
-  const int4* small_items;
-  const int4* medium_items;
-  const int4* large_items;
-  const int32_t* item_counts;  // [3]: small, medium, large
-  int max_small, max_medium, max_large;
+  const int4* items[kNumVariants];
+  const int32_t* item_counts;  // [kNumVariants]
+  int max_items[kNumVariants];
   int max_group_rows;          // upper bound on any group's row count
   uint32_t* status;
 };

@@ -231,8 +231,9 @@ __global__ void __launch_bounds__(kPermTokens) k_permute_block(
 // Per group g with M = offsets[g+1] - offsets[g] rows (the effective M the pages tune
 // for): M <= kSmallBN -> one small-M item (padded only to 16 tokens, never to a large
 // tile); M <= kMediumBN -> one medium item; larger groups are split into
-// ceil(M / kLargeBN) near-equal chunks (multiples of 16 rows except the last) for the
-// large-M kernel.  Items are {group, row0, rows, 0}.  One CTA of 1024 threads; each
+// ceil(M / kLargeBN) near-equal chunks (multiples of 16 rows except the last), which go
+// to the mid kernel when they are at most kMidBN rows and to the large kernel
+// otherwise.  Items are {group, row0, rows, 0}.  One CTA of 1024 threads; each
 // thread owns a contiguous run of groups; positions come from block-wide scans, so
 // the lists are in group order and deterministic.
 __device__ __forceinline__ int32_t block_exclusive_scan(int32_t v, int32_t* s_warp,
@@ -262,61 +263,63 @@ __device__ __forceinline__ int32_t block_exclusive_scan(int32_t v, int32_t* s_wa
   return excl;
 }
 
-// Builds the three item lists from group offsets (global or shared memory).  Called
-// by all 1024 threads of one CTA.
-__device__ void plan_groups(const int32_t* offsets, int G, int4* __restrict__ small_items,
-                            int4* __restrict__ medium_items, int4* __restrict__ large_items,
-                            int32_t* __restrict__ item_counts, uint32_t* status,
-                            int32_t* s_warp) {
+// Variant of a group with m > 0 rows and the chunking of the two chunked variants.
+__device__ __forceinline__ int plan_variant(int32_t m, int32_t& nch, int32_t& base) {
+  nch = 1;
+  base = m;
+  if (m <= kSmallBN) return 0;
+  if (m <= kMediumBN) return 1;
+  nch = (m + kLargeBN - 1) / kLargeBN;
+  base = ((m + nch - 1) / nch + 15) / 16 * 16;
+  return base <= kMidBN ? 2 : 3;
+}
+
+// Builds the per-variant item lists from group offsets (global or shared memory).
+// Called by all 1024 threads of one CTA.
+__device__ void plan_groups(const int32_t* offsets, int G, const PlanOut& plan,
+                            uint32_t* status, int32_t* s_warp) {
   const int tid = threadIdx.x;
   const int per = (G + 1023) / 1024;
   const int g0 = tid * per, g1 = min(G, g0 + per);
-  int32_t ns = 0, nm = 0, nl = 0;
+  int32_t n[kNumVariants] = {0, 0, 0, 0};
   for (int g = g0; g < g1; ++g) {
     int32_t m = offsets[g + 1] - offsets[g];
     if (m < 0) set_status(status, STATUS_BAD_PLAN);
     if (m <= 0) continue;
-    if (m <= kSmallBN) ++ns;
-    else if (m <= kMediumBN) ++nm;
-    else nl += (m + kLargeBN - 1) / kLargeBN;
+    int32_t nch, base;
+    const int v = plan_variant(m, nch, base);  // (not folded into n[...] += nch: the
+    n[v] += nch;                               // right operand would be read first)
   }
-  int32_t ts, tm, tl;
-  int32_t ps = block_exclusive_scan(ns, s_warp, &ts);
-  int32_t pm = block_exclusive_scan(nm, s_warp, &tm);
-  int32_t pl = block_exclusive_scan(nl, s_warp, &tl);
+  int32_t pos[kNumVariants], tot[kNumVariants];
+#pragma unroll
+  for (int v = 0; v < kNumVariants; ++v) pos[v] = block_exclusive_scan(n[v], s_warp, &tot[v]);
   for (int g = g0; g < g1; ++g) {
     int32_t r0 = offsets[g], m = offsets[g + 1] - r0;
     if (m <= 0) continue;
-    if (m <= kSmallBN) {
-      small_items[ps++] = make_int4(g, r0, m, 0);
-    } else if (m <= kMediumBN) {
-      medium_items[pm++] = make_int4(g, r0, m, 0);
-    } else {
-      int32_t nch = (m + kLargeBN - 1) / kLargeBN;
-      int32_t base = ((m + nch - 1) / nch + 15) / 16 * 16;
-      for (int c = 0; c < nch; ++c) {
-        int32_t a = c * base, b = min(m, a + base);
-        large_items[pl++] = make_int4(g, r0 + a, a < m ? b - a : 0, 0);
+    int32_t nch, base;
+    const int v = plan_variant(m, nch, base);
+    for (int c = 0; c < nch; ++c) {
+      int32_t a = c * base, b = min(m, a + base);
+      const int32_t p = pos[v]++;
+      if (p >= plan.capacity[v]) {  // cannot happen with consistent offsets; never write past
+        set_status(status, STATUS_BAD_PLAN);
+        continue;
       }
+      plan.items[v][p] = make_int4(g, r0 + a, a < m ? b - a : 0, 0);
     }
   }
   if (tid == 0) {
-    item_counts[0] = ts;
-    item_counts[1] = tm;
-    item_counts[2] = tl;
+#pragma unroll
+    for (int v = 0; v < kNumVariants; ++v) plan.counts[v] = min(tot[v], plan.capacity[v]);
   }
 }
 
 __global__ void __launch_bounds__(1024) k_plan(const int32_t* __restrict__ offsets, int G,
-                                               int4* __restrict__ small_items,
-                                               int4* __restrict__ medium_items,
-                                               int4* __restrict__ large_items,
-                                               int32_t* __restrict__ item_counts,
-                                               uint32_t* status) {
+                                               const PlanOut plan, uint32_t* status) {
   pdl_wait();
   pdl_trigger();
   __shared__ int32_t s_warp[32];
-  plan_groups(offsets, G, small_items, medium_items, large_items, item_counts, status, s_warp);
+  plan_groups(offsets, G, plan, status, s_warp);
 }
 
 // ------------------------------------------------ a1 + a2 + a8 in one CTA (small T) ---
@@ -331,8 +334,7 @@ __global__ void __launch_bounds__(1024) k_prep_small(
     const float* __restrict__ logits, int T, int E, int k, int has_shared,
     int32_t* __restrict__ idx, float* __restrict__ w, int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ perm_src, int32_t* __restrict__ inv,
-    int4* __restrict__ small_items, int4* __restrict__ medium_items,
-    int4* __restrict__ large_items, int32_t* __restrict__ item_counts, uint32_t* status) {
+    const PlanOut plan, uint32_t* status) {
   pdl_wait();
   pdl_trigger();
   // the first kernel of a call clears the call's status word; every later set of a
@@ -400,7 +402,7 @@ __global__ void __launch_bounds__(1024) k_prep_small(
     perm_src[p] = i;
     inv[i] = p;
   }
-  plan_groups(s_off, G, small_items, medium_items, large_items, item_counts, status, s_warp);
+  plan_groups(s_off, G, plan, status, s_warp);
 }
 
 // ---------------------------------------------------------------- launchers -------
@@ -449,25 +451,21 @@ cudaError_t launch_permute(const int32_t* idx, int T, int E, int k, int has_shar
                   perm_src, inv);
 }
 
-cudaError_t launch_plan(const int32_t* offsets, int G, int4* small_items, int4* medium_items,
-                        int4* large_items, int32_t* item_counts, uint32_t* status,
+cudaError_t launch_plan(const int32_t* offsets, int G, PlanOut plan, uint32_t* status,
                         cudaStream_t st) {
-  return launch_k(k_plan, 1, 1024, 0, st, offsets, G, small_items, medium_items, large_items,
-                  item_counts, status);
+  return launch_k(k_plan, 1, 1024, 0, st, offsets, G, plan, status);
 }
 
 cudaError_t launch_prep_small(const float* logits, int T, int E, int k, int has_shared,
                               int32_t* idx, float* w, int32_t* counts, int32_t* offsets,
-                              int32_t* perm_src, int32_t* inv, int4* small_items,
-                              int4* medium_items, int4* large_items, int32_t* item_counts,
-                              uint32_t* status, cudaStream_t st) {
+                              int32_t* perm_src, int32_t* inv, PlanOut plan, uint32_t* status,
+                              cudaStream_t st) {
   if (T > kPrepMaxT) return cudaErrorInvalidValue;
   const int epl = (E + 31) / 32;
 #define MOE_PREP_CASE(N)                                                                    \
   if (epl <= N) {                                                                           \
     return launch_k(k_prep_small<N>, 1, 1024, 0, st, logits, T, E, k, has_shared, idx, w,   \
-                    counts, offsets, perm_src, inv, small_items, medium_items, large_items, \
-                    item_counts, status);                                                   \
+                    counts, offsets, perm_src, inv, plan, status);                          \
   }
   MOE_PREP_CASE(1)
   MOE_PREP_CASE(2)
