@@ -488,7 +488,11 @@ def run_ours(args, rank, world, local):
                "sample": f"{n} token of the {args.workload} workload (its top-{d.k} experts + "
                          f"shared expert), full layer in float64 numpy, {dt:.2f} s"}
 
-    launches_per_step = (6 if d.T <= 128 else 10) + (2 if d.T > 16 else 0) + (2 if d.T > 64 else 0)
+    # per forward: prep / quant-scatter / SwiGLU / combine (T <= 128) or route, histogram,
+    # scan, permute, quant-scatter, plan, SwiGLU, combine; per GEMM one launch per
+    # variant a group of up to T rows can need (small, medium > 16, mid > 64, large > 128)
+    gemm_variants = 1 + (d.T > 16) + (d.T > 64) + (d.T > 128)
+    launches_per_step = (4 if d.T <= 128 else 8) + 2 * gemm_variants
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
