@@ -223,6 +223,15 @@ int moe_forward_timed(const moe_dims* d, const uint16_t* x, const float* logits,
  * cleared by moe_forward / moe_route / the GEMMs at their start. */
 int moe_check_status(const void* ws, void* stream, uint32_t* bits_out);
 
+/* Failure-path self-test; the pages have no counterpart.  Launches one CTA whose
+ * mbarrier wait can never complete (nothing arrives), so the library's bounded wait
+ * (kWaitLimitNs = 2 s of the GPU's global timer) gives up, sets STATUS_WAIT_TIMEOUT
+ * (bit 0) in the status word at the start of ws and returns: the path every GEMM wait
+ * takes if a TMA copy or MMA never completes.  moe_check_status(ws) then returns
+ * MOE_ERR_DEVICE_CHECK with bit 0 set, and the context stays usable.  About 2 s of GPU
+ * time.  ws: >= 256 bytes, 256-byte aligned (its status word is overwritten). */
+int moe_selftest_wait_timeout(void* ws, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

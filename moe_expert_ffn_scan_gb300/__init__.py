@@ -84,6 +84,7 @@ def lib():
                                         ctypes.POINTER(moe_debug_out), ctypes.POINTER(_P), _P,
                                         _SZ, _P]
         L.moe_check_status.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_uint32)]
+        L.moe_selftest_wait_timeout.argtypes = [_P, _P]
         for fn in ("moe_route", "moe_quant_act", "moe_grouped_gemm_w13", "moe_swiglu_quant",
                    "moe_grouped_gemm_w2", "moe_combine", "moe_forward", "moe_forward_timed",
                    "moe_check_status"):
@@ -240,6 +241,11 @@ def moe_check_status(ws, stream=None) -> int:
     if rc not in (MOE_OK, 5):
         raise MoeError("moe_check_status", rc)
     return bits.value
+
+
+def moe_selftest_wait_timeout(ws, stream=None):
+    """Runs the failure-path self-test (a wait that must time out) on ws's status word."""
+    _check("moe_selftest_wait_timeout", lib().moe_selftest_wait_timeout(_p(ws), _stream(stream)))
 
 
 def debug_buffers(d, device="cuda"):

@@ -167,6 +167,25 @@ int run_gemm(const moe_dims* d, const uint8_t* act, const uint8_t* act_s, const 
   return cuda_rc(launch_grouped_gemm(a, st));
 }
 
+// One CTA, one waiting thread: an mbarrier that nothing arrives at.  The bounded wait
+// must give up (STATUS_WAIT_TIMEOUT) and raise the CTA's abort flag; anything else is
+// reported as STATUS_BAD_PLAN.
+__global__ void k_selftest_wait(uint32_t* status) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    volatile int* ab = &abort_flag;
+    const bool completed = mbar_wait(&bar, 0, status, ab);
+    if (completed || *ab == 0) set_status(status, STATUS_BAD_PLAN);
+  }
+}
+
 bool weights_ok(const uint8_t* c, const uint8_t* s) {
   return c && s && aligned(c, 32) && aligned(s, 16);
 }
@@ -417,6 +436,14 @@ int moe_forward_timed(const moe_dims* d, const uint16_t* x, const float* logits,
 #undef MOE_TRY
 #undef MOE_MARK
   return MOE_OK;
+}
+
+int moe_selftest_wait_timeout(void* ws, void* stream) {
+  if (!ws || !aligned(ws, kAlign)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t* status = static_cast<uint32_t*>(ws);
+  if (cudaMemsetAsync(status, 0, sizeof(uint32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
+  return cuda_rc(launch_k(k_selftest_wait, 1, 32, 0, st, status));
 }
 
 int moe_check_status(const void* ws, void* stream, uint32_t* bits_out) {

@@ -81,6 +81,8 @@ def test_validation_happens_before_any_launch(lib):
     # workspace too small
     assert lib.moe_route(ctypes.byref(d), P(0x1000), P(0x1000), P(0x1000), P(0x1000),
                          P(0x1000), P(0x1000), P(0x1000), P(0x10000), 16, None) == 3
+    assert lib.moe_selftest_wait_timeout(None, None) == 1
+    assert lib.moe_selftest_wait_timeout(P(0x1008), None) == 1
     # host-buffer forward: dims, nulls, workspace size and alignment
     w = moe.moe_weights(0x10000, 0x10000, 0x10000, 0x10000)
     assert lib.moe_forward_host(ctypes.byref(bad), P(0x1000), P(0x1000), ctypes.byref(w),
