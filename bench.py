@@ -279,7 +279,11 @@ def run_reference(args, rank, world):
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     d, t = make_layer(args, args.seed, dev)
     hv = host_view(d, t)
-    tokens = 1
+    # tokens per step: one, or more when one is quick, keeping the whole run at about
+    # three minutes (the tiny layer runs in full every step)
+    _, t1 = oracle_sample(d, hv, 1, args.seed)
+    per_step = min(10.0, 180.0 / max(1, args.steps + args.warmup))
+    tokens = max(1, min(d.T, int(per_step / max(t1, 1e-3))))
     times = []
     n_done = 0
     for i in range(args.warmup + args.steps):
@@ -298,8 +302,11 @@ def run_reference(args, rank, world):
                    "k": d.k, "shared_experts": d.has_shared},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": blas_threads(),
                          "kind": "oracle",
-                         "sample": f"{tokens} token(s) per step, its top-{d.k} experts and "
-                                   "the shared expert, full layer in float64 numpy"},
+                         "sample": f"{tokens} token(s) per step"
+                                   + (" (the whole layer)" if tokens == d.T else "")
+                                   + f", their top-{d.k} experts"
+                                   + (" and the shared expert" if d.has_shared else "")
+                                   + ", full layer in float64 numpy"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -399,6 +406,9 @@ def run_ours(args, rank, world, local):
         torch.cuda.synchronize()
         flushed_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in fe), world)
     ms = statistics.mean(step_ms)
+    qs = (statistics.quantiles(step_ms, n=10, method="inclusive") if len(step_ms) >= 2
+          else [ms] * 9)
+    pct = {"p10": qs[0], "p50": statistics.median(step_ms), "p90": qs[8]}
     ms_max = max_over_ranks(ms, world)
     value = world * d.T / (ms_max * 1e-3)
     stage_mean = {s: statistics.mean(v) for s, v in stage_ms.items()}
@@ -483,10 +493,17 @@ def run_ours(args, rank, world, local):
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         hv = host_view(d, t)
+        # one token first; when that is quick, as many more as about 10 s of oracle
+        # work allows (the tiny layer runs in full)
         n, dt = oracle_sample(d, hv, 1, args.seed)
+        more = min(d.T, int(10.0 / max(dt, 1e-3)))
+        if more > 1:
+            n, dt = oracle_sample(d, hv, more, args.seed)
+        whole = " (the whole layer)" if n == d.T else ""
+        shared = " + shared expert" if d.has_shared else ""
         cpu = {"value": n / dt, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
-               "sample": f"{n} token of the {args.workload} workload (its top-{d.k} experts + "
-                         f"shared expert), full layer in float64 numpy, {dt:.2f} s"}
+               "sample": f"{n} token(s) of the {args.workload} workload{whole}, their top-{d.k} "
+                         f"experts{shared}, full layer in float64 numpy, {dt:.2f} s"}
 
     # per forward: prep / quant-scatter / SwiGLU / combine (T <= 128) or route, histogram,
     # scan, permute, quant-scatter, plan, SwiGLU, combine; per GEMM one launch per
@@ -507,6 +524,7 @@ def run_ours(args, rank, world, local):
             "stage_ms": stage_mean,
             "stream_ms_per_step": stream_step_ms,
             "ms_per_step_l2_write_flushed": flushed_ms,
+            "ms_per_step_percentiles": pct,
             "weight_gbs": (w13_bytes + w2_bytes) / ((stage_mean["gemm_w13"] +
                                                      stage_mean["gemm_w2"]) * 1e-3) / 1e9,
             "gemm_tflops": (flops13 + flops2) / ((stage_mean["gemm_w13"] +
