@@ -112,3 +112,14 @@ def test_python_binding_rejects_host_tensors(lib):
     with pytest.raises(ValueError):
         moe.moe_quant_act(x, torch.zeros(4, 128, dtype=torch.uint8),
                           torch.zeros(4, 1, dtype=torch.uint8))
+
+
+def test_missing_library_fails_loudly(monkeypatch):
+    """No fallback: with the library absent every call raises instead of computing
+    anything another way."""
+    monkeypatch.setattr(moe, "_LIB", None)
+    monkeypatch.setattr(moe, "LIB_PATH", os.path.join(ROOT, "no_such_dir", "libmoe.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        moe.workspace_size(moe.dims(7, 512, 256, 8, 2, 0))
+    with pytest.raises(RuntimeError, match="missing"):
+        moe.MoELayer(512, 256, 8, 2, 0, None, None, None, None).workspace(7)
