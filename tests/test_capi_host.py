@@ -123,3 +123,26 @@ def test_missing_library_fails_loudly(monkeypatch):
         moe.workspace_size(moe.dims(7, 512, 256, 8, 2, 0))
     with pytest.raises(RuntimeError, match="missing"):
         moe.MoELayer(512, 256, 8, 2, 0, None, None, None, None).workspace(7)
+
+
+def test_header_is_plain_c_and_links(lib, tmp_path):
+    """include/moe.h compiles as pedantic C99 and a C program links against libmoe.so
+    and queries a workspace size (host-only call)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "t.c"
+    src.write_text(
+        '#include "moe.h"\n#include <stdio.h>\n'
+        'int main(void) { moe_dims d = {7, 7168, 3072, 384, 8, 1};\n'
+        '  printf("%zu\\n", moe_workspace_size(&d)); return 0; }\n')
+    exe = tmp_path / "t"
+    libdir = os.path.dirname(moe.LIB_PATH)
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                        "-I" + os.path.join(ROOT, "include"), str(src), "-L" + libdir, "-lmoe",
+                        "-Wl,-rpath," + libdir, "-o", str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout
+    assert int(out) == moe.workspace_size(moe.dims(7, 7168, 3072, 384, 8, 1)) > 0
