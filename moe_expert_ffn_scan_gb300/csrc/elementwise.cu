@@ -22,57 +22,84 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
   }
 }
 
-// Quantise 8 values held by one lane of a 16-lane group that covers a 128-column
-// block.  Returns the 8 codes packed little-endian; writes the scale byte via lane 0
-// of the group.
-__device__ __forceinline__ uint2 quant8(const float (&f)[8], uint8_t* scale_out, int sublane) {
-  // every lane of the 16-lane group gets the same scale; lane `sublane == 0` stores it
+// Quantise the 16 values one lane of an 8-lane group holds; the group covers one
+// 128-column block.  Returns the 16 codes packed little-endian and the block's scale
+// exponent (the same in every lane of the group).  All 32 lanes must call it.
+__device__ __forceinline__ uint4 quant16(const float (&f)[16], int& e) {
   float amax = 0.f;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
 #pragma unroll
-  for (int off = 8; off > 0; off >>= 1)
+  for (int off = 4; off > 0; off >>= 1)
     amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
-  const int e = fp8_scale_exponent(amax);
+  e = fp8_scale_exponent(amax);
   const float s = pow2_neg(e);
-  uint32_t c[4];
+  uint32_t c[8];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) c[i] = e4m3x2(f[2 * i] * s, f[2 * i + 1] * s);
-  if (sublane == 0) *scale_out = static_cast<uint8_t>(e + 127);
-  return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+  for (int i = 0; i < 8; ++i) c[i] = e4m3x2(f[2 * i] * s, f[2 * i + 1] * s);
+  return make_uint4(c[0] | (c[1] << 16), c[2] | (c[3] << 16), c[4] | (c[5] << 16),
+                    c[6] | (c[7] << 16));
 }
+
+__device__ __forceinline__ void load_bf16x16(const uint16_t* p, float (&f)[16]) {
+  const uint4* q = reinterpret_cast<const uint4*>(p);
+  float lo[8], hi[8];
+  bf16x8_to_f32(q[0], lo);
+  bf16x8_to_f32(q[1], hi);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    f[i] = lo[i];
+    f[8 + i] = hi[i];
+  }
+}
+
+// Thread -> (row, 128-column block, lane in the block's 8-lane group).  Idx is the
+// index type: 32-bit whenever 8 x rows x blocks-per-row fits (one 32-bit division per
+// thread), 64-bit otherwise.
+template <typename Idx>
+struct BlockLane {
+  Idx r, b;
+  int sub;
+  bool live;
+  __device__ __forceinline__ BlockLane(int rows, int nblk) {
+    const Idx gid = static_cast<Idx>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const Idx blk = gid >> 3;
+    sub = static_cast<int>(gid & 7);
+    live = blk < static_cast<Idx>(rows) * static_cast<Idx>(nblk);
+    r = live ? blk / static_cast<Idx>(nblk) : 0;
+    b = live ? blk - r * static_cast<Idx>(nblk) : 0;
+  }
+};
 
 }  // namespace
 
-// a3.  One warp per two 128-column blocks; 16 lanes x 8 values per block.
+// a3.  Eight lanes per 128-column block, 16 values (two 16-byte loads) per lane.
+template <typename Idx>
 __global__ void __launch_bounds__(256) k_quant_act(const uint16_t* __restrict__ x, int rows,
                                                    int cols, uint8_t* __restrict__ q,
                                                    uint8_t* __restrict__ s) {
   pdl_wait();
   pdl_trigger();
   const int nblk = cols / 128;
-  const long long gw = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31, half = lane >> 4, sub = lane & 15;
-  const long long blk = gw * 2 + half;  // global 128-block id
-  const long long total = static_cast<long long>(rows) * nblk;
-  const bool live = blk < total;
-  const long long r = live ? blk / nblk : 0, b = live ? blk % nblk : 0;
-  float f[8];
-  if (live) {
-    uint4 u = *reinterpret_cast<const uint4*>(x + r * cols + b * 128 + sub * 8);
-    bf16x8_to_f32(u, f);
+  const BlockLane<Idx> L(rows, nblk);
+  float f[16];
+  if (L.live) {
+    load_bf16x16(x + static_cast<size_t>(L.r) * cols + L.b * 128 + L.sub * 16, f);
   } else {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) f[i] = 0.f;
+    for (int i = 0; i < 16; ++i) f[i] = 0.f;
   }
-  uint8_t dummy;
-  uint2 c = quant8(f, live ? s + r * nblk + b : &dummy, sub);
-  if (live) *reinterpret_cast<uint2*>(q + r * cols + b * 128 + sub * 8) = c;
+  int e;
+  const uint4 c = quant16(f, e);
+  if (!L.live) return;
+  *reinterpret_cast<uint4*>(q + static_cast<size_t>(L.r) * cols + L.b * 128 + L.sub * 16) = c;
+  if (L.sub == 0) s[static_cast<size_t>(L.r) * nblk + L.b] = static_cast<uint8_t>(e + 127);
 }
 
 // a3 fused with the packed-row gather: token t's codes and scales go to xq / xs
 // (when given) and straight to its k routed rows inv[t*k + j] and its shared row R + t
 // of the packed activations, so no separate gather pass re-reads them.
+template <typename Idx>
 __global__ void __launch_bounds__(256) k_quant_scatter(const uint16_t* __restrict__ x, int T,
                                                        int H, int k, int has_shared,
                                                        const int32_t* __restrict__ inv,
@@ -84,44 +111,42 @@ __global__ void __launch_bounds__(256) k_quant_scatter(const uint16_t* __restric
   pdl_wait();
   pdl_trigger();
   const int nblk = H / 128;
-  const long long gw = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31, half = lane >> 4, sub = lane & 15;
-  const long long blk = gw * 2 + half;
-  const long long total = static_cast<long long>(T) * nblk;
-  const bool live = blk < total;
-  const long long t = live ? blk / nblk : 0, b = live ? blk % nblk : 0;
-  float f[8];
-  if (live) {
-    uint4 u = *reinterpret_cast<const uint4*>(x + t * H + b * 128 + sub * 8);
-    bf16x8_to_f32(u, f);
+  const BlockLane<Idx> L(T, nblk);
+  float f[16];
+  if (L.live) {
+    load_bf16x16(x + static_cast<size_t>(L.r) * H + L.b * 128 + L.sub * 16, f);
   } else {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) f[i] = 0.f;
+    for (int i = 0; i < 16; ++i) f[i] = 0.f;
   }
-  uint8_t scale;
-  uint2 c = quant8(f, &scale, 0);
-  if (!live) return;
+  int e;
+  const uint4 c = quant16(f, e);
+  if (!L.live) return;
+  const uint8_t scale = static_cast<uint8_t>(e + 127);
+  const size_t t = static_cast<size_t>(L.r);
+  const int col = static_cast<int>(L.b) * 128 + L.sub * 16;
+  if (xq) *reinterpret_cast<uint4*>(xq + t * H + col) = c;
+  if (xs && L.sub == 0) xs[t * nblk + L.b] = scale;
   const long long R = static_cast<long long>(T) * k;
-  if (xq) *reinterpret_cast<uint2*>(xq + t * H + b * 128 + sub * 8) = c;
-  if (xs && sub == 0) xs[t * nblk + b] = scale;
   for (int j = 0; j <= k; ++j) {
     long long r;
     if (j < k) {
       r = inv[t * k + j];
       if (r < 0 || r >= R) {
-        if (sub == 0) set_status(status, STATUS_BAD_INDEX);
+        if (L.sub == 0) set_status(status, STATUS_BAD_INDEX);
         continue;
       }
     } else {
       if (!has_shared) break;
-      r = R + t;
+      r = R + static_cast<long long>(t);
     }
-    *reinterpret_cast<uint2*>(xg + r * H + b * 128 + sub * 8) = c;
-    if (sub == 0) xsg[r * nblk + b] = scale;
+    *reinterpret_cast<uint4*>(xg + r * H + col) = c;
+    if (L.sub == 0) xsg[r * nblk + L.b] = scale;
   }
 }
 
 // a5.  Row r of y13 holds [gate(I) | up(I)] in bf16; h = silu(gate) * up in fp32.
+template <typename Idx>
 __global__ void __launch_bounds__(256) k_swiglu_quant(const uint16_t* __restrict__ y13,
                                                       int rows, int I,
                                                       uint8_t* __restrict__ hq,
@@ -129,29 +154,25 @@ __global__ void __launch_bounds__(256) k_swiglu_quant(const uint16_t* __restrict
   pdl_wait();
   pdl_trigger();
   const int nblk = I / 128;
-  const long long gw = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31, half = lane >> 4, sub = lane & 15;
-  const long long blk = gw * 2 + half;
-  const long long total = static_cast<long long>(rows) * nblk;
-  const bool live = blk < total;
-  const long long r = live ? blk / nblk : 0, b = live ? blk % nblk : 0;
-  float h[8];
-  if (live) {
-    const uint16_t* row = y13 + r * (2LL * I);
-    uint4 ug = *reinterpret_cast<const uint4*>(row + b * 128 + sub * 8);
-    uint4 uu = *reinterpret_cast<const uint4*>(row + I + b * 128 + sub * 8);
-    float g[8], u[8];
-    bf16x8_to_f32(ug, g);
-    bf16x8_to_f32(uu, u);
+  const BlockLane<Idx> L(rows, nblk);
+  float h[16];
+  if (L.live) {
+    const uint16_t* g_at = y13 + static_cast<size_t>(L.r) * (2 * static_cast<size_t>(I)) +
+                           L.b * 128 + L.sub * 16;
+    float g[16], u[16];
+    load_bf16x16(g_at, g);
+    load_bf16x16(g_at + I, u);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) h[i] = __fdividef(g[i], 1.0f + __expf(-g[i])) * u[i];
+    for (int i = 0; i < 16; ++i) h[i] = __fdividef(g[i], 1.0f + __expf(-g[i])) * u[i];
   } else {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) h[i] = 0.f;
+    for (int i = 0; i < 16; ++i) h[i] = 0.f;
   }
-  uint8_t dummy;
-  uint2 c = quant8(h, live ? hs + r * nblk + b : &dummy, sub);
-  if (live) *reinterpret_cast<uint2*>(hq + r * I + b * 128 + sub * 8) = c;
+  int e;
+  const uint4 c = quant16(h, e);
+  if (!L.live) return;
+  *reinterpret_cast<uint4*>(hq + static_cast<size_t>(L.r) * I + L.b * 128 + L.sub * 16) = c;
+  if (L.sub == 0) hs[static_cast<size_t>(L.r) * nblk + L.b] = static_cast<uint8_t>(e + 127);
 }
 
 // Packed-row gather: row r of the packed activations is token tok(r)'s row.
@@ -247,33 +268,36 @@ __global__ void __launch_bounds__(128) k_combine(const uint16_t* __restrict__ y2
 
 // ---------------------------------------------------------------- launchers -------
 
-static unsigned grid_for_blocks(long long nblocks128) {
-  // two 128-column blocks per warp, 8 warps per CTA
-  long long warps = (nblocks128 + 1) / 2;
-  return static_cast<unsigned>((warps + 7) / 8);
+// Eight threads per 128-column block, 256 threads per CTA; the 32-bit-index kernel
+// runs whenever every thread index fits in 32 bits.
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_blocks(void (*k32)(KArgs...), void (*k64)(KArgs...),
+                                 long long nblocks128, cudaStream_t st, Args... args) {
+  if (nblocks128 == 0) return cudaSuccess;
+  const long long grid = (nblocks128 + 31) / 32;
+  if (grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+  return launch_k(grid * 256 <= 0xFFFFFFFFLL ? k32 : k64, static_cast<unsigned>(grid), 256, 0,
+                  st, args...);
 }
 
 cudaError_t launch_quant_act(const uint16_t* x, int rows, int cols, uint8_t* q, uint8_t* s,
                              cudaStream_t st) {
-  long long nb = static_cast<long long>(rows) * (cols / 128);
-  if (nb == 0) return cudaSuccess;
-  return launch_k(k_quant_act, grid_for_blocks(nb), 256, 0, st, x, rows, cols, q, s);
+  return launch_blocks(k_quant_act<uint32_t>, k_quant_act<unsigned long long>,
+                       static_cast<long long>(rows) * (cols / 128), st, x, rows, cols, q, s);
 }
 
 cudaError_t launch_quant_scatter(const uint16_t* x, int T, int H, int k, int has_shared,
                                  const int32_t* inv, uint8_t* xq, uint8_t* xs, uint8_t* xg,
                                  uint8_t* xsg, uint32_t* status, cudaStream_t st) {
-  long long nb = static_cast<long long>(T) * (H / 128);
-  if (nb == 0) return cudaSuccess;
-  return launch_k(k_quant_scatter, grid_for_blocks(nb), 256, 0, st, x, T, H, k, has_shared, inv,
-                  xq, xs, xg, xsg, status);
+  return launch_blocks(k_quant_scatter<uint32_t>, k_quant_scatter<unsigned long long>,
+                       static_cast<long long>(T) * (H / 128), st, x, T, H, k, has_shared, inv, xq,
+                       xs, xg, xsg, status);
 }
 
 cudaError_t launch_swiglu_quant(const uint16_t* y13, int rows, int I, uint8_t* hq, uint8_t* hs,
                                 cudaStream_t st) {
-  long long nb = static_cast<long long>(rows) * (I / 128);
-  if (nb == 0) return cudaSuccess;
-  return launch_k(k_swiglu_quant, grid_for_blocks(nb), 256, 0, st, y13, rows, I, hq, hs);
+  return launch_blocks(k_swiglu_quant<uint32_t>, k_swiglu_quant<unsigned long long>,
+                       static_cast<long long>(rows) * (I / 128), st, y13, rows, I, hq, hs);
 }
 
 cudaError_t launch_gather_rows(const uint8_t* xq, const uint8_t* xs, const int32_t* perm_src,
