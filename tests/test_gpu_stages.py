@@ -154,6 +154,11 @@ GEMM_SHAPES = [
     # mid variant: one chunk of 65..128 rows, or two of <= 128 (M = 241..256)
     ("w13", 3, 512, 1024, [256, 100, 250]),
     ("w2", 2, 1024, 640, [80, 128]),        # K/128 odd: one-sub-tile stages
+    # large variant: many weight tiles, long K with quads of scale bytes in flight, and
+    # N not a multiple of 256
+    ("w2", 2, 1536, 1536, [200, 129]),
+    ("w13", 3, 512, 7168, [224, 0, 190]),
+    ("w2", 2, 384, 512, [200, 150]),
 ]
 
 
@@ -175,11 +180,13 @@ def test_grouped_gemm_random_mxfp4(which, G, N, K, sizes):
     assert_float_close(y, ref, f"{which} y")
 
 
-def test_grouped_gemm_scale_addressing():
+@pytest.mark.parametrize("sizes", [[3, 20], [3, 200]])
+def test_grouped_gemm_scale_addressing(sizes):
     """Non-unit weight scales at one (row, 32-block) and activation scale at one
-    (row, 128-block): bit-exact on integer inputs."""
+    (row, 128-block): bit-exact on integer inputs (small variant; large variant, with
+    weight rows 129 and 200 in the second 128-row tile and token 150 in the second
+    token-scale atom)."""
     G, N, K = 2, 256, 512
-    sizes = [3, 20]
     offsets, aq, asc, wq, wsc = _gemm_case(G, N, K, sizes, seed=99, integer=True)
     wsc = wsc.clone()
     asc = asc.clone()
@@ -188,6 +195,8 @@ def test_grouped_gemm_scale_addressing():
     wsc[1, 129, 0] = 126
     asc[10, 2] = 128
     asc[1, 0] = 125
+    if offsets[-1] > 150:
+        asc[150, 3] = 126  # a token past the first 128 of a large-variant chunk
     y = _run_gemm("w13", G, N, K, offsets, aq, asc, wq, wsc)
     ref = o.grouped_gemm(aq.numpy(), asc.numpy(), offsets, wq.numpy(), wsc.numpy())
     assert np.array_equal(y, ref)
