@@ -208,6 +208,41 @@ int moe_forward_host(const moe_dims* d, const uint16_t* x_host, const float* log
                      const moe_weights* W, uint16_t* out_host, void* ws, size_t ws_bytes,
                      void* stream);
 
+/* Host-buffer pipeline: a sequence of layer steps whose inputs and outputs live in
+ * host memory, with the copies of one step overlapping the kernels of its neighbours.
+ * The library owns three CUDA streams (host->device copies, the layer, device->host
+ * copy) and 3 x depth events, created by moe_host_pipeline_create and released by
+ * moe_host_pipeline_destroy (the only calls here that create anything, and neither
+ * allocates device memory).  Step i uses staging slot i % depth of the caller's
+ * workspace: its two host->device copies wait until step i - depth has finished
+ * reading that slot, its kernels run in submission order on the pipeline's compute
+ * stream (so one forward workspace serves every step) once its copies landed and
+ * step i - depth's output left the slot, and its device->host copy follows its
+ * kernels.  Same results as moe_forward_host, step by step.  The pages have no
+ * counterpart (their layers run inside a serving engine with device-resident
+ * activations).
+ *   depth: 1..8 staging slots (2 overlaps each step's copies with its neighbours).
+ *   ws: moe_host_pipeline_workspace_size(d, depth) bytes, 256-byte aligned, owned
+ *       by the caller and not touched by anything else until destroy; the status
+ *       word moe_check_status reads is at its start.
+ *   W: copied (the pointers), the weights must stay valid until destroy.
+ *   submit: x_host [T][H] bf16, logits_host [T][E] fp32, out_host [T][H] bf16, host
+ *       pointers (pinned, or the copies are not asynchronous).  Returns after
+ *       enqueueing; the caller must not modify x_host / logits_host or read out_host
+ *       until moe_host_pipeline_sync returns (or until depth later submits were
+ *       made and synchronised).
+ *   sync: blocks until every submitted step's output is in host memory; MOE_ERR_CUDA
+ *       if a stream reported an error.
+ *   destroy: synchronises, then releases the streams, events and the handle. */
+typedef struct moe_host_pipeline moe_host_pipeline;
+size_t moe_host_pipeline_workspace_size(const moe_dims* d, int depth);
+int moe_host_pipeline_create(const moe_dims* d, const moe_weights* W, int depth, void* ws,
+                             size_t ws_bytes, moe_host_pipeline** out);
+int moe_host_pipeline_submit(moe_host_pipeline* p, const uint16_t* x_host,
+                             const float* logits_host, uint16_t* out_host);
+int moe_host_pipeline_sync(moe_host_pipeline* p);
+int moe_host_pipeline_destroy(moe_host_pipeline* p);
+
 /* moe_forward with per-stage timing.  events points to 8 cudaEvent_t handles created
  * by the caller (cudaEventCreate); the call records events[0] before the first stage
  * and events[i] after stage i: 1 route + histogram/scan/permute, 2 activation

@@ -85,6 +85,16 @@ def lib():
                                         _SZ, _P]
         L.moe_check_status.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_uint32)]
         L.moe_selftest_wait_timeout.argtypes = [_P, _P]
+        L.moe_host_pipeline_workspace_size.argtypes = [_DP, _I]
+        L.moe_host_pipeline_workspace_size.restype = _SZ
+        L.moe_host_pipeline_create.argtypes = [_DP, ctypes.POINTER(moe_weights), _I, _P, _SZ,
+                                               ctypes.POINTER(_P)]
+        L.moe_host_pipeline_submit.argtypes = [_P, _P, _P, _P]
+        L.moe_host_pipeline_sync.argtypes = [_P]
+        L.moe_host_pipeline_destroy.argtypes = [_P]
+        for fn in ("moe_host_pipeline_create", "moe_host_pipeline_submit",
+                   "moe_host_pipeline_sync", "moe_host_pipeline_destroy"):
+            getattr(L, fn).restype = ctypes.c_int
         for fn in ("moe_route", "moe_quant_act", "moe_grouped_gemm_w13", "moe_swiglu_quant",
                    "moe_grouped_gemm_w2", "moe_combine", "moe_forward", "moe_forward_timed",
                    "moe_check_status"):
@@ -131,6 +141,10 @@ def workspace_size(d) -> int:
 
 def host_workspace_size(d) -> int:
     return lib().moe_host_workspace_size(_d(d))
+
+
+def host_pipeline_workspace_size(d, depth) -> int:
+    return lib().moe_host_pipeline_workspace_size(_d(d), depth)
 
 
 def route_workspace_size(d) -> int:
@@ -290,6 +304,54 @@ class HostGraph:
         return self.out_host
 
 
+class HostPipeline:
+    """The native host-buffer pipeline (moe_host_pipeline_*): submit() enqueues one
+    layer step from pinned host buffers to a pinned host buffer and returns; step i's
+    copies overlap steps i-1 and i+1 on the pipeline's own streams; sync() waits for
+    every submitted step.  Buffers passed to submit() stay in use until sync()."""
+
+    def __init__(self, layer, T, depth=2):
+        self.T, self.H, self.E, self.depth = T, layer.H, layer.E, depth
+        d = layer.dims(T)
+        size = host_pipeline_workspace_size(d, depth)
+        if size == 0:
+            raise ValueError(f"unsupported dims or depth {depth} (1..8)")
+        self.ws = alloc_workspace(size, layer.w13.device)
+        self._weights = (layer.w13, layer.w13_s, layer.w2, layer.w2_s)  # kept alive
+        W = moe_weights(*[_p(t) for t in self._weights])
+        h = _P()
+        _check("moe_host_pipeline_create", lib().moe_host_pipeline_create(
+            _d(d), ctypes.byref(W), depth, _p(self.ws), self.ws.numel(), ctypes.byref(h)))
+        self._h = h
+
+    def _host(self, t, shape, dtype):
+        if tuple(t.shape) != shape or t.dtype != dtype:
+            raise ValueError(f"expected {dtype} {shape}, got {t.dtype} {tuple(t.shape)}")
+        return _host_p(t)
+
+    def submit(self, x_host, logits_host, out_host):
+        if self._h is None:
+            raise RuntimeError("pipeline closed")
+        _check("moe_host_pipeline_submit", lib().moe_host_pipeline_submit(
+            self._h, self._host(x_host, (self.T, self.H), torch.bfloat16),
+            self._host(logits_host, (self.T, self.E), torch.float32),
+            self._host(out_host, (self.T, self.H), torch.bfloat16)))
+
+    def sync(self):
+        _check("moe_host_pipeline_sync", lib().moe_host_pipeline_sync(self._h))
+
+    def close(self):
+        if getattr(self, "_h", None) is not None:
+            h, self._h = self._h, None
+            _check("moe_host_pipeline_destroy", lib().moe_host_pipeline_destroy(h))
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 class MoELayer:
     """The user-facing layer: resident MXFP4 weights plus a reusable workspace.
 
@@ -316,6 +378,10 @@ class MoELayer:
             self._hws = alloc_workspace(host_workspace_size(self.dims(T)), self.w13.device)
             self._hT = T
         return self._hws
+
+    def host_pipeline(self, T, depth=2):
+        """A HostPipeline for T-token steps (its own workspace and streams)."""
+        return HostPipeline(self, T, depth)
 
     def forward_host(self, x_host, logits_host, out_host, stream=None):
         """End to end from host memory: x_host [T, H] bf16 and logits_host [T, E] fp32

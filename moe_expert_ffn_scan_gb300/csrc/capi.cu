@@ -2,6 +2,8 @@
 // No allocation, no host synchronisation (except moe_check_status).
 #include <stdio.h>
 
+#include <new>
+
 #include "kernels.cuh"
 
 using namespace moe;
@@ -363,6 +365,132 @@ int moe_forward_host(const moe_dims* d, const uint16_t* x_host, const float* log
   if (cudaMemcpyAsync(out_host, h.out, xb, cudaMemcpyDeviceToHost, st) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
+}
+
+}  // extern "C"
+
+namespace {
+constexpr int kMaxPipelineDepth = 8;
+}  // namespace
+
+struct moe_host_pipeline {
+  moe_dims d;
+  moe_weights W;
+  int depth;
+  void* ws;
+  size_t fwd_bytes;  // the forward's workspace, at the start of ws
+  HostStagingWs slot[kMaxPipelineDepth];
+  cudaStream_t s_in, s_comp, s_out;
+  cudaEvent_t in_done[kMaxPipelineDepth], comp_done[kMaxPipelineDepth],
+      out_done[kMaxPipelineDepth];
+  long long submitted;
+};
+
+namespace {
+void pipeline_release(moe_host_pipeline* p) {
+  for (int j = 0; j < kMaxPipelineDepth; ++j) {
+    if (p->in_done[j]) cudaEventDestroy(p->in_done[j]);
+    if (p->comp_done[j]) cudaEventDestroy(p->comp_done[j]);
+    if (p->out_done[j]) cudaEventDestroy(p->out_done[j]);
+  }
+  if (p->s_in) cudaStreamDestroy(p->s_in);
+  if (p->s_comp) cudaStreamDestroy(p->s_comp);
+  if (p->s_out) cudaStreamDestroy(p->s_out);
+  delete p;
+}
+}  // namespace
+
+extern "C" {
+
+size_t moe_host_pipeline_workspace_size(const moe_dims* d, int depth) {
+  if (!dims_ok(d) || depth < 1 || depth > kMaxPipelineDepth) return 0;
+  Carver c(nullptr);
+  carve_forward(c, d);
+  for (int j = 0; j < depth; ++j) carve_host_staging(c, d);
+  return c.used;
+}
+
+int moe_host_pipeline_create(const moe_dims* d, const moe_weights* W, int depth, void* ws,
+                             size_t ws_bytes, moe_host_pipeline** out) {
+  if (!out) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!dims_ok(d)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!W || !ws || depth < 1 || depth > kMaxPipelineDepth) return MOE_ERR_INVALID_ARG;
+  if (!weights_ok(W->w13, W->w13_s) || !weights_ok(W->w2, W->w2_s)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(ws, kAlign)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < moe_host_pipeline_workspace_size(d, depth)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  moe_host_pipeline* p = new (std::nothrow) moe_host_pipeline{};
+  if (!p) return MOE_ERR_CUDA;
+  p->d = *d;
+  p->W = *W;
+  p->depth = depth;
+  p->ws = ws;
+  Carver c(ws);
+  carve_forward(c, d);
+  p->fwd_bytes = c.used;
+  for (int j = 0; j < depth; ++j) p->slot[j] = carve_host_staging(c, d);
+  bool ok = cudaStreamCreateWithFlags(&p->s_in, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&p->s_comp, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&p->s_out, cudaStreamNonBlocking) == cudaSuccess;
+  for (int j = 0; ok && j < depth; ++j)
+    ok = cudaEventCreateWithFlags(&p->in_done[j], cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&p->comp_done[j], cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&p->out_done[j], cudaEventDisableTiming) == cudaSuccess;
+  if (!ok) {
+    pipeline_release(p);
+    return MOE_ERR_CUDA;
+  }
+  *out = p;
+  return MOE_OK;
+}
+
+int moe_host_pipeline_submit(moe_host_pipeline* p, const uint16_t* x_host,
+                             const float* logits_host, uint16_t* out_host) {
+  if (!p || !x_host || !logits_host || !out_host) return MOE_ERR_INVALID_ARG;
+  const moe_dims* d = &p->d;
+  const int j = static_cast<int>(p->submitted % p->depth);
+  const bool reuse = p->submitted >= p->depth;  // slot j held step submitted - depth
+  const HostStagingWs& h = p->slot[j];
+  const size_t xb = static_cast<size_t>(d->T) * d->H * sizeof(uint16_t);
+  const size_t lb = static_cast<size_t>(d->T) * d->E * sizeof(float);
+  // inputs: once the previous user of the slot has consumed its inputs
+  if (reuse && cudaStreamWaitEvent(p->s_in, p->comp_done[j], 0) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaMemcpyAsync(h.x, x_host, xb, cudaMemcpyHostToDevice, p->s_in) != cudaSuccess ||
+      cudaMemcpyAsync(h.logits, logits_host, lb, cudaMemcpyHostToDevice, p->s_in) !=
+          cudaSuccess ||
+      cudaEventRecord(p->in_done[j], p->s_in) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  // the layer: once the inputs landed and the slot's previous output was copied out
+  if (cudaStreamWaitEvent(p->s_comp, p->in_done[j], 0) != cudaSuccess) return MOE_ERR_CUDA;
+  if (reuse && cudaStreamWaitEvent(p->s_comp, p->out_done[j], 0) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  int rc = moe_forward_timed(d, h.x, h.logits, &p->W, h.out, nullptr, nullptr, p->ws,
+                             p->fwd_bytes, p->s_comp);
+  if (rc != MOE_OK) return rc;
+  if (cudaEventRecord(p->comp_done[j], p->s_comp) != cudaSuccess) return MOE_ERR_CUDA;
+  // output
+  if (cudaStreamWaitEvent(p->s_out, p->comp_done[j], 0) != cudaSuccess ||
+      cudaMemcpyAsync(out_host, h.out, xb, cudaMemcpyDeviceToHost, p->s_out) != cudaSuccess ||
+      cudaEventRecord(p->out_done[j], p->s_out) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  ++p->submitted;
+  return MOE_OK;
+}
+
+int moe_host_pipeline_sync(moe_host_pipeline* p) {
+  if (!p) return MOE_ERR_INVALID_ARG;
+  const bool ok = cudaStreamSynchronize(p->s_in) == cudaSuccess &&
+                  cudaStreamSynchronize(p->s_comp) == cudaSuccess &&
+                  cudaStreamSynchronize(p->s_out) == cudaSuccess;
+  return ok ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int moe_host_pipeline_destroy(moe_host_pipeline* p) {
+  if (!p) return MOE_ERR_INVALID_ARG;
+  const int rc = moe_host_pipeline_sync(p);
+  pipeline_release(p);
+  return rc;
 }
 
 int moe_forward_timed(const moe_dims* d, const uint16_t* x, const float* logits,

@@ -94,6 +94,31 @@ def test_validation_happens_before_any_launch(lib):
     assert lib.moe_forward_host(ctypes.byref(d), P(0x1000), P(0x1000), ctypes.byref(w),
                                 P(0x1000), P(0x10008), 1 << 30, None) == 1
     assert moe.host_workspace_size(d) > moe.workspace_size(d)
+    # host-buffer pipeline: sizes, then checks before any stream or event is created
+    assert moe.host_pipeline_workspace_size(d, 1) == moe.host_workspace_size(d)
+    assert moe.host_pipeline_workspace_size(d, 2) > moe.host_pipeline_workspace_size(d, 1)
+    assert moe.host_pipeline_workspace_size(d, 0) == 0
+    assert moe.host_pipeline_workspace_size(d, 9) == 0
+    assert moe.host_pipeline_workspace_size(bad, 2) == 0
+    h = P()
+    big = moe.host_pipeline_workspace_size(d, 2)
+    assert lib.moe_host_pipeline_create(ctypes.byref(d), ctypes.byref(w), 2, P(0x10000), big,
+                                        None) == 1
+    assert lib.moe_host_pipeline_create(ctypes.byref(bad), ctypes.byref(w), 2, P(0x10000), big,
+                                        ctypes.byref(h)) == 2
+    for depth in (0, 9):
+        assert lib.moe_host_pipeline_create(ctypes.byref(d), ctypes.byref(w), depth,
+                                            P(0x10000), big, ctypes.byref(h)) == 1
+    assert lib.moe_host_pipeline_create(ctypes.byref(d), None, 2, P(0x10000), big,
+                                        ctypes.byref(h)) == 1
+    assert lib.moe_host_pipeline_create(ctypes.byref(d), ctypes.byref(w), 2, P(0x10008), big,
+                                        ctypes.byref(h)) == 1
+    assert lib.moe_host_pipeline_create(ctypes.byref(d), ctypes.byref(w), 2, P(0x10000),
+                                        big - 1, ctypes.byref(h)) == 3
+    assert h.value is None  # nothing was created
+    assert lib.moe_host_pipeline_submit(None, P(0x1000), P(0x1000), P(0x1000)) == 1
+    assert lib.moe_host_pipeline_sync(None) == 1
+    assert lib.moe_host_pipeline_destroy(None) == 1
     # router projection: shape checks, then null / misaligned pointers
     assert lib.moe_router_logits(0, 128, 8, P(0x1000), P(0x1000), P(0x1000), None) == 2
     assert lib.moe_router_logits(4, 120, 8, P(0x1000), P(0x1000), P(0x1000), None) == 2
