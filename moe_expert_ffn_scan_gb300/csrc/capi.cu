@@ -146,9 +146,11 @@ HostStagingWs carve_host_staging(Carver& c, const moe_dims* d) {
   return h;
 }
 
+// early_plan: the plan's producer ran at least two launches before this GEMM (see
+// GemmLaunch).
 int run_gemm(const moe_dims* d, const uint8_t* act, const uint8_t* act_s, const int32_t* offsets,
              const uint8_t* w, const uint8_t* w_s, int N, int K, uint16_t* y, const PlanWs& plan,
-             int max_group_rows, uint32_t* status, cudaStream_t st) {
+             int max_group_rows, uint32_t* status, cudaStream_t st, int early_plan) {
   GemmLaunch a{};
   a.w_codes = w;
   a.w_scales = w_s;
@@ -166,6 +168,7 @@ int run_gemm(const moe_dims* d, const uint8_t* act, const uint8_t* act_s, const 
   a.item_counts = plan.out.counts;
   a.max_group_rows = max_group_rows;
   a.status = status;
+  a.early_plan = early_plan;
   return cuda_rc(launch_grouped_gemm(a, st));
 }
 
@@ -290,7 +293,7 @@ int moe_grouped_gemm_w13(const moe_dims* d, const uint8_t* xq, const uint8_t* xs
     act_s = g.xsg;
   }
   return run_gemm(d, act, act_s, group_offsets, w13, w13_s, 2 * d->I, d->H, y13, g.plan,
-                  static_cast<int>(rows_Rs(d)), g.status, st);
+                  static_cast<int>(rows_Rs(d)), g.status, st, /*early_plan=*/0);
 }
 
 int moe_swiglu_quant(int32_t rows, int32_t I, const uint16_t* y13, uint8_t* hq, uint8_t* hs,
@@ -317,7 +320,7 @@ int moe_grouped_gemm_w2(const moe_dims* d, const uint8_t* hq, const uint8_t* hs,
   cudaError_t e = launch_plan(group_offsets, groups_G(d), g.plan.out, g.status, st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   return run_gemm(d, hq, hs, group_offsets, w2, w2_s, d->H, d->I, y2, g.plan,
-                  static_cast<int>(rows_Rs(d)), g.status, st);
+                  static_cast<int>(rows_Rs(d)), g.status, st, /*early_plan=*/0);
 }
 
 int moe_combine(const moe_dims* d, const uint16_t* y2, const int32_t* inv, const float* w,
@@ -549,14 +552,16 @@ int moe_forward_timed(const moe_dims* d, const uint16_t* x, const float* logits,
   }
   MOE_MARK(3)
   // every group (a routed expert or the shared expert) holds at most T rows
+  // W13 follows the quant-scatter; the one-CTA prep (decode) wrote the plan before it,
+  // the plan kernel (larger T) right before W13
   int rc = run_gemm(d, f.gemm.xg, f.gemm.xsg, f.offsets, W->w13, W->w13_s, 2 * I, H, f.y13,
-                    f.gemm.plan, T, status, st);
+                    f.gemm.plan, T, status, st, /*early_plan=*/T <= kPrepMaxT ? 1 : 0);
   if (rc != MOE_OK) return rc;
   MOE_MARK(4)
   MOE_TRY(launch_swiglu_quant(f.y13, Rs, I, f.hq, f.hs, st))
   MOE_MARK(5)
   rc = run_gemm(d, f.hq, f.hs, f.offsets, W->w2, W->w2_s, H, I, f.y2, f.gemm.plan, T, status,
-                st);
+                st, /*early_plan=*/1);  // follows SwiGLU; the plan preceded W13
   if (rc != MOE_OK) return rc;
   MOE_MARK(6)
   MOE_TRY(launch_combine(f.y2, f.inv, f.w, T, k, H, d->has_shared, out, status, st))

@@ -40,6 +40,7 @@ struct GemmParams {
   uint16_t* y;                // [rows_total][N]
   int N, K, G, rows_total;
   uint32_t* status;
+  int early;  // the plan may be read, and weights loaded, before griddepcontrol.wait
 };
 
 // Quads (4 sub-tiles = 512 K elements) of scale bytes the scale-factor warp keeps in
@@ -168,8 +169,12 @@ __global__ void __launch_bounds__(256, OCC)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // prologue done: wait for the producer of the tile plan / activations
-  pdl_wait();
+  // Prologue done.  Wait for the preceding kernel (the producer of the activations,
+  // and of the tile plan unless p.early).  With p.early the plan is already complete,
+  // so only the roles that read the preceding kernel's output wait: the weight
+  // producer after issuing its first stages' weight loads, the token thread and the
+  // scale-factor warp; the MMA issuer and the epilogue consume only what those load.
+  if (!p.early) pdl_wait();
   const uint32_t tmem = *tmem_slot;
 
   const int n_tiles = p.N / 128;
@@ -199,11 +204,39 @@ __global__ void __launch_bounds__(256, OCC)
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
+      // Early start: the weights of the first item's first stages (free ring slots)
+      // before the wait, their token tiles after it.
+      long long L0 = -1;
+      int pre = 0;
+      if (p.early) {
+        int g, row0, rows, nt;
+        for (long long L = blockIdx.x; L < total; L += gridDim.x)
+          if (load_item(L, g, row0, rows, nt)) {
+            L0 = L;
+            break;
+          }
+        if (L0 >= 0) {
+          pre = nk < STAGES ? nk : STAGES;
+          for (int kb = 0; kb < pre; ++kb) {  // ring slot kb, first use: no empty wait
+            uint64_t* fb = &full[(kb % C::kIssuers) * STAGES + kb];
+            mbar_arrive_expect_tx(fb, C::kTokenThread ? KO * kWeightTileTxBytes
+                                                      : KO * kWeightTileTxBytes + BN_MAX * KO * 128);
+            tma_load_4d(smem + C::kOffA + kb * C::kABytes, &tmW, fb, 0, nt * 128, kb * KO, g);
+          }
+        }
+        pdl_wait();
+        if constexpr (!C::kTokenThread) {
+          for (int kb = 0; kb < pre; ++kb)
+            tma_load_3d(smem + C::kOffB + kb * C::kBBytes, &tmX,
+                        &full[(kb % C::kIssuers) * STAGES + kb], 0, row0, kb * KO);
+        }
+      }
       uint32_t it = 0;
       for (long long L = blockIdx.x; L < total && !*abort_flag; L += gridDim.x) {
         int g, row0, rows, nt;
         if (!load_item(L, g, row0, rows, nt)) continue;
         for (int kb = 0; kb < nk; ++kb, ++it) {
+          if (L == L0 && kb < pre) continue;  // issued above
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1u;
           if (it >= STAGES && !mbar_wait(&empty[s], ph ^ 1u, p.status, abort_flag)) break;
@@ -223,6 +256,7 @@ __global__ void __launch_bounds__(256, OCC)
     // ---------------------------------------------------------------- token TMA
     // (its own thread, so the weight stream's issue slots carry weight loads only)
     if (lane == 0) {
+      if (p.early) pdl_wait();
       uint32_t it = 0;
       for (long long L = blockIdx.x; L < total && !*abort_flag; L += gridDim.x) {
         int g, row0, rows, nt;
@@ -390,24 +424,44 @@ __global__ void __launch_bounds__(256, OCC)
       Pos ld{}, cs{};
       bool ld_ok = seek(blockIdx.x, ld);
       bool cs_ok = seek(blockIdx.x, cs);
-      auto fetch = [&](uint4 (&w4)[4], uint32_t (&a)[J]) {
+      auto fetch_w = [&](const Pos& P, uint4 (&w4)[4]) {
         const uint8_t* wsp =
-            p.w_scales + (static_cast<size_t>(ld.g) * p.N + ld.nt * 128) * kw + ld.kq * 16;
+            p.w_scales + (static_cast<size_t>(P.g) * p.N + P.nt * 128) * kw + P.kq * 16;
 #pragma unroll
         for (int j = 0; j < 4; ++j)
           w4[j] = __ldg(reinterpret_cast<const uint4*>(wsp + static_cast<size_t>(j * 32 + lane) * kw));
+      };
+      auto fetch_x = [&](const Pos& P, uint32_t (&a)[J]) {
 #pragma unroll
         for (int j = 0; j < J; ++j) {
           const int r = j * 32 + lane;
-          a[j] = r < ld.rows ? __ldg(reinterpret_cast<const uint32_t*>(
-                                   p.x_scales + static_cast<size_t>(ld.row0 + r) * kx + ld.kq * 4))
-                             : 0x7F7F7F7Fu;
+          a[j] = r < P.rows ? __ldg(reinterpret_cast<const uint32_t*>(
+                                  p.x_scales + static_cast<size_t>(P.row0 + r) * kx + P.kq * 4))
+                            : 0x7F7F7F7Fu;
         }
+      };
+      auto fetch = [&](uint4 (&w4)[4], uint32_t (&a)[J]) {
+        fetch_w(ld, w4);
+        fetch_x(ld, a);
         ld_ok = step(ld);
       };
+      // The first Q quads: weight scales before the wait for the preceding kernel
+      // (with p.early), token scales (its output) after it.
+      Pos first[Q];
+      bool first_ok[Q];
+#pragma unroll
+      for (int i = 0; i < Q; ++i) {
+        first_ok[i] = ld_ok;
+        if (ld_ok) {
+          first[i] = ld;
+          fetch_w(ld, wv[i]);
+          ld_ok = step(ld);
+        }
+      }
+      if (p.early) pdl_wait();
 #pragma unroll
       for (int i = 0; i < Q; ++i)
-        if (ld_ok) fetch(wv[i], av[i]);
+        if (first_ok[i]) fetch_x(first[i], av[i]);
       uint32_t it = 0;
       bool ok = true;
       while (cs_ok && ok) {
@@ -444,6 +498,7 @@ __global__ void __launch_bounds__(256, OCC)
       }
     } else {
       // General path (K not a multiple of 512): one stage at a time.
+      if (p.early) pdl_wait();  // token scales come from the preceding kernel
       uint32_t it = 0;
       for (long long L = blockIdx.x; L < total && !*abort_flag; L += gridDim.x) {
         int g, row0, rows, nt;
@@ -668,9 +723,13 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& a, cudaStream_t st) {
   p.status = a.status;
   // A list whose groups cannot exist (no group has more than max_group_rows rows) is
   // provably empty and not launched.
+  // The first launch inherits the caller's word on the plan; each later variant
+  // follows a GEMM launch that waited for the plan's producer before it started.
+  p.early = a.early_plan;
   cudaError_t e = launch_variant<kSmallBN, kSmallStages, kSmallStagesKO1, kSmallOcc>(
       a, p, a.items[0], a.item_counts, a.max_items[0], st);
   if (e != cudaSuccess || a.max_group_rows <= kSmallBN) return e;
+  p.early = 1;
   e = launch_variant<kMediumBN, kMediumStages, kMediumStagesKO1, kMediumOcc>(
       a, p, a.items[1], a.item_counts + 1, a.max_items[1], st);
   if (e != cudaSuccess || a.max_group_rows <= kMediumBN) return e;

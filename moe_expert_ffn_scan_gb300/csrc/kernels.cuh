@@ -111,6 +111,10 @@ struct GemmLaunch {
   int max_items[kNumVariants];
   int max_group_rows;          // upper bound on any group's row count
   uint32_t* status;
+  // 1 when the tile plan was complete before the launch preceding this GEMM started
+  // (its producer ran two or more launches earlier): the weight loads of each CTA's
+  // first stages then go out before the wait for the preceding kernel.
+  int early_plan;
 };
 cudaError_t launch_grouped_gemm(const GemmLaunch& a, cudaStream_t st);
 
