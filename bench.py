@@ -136,7 +136,7 @@ def fp8_tensor_peak_tflops():
 # one small-M W13 GEMM launch, from the ncu capture summarised in
 # profiles/k_gemm_mx_small_decode_T7_E64.md, keyed by the hash of the GEMM sources it
 # was taken on.  A changed kernel reports traffic null until it is captured again.
-NCU_SMALL_W13_TRAFFIC = {"src": "9d059e044c5306cd", "bytes_per_group": (966.78e6 + 3.87e6) / 41}
+NCU_SMALL_W13_TRAFFIC = {"src": "5e1487b2500bb657", "bytes_per_group": (966.79e6 + 3.86e6) / 41}
 
 
 def gemm_src_hash():
