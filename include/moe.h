@@ -15,10 +15,13 @@
  *   - All tensors are caller-owned, row-major, contiguous DEVICE pointers, unless
  *     stated otherwise.  Pointers must be 16-byte aligned (the weight code tensors
  *     32-byte aligned).  bf16 tensors are passed as uint16_t storage.
- *   - Nothing allocates.  Scratch comes from the caller's workspace, sized by the
- *     matching *_workspace_size() query.  Workspace must be 256-byte aligned.
+ *   - Nothing allocates device memory.  Scratch comes from the caller's workspace,
+ *     sized by the matching *_workspace_size() query.  Workspace must be 256-byte
+ *     aligned.  (moe_host_pipeline_create creates CUDA streams and events, and a
+ *     small host-side handle; see there.)
  *   - Every call is asynchronous on `stream` (a cudaStream_t, NULL = legacy default
- *     stream) and never synchronises the host, except moe_check_status.
+ *     stream) and never synchronises the host, except moe_check_status and
+ *     moe_host_pipeline_sync / moe_host_pipeline_destroy.
  *   - Return value: MOE_OK or an MOE_ERR_* code.  Shapes and pointers are checked
  *     on the host before any launch; nothing is launched when a check fails.
  *     Launch failures return MOE_ERR_CUDA.  Data-dependent device checks (an index
