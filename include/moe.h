@@ -248,9 +248,11 @@ int moe_host_pipeline_destroy(moe_host_pipeline* p);
 
 /* moe_forward with per-stage timing.  events points to 8 cudaEvent_t handles created
  * by the caller (cudaEventCreate); the call records events[0] before the first stage
- * and events[i] after stage i: 1 route + histogram/scan/permute, 2 activation
- * quantisation, 3 tile plan + packed-row gather, 4 W13 grouped GEMM, 5 SwiGLU +
- * quantisation, 6 W2 grouped GEMM, 7 combine.  Same results as moe_forward. */
+ * and events[i] after stage i: 1 route + histogram/scan/permute + tile plan, 2
+ * activation quantisation with the packed-row scatter, 3 (empty: the plan runs in
+ * stage 1 and the gather in stage 2; kept so that the indices stay fixed), 4 W13
+ * grouped GEMM, 5 SwiGLU + quantisation, 6 W2 grouped GEMM, 7 combine.  Same results
+ * as moe_forward. */
 int moe_forward_timed(const moe_dims* d, const uint16_t* x, const float* logits,
                       const moe_weights* W, uint16_t* out, const moe_debug_out* dbg,
                       void* const* events, void* ws, size_t ws_bytes, void* stream);

@@ -540,6 +540,9 @@ int moe_forward_timed(const moe_dims* d, const uint16_t* x, const float* logits,
     MOE_TRY(launch_route(logits, T, E, k, f.idx, f.w, status, st))
     MOE_TRY(launch_permute(f.idx, T, E, k, d->has_shared, f.route.blockcnt, f.route.blockbase,
                            f.counts, f.offsets, f.perm_src, f.inv, status, st))
+    // the tile plan before the quant-scatter, as in the one-CTA path, so that the
+    // plan is complete two launches before W13
+    MOE_TRY(launch_plan(f.offsets, groups_G(d), f.gemm.plan.out, status, st))
   }
   MOE_MARK(1)
   // quantise each token once, writing its codes straight into its packed rows
@@ -547,15 +550,11 @@ int moe_forward_timed(const moe_dims* d, const uint16_t* x, const float* logits,
                                dbg && dbg->xs ? f.xs : nullptr, f.gemm.xg, f.gemm.xsg, status,
                                st))
   MOE_MARK(2)
-  if (T > kPrepMaxT) {
-    MOE_TRY(launch_plan(f.offsets, groups_G(d), f.gemm.plan.out, status, st))
-  }
-  MOE_MARK(3)
-  // every group (a routed expert or the shared expert) holds at most T rows
-  // W13 follows the quant-scatter; the one-CTA prep (decode) wrote the plan before it,
-  // the plan kernel (larger T) right before W13
+  MOE_MARK(3)  // (stage 3, the plan, now runs inside stage 1)
+  // every group (a routed expert or the shared expert) holds at most T rows; W13
+  // follows the quant-scatter, and the plan was written before it
   int rc = run_gemm(d, f.gemm.xg, f.gemm.xsg, f.offsets, W->w13, W->w13_s, 2 * I, H, f.y13,
-                    f.gemm.plan, T, status, st, /*early_plan=*/T <= kPrepMaxT ? 1 : 0);
+                    f.gemm.plan, T, status, st, /*early_plan=*/1);
   if (rc != MOE_OK) return rc;
   MOE_MARK(4)
   MOE_TRY(launch_swiglu_quant(f.y13, Rs, I, f.hq, f.hs, st))
