@@ -236,7 +236,9 @@ int moe_forward_host(const moe_dims* d, const uint16_t* x_host, const float* log
  *       made and synchronised).
  *   sync: blocks until every submitted step's output is in host memory; MOE_ERR_CUDA
  *       if a stream reported an error.
- *   destroy: synchronises, then releases the streams, events and the handle. */
+ *   destroy: synchronises, then releases the streams, events and the handle.
+ * A pipeline is driven by one host thread at a time.  After a call returns an error
+ * other than MOE_ERR_INVALID_ARG, sync and destroy it rather than submit again. */
 typedef struct moe_host_pipeline moe_host_pipeline;
 size_t moe_host_pipeline_workspace_size(const moe_dims* d, int depth);
 int moe_host_pipeline_create(const moe_dims* d, const moe_weights* W, int depth, void* ws,
