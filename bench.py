@@ -12,7 +12,14 @@ L2-resident and the write-flush would only add its own dirty-line write-back to 
 next step; such runs also report the write-flushed step time.  Prints one JSON line
 on rank 0.
 
+The default run (--workload decode) times the 7-token decode layer for the line's
+headline value, and in the same invocation measures the 256-token decode layer, the
+32K-token prefill chunk (each for >= 2 s, with its own clock samples) and the
+grouped-GEMM shape sweep; those are reported under "workloads" and "sweep" in the same
+line (--no-extra skips them).
+
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|decode256|prefill|tiny]
+  python bench.py --workload sweep       (the grouped-GEMM sweep alone, every point)
   python bench.py --impl reference ...   (the CPU oracle on a bounded sample)
 
 Multi-GPU: one independent replica per GPU (the layer is not sharded; no
@@ -22,6 +29,7 @@ collective); value = tokens processed by all ranks / max-over-ranks time.
 from __future__ import annotations
 
 import argparse
+import datetime
 import json
 import os
 import statistics
@@ -58,6 +66,8 @@ def parse():
     ap.add_argument("--experts", type=int, default=None,
                     help="override E (a smaller layer of the same shape, for ncu captures)")
     ap.add_argument("--tokens", type=int, default=None, help="override T")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="decode only: skip the decode256 / prefill / sweep records")
     return ap.parse_args()
 
 
@@ -133,9 +143,9 @@ def fp8_tensor_peak_tflops():
 
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per active weight group of
-# one small-M W13 GEMM launch, from the ncu capture summarised in
-# profiles/k_gemm_mx_small_decode_T7_E64.md, keyed by the hash of the GEMM sources it
-# was taken on.  A changed kernel reports traffic null until it is captured again.
+# one small-M W13 GEMM launch, from the committed ncu summary of the small-M W13 launch
+# on the 7-token, 64-expert layer, keyed by the hash of the GEMM sources it was taken
+# on.  A changed kernel reports traffic null until it is captured again.
 NCU_SMALL_W13_TRAFFIC = {"src": "5e1487b2500bb657", "bytes_per_group": (966.79e6 + 3.86e6) / 41}
 
 
@@ -150,9 +160,13 @@ def gemm_src_hash():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running.
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    `load()` brackets a region of GPU work (a context manager); `summary(tag)` reports
+    only the samples whose nvidia-smi timestamps fall inside the regions marked with
+    that tag, so idle time before and after them does not count."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -160,6 +174,7 @@ class ClockSampler:
         self.idx = gpu_index
         self.proc = None
         self.path = os.path.join("/tmp", f"moe_clocks_{os.getpid()}.csv")
+        self.windows = []  # (tag, t0, t1) host wall-clock times
 
     def __enter__(self):
         try:
@@ -182,21 +197,45 @@ class ClockSampler:
                 self.proc.kill()
             self.f.close()
 
-    def summary(self):
+    class _Load:
+        def __init__(self, owner, tag):
+            self.owner, self.tag = owner, tag
+
+        def __enter__(self):
+            self.t0 = datetime.datetime.now()
+            return self
+
+        def __exit__(self, *a):
+            self.owner.windows.append((self.tag, self.t0, datetime.datetime.now()))
+
+    def load(self, tag):
+        return ClockSampler._Load(self, tag)
+
+    def summary(self, tag=None):
         if not self.proc:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        wins = [(a, b) for t, a, b in self.windows if tag is None or t == tag]
         sm, smax, reasons = [], [], set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for line in open(self.path):
+        try:
+            lines = open(self.path).read().splitlines()
+        except OSError:
+            lines = []
+        for line in lines:
             p = [x.strip() for x in line.split(",")]
-            if len(p) < 9:
+            if len(p) < 10:
                 continue
             try:
-                sm.append(float(p[1]))
-                smax.append(float(p[2]))
+                ts = datetime.datetime.strptime(p[0], "%Y/%m/%d %H:%M:%S.%f")
+                f_sm, f_max = float(p[2]), float(p[3])
             except ValueError:
                 continue
-            for n, v in zip(names, p[5:9]):
+            if wins and not any(a <= ts <= b for a, b in wins):
+                continue
+            sm.append(f_sm)
+            smax.append(f_max)
+            for n, v in zip(names, p[6:10]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None,
@@ -204,13 +243,13 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def make_layer(args, seed, dev):
+def make_layer_for(args, workload, seed, dev):
     if args.experts is None and args.tokens is None:
-        return gi.make_layer(args.workload, seed=seed, device=dev)
+        return gi.make_layer(workload, seed=seed, device=dev)
     import dataclasses
-    d = gi.WORKLOADS[args.workload]
+    d = gi.WORKLOADS[workload]
     d = dataclasses.replace(d, E=args.experts or d.E, T=args.tokens or d.T)
-    return d, gi.custom_layer(d, seed=seed, device=dev, logits_kind=gi.LOGITS_KIND[args.workload])
+    return d, gi.custom_layer(d, seed=seed, device=dev, logits_kind=gi.LOGITS_KIND[workload])
 
 
 def active_groups(counts, has_shared):
@@ -277,7 +316,7 @@ def run_reference(args, rank, world):
                           "run a layer workload"}), flush=True)
         return
     dev = "cuda" if torch.cuda.is_available() else "cpu"
-    d, t = make_layer(args, args.seed, dev)
+    d, t = make_layer_for(args, args.workload, args.seed, dev)
     hv = host_view(d, t)
     # tokens per step: one, or more when one is quick, keeping the whole run at about
     # three minutes (the tiny layer runs in full every step)
@@ -313,11 +352,40 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def run_ours(args, rank, world, local):
+def gemm_roofline(d, groups, t_ms, which, hbm, hbm_src, tpk, tpk_src):
+    """Roofline of one grouped GEMM launch sequence (W13 or W2) of a layer step.
+    Algorithmic bytes: the active groups' weight bytes (codes + scales) plus the packed
+    FP8 rows and scales read and the bf16 rows written; flops: 2 x rows x N x K.  The
+    bound is HBM when the flops per byte sit below the ridge point, else the tensor
+    pipe (kind::mxf8f6f4 runs at the FP8 rate)."""
+    Rs = d.R + (d.T if d.has_shared else 0)
+    if which == "w13":
+        N, K = 2 * d.I, d.H
+    else:
+        N, K = d.H, d.I
+    wbytes = groups * N * K * WEIGHT_BYTES_PER_ELEM
+    abytes = Rs * (K + K / 128) + Rs * N * 2
+    flops = 2.0 * Rs * N * K
+    t = t_ms * 1e-3
+    if flops / (wbytes + abytes) < (tpk * 1e12) / (hbm * 1e9):
+        ach = (wbytes + abytes) / t / 1e9
+        return {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
+                "frac": ach / hbm, "traffic": None, "peak_source": f"{hbm_src} HBM copy bandwidth",
+                "algorithmic_bytes": wbytes + abytes}
+    ach = flops / t / 1e12
+    return {"bound": "tensor", "achieved": ach, "peak": tpk, "unit": "TFLOP/s",
+            "frac": ach / tpk, "traffic": None, "peak_source": tpk_src,
+            "algorithmic_flops": flops}
+
+
+def measure_layer(args, workload, steps, warmup, rank, world, local, clocks, *, soak_s=0.0,
+                  e2e_steps=None, router=False, cpu=False):
+    """One workload: the layer step captured as a CUDA graph, timed over `steps` replays
+    (each followed by an event-instrumented forward for the stage times), inside a
+    clock-sampling window tagged with the workload's name.  Returns a dict."""
     import moe_expert_ffn_scan_gb300 as moe
-    moe.lib()
     dev = torch.device("cuda", local)
-    d, t = make_layer(args, args.seed + rank, dev)
+    d, t = make_layer_for(args, workload, args.seed + rank, dev)
     if t["logits"] is None:  # logits are the gate projection of x: the library's router
         t["logits"] = torch.empty(d.T, d.E, dtype=torch.float32, device=dev)
         moe.moe_router_logits(t["x"], t["wg"], t["logits"])
@@ -338,7 +406,6 @@ def run_ours(args, rank, world, local):
         raise RuntimeError(f"device status bits {bits:#x}")
     counts = dbg["counts"].cpu().numpy()
     groups = active_groups(counts, d.has_shared)
-    Rs = d.R + (d.T if d.has_shared else 0)
     step_weight_bytes = groups * 3 * d.I * d.H * WEIGHT_BYTES_PER_ELEM
     l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
     policy = "none" if args.no_flush else args.l2
@@ -349,12 +416,11 @@ def run_ours(args, rank, world, local):
         l2_note = (f"not flushed: each step streams {step_weight_bytes / 1e9:.2f} GB of expert "
                    f"weights ({step_weight_bytes / l2_bytes:.0f}x the {l2_bytes >> 20} MiB L2)")
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)]
-           for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(steps)]
     for row in evs:
         for e in row:
             e.record(stream)  # creates the event handles
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         layer.forward(x, lg, out=out)
     torch.cuda.synchronize()
     # One step = one replay of the layer captured as a CUDA graph (every launch of the
@@ -363,17 +429,24 @@ def run_ours(args, rank, world, local):
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         layer.forward(x, lg, out=out)
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         graph.replay()
     torch.cuda.synchronize()
     step_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                for _ in range(args.steps)]
+                for _ in range(steps)]
 
-    clocks = ClockSampler(local)
-    with clocks:
+    with clocks.load(workload):
+        if soak_s > 0:
+            # back-to-back replays of the same graph right before the timed region, so
+            # that the clock sampler sees the GPU under this load for a few seconds
+            t_end = time.perf_counter() + soak_s
+            while time.perf_counter() < t_end:
+                for _ in range(64):
+                    graph.replay()
+                torch.cuda.synchronize()
         barrier(world)
         torch.cuda.synchronize()
-        for i in range(args.steps):
+        for i in range(steps):
             if do_flush:
                 flush.fill_(i & 0xFF)
             step_evs[i][0].record(stream)
@@ -388,144 +461,71 @@ def run_ours(args, rank, world, local):
     bits = moe.moe_check_status(ws)
     if bits:
         raise RuntimeError(f"device status bits {bits:#x}")
-    stage_ms = {s: [] for s in moe.STAGES}
-    step_ms = [a.elapsed_time(b) for a, b in step_evs]
+    stage_ms = {s_: [] for s_ in moe.STAGES}
+    step_ms = [a_.elapsed_time(b_) for a_, b_ in step_evs]
     for row in evs:
-        for j, s in enumerate(moe.STAGES):
-            stage_ms[s].append(row[j].elapsed_time(row[j + 1]))
+        for j, s_ in enumerate(moe.STAGES):
+            stage_ms[s_].append(row[j].elapsed_time(row[j + 1]))
     stream_step_ms = statistics.mean(row[0].elapsed_time(row[7]) for row in evs)
     flushed_ms = None
     if not do_flush:  # the same graph with the 512 MiB write-flush before each step
+        n_f = min(steps, 50)
         fe = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
-        for i in range(args.steps):
+              for _ in range(n_f)]
+        for i in range(n_f):
             flush.fill_(i & 0xFF)
             fe[i][0].record(stream)
             graph.replay()
             fe[i][1].record(stream)
         torch.cuda.synchronize()
-        flushed_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in fe), world)
+        flushed_ms = max_over_ranks(statistics.mean(a_.elapsed_time(b_) for a_, b_ in fe), world)
     ms = statistics.mean(step_ms)
     qs = (statistics.quantiles(step_ms, n=10, method="inclusive") if len(step_ms) >= 2
           else [ms] * 9)
     pct = {"p10": qs[0], "p50": statistics.median(step_ms), "p90": qs[8]}
     ms_max = max_over_ranks(ms, world)
-    value = world * d.T / (ms_max * 1e-3)
-    stage_mean = {s: statistics.mean(v) for s, v in stage_ms.items()}
+    stage_mean = {s_: statistics.mean(v) for s_, v in stage_ms.items()}
 
-    # roofline of the dominant kernel (the W13 grouped GEMM)
-    w13_bytes = groups * (2 * d.I) * d.H * WEIGHT_BYTES_PER_ELEM
-    w2_bytes = groups * d.H * d.I * WEIGHT_BYTES_PER_ELEM
-    act13 = Rs * (d.H + d.H / 128) + Rs * 2 * d.I * 2
-    act2 = Rs * (d.I + d.I / 128) + Rs * d.H * 2
-    flops13 = 2.0 * Rs * 2 * d.I * d.H
-    flops2 = 2.0 * Rs * d.H * d.I
     hbm, hbm_src = hbm_peak_gbs()
     tpk, tpk_src = fp8_tensor_peak_tflops()
-    t13 = stage_mean["gemm_w13"] * 1e-3
-    decode_like = (flops13 / (w13_bytes + act13)) < (tpk * 1e12) / (hbm * 1e9)
-    if decode_like:
-        ach = (w13_bytes + act13) / t13 / 1e9
-        traffic = None
-        if d.T <= 16 and gemm_src_hash() == NCU_SMALL_W13_TRAFFIC["src"]:
-            traffic = groups * NCU_SMALL_W13_TRAFFIC["bytes_per_group"]
-        roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
-                "frac": ach / hbm, "traffic": traffic,
-                "kernel": "k_gemm_mx (W13 grouped GEMM)",
-                "peak_source": f"{hbm_src} HBM copy bandwidth"}
-    else:
-        ach = flops13 / t13 / 1e12
-        roof = {"bound": "tensor", "achieved": ach, "peak": tpk, "unit": "TFLOP/s",
-                "frac": ach / tpk, "traffic": None,
-                "kernel": "k_gemm_mx (W13 grouped GEMM)", "peak_source": tpk_src}
+    roof13 = gemm_roofline(d, groups, stage_mean["gemm_w13"], "w13", hbm, hbm_src, tpk, tpk_src)
+    roof2 = gemm_roofline(d, groups, stage_mean["gemm_w2"], "w2", hbm, hbm_src, tpk, tpk_src)
+    roof13["kernel"] = "k_gemm_mx (W13 grouped GEMM)"
+    roof2["kernel"] = "k_gemm_mx (W2 grouped GEMM)"
+    if roof13["bound"] == "hbm" and d.T <= 16 and gemm_src_hash() == NCU_SMALL_W13_TRAFFIC["src"]:
+        roof13["traffic"] = groups * NCU_SMALL_W13_TRAFFIC["bytes_per_group"]
 
     # end to end through the public API, host buffers, copies inside the timed region
     e2e = None
-    if not args.no_e2e:
-        # single step, serialised: one graph replay = two copies in, the layer, one out
-        hg = layer.host_graph(d.T)  # pinned host buffers, one graph launch per step
-        hg.x_host.copy_(x.cpu())
-        hg.logits_host.copy_(lg.cpu())
+    if e2e_steps:
+        e2e = measure_e2e(layer, d, x, lg, out, e2e_steps, do_flush, flush, world)
+
+    router_rec = None
+    if router:
+        # the router gate projection for this workload's T (outside the layer step: the
+        # layer's boundary takes logits); W_g synthetic fp32 [E, H]
+        wg = t["wg"] if t.get("wg") is not None else gi.gate_weight(d.E, d.H, args.seed, dev)
+        rlg = torch.empty(d.T, d.E, dtype=torch.float32, device=dev)
         for _ in range(3):
-            hg.replay()
-        torch.cuda.synchronize()
-        e_ms = []
-        for i in range(args.steps):
+            moe.moe_router_logits(x, wg, rlg)
+        n_r = min(steps, 20)
+        r_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(n_r)]
+        for i in range(n_r):
             if do_flush:
                 flush.fill_(i & 0xFF)
-            torch.cuda.synchronize()
-            t0 = time.perf_counter()
-            hg.replay()  # copies in, the layer, copy out
-            torch.cuda.synchronize()
-            e_ms.append((time.perf_counter() - t0) * 1e3)
-        layer.forward(x, lg, out=out)
+            r_ev[i][0].record(stream)
+            moe.moe_router_logits(x, wg, rlg)
+            r_ev[i][1].record(stream)
         torch.cuda.synchronize()
-        out_ref = out.cpu()
-        if not torch.equal(hg.out_host, out_ref):
-            raise RuntimeError("host-buffer forward differs from the device forward")
-        xh, lgh, oh = hg.x_host, hg.logits_host, hg.out_host
-        single_ms = max_over_ranks(statistics.mean(e_ms), world)
-        e2e = {"h2d_bytes_per_step": int(xh.numel() * 2 + lgh.numel() * 4),
-               "d2h_bytes_per_step": int(oh.numel() * 2), "single_step_ms": single_ms}
-        del hg
-        if do_flush:
-            # L2 flushed between steps: steps cannot overlap, the serialised form stands
-            e2e.update(value=world * d.T / (single_ms * 1e-3), unit="tokens/s",
-                       ms_per_step=single_ms,
-                       api="MoELayer.host_graph(T).replay(): moe_forward_host captured as "
-                           "one CUDA graph over pinned host buffers, one step at a time")
-        else:
-            # steps through the native host-buffer pipeline: step i's copies overlap
-            # the kernels of steps i-1 and i+1; every step still copies its inputs in
-            # and its output out; the first copy-in and last copy-out are in the time
-            depth = 2
-            pipe = layer.host_pipeline(d.T, depth)
-            pxh = [xh.clone().pin_memory() for _ in range(depth)]
-            plh = [lgh.clone().pin_memory() for _ in range(depth)]
-            poh = [torch.empty_like(oh).pin_memory() for _ in range(depth)]
-            for i in range(2 * depth):
-                pipe.submit(pxh[i % depth], plh[i % depth], poh[i % depth])
-            pipe.sync()
-            torch.cuda.synchronize()
-            t0 = time.perf_counter()
-            for i in range(args.steps):
-                pipe.submit(pxh[i % depth], plh[i % depth], poh[i % depth])
-            pipe.sync()
-            pipe_ms = (time.perf_counter() - t0) * 1e3 / args.steps
-            for j in range(depth):
-                if not torch.equal(poh[j], out_ref):
-                    raise RuntimeError("pipelined host-buffer forward differs from the "
-                                       "device forward")
-            pipe.close()
-            em = max_over_ranks(pipe_ms, world)
-            e2e.update(value=world * d.T / (em * 1e-3), unit="tokens/s", ms_per_step=em,
-                       api=f"MoELayer.host_pipeline(T, depth={depth}).submit() x steps + "
-                           "sync(): moe_host_pipeline_*, pinned host buffers, copies on "
-                           "their own streams overlapping neighbouring steps' kernels")
+        r_ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in r_ev)
+        r_bytes = d.E * d.H * 4 + d.T * d.H * 2 + d.T * d.E * 4
+        router_rec = {"ms": r_ms, "gbs": r_bytes / (r_ms * 1e-3) / 1e9,
+                      "tflops": 2.0 * d.T * d.E * d.H / (r_ms * 1e-3) / 1e12,
+                      "kernel": "k_router_gemv" if d.T <= 1024 else "k_router_tiled"}
 
-    # the router gate projection for this workload's T (outside the layer step: the
-    # layer's boundary takes logits); W_g synthetic fp32 [E, H]
-    wg = t["wg"] if t.get("wg") is not None else gi.gate_weight(d.E, d.H, args.seed, dev)
-    rlg = torch.empty(d.T, d.E, dtype=torch.float32, device=dev)
-    for _ in range(3):
-        moe.moe_router_logits(x, wg, rlg)
-    r_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(args.steps)]
-    for i in range(args.steps):
-        if do_flush:
-            flush.fill_(i & 0xFF)
-        r_ev[i][0].record(stream)
-        moe.moe_router_logits(x, wg, rlg)
-        r_ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    r_ms = statistics.mean(a.elapsed_time(b) for a, b in r_ev)
-    r_bytes = d.E * d.H * 4 + d.T * d.H * 2 + d.T * d.E * 4
-    router = {"ms": r_ms, "gbs": r_bytes / (r_ms * 1e-3) / 1e9,
-              "tflops": 2.0 * d.T * d.E * d.H / (r_ms * 1e-3) / 1e12,
-              "kernel": "k_router_gemv" if d.T <= 1024 else "k_router_tiled (fp32 CUDA cores)"}
-
-    cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
+    cpu_rec = None
+    if cpu and rank == 0:
         hv = host_view(d, t)
         # one token first; when that is quick, as many more as about 10 s of oracle
         # work allows (the tiny layer runs in full)
@@ -535,57 +535,189 @@ def run_ours(args, rank, world, local):
             n, dt = oracle_sample(d, hv, more, args.seed)
         whole = " (the whole layer)" if n == d.T else ""
         shared = " + shared expert" if d.has_shared else ""
-        cpu = {"value": n / dt, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
-               "sample": f"{n} token(s) of the {args.workload} workload{whole}, their top-{d.k} "
-                         f"experts{shared}, full layer in float64 numpy, {dt:.2f} s"}
+        cpu_rec = {"value": n / dt, "unit": "tokens/s", "cores": blas_threads(),
+                   "kind": "oracle",
+                   "sample": f"{n} token(s) of the {workload} workload{whole}, their top-{d.k} "
+                             f"experts{shared}, full layer in float64 numpy, {dt:.2f} s"}
 
     # per forward: prep / quant-scatter / SwiGLU / combine (T <= 128) or route, histogram,
     # scan, permute, quant-scatter, plan, SwiGLU, combine; per GEMM one launch per
     # variant a group of up to T rows can need (small, medium > 16, mid > 64, large > 128)
     gemm_variants = 1 + (d.T > 16) + (d.T > 64) + (d.T > 128)
     launches_per_step = (4 if d.T <= 128 else 8) + 2 * gemm_variants
+    rec = {
+        "workload": workload, "d": d, "value": world * d.T / (ms_max * 1e-3),
+        "ms_per_step": ms_max, "steps": steps, "warmup": warmup,
+        "config": {"workload": workload, "T": d.T, "H": d.H, "I": d.I, "E": d.E, "k": d.k,
+                   "shared_experts": d.has_shared, "active_groups": groups,
+                   "routed_rows": d.R, "l2": l2_note, "parallelism": f"replicas x{world}"},
+        "roofline": roof13, "roofline_w2": roof2, "stage_ms": stage_mean,
+        "stream_ms_per_step": stream_step_ms, "ms_per_step_l2_write_flushed": flushed_ms,
+        "ms_per_step_percentiles": pct,
+        "weight_gbs": groups * 3 * d.I * d.H * WEIGHT_BYTES_PER_ELEM /
+                      ((stage_mean["gemm_w13"] + stage_mean["gemm_w2"]) * 1e-3) / 1e9,
+        "gemm_tflops": 2.0 * (d.R + (d.T if d.has_shared else 0)) * 3 * d.I * d.H /
+                       ((stage_mean["gemm_w13"] + stage_mean["gemm_w2"]) * 1e-3) / 1e12,
+        "router_gate": router_rec, "cpu_baseline": cpu_rec, "e2e": e2e,
+        "gpu_launches": 2 * launches_per_step * steps,
+        "clocks": clocks.summary(workload),
+    }
+    del graph, layer, t, x, lg, out, ws, flush
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return rec
+
+
+def measure_e2e(layer, d, x, lg, out, steps, do_flush, flush, world):
+    """The same layer end to end through the public API from and to pinned host
+    buffers, copies inside the timed region."""
+    # single step, serialised: one graph replay = two copies in, the layer, one out
+    hg = layer.host_graph(d.T)  # pinned host buffers, one graph launch per step
+    hg.x_host.copy_(x.cpu())
+    hg.logits_host.copy_(lg.cpu())
+    for _ in range(3):
+        hg.replay()
+    torch.cuda.synchronize()
+    e_ms = []
+    for i in range(steps):
+        if do_flush:
+            flush.fill_(i & 0xFF)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        hg.replay()  # copies in, the layer, copy out
+        torch.cuda.synchronize()
+        e_ms.append((time.perf_counter() - t0) * 1e3)
+    layer.forward(x, lg, out=out)
+    torch.cuda.synchronize()
+    out_ref = out.cpu()
+    if not torch.equal(hg.out_host, out_ref):
+        raise RuntimeError("host-buffer forward differs from the device forward")
+    xh, lgh, oh = hg.x_host, hg.logits_host, hg.out_host
+    single_ms = max_over_ranks(statistics.mean(e_ms), world)
+    e2e = {"h2d_bytes_per_step": int(xh.numel() * 2 + lgh.numel() * 4),
+           "d2h_bytes_per_step": int(oh.numel() * 2), "single_step_ms": single_ms}
+    del hg
+    if do_flush:
+        # L2 flushed between steps: steps cannot overlap, the serialised form stands
+        e2e.update(value=world * d.T / (single_ms * 1e-3), unit="tokens/s",
+                   ms_per_step=single_ms, steps=steps,
+                   api="MoELayer.host_graph(T).replay(): moe_forward_host captured as "
+                       "one CUDA graph over pinned host buffers, one step at a time")
+        return e2e
+    # steps through the native host-buffer pipeline: step i's copies overlap the
+    # kernels of steps i-1 and i+1; every step still copies its inputs in and its output
+    # out; the first copy-in and last copy-out are in the time
+    depth = 2
+    pipe = layer.host_pipeline(d.T, depth)
+    pxh = [xh.clone().pin_memory() for _ in range(depth)]
+    plh = [lgh.clone().pin_memory() for _ in range(depth)]
+    poh = [torch.empty_like(oh).pin_memory() for _ in range(depth)]
+    for i in range(2 * depth):
+        pipe.submit(pxh[i % depth], plh[i % depth], poh[i % depth])
+    pipe.sync()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        pipe.submit(pxh[i % depth], plh[i % depth], poh[i % depth])
+    pipe.sync()
+    pipe_ms = (time.perf_counter() - t0) * 1e3 / steps
+    for j in range(depth):
+        if not torch.equal(poh[j], out_ref):
+            raise RuntimeError("pipelined host-buffer forward differs from the device forward")
+    pipe.close()
+    em = max_over_ranks(pipe_ms, world)
+    e2e.update(value=world * d.T / (em * 1e-3), unit="tokens/s", ms_per_step=em, steps=steps,
+               api=f"MoELayer.host_pipeline(T, depth={depth}).submit() x steps + sync(): "
+                   "moe_host_pipeline_*, pinned host buffers, copies on their own streams "
+                   "overlapping neighbouring steps' kernels")
+    return e2e
+
+
+def sub_record(rec):
+    """The compact form of a workload's measurement carried inside the headline line."""
+    keep = ("value", "ms_per_step", "steps", "config", "roofline", "roofline_w2", "stage_ms",
+            "ms_per_step_l2_write_flushed", "ms_per_step_percentiles", "weight_gbs",
+            "gemm_tflops", "router_gate", "e2e", "clocks")
+    out = {k: rec[k] for k in keep}
+    out["unit"] = "tokens/s"
+    return out
+
+
+# Steps of the extra workloads the default run measures beside the headline line:
+# enough that each timed region lasts >= 2 s (>= 10 clock samples at 200 ms).
+EXTRA_STEPS = {"decode256": 600, "prefill": 60}
+EXTRA_E2E_STEPS = {"decode256": 50, "prefill": 20}
+
+
+def run_ours(args, rank, world, local):
+    import moe_expert_ffn_scan_gb300 as moe
+    moe.lib()
+    clocks = ClockSampler(local)
+    with clocks:
+        head = measure_layer(args, args.workload, args.steps, args.warmup, rank, world, local,
+                             clocks, soak_s=2.5, e2e_steps=None if args.no_e2e else args.steps,
+                             router=True, cpu=not args.no_cpu_baseline)
+        extras = {}
+        sweep = None
+        if args.workload == "decode" and not args.no_extra and args.experts is None \
+                and args.tokens is None:
+            for wl in ("decode256", "prefill"):
+                extras[wl] = sub_record(measure_layer(
+                    args, wl, EXTRA_STEPS[wl], args.warmup, rank, world, local, clocks,
+                    e2e_steps=None if args.no_e2e else EXTRA_E2E_STEPS[wl],
+                    router=(wl == "prefill")))
+            with clocks.load("sweep"):
+                pts = sweep_points(args, local, steps=5, warmup=3)
+            sweep = {"points": [{"gemm": p_["gemm"], "M": p_["M"], "ms": p_["ms"],
+                                 "bound": "hbm" if p_["hbm_frac"] >= p_["tensor_frac"]
+                                 else "tensor", "frac": p_["roofline_frac"]} for p_ in pts],
+                     "steps_per_point": 5, "l2": "flushed before each call",
+                     "clocks": clocks.summary("sweep")}
     if rank == 0:
+        d = head["d"]
+        clk = head["clocks"]
+        clk["window"] = ("the timed region and 2.5 s of back-to-back replays of the same "
+                         "step graph right before it")
         line = {
-            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+            "metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "mxfp4xfp8->f32", "data": "synthetic",
-            "config": {"workload": args.workload, "T": d.T, "H": d.H, "I": d.I, "E": d.E,
-                       "k": d.k, "shared_experts": d.has_shared, "active_groups": groups,
-                       "routed_rows": d.R, "l2": l2_note,
-                       "parallelism": f"replicas x{world}"},
-            "roofline": roof,
-            "stage_ms": stage_mean,
-            "stream_ms_per_step": stream_step_ms,
-            "ms_per_step_l2_write_flushed": flushed_ms,
-            "ms_per_step_percentiles": pct,
-            "weight_gbs": (w13_bytes + w2_bytes) / ((stage_mean["gemm_w13"] +
-                                                     stage_mean["gemm_w2"]) * 1e-3) / 1e9,
-            "gemm_tflops": (flops13 + flops2) / ((stage_mean["gemm_w13"] +
-                                                  stage_mean["gemm_w2"]) * 1e-3) / 1e12,
-            "router_gate": router,
-            "cpu_baseline": cpu,
-            "e2e": e2e,
-            "gpu_launches": 2 * launches_per_step * args.steps,
-            "clocks": clocks.summary(),
+            "config": head["config"],
+            "roofline": head["roofline"],
+            "roofline_w2": head["roofline_w2"],
+            "stage_ms": head["stage_ms"],
+            "stream_ms_per_step": head["stream_ms_per_step"],
+            "ms_per_step_l2_write_flushed": head["ms_per_step_l2_write_flushed"],
+            "ms_per_step_percentiles": head["ms_per_step_percentiles"],
+            "weight_gbs": head["weight_gbs"],
+            "gemm_tflops": head["gemm_tflops"],
+            "router_gate": head["router_gate"],
+            "cpu_baseline": head["cpu_baseline"],
+            "e2e": head["e2e"],
+            "gpu_launches": head["gpu_launches"],
+            "clocks": clk,
         }
+        if extras:
+            line["workloads"] = extras
+        if sweep:
+            line["sweep"] = sweep
         print(json.dumps(line), flush=True)
 
 
-def run_sweep(args, rank, world, local):
-    """Grouped-GEMM shape sweep: W13 (N=6144, K=7168) and W2 (N=7168, K=3072), G groups
-    of M rows each (G*M ~ 32768 for M >= 64, else G = 64).  Activations bf16 N(0,1),
-    quantised by the library's FP8 quantiser.  One JSON line with every point."""
+def sweep_points(args, local, steps, warmup, ms=None):
+    """Grouped-GEMM shape sweep points: W13 (N=6144, K=7168) and W2 (N=7168, K=3072), G
+    groups of M rows each (G*M ~ 32768 for M >= 64, else G = 64).  Activations bf16
+    N(0,1), quantised by the library's FP8 quantiser; L2 flushed before each call."""
     import moe_expert_ffn_scan_gb300 as moe
-    moe.lib()
     dev = torch.device("cuda", local)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
-    hbm, hbm_src = hbm_peak_gbs()
-    tpk, tpk_src = fp8_tensor_peak_tflops()
+    hbm, _ = hbm_peak_gbs()
+    tpk, _ = fp8_tensor_peak_tflops()
     points = []
     for which in ("w13", "w2"):
         N, K = gi.SWEEP_SHAPES[which]
-        for M in gi.SWEEP_M:
+        for M in (ms or gi.SWEEP_M):
             x, offsets, w, ws_ = gi.sweep_point(which, M, seed=args.seed, device=dev)
             rows, G = x.shape[0], offsets.numel() - 1
             q = torch.empty(rows, K, dtype=torch.uint8, device=dev)
@@ -604,12 +736,12 @@ def run_sweep(args, rank, world, local):
                     moe.moe_grouped_gemm_w13(d, q, qs, None, offsets, w, ws_, y, wsp)
                 else:
                     moe.moe_grouped_gemm_w2(d, q, qs, offsets, w, ws_, y, wsp)
-            for _ in range(args.warmup):
+            for _ in range(warmup):
                 call()
             torch.cuda.synchronize()
             evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                   for _ in range(args.steps)]
-            for i in range(args.steps):
+                   for _ in range(steps)]
+            for i in range(steps):
                 flush.fill_(i & 0xFF)
                 evs[i][0].record()
                 call()
@@ -618,16 +750,28 @@ def run_sweep(args, rank, world, local):
             bits = moe.moe_check_status(wsp)
             if bits:
                 raise RuntimeError(f"device status bits {bits:#x}")
-            ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+            ms_ = statistics.median(a.elapsed_time(b) for a, b in evs)
             wbytes = G * N * K * WEIGHT_BYTES_PER_ELEM
             flops = 2.0 * rows * N * K
-            gbs = wbytes / (ms * 1e-3) / 1e9
-            tfl = flops / (ms * 1e-3) / 1e12
-            points.append({"gemm": which, "M": M, "G": G, "ms": ms, "weight_gbs": gbs,
+            gbs = wbytes / (ms_ * 1e-3) / 1e9
+            tfl = flops / (ms_ * 1e-3) / 1e12
+            points.append({"gemm": which, "M": M, "G": G, "ms": ms_, "weight_gbs": gbs,
                            "tflops": tfl, "hbm_frac": gbs / hbm, "tensor_frac": tfl / tpk,
                            "roofline_frac": max(gbs / hbm, tfl / tpk)})
             del q, qs, y, w, ws_, wsp
             torch.cuda.empty_cache()
+    del flush
+    torch.cuda.empty_cache()
+    return points
+
+
+def run_sweep(args, rank, world, local):
+    """The grouped-GEMM sweep on its own: one JSON line with every point."""
+    import moe_expert_ffn_scan_gb300 as moe
+    moe.lib()
+    hbm, hbm_src = hbm_peak_gbs()
+    tpk, tpk_src = fp8_tensor_peak_tflops()
+    points = sweep_points(args, local, args.steps, args.warmup)
     if rank == 0:
         line = {"metric": "grouped-GEMM sweep (weight GB/s, TFLOP/s per M)",
                 "value": statistics.mean(p["roofline_frac"] for p in points),

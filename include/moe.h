@@ -20,8 +20,8 @@
  *     aligned.  (moe_host_pipeline_create creates CUDA streams and events, and a
  *     small host-side handle; see there.)
  *   - Every call is asynchronous on `stream` (a cudaStream_t, NULL = legacy default
- *     stream) and never synchronises the host, except moe_check_status and
- *     moe_host_pipeline_sync / moe_host_pipeline_destroy.
+ *     stream) and never synchronises the host, except moe_check_status,
+ *     moe_route_static_status and moe_host_pipeline_sync / moe_host_pipeline_destroy.
  *   - Return value: MOE_OK or an MOE_ERR_* code.  Shapes and pointers are checked
  *     on the host before any launch; nothing is launched when a check fails.
  *     Launch failures return MOE_ERR_CUDA.  Data-dependent device checks (an index
@@ -121,19 +121,30 @@ int moe_route(const moe_dims* d, const float* logits, int32_t* idx, float* w, in
  * memory (a host framework whose pool owns every device byte, or a latency-critical
  * loop that cannot afford cudaMalloc/cudaFree and their implicit synchronisation).
  * The pages have no counterpart: this is an interface convenience, not a step of
- * the method.  Same arguments and results as moe_route minus ws / ws_bytes.
+ * the method.  Same arguments and results as moe_route minus ws / ws_bytes; logits
+ * and the six outputs must be 4-byte aligned (else MOE_ERR_INVALID_ARG).
  *   - Scratch lives in a fixed device array of 256 KiB + 256 bytes inside the
  *     library, held on every GPU that loads it until the process exits.  Limit:
  *     ceil(T/256) * E <= 32768 (T <= 8192 at E = 1024, T <= 21760 at E = 384);
  *     larger inputs return MOE_ERR_UNSUPPORTED_SHAPE.
- *   - The first call on each device looks up the array's device address (with that
- *     device current); make that first call before any stream capture.
+ *   - The first call in each CUDA context (per device, and again after
+ *     cudaDeviceReset) looks up the array's device address with that context
+ *     current; make that first call before any stream capture.
  *   - All calls share the array and it keeps the last call's contents; calls that
  *     overlap on the GPU (other streams, other host threads) race on it and must be
- *     serialised by the caller.  Nothing is allocated. */
+ *     serialised by the caller.  Nothing is allocated.
+ *   - Device-side checks (an expert index out of range) set bits in a status word
+ *     at the start of the array, cleared by each call's first kernel; read it with
+ *     moe_route_static_status. */
 int moe_route_static(const moe_dims* d, const float* logits, int32_t* idx, float* w,
                      int32_t* counts, int32_t* offsets, int32_t* perm_src, int32_t* inv,
                      void* stream);
+
+/* Debug helper for moe_route_static (synchronises `stream`): reads the status word of
+ * its fixed array as moe_check_status reads a workspace's.  Returns MOE_OK if no bit
+ * is set, else MOE_ERR_DEVICE_CHECK and the bits in *bits_out (if not NULL); the
+ * bits are those of the last moe_route_static call in the current context. */
+int moe_route_static_status(void* stream, uint32_t* bits_out);
 
 /* f4: router gate projection in front of moe_route:
  *     logits[t][e] = sum_h x[t][h] * wg[e][h],  fp32 products and fp32 sums,

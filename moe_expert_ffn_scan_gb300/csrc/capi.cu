@@ -2,11 +2,40 @@
 // No allocation, no host synchronisation (except moe_check_status).
 #include <stdio.h>
 
+#include <mutex>
 #include <new>
 
 #include "kernels.cuh"
 
 using namespace moe;
+
+namespace moe {
+
+unsigned long long current_context_id() {
+  using GetCurrentFn = CUresult (*)(CUcontext*);
+  using GetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrentFn get_current = nullptr;
+  static GetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPoint("cuCtxGetCurrent", &p, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrentFn>(p);
+    if (cudaGetDriverEntryPoint("cuCtxGetId", &p, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetIdFn>(p);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  // a destroyed context that still reads as current makes cuCtxGetId fail: report 0
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+}  // namespace moe
 
 namespace {
 
@@ -238,7 +267,9 @@ int moe_route(const moe_dims* d, const float* logits, int32_t* idx, float* w, in
   if (!dims_ok(d)) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (!logits || !idx || !w || !counts || !offsets || !perm_src || !inv || !ws)
     return MOE_ERR_INVALID_ARG;
-  if (!aligned(ws, kAlign) || !aligned(logits, 4)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(ws, kAlign) || !aligned(logits, 4) || !aligned(idx, 4) || !aligned(w, 4) ||
+      !aligned(counts, 4) || !aligned(offsets, 4) || !aligned(perm_src, 4) || !aligned(inv, 4))
+    return MOE_ERR_INVALID_ARG;
   if (ws_bytes < moe_route_workspace_size(d)) return MOE_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   Carver c(ws);

@@ -107,6 +107,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
   }
 }
 
+// Wait for a phase on the abort path itself: no abort flag to consult, a short limit,
+// no status bit (the failure that led here is already recorded).  Returns whether the
+// phase completed.
+constexpr uint64_t kDrainLimitNs = 100000000ull;
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > kDrainLimitNs) return false;
+  return true;
+}
+
 // ------------------------------------------------------------------ TMA -----------
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {

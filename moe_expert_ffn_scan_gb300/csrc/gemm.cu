@@ -89,8 +89,9 @@ struct GemmCfg {
   static constexpr int kIssuers = BN_MAX <= 16 ? 2 : 1;
   static constexpr int kAccCols = kIssuers * BN_MAX;  // one accumulator buffer
   // full[issuer][stage] (each issuer waits only on its own, so it sees every phase of
-  // every barrier it waits on), empty[stage], acc_full[2], acc_empty[2], sf_full[stage]
-  static constexpr int kNumBars = (kIssuers + 2) * STAGES + 4;
+  // every barrier it waits on), empty[stage], acc_full[2], acc_empty[2], sf_full[stage],
+  // drain[issuer] (the abort path's wait for MMAs already issued)
+  static constexpr int kNumBars = (kIssuers + 2) * STAGES + 4 + kIssuers;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16;
   static constexpr int kSfCols = 4 * (KO + kSfbAtoms);      // TMEM columns per stage
@@ -143,6 +144,7 @@ __global__ void __launch_bounds__(256, OCC)
   uint64_t* acc_full = empty + STAGES;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* sf_full = acc_empty + 2;
+  uint64_t* drain = sf_full + STAGES;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
@@ -160,6 +162,7 @@ __global__ void __launch_bounds__(256, OCC)
       mbar_init(&acc_full[b], C::kIssuers);  // one tcgen05.commit per issuer
       mbar_init(&acc_empty[b], 4);  // four epilogue warps
     }
+    for (int i = 0; i < C::kIssuers; ++i) mbar_init(&drain[i], 1);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmW);
@@ -580,6 +583,14 @@ __global__ void __launch_bounds__(256, OCC)
     }
   }
 
+  // After an abort, each MMA issuer waits (briefly, bounded) until the MMAs it already
+  // issued have completed, so that TMEM is not released under them.  TMA loads still in
+  // flight at an abort are not waited for: that unwind is best effort.
+  if ((warp == 1 || (C::kIssuers == 2 && warp == 3)) && lane == 0 && *abort_flag) {
+    uint64_t* db = &drain[warp == 1 ? 0 : 1];
+    tc_commit(db);
+    mbar_wait_drain(db, 0);
+  }
   // Let the next kernel's CTAs in only now, so that none of them sits on an SM waiting
   // for this grid for the whole GEMM; the overlap left is this grid's drain.
   pdl_trigger();
@@ -632,14 +643,17 @@ cudaError_t launch_one(const CUtensorMap& tmW, const CUtensorMap& tmX, const Gem
                        int max_items, cudaStream_t st) {
   using C = GemmCfg<BN_MAX, STAGES, KO, OCC>;
   auto kern = k_gemm_mx<BN_MAX, STAGES, KO, OCC>;
-  static bool attr_set[64] = {};
+  // the shared-memory attribute is set once per context (again after a reset)
+  static unsigned long long attr_ctx[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (!attr_set[dev]) {
+  const unsigned long long ctx = current_context_id();
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (ctx == 0 || attr_ctx[dev] != ctx) {
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    attr_ctx[dev] = current_context_id();
   }
   const long long tiles = static_cast<long long>(max_items) * (p.N / 128);
   if (tiles == 0) return cudaSuccess;

@@ -118,6 +118,12 @@ struct GemmLaunch {
 };
 cudaError_t launch_grouped_gemm(const GemmLaunch& a, cudaStream_t st);
 
+// Unique id of the calling thread's current CUDA context (cuCtxGetId), 0 when no
+// context is current or the driver entry points are unavailable.  Host-side caches of
+// per-context state (a function attribute, a symbol's device address) are keyed on it:
+// a context created after cudaDeviceReset has a new id, so the state is set up again.
+unsigned long long current_context_id();
+
 // Transaction bytes one 128 x 128 weight-tile TMA load reports to its mbarrier: the
 // packed global size (128 rows x 64 bytes), not the 16-byte-aligned shared-memory
 // footprint (which is twice that).

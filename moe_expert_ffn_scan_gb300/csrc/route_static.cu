@@ -24,10 +24,15 @@ constexpr size_t kStatusBytes = 256;
 
 __device__ __align__(256) uint8_t g_route_scratch[kStaticScratchBytes];
 
-// Device address of g_route_scratch per device, looked up once per device with that
-// device current (in host code the array's name is only a host-side stand-in).
+// Device address of g_route_scratch, looked up with cudaGetSymbolAddress (in host code
+// the array's name is only a host-side stand-in) once per CUDA context and cached
+// under that context's unique id.  A context that replaces the one the address was
+// taken in (after cudaDeviceReset, or a different context made current on the same
+// device) has another id, so the address is looked up again there: the module, and
+// with it the array, may have moved.
 struct SymbolCache {
   std::mutex mu;
+  unsigned long long ctx_id[64] = {};
   void* addr[64] = {};
 };
 
@@ -43,15 +48,22 @@ cudaError_t scratch_address(void** out) {
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   SymbolCache& c = cache();
   std::lock_guard<std::mutex> lock(c.mu);
-  if (!c.addr[dev]) {
+  // id 0: no current context yet, or a destroyed one (cudaDeviceReset) still reads as
+  // current; the lookup below makes the runtime's context current, and the id is read
+  // again after it.
+  const unsigned long long id = moe::current_context_id();
+  if (id == 0 || c.ctx_id[dev] != id || !c.addr[dev]) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_route_scratch);
     if (e != cudaSuccess) return e;
+    c.ctx_id[dev] = moe::current_context_id();
     c.addr[dev] = p;
   }
   *out = c.addr[dev];
   return cudaSuccess;
 }
+
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 }  // namespace
 
@@ -63,6 +75,9 @@ extern "C" int moe_route_static(const moe_dims* d, const float* logits, int32_t*
     return MOE_ERR_UNSUPPORTED_SHAPE;
   if (static_cast<long long>(d->T) * d->k + d->T >= (1LL << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (!logits || !idx || !w || !counts || !offsets || !perm_src || !inv)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned4(logits) || !aligned4(idx) || !aligned4(w) || !aligned4(counts) ||
+      !aligned4(offsets) || !aligned4(perm_src) || !aligned4(inv))
     return MOE_ERR_INVALID_ARG;
   // the two per-(token block, expert) tables must fit the fixed scratch
   const size_t table = static_cast<size_t>(moe::perm_blocks(d->T)) * d->E * sizeof(int32_t);
@@ -83,4 +98,12 @@ extern "C" int moe_route_static(const moe_dims* d, const float* logits, int32_t*
                           offsets, perm_src, inv, status, st) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
+}
+
+extern "C" int moe_route_static_status(void* stream, uint32_t* bits_out) {
+  if (bits_out) *bits_out = 0;
+  void* base = nullptr;
+  if (scratch_address(&base) != cudaSuccess) return MOE_ERR_CUDA;
+  // the status word is the first word of the fixed array (see moe_route_static)
+  return moe_check_status(base, stream, bits_out);
 }

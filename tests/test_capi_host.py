@@ -78,6 +78,13 @@ def test_validation_happens_before_any_launch(lib):
     fake = P(0x1000 + 8)
     assert lib.moe_route(ctypes.byref(d), P(0x1000), P(0x1000), P(0x1000), P(0x1000),
                          P(0x1000), P(0x1000), P(0x1000), fake, 1 << 20, None) == 1
+    # misaligned logits or outputs -> invalid argument
+    for i in range(7):
+        ptrs = [P(0x1000)] * 7
+        ptrs[i] = P(0x1002)
+        assert lib.moe_route(ctypes.byref(d), *ptrs, P(0x10000), 1 << 20, None) == 1
+        lib.moe_route_static.argtypes = [ctypes.POINTER(moe.moe_dims)] + [P] * 8
+        assert lib.moe_route_static(ctypes.byref(d), *ptrs, None) == 1
     # workspace too small
     assert lib.moe_route(ctypes.byref(d), P(0x1000), P(0x1000), P(0x1000), P(0x1000),
                          P(0x1000), P(0x1000), P(0x1000), P(0x10000), 16, None) == 3

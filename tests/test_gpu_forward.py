@@ -144,6 +144,66 @@ def test_forward_zero_input():
 
 # ---------------------------------------------------------------- full size ---------
 
+def _group_rows_at_tile_positions(offsets, G, rng, n_large=6, edge=720):
+    """Packed rows to check: in every group its first and last row and two random ones;
+    in the n_large largest groups also the rows on both sides of every 16-row boundary
+    within `edge` rows of either end.  Groups above 240 rows are cut by the tile plan
+    into near-equal chunks of multiples of 16 rows (mid variant up to 128, large up to
+    240), so these rows land on every token-tile position of the first and last chunks,
+    the ragged final chunk included."""
+    sizes = np.diff(offsets[:G + 1])
+    large = set(np.argsort(-sizes, kind="stable")[:n_large].tolist())
+    rows = []
+    for g in range(G):
+        r0, m = int(offsets[g]), int(sizes[g])
+        if m == 0:
+            continue
+        pos = {0, m - 1}
+        pos.update(rng.integers(0, m, size=min(2, m)).tolist())
+        if g in large:
+            for b in range(16, m, 16):
+                if b <= edge or b >= m - edge:
+                    pos.update((b - 1, b))
+        rows += [r0 + p for p in sorted(pos)]
+    return np.array(sorted(set(rows)), dtype=np.int64)
+
+
+def _packed_rows_check(d, t, dbg, offsets, perm_src, rows, n_cols, seed):
+    """Stage-isolated checks of W13, SwiGLU + quant and W2 on the given packed rows:
+    y13 against the oracle GEMM of the token's FP8 row with the group's weights, hq/hs
+    against the oracle's quantisation of the GPU's own y13 row, and y2 against the
+    oracle GEMM of the GPU's own hq/hs row; sampled output columns."""
+    R = d.T * d.k
+    rng = np.random.default_rng(seed)
+    G = len(offsets) - 1
+    grp = np.searchsorted(offsets, rows, side="right") - 1
+    tok = np.where(rows < R, perm_src[np.minimum(rows, R - 1)] // d.k, rows - R)
+    xq, xs = o.quant_act(bits_np(t["x"][torch.from_numpy(tok).to(DEV)]))
+    sel = torch.from_numpy(rows).to(DEV)
+    y13_rows = bf16_np(dbg["y13"][sel])
+    hq_rows = dbg["hq"][sel].cpu().numpy()
+    hs_rows = dbg["hs"][sel].cpu().numpy()
+    y2_rows = bf16_np(dbg["y2"][sel])
+    c13 = np.sort(rng.choice(2 * d.I, size=n_cols, replace=False))
+    c2 = np.sort(rng.choice(d.H, size=n_cols, replace=False))
+    ref13 = np.empty((len(rows), n_cols))
+    ref2 = np.empty((len(rows), n_cols))
+    for g in np.unique(grp):
+        i = np.where(grp == g)[0]
+        off = np.array([0, len(i)], np.int32)
+        cc = torch.from_numpy(c13).to(DEV)
+        ref13[i] = o.grouped_gemm(xq[i], xs[i], off, t["w13"][int(g)][cc].cpu().numpy()[None],
+                                  t["w13_s"][int(g)][cc].cpu().numpy()[None])
+        cc = torch.from_numpy(c2).to(DEV)
+        ref2[i] = o.grouped_gemm(hq_rows[i], hs_rows[i], off,
+                                 t["w2"][int(g)][cc].cpu().numpy()[None],
+                                 t["w2_s"][int(g)][cc].cpu().numpy()[None])
+    assert_float_close(y13_rows[:, c13], ref13, "y13 packed rows")
+    rq, rs = o.swiglu_quant(y13_rows)
+    assert_fp8_codes_close(hq_rows, hs_rows, rq, rs, "hq packed rows", max_mismatch=1e-3)
+    assert_float_close(y2_rows[:, c2], ref2, "y2 packed rows")
+
+
 def _sampled_check(workload, n_tokens, n_cols, seed=0):
     d, t = gi.make_layer(workload, seed=seed, device=DEV)
     md = moe.dims(d.T, d.H, d.I, d.E, d.k, d.has_shared)
@@ -190,6 +250,11 @@ def _sampled_check(workload, n_tokens, n_cols, seed=0):
     assert_float_close(y13, ref["y13"][ref_rows], "y13 rows")
     y2 = bf16_np(dbg["y2"][torch.from_numpy(rows).to(DEV)])
     assert_float_close(y2, ref["y2"][ref_rows], "y2 rows")
+    if n_cols:
+        # packed rows at every tile position of every group (the largest groups reach
+        # the mid and large GEMM variants), checked stage by stage on sampled columns
+        prow = _group_rows_at_tile_positions(roff, d.G, np.random.default_rng(seed + 2))
+        _packed_rows_check(d, t, dbg, roff, g["perm_src"], prow, n_cols, seed + 3)
     del t, dbg
     torch.cuda.empty_cache()
 
@@ -199,8 +264,8 @@ def test_forward_decode_full_size_sampled():
 
 
 def test_forward_decode256_full_size_sampled():
-    _sampled_check("decode256", n_tokens=2, n_cols=0)
+    _sampled_check("decode256", n_tokens=16, n_cols=64)
 
 
 def test_forward_prefill_full_size_sampled():
-    _sampled_check("prefill", n_tokens=1, n_cols=0)
+    _sampled_check("prefill", n_tokens=1, n_cols=96)

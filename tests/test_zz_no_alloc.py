@@ -55,6 +55,16 @@ def _route_ws(d, logits):
     return o
 
 
+def _static_status():
+    fn = moe.lib().moe_route_static_status
+    fn.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32)]
+    fn.restype = ctypes.c_int
+    bits = ctypes.c_uint32(0xFFFFFFFF)
+    rc = fn(ctypes.c_void_p(torch.cuda.current_stream().cuda_stream), ctypes.byref(bits))
+    assert rc in (0, 5), rc
+    return bits.value
+
+
 def test_route_static_matches_route_two_calls_in_a_row():
     cases = [(moe.dims(4096, 128, 128, 384, 8, 1), "zipf", 1),
              (moe.dims(7, 128, 128, 384, 8, 1), "normal", 2)]
@@ -69,6 +79,8 @@ def test_route_static_matches_route_two_calls_in_a_row():
         # same kernels on the same inputs: the weights agree bit for bit too, well
         # inside the float tolerance the other tests use (rtol 2e-6)
         np.testing.assert_allclose(got["w"].cpu().numpy(), ref["w"].cpu().numpy(), rtol=2e-6)
+        # the device-side index checks of the call found nothing
+        assert _static_status() == 0
 
 
 def test_route_static_rejects_sizes_beyond_its_scratch():
@@ -78,3 +90,20 @@ def test_route_static_rejects_sizes_beyond_its_scratch():
     fn.restype = ctypes.c_int
     d = moe.dims(8193, 128, 128, 1024, 8, 0)   # ceil(8193/256) * 1024 > 32768
     assert fn(ctypes.byref(d), *[P(0x1000)] * 7, None) == 2
+    # a misaligned pointer is rejected on the host, before any launch
+    d = moe.dims(64, 128, 128, 8, 2, 0)
+    assert fn(ctypes.byref(d), P(0x1002), *[P(0x1000)] * 6, None) == 1
+    assert fn(ctypes.byref(d), P(0x1000), P(0x1000), P(0x1001), *[P(0x1000)] * 4, None) == 1
+
+
+def test_route_static_survives_device_reset():
+    """After cudaDeviceReset the library's module, and the fixed array with it, is
+    loaded again, possibly elsewhere: the array's address is looked up again in the new
+    context.  Run in a child process, whose context the reset may end."""
+    import os
+    import subprocess
+    import sys
+    here = os.path.dirname(os.path.abspath(__file__))
+    r = subprocess.run([sys.executable, os.path.join(here, "_route_static_reset_child.py")],
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout + r.stderr
