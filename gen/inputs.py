@@ -16,7 +16,9 @@ DeepSeek-V4-Pro" -- 384 routed experts, one shared expert -- and the GB10
 
 Weights are MXFP4: E2M1 code bytes uniform over all 256 values (so each nibble is
 uniform over the 16 codes), E8M0 scale bytes uniform over {123..127} (exponent
-uniform in [-4, 0]).  Activations are bf16 N(0, 1).
+uniform in [-4, 0]).  The NVFP4 form (nvfp4_layer_weights) draws the same code
+bytes, E4M3 block scales uniform over the 40 positive codes 2^-4 .. 1.875, and fp32
+tensor scales uniform in [0.5, 1.5).  Activations are bf16 N(0, 1).
 
 Router logits:
   tiny:            logits = the gate projection x . W_g^T with W_g fp32 ~ N(0, 0.02);
@@ -93,6 +95,34 @@ def mxfp4_weights(G, N, K, seed, device, name="w13", exp_lo=-4, exp_hi=0):
                            generator=_gen(seed, name + "_s", device), device=device,
                            dtype=torch.uint8)
     return codes, scales
+
+
+# NVFP4 block scales: positive E4M3 codes with exponent field 3..7 and any mantissa,
+# i.e. values 2^-4 .. 1.875 (the same binades as the MXFP4 scales above).
+NVFP4_SCALE_CODES = tuple((e << 3) | m for e in range(3, 8) for m in range(8))
+
+
+def nvfp4_weights(G, N, K, seed, device, name="w13", segments=1):
+    """Random NVFP4 matrices: code bytes u8 [G, N, K/2] (each nibble uniform over the
+    16 E2M1 codes), E4M3 block-scale bytes u8 [G, N, K/16] uniform over
+    NVFP4_SCALE_CODES, fp32 tensor scales [G, segments] uniform in [0.5, 1.5)."""
+    codes = torch.randint(0, 256, (G, N, K // 2), generator=_gen(seed, name, device),
+                          device=device, dtype=torch.uint8)
+    table = torch.tensor(NVFP4_SCALE_CODES, dtype=torch.uint8, device=device)
+    i = torch.randint(0, len(table), (G, N, K // 16), generator=_gen(seed, name + "_s", device),
+                      device=device)
+    gs = 0.5 + torch.rand(G, segments, generator=_gen(seed, name + "_s", "cpu"),
+                          dtype=torch.float32)
+    return codes, table[i], gs.to(device)
+
+
+def nvfp4_layer_weights(d, seed=0, device="cpu"):
+    """NVFP4 expert weights of a layer: w13 [G, 2I, H/2] + w13_s [G, 2I, H/16] + w13_gs
+    [G, 2] (gate rows, up rows), w2 [G, H, I/2] + w2_s [G, H, I/16] + w2_gs [G]."""
+    w13, w13_s, w13_gs = nvfp4_weights(d.G, 2 * d.I, d.H, seed, device, "w13", segments=2)
+    w2, w2_s, w2_gs = nvfp4_weights(d.G, d.H, d.I, seed, device, "w2", segments=1)
+    return dict(w13=w13, w13_s=w13_s, w13_gs=w13_gs, w2=w2, w2_s=w2_s,
+                w2_gs=w2_gs.reshape(d.G))
 
 
 def activations(T, H, seed, device, name="x"):

@@ -15,7 +15,8 @@ What it computes, stage by stage, follows the routed-MoE expert path described i
   * §4.3 (decode hot path): SwiGLU fused with the FP8 quantisation that directly
     produces W2's data and scales;
 and from the GB10 "Optimization progress report", Optimization 14 (route preplan:
-tokens packed by expert before the MoE launch).
+tokens packed by expert before the MoE launch) and Optimization 05 (native NVFP4
+MoE: the expert weights kept in NVFP4 and read as such by the expert GEMMs).
 
 The pages do not define bit formats, block sizes, routing or tie rules.  The
 readings taken here (each one a plain, checkable definition):
@@ -23,6 +24,9 @@ readings taken here (each one a plain, checkable definition):
     OCP 8-bit floating point "FN" variant (bias 7, max 448, no infinities).
   * MXFP4 weight block = 32 consecutive K elements sharing one E8M0 scale; two
     E2M1 codes per byte with the even K index in the low nibble.
+  * NVFP4 weights (the second format): the same E2M1 codes and packing, one FP8
+    E4M3 scale per 16 consecutive K elements, and one fp32 scale per weight tensor
+    (W13's gate rows and up rows are two tensors, W2 is one).
   * FP8 activations: one power-of-two scale per row per 128 columns; the scale
     exponent is the smallest integer e with amax <= 448 * 2**e, stored as e + 127;
     codes are round-to-nearest-even of x * 2**-e (saturating, never needed).
@@ -201,6 +205,48 @@ def mxfp4_dequant(codes, scales):
 
 
 # ---------------------------------------------------------------------------
+# f3: NVFP4 weights
+# ---------------------------------------------------------------------------
+
+NVBLOCK = 16
+
+
+def nvfp4_dequant(codes, scales, global_scale=None):
+    """NVFP4 weight matrix -> float64 (GB10 "Optimization progress report",
+    Optimization 05: the MoE expert weights stay in their native NVFP4 form and the
+    expert kernel reads them as such).  The page names the format without defining
+    it; the reading is NVIDIA's NVFP4: E2M1 values in blocks of 16 consecutive K
+    elements, each block with one FP8 E4M3 scale, and one fp32 scale per tensor.
+
+    codes u8 [N, K/2] (two E2M1 codes per byte, even K index in the low nibble, as
+    for MXFP4), scales u8 [N, K/16] (E4M3 codes), global_scale: None (1.0), a
+    scalar, or an array [S] of fp32 scales for S equal segments of the N rows (W13
+    keeps the gate rows and the up rows as two tensors, each with its own scale).
+    Returns [N, K]: e2m1(code) * e4m3(scale of its 16-block) * segment scale."""
+    codes = np.asarray(codes)
+    n, kh = codes.shape
+    k = kh * 2
+    vals = np.empty((n, k), dtype=np.float64)
+    vals[:, 0::2] = e2m1_decode(codes & 0xF)
+    vals[:, 1::2] = e2m1_decode(codes >> 4)
+    s = e4m3_decode(scales)
+    w = (vals.reshape(n, k // NVBLOCK, NVBLOCK) * s[:, :, None]).reshape(n, k)
+    if global_scale is not None:
+        gs = np.atleast_1d(np.asarray(global_scale, dtype=np.float32).astype(np.float64))
+        w = w * np.repeat(gs, n // len(gs))[:, None]
+    return w
+
+
+def weight_dequant(fmt, codes, scales, global_scale=None):
+    """Expert weight matrix of either format -> float64 [N, K]."""
+    if fmt == "mxfp4":
+        return mxfp4_dequant(codes, scales)
+    if fmt == "nvfp4":
+        return nvfp4_dequant(codes, scales, global_scale)
+    raise ValueError(fmt)
+
+
+# ---------------------------------------------------------------------------
 # f4: router gate projection (the scores the TopK step ranks)
 # ---------------------------------------------------------------------------
 
@@ -283,12 +329,14 @@ def packed_row_token(perm_src, T, k, has_shared):
 # a4 / a6: grouped GEMMs
 # ---------------------------------------------------------------------------
 
-def grouped_gemm(act_codes, act_scales, offsets, w_codes, w_scales, groups=None):
+def grouped_gemm(act_codes, act_scales, offsets, w_codes, w_scales, groups=None,
+                 fmt="mxfp4", w_global=None):
     """Stages a4 / a6 (LMSYS-H20 §3.3: W13 and W2 grouped GEMMs over the experts).
 
     For every group g and packed row r in [offsets[g], offsets[g+1]):
         y[r, n] = sum_k deq(act)[r, k] * deq(W[g])[n, k]
-    with act = FP8 E4M3 codes [Rows, K] + per-128 scales, W[g] = MXFP4 [N, K];
+    with act = FP8 E4M3 codes [Rows, K] + per-128 scales, W[g] = MXFP4 [N, K] (or
+    NVFP4 with fmt="nvfp4" and per-group tensor scales w_global [G] or [G, S]);
     summed in float64 and rounded once to bf16.  Returns float64 [Rows, N] holding
     bf16 values.  `groups` restricts the work to a subset of groups (the other rows
     are left as NaN)."""
@@ -301,7 +349,8 @@ def grouped_gemm(act_codes, act_scales, offsets, w_codes, w_scales, groups=None)
         if r1 == r0:
             continue
         a = dequant_rows(act_codes[r0:r1], act_scales[r0:r1])
-        w = mxfp4_dequant(w_codes[g], w_scales[g])
+        gs = None if w_global is None else np.asarray(w_global)[g]
+        w = weight_dequant(fmt, w_codes[g], w_scales[g], gs)
         y[r0:r1] = bf16_round(a @ w.T)
     return y
 
@@ -353,12 +402,15 @@ def combine(y2, inv, w, T, k, has_shared):
 # Whole layer
 # ---------------------------------------------------------------------------
 
-def moe_forward(x_bf16_bits, logits, k, w13, w13_s, w2, w2_s, has_shared):
+def moe_forward(x_bf16_bits, logits, k, w13, w13_s, w2, w2_s, has_shared, fmt="mxfp4",
+                w13_gs=None, w2_gs=None):
     """The whole routed-expert FFN, stages a1..a7 in order.
 
     x_bf16_bits uint16 [T, H]; logits fp32 [T, E]; w13 u8 [G, 2I, H/2],
     w13_s u8 [G, 2I, H/32], w2 u8 [G, H, I/2], w2_s u8 [G, H, I/32] with
-    G = E + has_shared (the shared expert is group E).
+    G = E + has_shared (the shared expert is group E).  With fmt="nvfp4" the scales
+    are E4M3 per 16 K ([G, 2I, H/16], [G, H, I/16]) and w13_gs [G, 2] (gate, up) /
+    w2_gs [G] hold the fp32 tensor scales (None: 1).
     Returns a dict with every intermediate (same names as the C interface)."""
     T, H = x_bf16_bits.shape
     E = logits.shape[1]
@@ -366,24 +418,26 @@ def moe_forward(x_bf16_bits, logits, k, w13, w13_s, w2, w2_s, has_shared):
     counts, offsets, perm_src, inv = permute(idx, E, has_shared)
     xq, xs = quant_act(x_bf16_bits)
     tok = packed_row_token(perm_src, T, k, has_shared)
-    y13 = grouped_gemm(xq[tok], xs[tok], offsets, w13, w13_s)
+    y13 = grouped_gemm(xq[tok], xs[tok], offsets, w13, w13_s, fmt=fmt, w_global=w13_gs)
     hq, hs = swiglu_quant(y13)
-    y2 = grouped_gemm(hq, hs, offsets, w2, w2_s)
+    y2 = grouped_gemm(hq, hs, offsets, w2, w2_s, fmt=fmt, w_global=w2_gs)
     out = combine(y2, inv, w, T, k, has_shared)
     return dict(idx=idx, w=w, counts=counts, offsets=offsets, perm_src=perm_src,
                 inv=inv, xq=xq, xs=xs, y13=y13, hq=hq, hs=hs, y2=y2, out=out)
 
 
-def moe_forward_tokens(x_bf16_bits, logits, k, w13, w13_s, w2, w2_s, has_shared, tokens):
+def moe_forward_tokens(x_bf16_bits, logits, k, w13, w13_s, w2, w2_s, has_shared, tokens,
+                       fmt="mxfp4", w13_gs=None, w2_gs=None):
     """The layer output for a subset of tokens only (each token's output depends only
     on its own row of x and logits).  Used to check full-size runs on a sample."""
     tokens = np.asarray(tokens, dtype=np.int64)
     res = moe_forward(x_bf16_bits[tokens], np.asarray(logits)[tokens], k,
-                      w13, w13_s, w2, w2_s, has_shared)
+                      w13, w13_s, w2, w2_s, has_shared, fmt, w13_gs, w2_gs)
     return res
 
 
-def dense_unrouted_forward(x_bf16_bits, logits, k, w13, w13_s, w2, w2_s, has_shared):
+def dense_unrouted_forward(x_bf16_bits, logits, k, w13, w13_s, w2, w2_s, has_shared,
+                           fmt="mxfp4", w13_gs=None, w2_gs=None):
     """Independent recomputation for pinning the routed path on tiny shapes: every
     token goes through every expert (no histogram, no permutation, no gather), and
     the top-k mask selects afterwards.  The per-(token, expert) arithmetic is the same
@@ -394,10 +448,13 @@ def dense_unrouted_forward(x_bf16_bits, logits, k, w13, w13_s, w2, w2_s, has_sha
     xq, xs = quant_act(x_bf16_bits)
     xa = dequant_rows(xq, xs)
     y2_all = np.zeros((G, T, w2.shape[1]))
+    g13 = (lambda g: None) if w13_gs is None else (lambda g: np.asarray(w13_gs)[g])
+    g2 = (lambda g: None) if w2_gs is None else (lambda g: np.asarray(w2_gs)[g])
     for g in range(G):
-        y13 = bf16_round(xa @ mxfp4_dequant(w13[g], w13_s[g]).T)
+        y13 = bf16_round(xa @ weight_dequant(fmt, w13[g], w13_s[g], g13(g)).T)
         hq, hs = swiglu_quant(y13)
-        y2_all[g] = bf16_round(dequant_rows(hq, hs) @ mxfp4_dequant(w2[g], w2_s[g]).T)
+        y2_all[g] = bf16_round(dequant_rows(hq, hs) @ weight_dequant(fmt, w2[g], w2_s[g],
+                                                                     g2(g)).T)
     # brute-force selection: k rounds of "largest remaining logit, lowest index on ties"
     lg = np.asarray(logits, dtype=np.float32).astype(np.float64)
     out = np.zeros((T, w2.shape[1]))
