@@ -66,6 +66,8 @@ def parse():
     ap.add_argument("--experts", type=int, default=None,
                     help="override E (a smaller layer of the same shape, for ncu captures)")
     ap.add_argument("--tokens", type=int, default=None, help="override T")
+    ap.add_argument("--weights", default="mxfp4", choices=["mxfp4", "nvfp4"],
+                    help="expert weight format of the measured layer")
     ap.add_argument("--no-extra", action="store_true",
                     help="decode only: skip the decode256 / prefill / sweep records")
     return ap.parse_args()
@@ -352,7 +354,22 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def gemm_roofline(d, groups, t_ms, which, hbm, hbm_src, tpk, tpk_src):
+def bf16_tensor_peak_tflops():
+    """Dense bf16 tensor peak (the NVFP4 path's kind::f16 MMAs): the measured cuBLAS
+    bf16 burst figure, else the fallback."""
+    peaks, _ = measured_peaks()
+    if peaks and "bf16_tflops" in peaks:
+        try:
+            return float(peaks["bf16_tflops"]), "measured bf16 (cuBLAS burst)"
+        except (TypeError, ValueError):
+            pass
+    return FALLBACK_BF16_TFLOPS, "fallback bf16"
+
+
+WEIGHT_BYTES = {"mxfp4": 0.5 + 1.0 / 32.0, "nvfp4": 0.5 + 1.0 / 16.0}
+
+
+def gemm_roofline(d, groups, t_ms, which, hbm, hbm_src, tpk, tpk_src, fmt="mxfp4"):
     """Roofline of one grouped GEMM launch sequence (W13 or W2) of a layer step.
     Algorithmic bytes: the active groups' weight bytes (codes + scales) plus the packed
     FP8 rows and scales read and the bf16 rows written; flops: 2 x rows x N x K.  The
@@ -363,8 +380,9 @@ def gemm_roofline(d, groups, t_ms, which, hbm, hbm_src, tpk, tpk_src):
         N, K = 2 * d.I, d.H
     else:
         N, K = d.H, d.I
-    wbytes = groups * N * K * WEIGHT_BYTES_PER_ELEM
-    abytes = Rs * (K + K / 128) + Rs * N * 2
+    wbytes = groups * N * K * WEIGHT_BYTES[fmt]
+    # packed activation rows read (FP8 codes + scales, or bf16 values) + bf16 rows out
+    abytes = Rs * ((K + K / 128) if fmt == "mxfp4" else 2 * K) + Rs * N * 2
     flops = 2.0 * Rs * N * K
     t = t_ms * 1e-3
     if flops / (wbytes + abytes) < (tpk * 1e12) / (hbm * 1e9):
@@ -379,19 +397,25 @@ def gemm_roofline(d, groups, t_ms, which, hbm, hbm_src, tpk, tpk_src):
 
 
 def measure_layer(args, workload, steps, warmup, rank, world, local, clocks, *, soak_s=0.0,
-                  e2e_steps=None, router=False, cpu=False):
+                  e2e_steps=None, router=False, cpu=False, fmt="mxfp4", tag=None):
     """One workload: the layer step captured as a CUDA graph, timed over `steps` replays
     (each followed by an event-instrumented forward for the stage times), inside a
-    clock-sampling window tagged with the workload's name.  Returns a dict."""
+    clock-sampling window tagged `tag` (the workload's name).  fmt: the expert weight
+    format (MXFP4, or NVFP4 drawn by gen.inputs.nvfp4_layer_weights).  Returns a dict."""
     import moe_expert_ffn_scan_gb300 as moe
+    tag = tag or workload
     dev = torch.device("cuda", local)
     d, t = make_layer_for(args, workload, args.seed + rank, dev)
     if t["logits"] is None:  # logits are the gate projection of x: the library's router
         t["logits"] = torch.empty(d.T, d.E, dtype=torch.float32, device=dev)
         moe.moe_router_logits(t["x"], t["wg"], t["logits"])
     md = moe.dims(d.T, d.H, d.I, d.E, d.k, d.has_shared)
+    if fmt == "nvfp4":
+        for n in ("w13", "w13_s", "w2", "w2_s"):
+            del t[n]
+        t.update(gi.nvfp4_layer_weights(d, seed=args.seed + rank, device=dev))
     layer = moe.MoELayer(d.H, d.I, d.E, d.k, d.has_shared, t["w13"], t["w13_s"], t["w2"],
-                         t["w2_s"])
+                         t["w2_s"], fmt=fmt, w13_gs=t.get("w13_gs"), w2_gs=t.get("w2_gs"))
     x, lg = t["x"], t["logits"]
     out = torch.empty(d.T, d.H, dtype=torch.bfloat16, device=dev)
     ws = layer.workspace(d.T)
@@ -400,13 +424,13 @@ def measure_layer(args, workload, steps, warmup, rank, world, local, clocks, *, 
 
     # routing statistics (for the algorithmic byte / flop counts)
     dbg = {"counts": torch.empty(d.E, dtype=torch.int32, device=dev)}
-    moe.moe_forward(md, x, lg, t["w13"], t["w13_s"], t["w2"], t["w2_s"], out, ws, debug=dbg)
+    layer.forward(x, lg, out=out, debug=dbg)
     bits = moe.moe_check_status(ws)
     if bits:
         raise RuntimeError(f"device status bits {bits:#x}")
     counts = dbg["counts"].cpu().numpy()
     groups = active_groups(counts, d.has_shared)
-    step_weight_bytes = groups * 3 * d.I * d.H * WEIGHT_BYTES_PER_ELEM
+    step_weight_bytes = groups * 3 * d.I * d.H * WEIGHT_BYTES[fmt]
     l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
     policy = "none" if args.no_flush else args.l2
     do_flush = policy == "flush" or (policy == "auto" and step_weight_bytes < 4 * l2_bytes)
@@ -435,7 +459,7 @@ def measure_layer(args, workload, steps, warmup, rank, world, local, clocks, *, 
     step_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                 for _ in range(steps)]
 
-    with clocks.load(workload):
+    with clocks.load(tag):
         if soak_s > 0:
             # back-to-back replays of the same graph right before the timed region, so
             # that the clock sampler sees the GPU under this load for a few seconds
@@ -454,8 +478,7 @@ def measure_layer(args, workload, steps, warmup, rank, world, local, clocks, *, 
             step_evs[i][1].record(stream)
             if do_flush:
                 flush.fill_((i + 128) & 0xFF)
-            moe.moe_forward_timed(md, x, lg, t["w13"], t["w13_s"], t["w2"], t["w2_s"], out, ws,
-                                  evs[i])
+            layer.forward_timed(x, lg, out, evs[i])
         torch.cuda.synchronize()
         barrier(world)
     bits = moe.moe_check_status(ws)
@@ -487,17 +510,21 @@ def measure_layer(args, workload, steps, warmup, rank, world, local, clocks, *, 
     stage_mean = {s_: statistics.mean(v) for s_, v in stage_ms.items()}
 
     hbm, hbm_src = hbm_peak_gbs()
-    tpk, tpk_src = fp8_tensor_peak_tflops()
-    roof13 = gemm_roofline(d, groups, stage_mean["gemm_w13"], "w13", hbm, hbm_src, tpk, tpk_src)
-    roof2 = gemm_roofline(d, groups, stage_mean["gemm_w2"], "w2", hbm, hbm_src, tpk, tpk_src)
-    roof13["kernel"] = "k_gemm_mx (W13 grouped GEMM)"
-    roof2["kernel"] = "k_gemm_mx (W2 grouped GEMM)"
-    if roof13["bound"] == "hbm" and d.T <= 16 and gemm_src_hash() == NCU_SMALL_W13_TRAFFIC["src"]:
+    tpk, tpk_src = fp8_tensor_peak_tflops() if fmt == "mxfp4" else bf16_tensor_peak_tflops()
+    roof13 = gemm_roofline(d, groups, stage_mean["gemm_w13"], "w13", hbm, hbm_src, tpk, tpk_src,
+                           fmt)
+    roof2 = gemm_roofline(d, groups, stage_mean["gemm_w2"], "w2", hbm, hbm_src, tpk, tpk_src,
+                          fmt)
+    kname = "k_gemm_mx" if fmt == "mxfp4" else "k_gemm_nv"
+    roof13["kernel"] = f"{kname} (W13 grouped GEMM)"
+    roof2["kernel"] = f"{kname} (W2 grouped GEMM)"
+    if fmt == "mxfp4" and roof13["bound"] == "hbm" and d.T <= 16 and \
+            gemm_src_hash() == NCU_SMALL_W13_TRAFFIC["src"]:
         roof13["traffic"] = groups * NCU_SMALL_W13_TRAFFIC["bytes_per_group"]
 
     # end to end through the public API, host buffers, copies inside the timed region
     e2e = None
-    if e2e_steps:
+    if e2e_steps and fmt == "mxfp4":
         e2e = measure_e2e(layer, d, x, lg, out, e2e_steps, do_flush, flush, world)
 
     router_rec = None
@@ -549,18 +576,18 @@ def measure_layer(args, workload, steps, warmup, rank, world, local, clocks, *, 
         "workload": workload, "d": d, "value": world * d.T / (ms_max * 1e-3),
         "ms_per_step": ms_max, "steps": steps, "warmup": warmup,
         "config": {"workload": workload, "T": d.T, "H": d.H, "I": d.I, "E": d.E, "k": d.k,
-                   "shared_experts": d.has_shared, "active_groups": groups,
+                   "shared_experts": d.has_shared, "weights": fmt, "active_groups": groups,
                    "routed_rows": d.R, "l2": l2_note, "parallelism": f"replicas x{world}"},
         "roofline": roof13, "roofline_w2": roof2, "stage_ms": stage_mean,
         "stream_ms_per_step": stream_step_ms, "ms_per_step_l2_write_flushed": flushed_ms,
         "ms_per_step_percentiles": pct,
-        "weight_gbs": groups * 3 * d.I * d.H * WEIGHT_BYTES_PER_ELEM /
+        "weight_gbs": groups * 3 * d.I * d.H * WEIGHT_BYTES[fmt] /
                       ((stage_mean["gemm_w13"] + stage_mean["gemm_w2"]) * 1e-3) / 1e9,
         "gemm_tflops": 2.0 * (d.R + (d.T if d.has_shared else 0)) * 3 * d.I * d.H /
                        ((stage_mean["gemm_w13"] + stage_mean["gemm_w2"]) * 1e-3) / 1e12,
         "router_gate": router_rec, "cpu_baseline": cpu_rec, "e2e": e2e,
         "gpu_launches": 2 * launches_per_step * steps,
-        "clocks": clocks.summary(workload),
+        "clocks": clocks.summary(tag),
     }
     del graph, layer, t, x, lg, out, ws, flush
     torch.cuda.synchronize()
@@ -645,7 +672,7 @@ def sub_record(rec):
 
 # Steps of the extra workloads the default run measures beside the headline line:
 # enough that each timed region lasts >= 2 s (>= 10 clock samples at 200 ms).
-EXTRA_STEPS = {"decode256": 600, "prefill": 60}
+EXTRA_STEPS = {"decode256": 600, "prefill": 60, "decode_nvfp4": 3000}
 EXTRA_E2E_STEPS = {"decode256": 50, "prefill": 20}
 
 
@@ -656,16 +683,20 @@ def run_ours(args, rank, world, local):
     with clocks:
         head = measure_layer(args, args.workload, args.steps, args.warmup, rank, world, local,
                              clocks, soak_s=2.5, e2e_steps=None if args.no_e2e else args.steps,
-                             router=True, cpu=not args.no_cpu_baseline)
+                             router=True, cpu=not args.no_cpu_baseline, fmt=args.weights)
         extras = {}
         sweep = None
-        if args.workload == "decode" and not args.no_extra and args.experts is None \
-                and args.tokens is None:
+        if args.workload == "decode" and args.weights == "mxfp4" and not args.no_extra \
+                and args.experts is None and args.tokens is None:
             for wl in ("decode256", "prefill"):
                 extras[wl] = sub_record(measure_layer(
                     args, wl, EXTRA_STEPS[wl], args.warmup, rank, world, local, clocks,
                     e2e_steps=None if args.no_e2e else EXTRA_E2E_STEPS[wl],
                     router=(wl == "prefill")))
+            # the decode layer again with NVFP4 expert weights (f3)
+            extras["decode_nvfp4"] = sub_record(measure_layer(
+                args, "decode", EXTRA_STEPS["decode_nvfp4"], args.warmup, rank, world, local,
+                clocks, fmt="nvfp4", tag="decode_nvfp4"))
             with clocks.load("sweep"):
                 pts = sweep_points(args, local, steps=5, warmup=3)
             sweep = {"points": [{"gemm": p_["gemm"], "M": p_["M"], "ms": p_["ms"],
@@ -682,7 +713,8 @@ def run_ours(args, rank, world, local):
             "metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "mxfp4xfp8->f32", "data": "synthetic",
+            "dtype": "mxfp4xfp8->f32" if args.weights == "mxfp4" else "nvfp4xfp8(bf16 mma)->f32",
+            "data": "synthetic",
             "config": head["config"],
             "roofline": head["roofline"],
             "roofline_w2": head["roofline_w2"],

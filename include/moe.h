@@ -222,6 +222,59 @@ int moe_forward_host(const moe_dims* d, const uint16_t* x_host, const float* log
                      const moe_weights* W, uint16_t* out_host, void* ws, size_t ws_bytes,
                      void* stream);
 
+/* ---------------------------------------------------------------------------------
+ * f3: NVFP4 expert weights (GB10 "Optimization progress report", Optimization 05,
+ * native NVFP4 MoE: the expert weights stay NVFP4 in memory and the expert GEMMs read
+ * them as such).  The page names the format without defining it; read as NVIDIA's
+ * NVFP4: E2M1 codes packed as for MXFP4 ([G][N][K/2], even K index in the low
+ * nibble), one FP8 E4M3 scale byte per 16 consecutive K elements ([G][N][K/16]), and
+ * one fp32 scale per weight tensor.  Activations stay online FP8 (same codes and
+ * scales as the MXFP4 path); the GEMMs multiply in bf16, where a weight (E2M1 x E4M3,
+ * at most 6 significant bits) and an activation (E4M3 code x 2^e) are both exact
+ * (activations below bf16's subnormal floor excepted: a 128-block with amax under
+ * about 2^-116), and accumulate in fp32; the tensor scale multiplies the fp32 sum
+ * before the bf16 rounding.  Requires H % 256 == 0 and I % 256 == 0 in addition to
+ * the shapes above (else MOE_ERR_UNSUPPORTED_SHAPE). */
+typedef struct moe_weights_nvfp4 {
+  const uint8_t* w13;    /* [G][2I][H/2]  E2M1 codes (rows 0..I-1 gate, I..2I-1 up)   */
+  const uint8_t* w13_s;  /* [G][2I][H/16] E4M3 block scales                          */
+  const float* w13_gs;   /* [G][2] fp32 tensor scales (gate rows, up rows); NULL = 1 */
+  const uint8_t* w2;     /* [G][H][I/2]                                              */
+  const uint8_t* w2_s;   /* [G][H][I/16]                                             */
+  const float* w2_gs;    /* [G] fp32 tensor scales; NULL = 1                         */
+} moe_weights_nvfp4;
+
+/* Workspace bytes of moe_forward_nvfp4 and of the two NVFP4 grouped GEMMs. */
+size_t moe_workspace_size_nvfp4(const moe_dims* d);
+size_t moe_gemm_workspace_size_nvfp4(const moe_dims* d);
+
+/* moe_forward with NVFP4 expert weights: the same stages and results' definition, the
+ * W13 / W2 GEMMs reading NVFP4 weights (y = bf16(gs * sum_k deq(a) * e2m1 * e4m3)).
+ * The quantisation stages also write the bf16 values of their FP8 codes, the NVFP4
+ * GEMMs' operand form.  dbg as for moe_forward.  ws: moe_workspace_size_nvfp4(d). */
+int moe_forward_nvfp4(const moe_dims* d, const uint16_t* x, const float* logits,
+                      const moe_weights_nvfp4* W, uint16_t* out, const moe_debug_out* dbg,
+                      void* ws, size_t ws_bytes, void* stream);
+
+/* moe_forward_nvfp4 with the stage events of moe_forward_timed. */
+int moe_forward_nvfp4_timed(const moe_dims* d, const uint16_t* x, const float* logits,
+                            const moe_weights_nvfp4* W, uint16_t* out, const moe_debug_out* dbg,
+                            void* const* events, void* ws, size_t ws_bytes, void* stream);
+
+/* a4 / a6 with NVFP4 weights: as moe_grouped_gemm_w13 / moe_grouped_gemm_w2 (same
+ * operands, FP8 codes + per-128 scales, same row mapping), weights w [G][N][K/2] codes,
+ * w_s [G][N][K/16] E4M3 scales, w_gs the fp32 tensor scales ([G][2] for W13, [G] for
+ * W2; NULL = 1, 4-byte aligned).  The FP8 operand is first expanded to bf16 rows in
+ * the workspace.  ws: moe_gemm_workspace_size_nvfp4(d). */
+int moe_grouped_gemm_w13_nvfp4(const moe_dims* d, const uint8_t* xq, const uint8_t* xs,
+                               const int32_t* perm_src, const int32_t* group_offsets,
+                               const uint8_t* w13, const uint8_t* w13_s, const float* w13_gs,
+                               uint16_t* y13, void* ws, size_t ws_bytes, void* stream);
+int moe_grouped_gemm_w2_nvfp4(const moe_dims* d, const uint8_t* hq, const uint8_t* hs,
+                              const int32_t* group_offsets, const uint8_t* w2,
+                              const uint8_t* w2_s, const float* w2_gs, uint16_t* y2, void* ws,
+                              size_t ws_bytes, void* stream);
+
 /* Host-buffer pipeline: a sequence of layer steps whose inputs and outputs live in
  * host memory, with the copies of one step overlapping the kernels of its neighbours.
  * The library owns three CUDA streams (host->device copies, the layer, device->host

@@ -40,6 +40,10 @@ class moe_weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("w13", "w13_s", "w2", "w2_s")]
 
 
+class moe_weights_nvfp4(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("w13", "w13_s", "w13_gs", "w2", "w2_s", "w2_gs")]
+
+
 DEBUG_FIELDS = ("idx", "w", "counts", "offsets", "perm_src", "inv", "xq", "xs", "y13", "hq",
                 "hs", "y2")
 
@@ -66,7 +70,8 @@ def lib():
         L.moe_error_string.argtypes = [ctypes.c_int]
         L.moe_error_string.restype = ctypes.c_char_p
         for fn in ("moe_workspace_size", "moe_route_workspace_size", "moe_gemm_workspace_size",
-                   "moe_host_workspace_size"):
+                   "moe_host_workspace_size", "moe_workspace_size_nvfp4",
+                   "moe_gemm_workspace_size_nvfp4"):
             getattr(L, fn).argtypes = [_DP]
             getattr(L, fn).restype = _SZ
         L.moe_route.argtypes = [_DP, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]
@@ -83,6 +88,17 @@ def lib():
         L.moe_forward_timed.argtypes = [_DP, _P, _P, ctypes.POINTER(moe_weights), _P,
                                         ctypes.POINTER(moe_debug_out), ctypes.POINTER(_P), _P,
                                         _SZ, _P]
+        _WN = ctypes.POINTER(moe_weights_nvfp4)
+        L.moe_forward_nvfp4.argtypes = [_DP, _P, _P, _WN, _P, ctypes.POINTER(moe_debug_out), _P,
+                                        _SZ, _P]
+        L.moe_forward_nvfp4_timed.argtypes = [_DP, _P, _P, _WN, _P,
+                                              ctypes.POINTER(moe_debug_out), ctypes.POINTER(_P),
+                                              _P, _SZ, _P]
+        L.moe_grouped_gemm_w13_nvfp4.argtypes = [_DP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
+                                                 _P]
+        L.moe_grouped_gemm_w2_nvfp4.argtypes = [_DP, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]
+        L.moe_route_static.argtypes = [_DP, _P, _P, _P, _P, _P, _P, _P, _P]
+        L.moe_route_static_status.argtypes = [_P, ctypes.POINTER(ctypes.c_uint32)]
         L.moe_check_status.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_uint32)]
         L.moe_selftest_wait_timeout.argtypes = [_P, _P]
         L.moe_host_pipeline_workspace_size.argtypes = [_DP, _I]
@@ -97,7 +113,9 @@ def lib():
             getattr(L, fn).restype = ctypes.c_int
         for fn in ("moe_route", "moe_quant_act", "moe_grouped_gemm_w13", "moe_swiglu_quant",
                    "moe_grouped_gemm_w2", "moe_combine", "moe_forward", "moe_forward_timed",
-                   "moe_check_status"):
+                   "moe_check_status", "moe_forward_nvfp4", "moe_forward_nvfp4_timed",
+                   "moe_grouped_gemm_w13_nvfp4", "moe_grouped_gemm_w2_nvfp4",
+                   "moe_route_static", "moe_route_static_status"):
             getattr(L, fn).restype = ctypes.c_int
         _LIB = L
     return _LIB
@@ -145,6 +163,14 @@ def host_workspace_size(d) -> int:
 
 def host_pipeline_workspace_size(d, depth) -> int:
     return lib().moe_host_pipeline_workspace_size(_d(d), depth)
+
+
+def workspace_size_nvfp4(d) -> int:
+    return lib().moe_workspace_size_nvfp4(_d(d))
+
+
+def gemm_workspace_size_nvfp4(d) -> int:
+    return lib().moe_gemm_workspace_size_nvfp4(_d(d))
 
 
 def route_workspace_size(d) -> int:
@@ -211,6 +237,63 @@ def moe_forward(d, x, logits, w13, w13_s, w2, w2_s, out, ws, debug=None, stream=
     _check("moe_forward", lib().moe_forward(
         _d(d), _p(x), _p(logits), ctypes.byref(W), _p(out),
         ctypes.byref(dbg) if dbg is not None else None, _p(ws), ws.numel(), _stream(stream)))
+
+
+def _nv_weights(w13, w13_s, w13_gs, w2, w2_s, w2_gs):
+    return moe_weights_nvfp4(_p(w13), _p(w13_s), _p(w13_gs), _p(w2), _p(w2_s), _p(w2_gs))
+
+
+def moe_forward_nvfp4(d, x, logits, w13, w13_s, w13_gs, w2, w2_s, w2_gs, out, ws, debug=None,
+                      stream=None):
+    """moe_forward with NVFP4 expert weights (codes, E4M3 scales per 16, fp32 tensor
+    scales [G, 2] / [G] or None); ws: workspace_size_nvfp4(d) bytes."""
+    W = _nv_weights(w13, w13_s, w13_gs, w2, w2_s, w2_gs)
+    dbg = None
+    if debug:
+        dbg = moe_debug_out(*[_p(debug.get(n)) for n in DEBUG_FIELDS])
+    _check("moe_forward_nvfp4", lib().moe_forward_nvfp4(
+        _d(d), _p(x), _p(logits), ctypes.byref(W), _p(out),
+        ctypes.byref(dbg) if dbg is not None else None, _p(ws), ws.numel(), _stream(stream)))
+
+
+def moe_forward_nvfp4_timed(d, x, logits, w13, w13_s, w13_gs, w2, w2_s, w2_gs, out, ws, events,
+                            stream=None):
+    W = _nv_weights(w13, w13_s, w13_gs, w2, w2_s, w2_gs)
+    ev = (_P * 8)(*[e.cuda_event for e in events])
+    _check("moe_forward_nvfp4_timed", lib().moe_forward_nvfp4_timed(
+        _d(d), _p(x), _p(logits), ctypes.byref(W), _p(out), None, ev, _p(ws), ws.numel(),
+        _stream(stream)))
+
+
+def moe_grouped_gemm_w13_nvfp4(d, xq, xs, perm_src, group_offsets, w13, w13_s, w13_gs, y13, ws,
+                               stream=None):
+    _check("moe_grouped_gemm_w13_nvfp4", lib().moe_grouped_gemm_w13_nvfp4(
+        _d(d), _p(xq), _p(xs), _p(perm_src), _p(group_offsets), _p(w13), _p(w13_s), _p(w13_gs),
+        _p(y13), _p(ws), ws.numel(), _stream(stream)))
+
+
+def moe_grouped_gemm_w2_nvfp4(d, hq, hs, group_offsets, w2, w2_s, w2_gs, y2, ws, stream=None):
+    _check("moe_grouped_gemm_w2_nvfp4", lib().moe_grouped_gemm_w2_nvfp4(
+        _d(d), _p(hq), _p(hs), _p(group_offsets), _p(w2), _p(w2_s), _p(w2_gs), _p(y2), _p(ws),
+        ws.numel(), _stream(stream)))
+
+
+def moe_route_static(d, logits, idx, w, counts, offsets, perm_src, inv, stream=None):
+    """moe_route without a workspace: its scratch is a fixed array inside the library
+    (calls must not overlap on the GPU)."""
+    _check("moe_route_static", lib().moe_route_static(
+        _d(d), _p(logits), _p(idx), _p(w), _p(counts), _p(offsets), _p(perm_src), _p(inv),
+        _stream(stream)))
+
+
+def moe_route_static_status(stream=None) -> int:
+    """Synchronises the stream and returns the device status bits of moe_route_static's
+    fixed array (those of its last call)."""
+    bits = ctypes.c_uint32(0)
+    rc = lib().moe_route_static_status(_stream(stream), ctypes.byref(bits))
+    if rc not in (MOE_OK, 5):
+        raise MoeError("moe_route_static_status", rc)
+    return bits.value
 
 
 def _host_p(t):
@@ -358,9 +441,13 @@ class MoELayer:
     `forward(x, logits)` runs moe_forward on the current stream and returns the
     bf16 output [T, H]."""
 
-    def __init__(self, H, I, E, k, has_shared, w13, w13_s, w2, w2_s):
+    def __init__(self, H, I, E, k, has_shared, w13, w13_s, w2, w2_s, fmt="mxfp4", w13_gs=None,
+                 w2_gs=None):
+        if fmt not in ("mxfp4", "nvfp4"):
+            raise ValueError(f"unknown weight format {fmt!r}")
         self.H, self.I, self.E, self.k, self.has_shared = H, I, E, k, has_shared
         self.w13, self.w13_s, self.w2, self.w2_s = w13, w13_s, w2, w2_s
+        self.fmt, self.w13_gs, self.w2_gs = fmt, w13_gs, w2_gs
         self._ws = None
         self._T = -1
 
@@ -369,11 +456,19 @@ class MoELayer:
 
     def workspace(self, T):
         if self._ws is None or self._T < T:
-            self._ws = alloc_workspace(workspace_size(self.dims(T)), self.w13.device)
+            size = (workspace_size if self.fmt == "mxfp4" else workspace_size_nvfp4)(self.dims(T))
+            if size == 0:
+                raise ValueError(f"unsupported dims for {self.fmt} weights")
+            self._ws = alloc_workspace(size, self.w13.device)
             self._T = T
         return self._ws
 
+    def _mxfp4_only(self, what):
+        if self.fmt != "mxfp4":
+            raise NotImplementedError(f"{what} takes MXFP4 weights")
+
     def host_workspace(self, T):
+        self._mxfp4_only("the host-buffer forward")
         if getattr(self, "_hws", None) is None or self._hT < T:
             self._hws = alloc_workspace(host_workspace_size(self.dims(T)), self.w13.device)
             self._hT = T
@@ -381,6 +476,7 @@ class MoELayer:
 
     def host_pipeline(self, T, depth=2):
         """A HostPipeline for T-token steps (its own workspace and streams)."""
+        self._mxfp4_only("the host-buffer pipeline")
         return HostPipeline(self, T, depth)
 
     def forward_host(self, x_host, logits_host, out_host, stream=None):
@@ -400,6 +496,23 @@ class MoELayer:
         T = x.shape[0]
         if out is None:
             out = torch.empty(T, self.H, dtype=torch.bfloat16, device=x.device)
-        moe_forward(self.dims(T), x, logits, self.w13, self.w13_s, self.w2, self.w2_s, out,
-                    self.workspace(T), debug=debug, stream=stream)
+        if self.fmt == "mxfp4":
+            moe_forward(self.dims(T), x, logits, self.w13, self.w13_s, self.w2, self.w2_s, out,
+                        self.workspace(T), debug=debug, stream=stream)
+        else:
+            moe_forward_nvfp4(self.dims(T), x, logits, self.w13, self.w13_s, self.w13_gs,
+                              self.w2, self.w2_s, self.w2_gs, out, self.workspace(T),
+                              debug=debug, stream=stream)
+        return out
+
+    def forward_timed(self, x, logits, out, events, stream=None):
+        """forward recording the 8 stage events of moe_forward_timed (see STAGES)."""
+        T = x.shape[0]
+        if self.fmt == "mxfp4":
+            moe_forward_timed(self.dims(T), x, logits, self.w13, self.w13_s, self.w2, self.w2_s,
+                              out, self.workspace(T), events, stream=stream)
+        else:
+            moe_forward_nvfp4_timed(self.dims(T), x, logits, self.w13, self.w13_s, self.w13_gs,
+                                    self.w2, self.w2_s, self.w2_gs, out, self.workspace(T),
+                                    events, stream=stream)
         return out

@@ -14,7 +14,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe.so")
-SOURCES = ("route.cu", "elementwise.cu", "gemm.cu", "capi.cu", "route_static.cu", "router.cu")
+SOURCES = ("route.cu", "elementwise.cu", "gemm.cu", "gemm_nv.cu", "capi.cu", "route_static.cu",
+           "router.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I" + os.path.join(ROOT, "include")]

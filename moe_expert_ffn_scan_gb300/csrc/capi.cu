@@ -112,20 +112,35 @@ PlanWs carve_plan(Carver& c, const moe_dims* d) {
   return p;
 }
 
+// Expert weight formats (moe.h): the MXFP4 path moves FP8 codes into the GEMMs, the
+// NVFP4 path bf16 rows holding the codes' exact values.
+enum WeightFormat { kMxfp4 = 0, kNvfp4 = 1 };
+
+struct LayerWeights {
+  WeightFormat fmt;
+  const uint8_t *w13, *w13_s, *w2, *w2_s;
+  const float *w13_gs, *w2_gs;  // NVFP4 tensor scales (null: 1.0)
+};
+
 struct GemmWs {
   uint32_t* status;
   PlanWs plan;
-  uint8_t* xg;   // packed FP8 rows for W13 [Rs][H]
+  uint8_t* xg;   // MXFP4: packed FP8 rows for W13 [Rs][H]
   uint8_t* xsg;  // their scales [Rs][H/128]
+  uint16_t* xe;  // NVFP4: packed bf16 rows for W13 (or W2's operand) [Rs][max(H, I)]
 };
 
-GemmWs carve_gemm(Carver& c, const moe_dims* d) {
-  GemmWs g;
+GemmWs carve_gemm(Carver& c, const moe_dims* d, WeightFormat fmt) {
+  GemmWs g{};
   g.status = c.take<uint32_t>(64);
   g.plan = carve_plan(c, d);
   const size_t Rs = static_cast<size_t>(rows_Rs(d));
-  g.xg = c.take<uint8_t>(Rs * d->H);
-  g.xsg = c.take<uint8_t>(Rs * (d->H / 128));
+  if (fmt == kMxfp4) {
+    g.xg = c.take<uint8_t>(Rs * d->H);
+    g.xsg = c.take<uint8_t>(Rs * (d->H / 128));
+  } else {
+    g.xe = c.take<uint16_t>(Rs * static_cast<size_t>(d->H > d->I ? d->H : d->I));
+  }
   return g;
 }
 
@@ -136,12 +151,13 @@ struct ForwardWs {
   float* w;
   uint8_t *xq, *xs, *hq, *hs;
   uint16_t *y13, *y2;
+  uint16_t* he;  // NVFP4: W2's operand as bf16 rows [Rs][I]
 };
 
-ForwardWs carve_forward(Carver& c, const moe_dims* d) {
-  ForwardWs f;
+ForwardWs carve_forward(Carver& c, const moe_dims* d, WeightFormat fmt = kMxfp4) {
+  ForwardWs f{};
   f.route = carve_route(c, d);  // status word first
-  f.gemm = carve_gemm(c, d);
+  f.gemm = carve_gemm(c, d, fmt);
   f.gemm.status = f.route.status;
   const size_t T = d->T, R = rows_R(d), Rs = rows_Rs(d), H = d->H, I = d->I;
   f.idx = c.take<int32_t>(R);
@@ -153,11 +169,19 @@ ForwardWs carve_forward(Carver& c, const moe_dims* d) {
   f.xq = c.take<uint8_t>(T * H);
   f.xs = c.take<uint8_t>(T * (H / 128));
   f.y13 = c.take<uint16_t>(Rs * 2 * I);
-  f.hq = c.take<uint8_t>(Rs * I);
-  f.hs = c.take<uint8_t>(Rs * (I / 128));
+  if (fmt == kMxfp4) {
+    f.hq = c.take<uint8_t>(Rs * I);
+    f.hs = c.take<uint8_t>(Rs * (I / 128));
+  } else {
+    f.he = c.take<uint16_t>(Rs * I);
+  }
   f.y2 = c.take<uint16_t>(Rs * H);
   return f;
 }
+
+// The NVFP4 GEMMs need K % 256 == 0 (their scale rows are TMA rows of K/16 bytes,
+// which must be whole 16-byte units).
+bool nv_dims_ok(const moe_dims* d) { return dims_ok(d) && d->H % 256 == 0 && d->I % 256 == 0; }
 
 // Device staging of the host-buffer forward, after the forward workspace.
 struct HostStagingWs {
@@ -199,6 +223,30 @@ int run_gemm(const moe_dims* d, const uint8_t* act, const uint8_t* act_s, const 
   a.status = status;
   a.early_plan = early_plan;
   return cuda_rc(launch_grouped_gemm(a, st));
+}
+
+int run_gemm_nv(const moe_dims* d, const uint16_t* act, const uint8_t* w, const uint8_t* w_s,
+                const float* gs, int gs_segments, int N, int K, uint16_t* y, const PlanWs& plan,
+                int max_group_rows, uint32_t* status, cudaStream_t st) {
+  NvGemmLaunch a{};
+  a.w_codes = w;
+  a.w_scales = w_s;
+  a.gs = gs;
+  a.gs_segments = gs_segments;
+  a.act = act;
+  a.y = y;
+  a.G = groups_G(d);
+  a.N = N;
+  a.K = K;
+  a.rows_total = static_cast<int>(rows_Rs(d));
+  for (int v = 0; v < kNumVariants; ++v) {
+    a.items[v] = plan.out.items[v];
+    a.max_items[v] = plan.max_items[v];
+  }
+  a.item_counts = plan.out.counts;
+  a.max_group_rows = max_group_rows;
+  a.status = status;
+  return cuda_rc(launch_grouped_gemm_nv(a, st));
 }
 
 // One CTA, one waiting thread: an mbarrier that nothing arrives at.  The bounded wait
@@ -250,7 +298,7 @@ size_t moe_route_workspace_size(const moe_dims* d) {
 size_t moe_gemm_workspace_size(const moe_dims* d) {
   if (!dims_ok(d)) return 0;
   Carver c(nullptr);
-  carve_gemm(c, d);
+  carve_gemm(c, d, kMxfp4);
   return c.used;
 }
 
@@ -310,7 +358,7 @@ int moe_grouped_gemm_w13(const moe_dims* d, const uint8_t* xq, const uint8_t* xs
   if (ws_bytes < moe_gemm_workspace_size(d)) return MOE_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   Carver c(ws);
-  GemmWs g = carve_gemm(c, d);
+  GemmWs g = carve_gemm(c, d, kMxfp4);
   if (cudaMemsetAsync(g.status, 0, sizeof(uint32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
   cudaError_t e = launch_plan(group_offsets, groups_G(d), g.plan.out, g.status, st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
@@ -346,7 +394,7 @@ int moe_grouped_gemm_w2(const moe_dims* d, const uint8_t* hq, const uint8_t* hs,
   if (ws_bytes < moe_gemm_workspace_size(d)) return MOE_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   Carver c(ws);
-  GemmWs g = carve_gemm(c, d);
+  GemmWs g = carve_gemm(c, d, kMxfp4);
   if (cudaMemsetAsync(g.status, 0, sizeof(uint32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
   cudaError_t e = launch_plan(group_offsets, groups_G(d), g.plan.out, g.status, st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
@@ -527,31 +575,40 @@ int moe_host_pipeline_destroy(moe_host_pipeline* p) {
   return rc;
 }
 
-int moe_forward_timed(const moe_dims* d, const uint16_t* x, const float* logits,
-                      const moe_weights* W, uint16_t* out, const moe_debug_out* dbg,
-                      void* const* events, void* ws, size_t ws_bytes, void* stream) {
-  if (!dims_ok(d)) return MOE_ERR_UNSUPPORTED_SHAPE;
-  if (!x || !logits || !W || !out || !ws) return MOE_ERR_INVALID_ARG;
-  if (!weights_ok(W->w13, W->w13_s) || !weights_ok(W->w2, W->w2_s)) return MOE_ERR_INVALID_ARG;
+}  // extern "C"
+
+namespace {
+
+// The layer a1..a7 on one stream for either weight format (see moe_forward_timed).
+int forward_impl(const moe_dims* d, const uint16_t* x, const float* logits,
+                 const LayerWeights& W, uint16_t* out, const moe_debug_out* dbg,
+                 void* const* events, void* ws, size_t ws_bytes, cudaStream_t st) {
+  if (!(W.fmt == kMxfp4 ? dims_ok(d) : nv_dims_ok(d))) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!x || !logits || !out || !ws) return MOE_ERR_INVALID_ARG;
+  if (!weights_ok(W.w13, W.w13_s) || !weights_ok(W.w2, W.w2_s)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(W.w13_gs, 4) || !aligned(W.w2_gs, 4)) return MOE_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(out, 16) || !aligned(ws, kAlign) || !aligned(logits, 4))
     return MOE_ERR_INVALID_ARG;
-  if (ws_bytes < moe_workspace_size(d)) return MOE_ERR_WORKSPACE_TOO_SMALL;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   Carver c(ws);
-  ForwardWs f = carve_forward(c, d);
+  ForwardWs f = carve_forward(c, d, W.fmt);
+  if (ws_bytes < c.used) return MOE_ERR_WORKSPACE_TOO_SMALL;
   // caller-visible intermediates replace the workspace buffers
+  uint8_t* dbg_hq = nullptr;
+  uint8_t* dbg_hs = nullptr;
   if (dbg) {
 #define MOE_DBG(field) \
   if (dbg->field) f.field = dbg->field;
     MOE_DBG(idx) MOE_DBG(w) MOE_DBG(counts) MOE_DBG(offsets) MOE_DBG(perm_src) MOE_DBG(inv)
     MOE_DBG(xq) MOE_DBG(xs) MOE_DBG(y13) MOE_DBG(hq) MOE_DBG(hs) MOE_DBG(y2)
 #undef MOE_DBG
+    dbg_hq = dbg->hq;
+    dbg_hs = dbg->hs;
     if (!aligned(f.xq, 16) || !aligned(f.y13, 16) || !aligned(f.hq, 16) || !aligned(f.y2, 16) ||
         !aligned(f.hs, 4) || !aligned(f.xs, 4))
       return MOE_ERR_INVALID_ARG;
   }
   const int T = d->T, H = d->H, I = d->I, E = d->E, k = d->k;
-  const int R = static_cast<int>(rows_R(d)), Rs = static_cast<int>(rows_Rs(d));
+  const int Rs = static_cast<int>(rows_Rs(d));
   uint32_t* status = f.route.status;  // cleared by the first kernel below
   auto mark = [&](int i) -> bool {
     return !events || cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st) == cudaSuccess;
@@ -576,22 +633,43 @@ int moe_forward_timed(const moe_dims* d, const uint16_t* x, const float* logits,
     MOE_TRY(launch_plan(f.offsets, groups_G(d), f.gemm.plan.out, status, st))
   }
   MOE_MARK(1)
-  // quantise each token once, writing its codes straight into its packed rows
-  MOE_TRY(launch_quant_scatter(x, T, H, k, d->has_shared, f.inv, dbg && dbg->xq ? f.xq : nullptr,
-                               dbg && dbg->xs ? f.xs : nullptr, f.gemm.xg, f.gemm.xsg, status,
-                               st))
+  // quantise each token once, writing its codes (MXFP4 path) or their exact bf16
+  // values (NVFP4 path) straight into its packed rows
+  uint8_t* xq_out = dbg && dbg->xq ? f.xq : nullptr;
+  uint8_t* xs_out = dbg && dbg->xs ? f.xs : nullptr;
+  if (W.fmt == kMxfp4) {
+    MOE_TRY(launch_quant_scatter(x, T, H, k, d->has_shared, f.inv, xq_out, xs_out, f.gemm.xg,
+                                 f.gemm.xsg, status, st))
+  } else {
+    MOE_TRY(launch_quant_scatter_bf16(x, T, H, k, d->has_shared, f.inv, xq_out, xs_out,
+                                      f.gemm.xe, status, st))
+  }
   MOE_MARK(2)
   MOE_MARK(3)  // (stage 3, the plan, now runs inside stage 1)
   // every group (a routed expert or the shared expert) holds at most T rows; W13
   // follows the quant-scatter, and the plan was written before it
-  int rc = run_gemm(d, f.gemm.xg, f.gemm.xsg, f.offsets, W->w13, W->w13_s, 2 * I, H, f.y13,
-                    f.gemm.plan, T, status, st, /*early_plan=*/1);
+  int rc;
+  if (W.fmt == kMxfp4) {
+    rc = run_gemm(d, f.gemm.xg, f.gemm.xsg, f.offsets, W.w13, W.w13_s, 2 * I, H, f.y13,
+                  f.gemm.plan, T, status, st, /*early_plan=*/1);
+  } else {
+    rc = run_gemm_nv(d, f.gemm.xe, W.w13, W.w13_s, W.w13_gs, 2, 2 * I, H, f.y13, f.gemm.plan, T,
+                     status, st);
+  }
   if (rc != MOE_OK) return rc;
   MOE_MARK(4)
-  MOE_TRY(launch_swiglu_quant(f.y13, Rs, I, f.hq, f.hs, st))
+  if (W.fmt == kMxfp4) {
+    MOE_TRY(launch_swiglu_quant(f.y13, Rs, I, f.hq, f.hs, st))
+  } else {
+    MOE_TRY(launch_swiglu_quant_bf16(f.y13, Rs, I, dbg_hq, dbg_hs, f.he, st))
+  }
   MOE_MARK(5)
-  rc = run_gemm(d, f.hq, f.hs, f.offsets, W->w2, W->w2_s, H, I, f.y2, f.gemm.plan, T, status,
-                st, /*early_plan=*/1);  // follows SwiGLU; the plan preceded W13
+  if (W.fmt == kMxfp4) {
+    rc = run_gemm(d, f.hq, f.hs, f.offsets, W.w2, W.w2_s, H, I, f.y2, f.gemm.plan, T, status,
+                  st, /*early_plan=*/1);  // follows SwiGLU; the plan preceded W13
+  } else {
+    rc = run_gemm_nv(d, f.he, W.w2, W.w2_s, W.w2_gs, 1, H, I, f.y2, f.gemm.plan, T, status, st);
+  }
   if (rc != MOE_OK) return rc;
   MOE_MARK(6)
   MOE_TRY(launch_combine(f.y2, f.inv, f.w, T, k, H, d->has_shared, out, status, st))
@@ -599,6 +677,98 @@ int moe_forward_timed(const moe_dims* d, const uint16_t* x, const float* logits,
 #undef MOE_TRY
 #undef MOE_MARK
   return MOE_OK;
+}
+
+LayerWeights mx_weights(const moe_weights* W) {
+  return LayerWeights{kMxfp4, W->w13, W->w13_s, W->w2, W->w2_s, nullptr, nullptr};
+}
+
+LayerWeights nv_weights(const moe_weights_nvfp4* W) {
+  return LayerWeights{kNvfp4, W->w13, W->w13_s, W->w2, W->w2_s, W->w13_gs, W->w2_gs};
+}
+
+// Stand-alone NVFP4 GEMM: plan, FP8 operand expanded to bf16 rows, GEMM.
+int gemm_nv_call(const moe_dims* d, const uint8_t* q, const uint8_t* qs, const int32_t* perm_src,
+                 const int32_t* group_offsets, const uint8_t* w, const uint8_t* w_s,
+                 const float* gs, int gs_segments, int N, int K, uint16_t* y, void* ws,
+                 size_t ws_bytes, cudaStream_t st) {
+  Carver c(ws);
+  GemmWs g = carve_gemm(c, d, kNvfp4);
+  if (ws_bytes < c.used) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (cudaMemsetAsync(g.status, 0, sizeof(uint32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_plan(group_offsets, groups_G(d), g.plan.out, g.status, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  const int Rs = static_cast<int>(rows_Rs(d));
+  if (launch_expand_rows(q, qs, perm_src, d->T, d->k, static_cast<int>(rows_R(d)), Rs, K, g.xe,
+                         g.status, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return run_gemm_nv(d, g.xe, w, w_s, gs, gs_segments, N, K, y, g.plan, Rs, g.status, st);
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_forward_timed(const moe_dims* d, const uint16_t* x, const float* logits,
+                      const moe_weights* W, uint16_t* out, const moe_debug_out* dbg,
+                      void* const* events, void* ws, size_t ws_bytes, void* stream) {
+  if (!W) return dims_ok(d) ? MOE_ERR_INVALID_ARG : MOE_ERR_UNSUPPORTED_SHAPE;
+  return forward_impl(d, x, logits, mx_weights(W), out, dbg, events, ws, ws_bytes,
+                      static_cast<cudaStream_t>(stream));
+}
+
+size_t moe_workspace_size_nvfp4(const moe_dims* d) {
+  if (!nv_dims_ok(d)) return 0;
+  Carver c(nullptr);
+  carve_forward(c, d, kNvfp4);
+  return c.used;
+}
+
+size_t moe_gemm_workspace_size_nvfp4(const moe_dims* d) {
+  if (!nv_dims_ok(d)) return 0;
+  Carver c(nullptr);
+  carve_gemm(c, d, kNvfp4);
+  return c.used;
+}
+
+int moe_forward_nvfp4(const moe_dims* d, const uint16_t* x, const float* logits,
+                      const moe_weights_nvfp4* W, uint16_t* out, const moe_debug_out* dbg,
+                      void* ws, size_t ws_bytes, void* stream) {
+  return moe_forward_nvfp4_timed(d, x, logits, W, out, dbg, nullptr, ws, ws_bytes, stream);
+}
+
+int moe_forward_nvfp4_timed(const moe_dims* d, const uint16_t* x, const float* logits,
+                            const moe_weights_nvfp4* W, uint16_t* out, const moe_debug_out* dbg,
+                            void* const* events, void* ws, size_t ws_bytes, void* stream) {
+  if (!W) return nv_dims_ok(d) ? MOE_ERR_INVALID_ARG : MOE_ERR_UNSUPPORTED_SHAPE;
+  return forward_impl(d, x, logits, nv_weights(W), out, dbg, events, ws, ws_bytes,
+                      static_cast<cudaStream_t>(stream));
+}
+
+int moe_grouped_gemm_w13_nvfp4(const moe_dims* d, const uint8_t* xq, const uint8_t* xs,
+                               const int32_t* perm_src, const int32_t* group_offsets,
+                               const uint8_t* w13, const uint8_t* w13_s, const float* w13_gs,
+                               uint16_t* y13, void* ws, size_t ws_bytes, void* stream) {
+  if (!nv_dims_ok(d)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!xq || !xs || !group_offsets || !y13 || !ws || !weights_ok(w13, w13_s))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned(xq, 16) || !aligned(ws, kAlign) || !aligned(y13, 16) || !aligned(w13_gs, 4))
+    return MOE_ERR_INVALID_ARG;
+  return gemm_nv_call(d, xq, xs, perm_src, group_offsets, w13, w13_s, w13_gs, 2, 2 * d->I, d->H,
+                      y13, ws, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+int moe_grouped_gemm_w2_nvfp4(const moe_dims* d, const uint8_t* hq, const uint8_t* hs,
+                              const int32_t* group_offsets, const uint8_t* w2,
+                              const uint8_t* w2_s, const float* w2_gs, uint16_t* y2, void* ws,
+                              size_t ws_bytes, void* stream) {
+  if (!nv_dims_ok(d)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!hq || !hs || !group_offsets || !y2 || !ws || !weights_ok(w2, w2_s))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned(hq, 16) || !aligned(ws, kAlign) || !aligned(y2, 16) || !aligned(w2_gs, 4))
+    return MOE_ERR_INVALID_ARG;
+  return gemm_nv_call(d, hq, hs, nullptr, group_offsets, w2, w2_s, w2_gs, 1, d->H, d->I, y2, ws,
+                      ws_bytes, static_cast<cudaStream_t>(stream));
 }
 
 int moe_selftest_wait_timeout(void* ws, void* stream) {

@@ -71,6 +71,35 @@ struct BlockLane {
   }
 };
 
+// 2^e as a float, exact for e in [-149, 127] (subnormal below -126).
+__device__ __forceinline__ float pow2f(int e) {
+  return e >= -126 ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23)
+                   : __uint_as_float(1u << (e + 149));
+}
+
+// 16 E4M3 codes (byte j = element j) of a block with scale exponent e -> the 16 exact
+// values code x 2^e as bf16 (element j at position j of lo:hi).  Exact whenever the
+// value is a bf16 value: always, except below bf16's subnormal floor (a block whose
+// amax is under about 2^-116 can lose its smallest codes there).
+__device__ __forceinline__ void fp8x16_expand(const uint4& c, int e, uint4& lo, uint4& hi) {
+  const float s = pow2f(e);
+  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+  uint32_t o[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(
+          static_cast<__nv_fp8x2_storage_t>((w[i] >> (16 * half)) & 0xFFFFu), __NV_E4M3);
+      const float2 f = __half22float2(__half2(hr));
+      __nv_bfloat162 b = __floats2bfloat162_rn(f.x * s, f.y * s);
+      o[2 * i + half] = *reinterpret_cast<uint32_t*>(&b);
+    }
+  }
+  lo = make_uint4(o[0], o[1], o[2], o[3]);
+  hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
 }  // namespace
 
 // a3.  Eight lanes per 128-column block, 16 values (two 16-byte loads) per lane.
@@ -266,6 +295,126 @@ __global__ void __launch_bounds__(128) k_combine(const uint16_t* __restrict__ y2
   }
 }
 
+// a3 for the NVFP4 path: quantise each token once (codes and scales to xq / xs when
+// given) and write the exact bf16 values of its codes (code x 2^e) straight into its
+// k routed rows and its shared row of the packed bf16 activations xe.
+template <typename Idx>
+__global__ void __launch_bounds__(256) k_quant_scatter_bf16(const uint16_t* __restrict__ x,
+                                                            int T, int H, int k, int has_shared,
+                                                            const int32_t* __restrict__ inv,
+                                                            uint8_t* __restrict__ xq,
+                                                            uint8_t* __restrict__ xs,
+                                                            uint16_t* __restrict__ xe,
+                                                            uint32_t* status) {
+  pdl_wait();
+  pdl_trigger();
+  const int nblk = H / 128;
+  const BlockLane<Idx> L(T, nblk);
+  float f[16];
+  if (L.live) {
+    load_bf16x16(x + static_cast<size_t>(L.r) * H + L.b * 128 + L.sub * 16, f);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) f[i] = 0.f;
+  }
+  int e;
+  const uint4 c = quant16(f, e);
+  if (!L.live) return;
+  const size_t t = static_cast<size_t>(L.r);
+  const int col = static_cast<int>(L.b) * 128 + L.sub * 16;
+  if (xq) *reinterpret_cast<uint4*>(xq + t * H + col) = c;
+  if (xs && L.sub == 0) xs[t * nblk + L.b] = static_cast<uint8_t>(e + 127);
+  uint4 lo, hi;
+  fp8x16_expand(c, e, lo, hi);
+  const long long R = static_cast<long long>(T) * k;
+  for (int j = 0; j <= k; ++j) {
+    long long r;
+    if (j < k) {
+      r = inv[t * k + j];
+      if (r < 0 || r >= R) {
+        if (L.sub == 0) set_status(status, STATUS_BAD_INDEX);
+        continue;
+      }
+    } else {
+      if (!has_shared) break;
+      r = R + static_cast<long long>(t);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(xe + r * H + col);
+    dst[0] = lo;
+    dst[1] = hi;
+  }
+}
+
+// a5 for the NVFP4 path: as k_swiglu_quant (codes and scales to hq / hs when given),
+// plus the exact bf16 values of the codes in he, W2's operand.
+template <typename Idx>
+__global__ void __launch_bounds__(256) k_swiglu_quant_bf16(const uint16_t* __restrict__ y13,
+                                                           int rows, int I,
+                                                           uint8_t* __restrict__ hq,
+                                                           uint8_t* __restrict__ hs,
+                                                           uint16_t* __restrict__ he) {
+  pdl_wait();
+  pdl_trigger();
+  const int nblk = I / 128;
+  const BlockLane<Idx> L(rows, nblk);
+  float h[16];
+  if (L.live) {
+    const uint16_t* g_at = y13 + static_cast<size_t>(L.r) * (2 * static_cast<size_t>(I)) +
+                           L.b * 128 + L.sub * 16;
+    float g[16], u[16];
+    load_bf16x16(g_at, g);
+    load_bf16x16(g_at + I, u);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) h[i] = __fdividef(g[i], 1.0f + __expf(-g[i])) * u[i];
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) h[i] = 0.f;
+  }
+  int e;
+  const uint4 c = quant16(h, e);
+  if (!L.live) return;
+  const size_t off = static_cast<size_t>(L.r) * I + L.b * 128 + L.sub * 16;
+  if (hq) *reinterpret_cast<uint4*>(hq + off) = c;
+  if (hs && L.sub == 0) hs[static_cast<size_t>(L.r) * nblk + L.b] = static_cast<uint8_t>(e + 127);
+  uint4 lo, hi;
+  fp8x16_expand(c, e, lo, hi);
+  uint4* dst = reinterpret_cast<uint4*>(he + off);
+  dst[0] = lo;
+  dst[1] = hi;
+}
+
+// FP8 rows -> bf16 rows of their exact values.  Thread -> (row, 16-column chunk); row r
+// reads row tok(r) of xq (perm_src[r] / k for r < R, r - R above) or row r itself.
+__global__ void __launch_bounds__(256) k_expand_rows(const uint8_t* __restrict__ xq,
+                                                     const uint8_t* __restrict__ xs,
+                                                     const int32_t* __restrict__ perm_src,
+                                                     int T, int k, int R, int rows, int K,
+                                                     uint16_t* __restrict__ xe,
+                                                     uint32_t* status) {
+  pdl_wait();
+  pdl_trigger();
+  const int chunks = K / 16;
+  const long long gid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (gid >= static_cast<long long>(rows) * chunks) return;
+  const long long r = gid / chunks;
+  const int c = static_cast<int>(gid - r * chunks);
+  long long src = r;
+  if (perm_src) {
+    src = r < R ? perm_src[r] / k : r - R;
+    if (src < 0 || src >= T) {
+      if (c == 0) set_status(status, STATUS_BAD_INDEX);
+      return;
+    }
+  }
+  const uint4 code = *reinterpret_cast<const uint4*>(xq + src * K + c * 16);
+  const int e = static_cast<int>(xs[src * (K / 128) + c / 8]) - 127;
+  uint4 lo, hi;
+  fp8x16_expand(code, e, lo, hi);
+  uint4* dst = reinterpret_cast<uint4*>(xe + r * K + c * 16);
+  dst[0] = lo;
+  dst[1] = hi;
+}
+
 // ---------------------------------------------------------------- launchers -------
 
 // Eight threads per 128-column block, 256 threads per CTA; the 32-bit-index kernel
@@ -292,6 +441,31 @@ cudaError_t launch_quant_scatter(const uint16_t* x, int T, int H, int k, int has
   return launch_blocks(k_quant_scatter<uint32_t>, k_quant_scatter<unsigned long long>,
                        static_cast<long long>(T) * (H / 128), st, x, T, H, k, has_shared, inv, xq,
                        xs, xg, xsg, status);
+}
+
+cudaError_t launch_quant_scatter_bf16(const uint16_t* x, int T, int H, int k, int has_shared,
+                                      const int32_t* inv, uint8_t* xq, uint8_t* xs,
+                                      uint16_t* xe, uint32_t* status, cudaStream_t st) {
+  return launch_blocks(k_quant_scatter_bf16<uint32_t>, k_quant_scatter_bf16<unsigned long long>,
+                       static_cast<long long>(T) * (H / 128), st, x, T, H, k, has_shared, inv,
+                       xq, xs, xe, status);
+}
+
+cudaError_t launch_swiglu_quant_bf16(const uint16_t* y13, int rows, int I, uint8_t* hq,
+                                     uint8_t* hs, uint16_t* he, cudaStream_t st) {
+  return launch_blocks(k_swiglu_quant_bf16<uint32_t>, k_swiglu_quant_bf16<unsigned long long>,
+                       static_cast<long long>(rows) * (I / 128), st, y13, rows, I, hq, hs, he);
+}
+
+cudaError_t launch_expand_rows(const uint8_t* xq, const uint8_t* xs, const int32_t* perm_src,
+                               int T, int k, int R, int rows, int K, uint16_t* xe,
+                               uint32_t* status, cudaStream_t st) {
+  const long long n = static_cast<long long>(rows) * (K / 16);
+  if (n == 0) return cudaSuccess;
+  const long long grid = (n + 255) / 256;
+  if (grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+  return launch_k(k_expand_rows, static_cast<unsigned>(grid), 256, 0, st, xq, xs, perm_src, T, k,
+                  R, rows, K, xe, status);
 }
 
 cudaError_t launch_swiglu_quant(const uint16_t* y13, int rows, int I, uint8_t* hq, uint8_t* hs,

@@ -605,14 +605,7 @@ __global__ void __launch_bounds__(256, OCC)
 
 // ---------------------------------------------------------------- host side -------
 
-namespace {
-
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn get_encode_fn() {
+EncodeTiledFn get_encode_tiled_fn() {
   static EncodeTiledFn fn = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
@@ -625,6 +618,8 @@ EncodeTiledFn get_encode_fn() {
   });
   return fn;
 }
+
+namespace {
 
 struct DevInfo {
   int sms = 0;
@@ -675,7 +670,7 @@ cudaError_t launch_one(const CUtensorMap& tmW, const CUtensorMap& tmX, const Gem
 // packed activation rows as a 3D view {128 bytes, rows, K/128} (box {128, xr, ko}).
 int gemm_encode_maps(const uint8_t* w_codes, int G, int N, int K, const uint8_t* act,
                      int rows_total, int ko, int xr, CUtensorMap* tmW, CUtensorMap* tmX) {
-  EncodeTiledFn enc = get_encode_fn();
+  EncodeTiledFn enc = get_encode_tiled_fn();
   if (!enc) return MOE_ERR_CUDA;
   {
     cuuint64_t dims[4] = {128, static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(K / 128),

@@ -1,0 +1,537 @@
+// f3: grouped GEMM with NVFP4 expert weights and FP8 activations on the tcgen05
+// tensor cores.
+//
+// Pages: GB10 "Optimization progress report", Optimization 05 (native NVFP4 MoE: the
+// expert weights stay NVFP4 in memory and the expert kernel reads them as such, with
+// no up-front dequantisation of whole matrices); "Pushing the Limits of Serving
+// DeepSeek-V4-Pro" (LMSYS, H20), §3.3 (W13 and W2 as grouped GEMMs shaped by the
+// routing histogram).
+//
+// NVFP4 = E2M1 codes, one E4M3 scale per 16 K elements, one fp32 scale per weight
+// tensor.  No block-scaled tensor-core kind pairs E4M3 block scales with FP8
+// activations (kind::mxf8f6f4 takes UE8M0 scales per 32; kind::mxf4nvf4 wants FP4 on
+// both sides), so this kernel multiplies in bf16, where both operands are exact:
+//   * a weight e2m1 x e4m3 has at most 2 + 4 significant bits and lies in
+//     [2^-10, 2688]: exact in bf16 (8 significant bits);
+//   * an FP8 activation code x its power-of-two block scale 2^e has 4 significant
+//     bits: exact in bf16 down to bf16's subnormal floor (a 128-block whose amax is
+//     below about 2^-116 loses its smallest codes).  The activations arrive already
+//     expanded to bf16 rows by the quantisation kernels.
+// kind::f16 MMAs accumulate those exact products in fp32, as the MXFP4 path does; the
+// tensor scale multiplies the fp32 sum in the epilogue before the bf16 rounding.
+//
+// Design (per CTA, one per SM, 16 warps):
+//   * warp 0: TMA of the packed codes (0.5 B / weight, 128B- or 64B-swizzled so the
+//     converters read them without bank conflicts) and the E4M3 scales of a K stage
+//     -- the weights cross HBM in their 0.5625 B / weight NVFP4 form;
+//   * warp 2: TMA of the bf16 token rows of the stage (their own ring);
+//   * warps 4-11: converters.  Warp w owns TMEM lanes 32 (w % 4) .. +31 (one weight
+//     row per thread) and half (w - 4) / 4 of the stage's K; it decodes its codes to
+//     bf16 with byte-permute table lookups, multiplies by the block scale (exact) and
+//     writes them into TMEM with tcgen05.st: the MMA's A operand lives in tensor
+//     memory, so the dequantised weights never pass through shared memory;
+//   * warp 1 (and warp 3 in the small variant): MMA issue, tcgen05.mma kind::f16 with
+//     A from TMEM and B (tokens) from shared memory, fp32 accumulators in TMEM;
+//   * warps 12-15: epilogue (TMEM -> registers, x tensor scale, -> bf16 rows).
+// Every wait is bounded; an expired wait sets a status bit and the CTA unwinds.
+#include "kernels.cuh"
+
+namespace moe {
+
+namespace {
+
+struct NvParams {
+  const int4* items;          // {group, row0, rows, 0}
+  const int32_t* item_count;  // device
+  int max_items;
+  uint16_t* y;                // [rows_total][N]
+  const float* gs;            // [G][S] tensor scales, or null (1.0)
+  int gs_segments;            // S: equal row segments of N with their own tensor scale
+  int N, K, G, rows_total;
+  uint32_t* status;
+};
+
+// BN: token tile; KS: K elements per stage; CS: code/scale ring slots; NA: token ring
+// slots = TMEM A buffers; ACC: accumulator buffers; ISS: MMA-issuing threads (each
+// takes every ISS-th stage of a tile into its own accumulator).
+template <int BN, int KS, int CS, int NA, int ACC, int ISS>
+struct NvCfg {
+  static constexpr int kCodeBytes = 128 * (KS / 2);  // [128 rows][KS/2 B], swizzled
+  static constexpr int kScaleBytes = 128 * 16;       // [128 rows][16 B] (256 K of scales)
+  static constexpr int kCodeStage = kCodeBytes + kScaleBytes;
+  static constexpr int kTokBytes = BN * KS * 2;      // [KS/64][BN rows][128 B], SW128
+  static constexpr int kOffTok = 0;
+  static constexpr int kOffCode = kOffTok + NA * kTokBytes;
+  static constexpr int kOffBar = kOffCode + CS * kCodeStage;
+  // code_full[CS], code_empty[CS], tok_full[NA], conv_full[ISS][NA], mma_done[NA],
+  // acc_full[ACC], acc_empty[ACC], drain[ISS]
+  static constexpr int kNumBars = 2 * CS + NA + ISS * NA + NA + 2 * ACC + ISS;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmemBytes = kOffMisc + 16;
+  static constexpr int kAccCols = ISS * BN;          // one accumulator buffer
+  static constexpr int kACols = KS / 2;              // bf16 pairs per A buffer row
+  static constexpr int kTmemNeed = ACC * kAccCols + NA * kACols;
+  static constexpr int kTmemCols = kTmemNeed <= 256 ? 256 : 512;
+  static constexpr int kConvWarps = 8;
+  static constexpr int kHalfK = KS / 2;              // K elements per converter thread
+  static constexpr int kBlocks = kHalfK / 16;        // E4M3 scale blocks per thread
+  static_assert(BN % 16 == 0 && BN <= 256, "token tile");
+  static_assert(KS == 128 || KS == 256, "stage K");
+  static_assert(kTmemNeed <= 512, "TMEM");
+  static_assert(kSmemBytes + 1024 <= 232448, "shared memory");
+  static_assert(kCodeBytes % 1024 == 0 && kTokBytes % 1024 == 0, "tile alignment");
+  static_assert(ISS == 1 || ISS == 2, "issuers");
+};
+
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, M = 128.
+__device__ __forceinline__ uint32_t idesc_bf16(int n) {
+  uint32_t d = 0;
+  d |= 1u << 4;                                 // D format: F32
+  d |= 1u << 7;                                 // A format: BF16
+  d |= 1u << 10;                                // B format: BF16
+  d |= static_cast<uint32_t>(n >> 3) << 17;     // N >> 3
+  d |= static_cast<uint32_t>(128 >> 4) << 24;   // M >> 4
+  return d;
+}
+
+// Eight E2M1 codes (one 32-bit word, element j in nibble j) -> eight bf16 values, two
+// per word (element 2w in the low half of word w).  Magnitudes come from two 8-entry
+// byte tables (high and low byte of the bf16 pattern of 0, 0.5, 1, 1.5, 2, 3, 4, 6),
+// looked up four at a time with byte permutes; the sign bits are moved into place the
+// same way.
+__device__ __forceinline__ void e2m1x8_to_bf16(uint32_t c, uint32_t (&o)[4]) {
+  const uint32_t mag = c & 0x77777777u;
+  uint32_t hb0 = __byte_perm(0x3F3F3F00u, 0x40404040u, mag);
+  uint32_t hb1 = __byte_perm(0x3F3F3F00u, 0x40404040u, mag >> 16);
+  const uint32_t lb0 = __byte_perm(0xC0800000u, 0xC0804000u, mag);
+  const uint32_t lb1 = __byte_perm(0xC0800000u, 0xC0804000u, mag >> 16);
+  const uint32_t even_s = (c << 4) & 0x80808080u;  // bit 7 of byte w: sign of element 2w
+  const uint32_t odd_s = c & 0x80808080u;          // bit 7 of byte w: sign of element 2w+1
+  hb0 |= __byte_perm(even_s, odd_s, 0x5140);
+  hb1 |= __byte_perm(even_s, odd_s, 0x7362);
+  o[0] = __byte_perm(lb0, hb0, 0x5140);
+  o[1] = __byte_perm(lb0, hb0, 0x7362);
+  o[2] = __byte_perm(lb1, hb1, 0x5140);
+  o[3] = __byte_perm(lb1, hb1, 0x7362);
+}
+
+// E4M3 byte -> the same value as a pair of bf16 (exact: 4 significant bits).
+__device__ __forceinline__ __nv_bfloat162 e4m3_to_bf16x2(uint32_t b) {
+  const __half_raw hr = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(b), __NV_E4M3);
+  const float f = __half2float(__half(hr));
+  return __float2bfloat162_rn(f);
+}
+
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, __nv_bfloat162 s) {
+  __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&a);
+  v = __hmul2(v, s);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <int BN, int KS, int CS, int NA, int ACC, int ISS>
+__global__ void __launch_bounds__(512, 1)
+    k_gemm_nv(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmS,
+              const __grid_constant__ CUtensorMap tmX, const NvParams p) {
+  using C = NvCfg<BN, KS, CS, NA, ACC, ISS>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (threadIdx.x == 0) set_status(p.status, STATUS_BAD_PLAN);
+    return;
+  }
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* code_full = bars;
+  uint64_t* code_empty = code_full + CS;
+  uint64_t* tok_full = code_empty + CS;
+  uint64_t* conv_full = tok_full + NA;   // [ISS][NA]
+  uint64_t* mma_done = conv_full + ISS * NA;
+  uint64_t* acc_full = mma_done + NA;
+  uint64_t* acc_empty = acc_full + ACC;
+  uint64_t* drain = acc_empty + ACC;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < CS; ++s) {
+      mbar_init(&code_full[s], 1);                 // TMA (+tx)
+      mbar_init(&code_empty[s], C::kConvWarps);    // every converter warp read its part
+    }
+    for (int s = 0; s < NA; ++s) {
+      mbar_init(&tok_full[s], 1);                  // TMA (+tx)
+      mbar_init(&mma_done[s], 1);                  // tcgen05.commit
+      for (int i = 0; i < ISS; ++i) mbar_init(&conv_full[i * NA + s], C::kConvWarps);
+    }
+    for (int b = 0; b < ACC; ++b) {
+      mbar_init(&acc_full[b], ISS);
+      mbar_init(&acc_empty[b], 4);
+    }
+    for (int i = 0; i < ISS; ++i) mbar_init(&drain[i], 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmC);
+    tma_prefetch_desc(&tmS);
+    tma_prefetch_desc(&tmX);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  pdl_wait();
+  const uint32_t tmem = *tmem_slot;
+
+  const int n_tiles = p.N / 128;
+  const int nk = (p.K + KS - 1) / KS;
+  int count = *p.item_count;
+  if (count > p.max_items) {
+    if (threadIdx.x == 0) set_status(p.status, STATUS_BAD_PLAN);
+    count = p.max_items;
+  }
+  const long long total = static_cast<long long>(count) * n_tiles;
+  auto load_item = [&](long long L, int& g, int& row0, int& rows, int& nt) -> bool {
+    const int4 it = p.items[L / n_tiles];
+    nt = static_cast<int>(L % n_tiles);
+    g = it.x;
+    row0 = it.y;
+    rows = it.z;
+    if (rows <= 0) return false;
+    if (g < 0 || g >= p.G || row0 < 0 || rows > BN || row0 + rows > p.rows_total) {
+      if (threadIdx.x == 0) set_status(p.status, STATUS_BAD_PLAN);
+      return false;
+    }
+    return true;
+  };
+  const uint32_t a_base = tmem + ACC * C::kAccCols;  // NA buffers of kACols columns
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ codes + scales TMA
+    if (lane == 0) {
+      uint32_t it = 0;
+      for (long long L = blockIdx.x; L < total && !*abort_flag; L += gridDim.x) {
+        int g, row0, rows, nt;
+        if (!load_item(L, g, row0, rows, nt)) continue;
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % CS;
+          if (it >= CS && !mbar_wait(&code_empty[s], ((it / CS) & 1u) ^ 1u, p.status,
+                                     abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint8_t* dst = smem + C::kOffCode + s * C::kCodeStage;
+          mbar_arrive_expect_tx(&code_full[s], C::kCodeStage);
+          tma_load_3d(dst, &tmC, &code_full[s], kb * (KS / 2), nt * 128, g);
+          tma_load_3d(dst + C::kCodeBytes, &tmS, &code_full[s], ((kb * KS) / 256) * 16,
+                      nt * 128, g);
+        }
+        if (!ok) break;
+      }
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ token TMA
+    if (lane == 0) {
+      uint32_t it = 0;
+      for (long long L = blockIdx.x; L < total && !*abort_flag; L += gridDim.x) {
+        int g, row0, rows, nt;
+        if (!load_item(L, g, row0, rows, nt)) continue;
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % NA;
+          if (it >= NA && !mbar_wait(&mma_done[s], ((it / NA) & 1u) ^ 1u, p.status,
+                                     abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&tok_full[s], C::kTokBytes);
+          tma_load_3d(smem + C::kOffTok + s * C::kTokBytes, &tmX, &tok_full[s], 0, row0,
+                      kb * (KS / 64));
+        }
+        if (!ok) break;
+      }
+    }
+  } else if (warp == 1 || (ISS == 2 && warp == 3)) {
+    // ------------------------------------------------------------ MMA issuer(s)
+    const int par = warp == 1 ? 0 : 1;
+    if (lane == 0) {
+      uint32_t it = 0, tc = 0;
+      uint32_t phases = 0;  // bit s: parity of the next phase of conv_full[par][s]
+      for (long long L = blockIdx.x; L < total && !*abort_flag; L += gridDim.x) {
+        int g, row0, rows, nt;
+        if (!load_item(L, g, row0, rows, nt)) continue;
+        const int bn = (rows + 15) & ~15;
+        const uint32_t b = tc % ACC, use = tc / ACC;
+        if (tc >= ACC && !mbar_wait(&acc_empty[b], (use - 1) & 1u, p.status, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + b * C::kAccCols + par * BN;
+        const uint32_t idesc = idesc_bf16(bn);
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          if (ISS == 2 && (kb & 1) != par) continue;
+          const int s = it % NA;
+          const uint32_t ph = (phases >> s) & 1u;
+          phases ^= 1u << s;
+          if (!mbar_wait(&conv_full[par * NA + s], ph, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_t = a_base + s * C::kACols;
+          const uint32_t b0 = smem_u32(smem + C::kOffTok + s * C::kTokBytes);
+#pragma unroll
+          for (int kk = 0; kk < KS / 16; ++kk) {
+            const uint64_t bd = smem_desc(b0 + (kk >> 2) * (BN * 128) + (kk & 3) * 32, 0, 1024,
+                                          kLayoutSw128);
+            mma_bf16_ts(d_tmem, a_t + kk * 8, bd, idesc, kb > par || kk != 0);
+          }
+          tc_commit(&mma_done[s]);
+        }
+        if (!ok) break;
+        tc_commit(&acc_full[b]);
+        ++tc;
+      }
+    }
+  } else if (warp >= 4 && warp < 4 + C::kConvWarps) {
+    // ------------------------------------------------------------ converters
+    const int q = warp & 3;            // TMEM lane quarter = weight rows 32q .. 32q+31
+    const int h = (warp - 4) >> 2;     // half of the stage's K
+    const int r = q * 32 + lane;       // weight row within the tile
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    uint32_t it = 0;
+    bool ok = true;
+    for (long long L = blockIdx.x; L < total && ok && !*abort_flag; L += gridDim.x) {
+      int g, row0, rows, nt;
+      if (!load_item(L, g, row0, rows, nt)) continue;
+      for (int kb = 0; kb < nk; ++kb, ++it) {
+        const int cs = it % CS, s = it % NA;
+        // the TMEM A buffer of this stage is free once the MMAs of stage it - NA are
+        // done (their commit); the code slot once its TMA has landed
+        int w_ok = 1;
+        if (lane == 0) {
+          if (it >= NA)
+            w_ok = mbar_wait(&mma_done[s], ((it / NA) & 1u) ^ 1u, p.status, abort_flag);
+          if (w_ok) w_ok = mbar_wait(&code_full[cs], (it / CS) & 1u, p.status, abort_flag);
+        }
+        if (!__shfl_sync(0xFFFFFFFFu, w_ok, 0)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint8_t* cbase = smem + C::kOffCode + cs * C::kCodeStage;
+        // this thread's codes: row r, bytes [h * KS/4, (h+1) * KS/4) of its KS/2-byte
+        // row, in 16-byte chunks stored at chunk ^ swizzle(r)
+        constexpr int kChunks = KS / 64;  // 16-byte chunks per thread
+        uint4 cw[kChunks];
+#pragma unroll
+        for (int j = 0; j < kChunks; ++j) {
+          const int chunk = h * kChunks + j;
+          const int phys = KS == 256 ? (chunk ^ (r & 7)) : (chunk ^ ((r >> 1) & 3));
+          cw[j] = *reinterpret_cast<const uint4*>(cbase + r * (KS / 2) + phys * 16);
+        }
+        // this thread's scale bytes: row r of the 16-byte scale row; a 128-K stage uses
+        // half of the 256 K it covers
+        const uint4 sv = *reinterpret_cast<const uint4*>(cbase + C::kCodeBytes + r * 16);
+        const int sbyte0 = (KS == 128 ? (kb & 1) * 8 : 0) + h * C::kBlocks;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&code_empty[cs]);
+        const uint32_t col0 = a_base + s * C::kACols + h * (C::kHalfK / 2);
+#pragma unroll
+        for (int blk = 0; blk < C::kBlocks; ++blk) {
+          const int sb = sbyte0 + blk;
+          const uint32_t sw = sb < 4 ? sv.x : sb < 8 ? sv.y : sb < 12 ? sv.z : sv.w;
+          const __nv_bfloat162 sc = e4m3_to_bf16x2((sw >> (8 * (sb & 3))) & 0xFFu);
+          // 16 elements = 8 code bytes = two 32-bit words of chunk blk / 2
+          const uint4 cv = cw[blk >> 1];
+          const uint32_t w0 = (blk & 1) ? cv.z : cv.x;
+          const uint32_t w1 = (blk & 1) ? cv.w : cv.y;
+          uint32_t o[8], t[4];
+          e2m1x8_to_bf16(w0, t);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) o[i] = bf16x2_mul(t[i], sc);
+          e2m1x8_to_bf16(w1, t);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) o[4 + i] = bf16x2_mul(t[i], sc);
+          tmem_st_32x32b_x8(lane_base + col0 + blk * 8, o);
+        }
+        tmem_st_wait();
+        // the tokens of this stage must have landed before the MMAs read them
+        if (lane == 0)
+          w_ok = mbar_wait(&tok_full[s], (it / NA) & 1u, p.status, abort_flag);
+        if (!__shfl_sync(0xFFFFFFFFu, w_ok, 0)) {
+          ok = false;
+          break;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&conv_full[(ISS == 2 ? (kb & 1) : 0) * NA + s]);
+      }
+    }
+  } else if (warp >= 12) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    uint32_t tc = 0;
+    for (long long L = blockIdx.x; L < total && !*abort_flag; L += gridDim.x) {
+      int g, row0, rows, nt;
+      if (!load_item(L, g, row0, rows, nt)) continue;
+      const uint32_t b = tc % ACC, use = tc / ACC;
+      int w_ok = 1;
+      if (lane == 0) w_ok = mbar_wait(&acc_full[b], use & 1u, p.status, abort_flag);
+      if (!__shfl_sync(0xFFFFFFFFu, w_ok, 0)) break;
+      tc_fence_after();
+      const int n = nt * 128 + q * 32 + lane;
+      float gsc = 1.0f;
+      if (p.gs) gsc = __ldg(p.gs + static_cast<size_t>(g) * p.gs_segments +
+                            n / (p.N / p.gs_segments));
+      uint16_t* ycol = p.y + static_cast<size_t>(row0) * p.N + n;
+      const uint32_t acc = tmem + (static_cast<uint32_t>(q * 32) << 16) + b * C::kAccCols;
+      for (int c0 = 0; c0 < rows; c0 += 16) {
+        uint32_t rr[16];
+        float v[16];
+        tmem_ld_32x32b_x16(acc + c0, rr);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(rr[i]);
+        if (ISS == 2 && nk > 1) {  // even-stage + odd-stage sums, in that order
+          tmem_ld_32x32b_x16(acc + BN + c0, rr);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] += __uint_as_float(rr[i]);
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          if (c0 + i < rows) {
+            const __nv_bfloat16 hv = __float2bfloat16_rn(v[i] * gsc);
+            ycol[static_cast<size_t>(c0 + i) * p.N] = *reinterpret_cast<const uint16_t*>(&hv);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[b]);
+      ++tc;
+    }
+  }
+
+  // After an abort, each MMA issuer waits (briefly, bounded) until the MMAs it issued
+  // have completed, so that TMEM is not released under them; TMA loads still in flight
+  // are not waited for (best effort).
+  if ((warp == 1 || (ISS == 2 && warp == 3)) && lane == 0 && *abort_flag) {
+    uint64_t* db = &drain[warp == 1 ? 0 : 1];
+    tc_commit(db);
+    mbar_wait_drain(db, 0);
+  }
+  pdl_trigger();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host side -------
+
+template <int BN, int KS, int CS, int NA, int ACC, int ISS>
+cudaError_t launch_nv_one(const NvGemmLaunch& a, int v, cudaStream_t st) {
+  using C = NvCfg<BN, KS, CS, NA, ACC, ISS>;
+  auto kern = k_gemm_nv<BN, KS, CS, NA, ACC, ISS>;
+  const int max_items = a.max_items[v];
+  const long long tiles = static_cast<long long>(max_items) * (a.N / 128);
+  if (tiles == 0) return cudaSuccess;
+  static unsigned long long attr_ctx[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  const unsigned long long ctx = current_context_id();
+  if (ctx == 0 || attr_ctx[dev] != ctx) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_ctx[dev] = current_context_id();
+  }
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  CUtensorMap tmC, tmS, tmX;
+  if (nv_encode_maps(a, KS, BN, &tmC, &tmS, &tmX) != MOE_OK) return cudaErrorInvalidValue;
+  NvParams p{};
+  p.items = a.items[v];
+  p.item_count = a.item_counts + v;
+  p.max_items = max_items;
+  p.y = a.y;
+  p.gs = a.gs;
+  p.gs_segments = a.gs_segments;
+  p.N = a.N;
+  p.K = a.K;
+  p.G = a.G;
+  p.rows_total = a.rows_total;
+  p.status = a.status;
+  const int grid = static_cast<int>(tiles < sms ? tiles : sms);
+  return launch_k(kern, grid, 512, C::kSmemBytes, st, tmC, tmS, tmX, p);
+}
+
+}  // namespace
+
+// Tensor maps: codes as {K/2 bytes, N rows, G} (box {KS/2, 128, 1}, swizzled so that
+// each converter thread's 16-byte chunks fall in distinct banks), scales as {K/16
+// bytes, N rows, G} (box {16, 128, 1}: 256 K of scales), bf16 token rows as {64
+// elements, rows, K/64} (box {64, BN, KS/64}, 128B-swizzled: the MMA's K-major layout).
+int nv_encode_maps(const NvGemmLaunch& a, int ks, int bn, CUtensorMap* tmC, CUtensorMap* tmS,
+                   CUtensorMap* tmX) {
+  EncodeTiledFn enc = get_encode_tiled_fn();
+  if (!enc) return MOE_ERR_CUDA;
+  {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(a.K / 2), static_cast<cuuint64_t>(a.N),
+                          static_cast<cuuint64_t>(a.G)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(a.K / 2),
+                             static_cast<cuuint64_t>(a.N) * static_cast<cuuint64_t>(a.K / 2)};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(ks / 2), 128, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (enc(tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(a.w_codes), dims,
+            strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            ks == 256 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return MOE_ERR_CUDA;
+  }
+  {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(a.K / 16), static_cast<cuuint64_t>(a.N),
+                          static_cast<cuuint64_t>(a.G)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(a.K / 16),
+                             static_cast<cuuint64_t>(a.N) * static_cast<cuuint64_t>(a.K / 16)};
+    cuuint32_t box[3] = {16, 128, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (enc(tmS, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(a.w_scales), dims,
+            strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return MOE_ERR_CUDA;
+  }
+  {
+    cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(a.rows_total > 0 ? a.rows_total : 1),
+                          static_cast<cuuint64_t>(a.K / 64)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(a.K) * 2, 128};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(bn), static_cast<cuuint32_t>(ks / 64)};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (enc(tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(a.act), dims,
+            strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+// Variants by the tile plan's lists (same row bounds as the MXFP4 GEMM's):
+//   small  rows <= 16:  256-K stages, 6 code slots, 3 token/TMEM slots, 2 issuers;
+//   medium rows <= 64:  256-K stages, 4 code slots, 3 token/TMEM slots;
+//   mid    rows <= 128: 256-K stages, 3 code slots, 2 token/TMEM slots;
+//   large  rows <= 240: 128-K stages (a 240-row bf16 token tile is 60 KB per 128 K),
+//          3 slots, one accumulator (240 of TMEM's 512 columns).
+cudaError_t launch_grouped_gemm_nv(const NvGemmLaunch& a, cudaStream_t st) {
+  cudaError_t e = launch_nv_one<kSmallBN, 256, 6, 3, 2, 2>(a, 0, st);
+  if (e != cudaSuccess || a.max_group_rows <= kSmallBN) return e;
+  e = launch_nv_one<kMediumBN, 256, 4, 3, 2, 1>(a, 1, st);
+  if (e != cudaSuccess || a.max_group_rows <= kMediumBN) return e;
+  e = launch_nv_one<kMidBN, 256, 3, 2, 2, 1>(a, 2, st);
+  if (e != cudaSuccess || a.max_group_rows <= kMidBN) return e;
+  return launch_nv_one<kLargeBN, 128, 3, 3, 1, 1>(a, 3, st);
+}
+
+}  // namespace moe

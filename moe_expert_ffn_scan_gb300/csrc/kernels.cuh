@@ -118,6 +118,46 @@ struct GemmLaunch {
 };
 cudaError_t launch_grouped_gemm(const GemmLaunch& a, cudaStream_t st);
 
+// f3: the NVFP4-weight grouped GEMM (gemm_nv.cu).  Activations arrive as bf16 rows
+// holding the exact values of their FP8 codes (code x 2^e).
+struct NvGemmLaunch {
+  const uint8_t* w_codes;     // [G][N][K/2] E2M1 codes
+  const uint8_t* w_scales;    // [G][N][K/16] E4M3 block scales
+  const float* gs;            // [G][gs_segments] fp32 tensor scales, or null (1.0)
+  int gs_segments;            // equal row segments of N, each with its tensor scale
+  const uint16_t* act;        // [rows_total][K] bf16
+  uint16_t* y;                // [rows_total][N] bf16
+  int G, N, K, rows_total;
+  const int4* items[kNumVariants];
+  const int32_t* item_counts;
+  int max_items[kNumVariants];
+  int max_group_rows;
+  uint32_t* status;
+};
+cudaError_t launch_grouped_gemm_nv(const NvGemmLaunch& a, cudaStream_t st);
+int nv_encode_maps(const NvGemmLaunch& a, int ks, int bn, CUtensorMap* tmC, CUtensorMap* tmS,
+                   CUtensorMap* tmX);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (null if absent).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn get_encode_tiled_fn();
+
+// FP8 codes -> bf16 rows of their exact values (code x 2^e), for the NVFP4 GEMMs:
+// the quant-scatter writes xe (the packed rows) directly; the stand-alone GEMM calls
+// expand their FP8 operand with launch_expand_rows (row r of xe from row tok(r) of
+// xq when perm_src is given, else from row r).
+cudaError_t launch_quant_scatter_bf16(const uint16_t* x, int T, int H, int k, int has_shared,
+                                      const int32_t* inv, uint8_t* xq, uint8_t* xs,
+                                      uint16_t* xe, uint32_t* status, cudaStream_t st);
+cudaError_t launch_swiglu_quant_bf16(const uint16_t* y13, int rows, int I, uint8_t* hq,
+                                     uint8_t* hs, uint16_t* he, cudaStream_t st);
+cudaError_t launch_expand_rows(const uint8_t* xq, const uint8_t* xs, const int32_t* perm_src,
+                               int T, int k, int R, int rows, int K, uint16_t* xe,
+                               uint32_t* status, cudaStream_t st);
+
 // Unique id of the calling thread's current CUDA context (cuCtxGetId), 0 when no
 // context is current or the driver entry points are unavailable.  Host-side caches of
 // per-context state (a function attribute, a symbol's device address) are keyed on it:

@@ -138,6 +138,32 @@ def test_validation_happens_before_any_launch(lib):
                            P(0x1000), None, P(0x10000), 1 << 30, None) == 1
 
 
+def test_nvfp4_validation_before_any_launch(lib):
+    P = ctypes.c_void_p
+    ok = moe.dims(7, 7168, 3072, 384, 8, 1)
+    assert moe.workspace_size_nvfp4(ok) > moe.gemm_workspace_size_nvfp4(ok) > 0
+    # the NVFP4 GEMMs need H and I multiples of 256 (their scale rows are whole TMA rows)
+    for bad in (moe.dims(7, 7168 + 128, 3072, 384, 8, 1), moe.dims(7, 7168, 3072 - 128, 384, 8, 1)):
+        assert moe.workspace_size(bad) > 0 and moe.workspace_size_nvfp4(bad) == 0
+        assert lib.moe_forward_nvfp4(ctypes.byref(bad), P(0x1000), P(0x1000), None, P(0x1000),
+                                     None, P(0x10000), 1 << 30, None) == 2
+        assert lib.moe_grouped_gemm_w13_nvfp4(ctypes.byref(bad), *[P(0x1000)] * 8, P(0x10000),
+                                              1 << 30, None) == 2
+    d = moe.dims(7, 512, 256, 8, 2, 0)
+    assert lib.moe_forward_nvfp4(ctypes.byref(d), P(0x1000), P(0x1000), None, P(0x1000), None,
+                                 P(0x10000), 1 << 30, None) == 1
+    w = moe.moe_weights_nvfp4(0x10000, 0x10000, 0x10002, 0x10000, 0x10000, None)  # gs misaligned
+    assert lib.moe_forward_nvfp4(ctypes.byref(d), P(0x1000), P(0x1000), ctypes.byref(w),
+                                 P(0x1000), None, P(0x10000), 1 << 30, None) == 1
+    w = moe.moe_weights_nvfp4(0x10000, 0x10000, None, 0x10000, 0x10000, None)
+    assert lib.moe_forward_nvfp4(ctypes.byref(d), P(0x1000), P(0x1000), ctypes.byref(w),
+                                 P(0x1000), None, P(0x10000), 16, None) == 3
+    assert lib.moe_grouped_gemm_w2_nvfp4(ctypes.byref(d), None, *[P(0x1000)] * 6, P(0x10000),
+                                         1 << 30, None) == 1
+    assert lib.moe_grouped_gemm_w2_nvfp4(ctypes.byref(d), *[P(0x1000)] * 7, P(0x10000), 16,
+                                         None) == 3
+
+
 def test_python_binding_rejects_host_tensors(lib):
     import torch
     x = torch.zeros(4, 128, dtype=torch.bfloat16)
