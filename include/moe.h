@@ -323,6 +323,25 @@ int moe_forward_timed(const moe_dims* d, const uint16_t* x, const float* logits,
                       const moe_weights* W, uint16_t* out, const moe_debug_out* dbg,
                       void* const* events, void* ws, size_t ws_bytes, void* stream);
 
+/* Options of moe_forward_ex (zero-initialise; every field 0 = moe_forward).
+ *   fuse_combine (f2): 1 = the W2 grouped GEMM's epilogue performs a7 (LMSYS-H20 §3.2,
+ *     the TopK reduction merged with the shared-expert add): once a tile has stored its
+ *     y2 rows, each row bumps its (token, 128-column block) arrival counter, and the
+ *     tile that brings a block to k + has_shared arrivals sums that token's rows for
+ *     those 128 columns in the stand-alone combine's order (fp32, j order, shared row
+ *     last) -- the same out bit for bit, deterministic, no float atomics -- and the
+ *     separate combine kernel is not launched.  MXFP4 weights only. */
+typedef struct moe_options {
+  int32_t fuse_combine;
+} moe_options;
+
+/* moe_forward_timed with options (opt may be NULL: all zero; events may be NULL).
+ * Returns MOE_ERR_INVALID_ARG for an option value other than 0 / 1. */
+int moe_forward_ex(const moe_dims* d, const uint16_t* x, const float* logits,
+                   const moe_weights* W, const moe_options* opt, uint16_t* out,
+                   const moe_debug_out* dbg, void* const* events, void* ws, size_t ws_bytes,
+                   void* stream);
+
 /* Debug helper (synchronises `stream`): reads the device status word at the start of
  * a workspace used by the calls above.  Returns MOE_OK if no bit is set, else
  * MOE_ERR_DEVICE_CHECK and the bits in *bits_out (if not NULL).  The word is

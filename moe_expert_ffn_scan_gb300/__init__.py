@@ -40,6 +40,10 @@ class moe_weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("w13", "w13_s", "w2", "w2_s")]
 
 
+class moe_options(ctypes.Structure):
+    _fields_ = [("fuse_combine", ctypes.c_int32)]
+
+
 class moe_weights_nvfp4(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("w13", "w13_s", "w13_gs", "w2", "w2_s", "w2_gs")]
 
@@ -97,6 +101,10 @@ def lib():
         L.moe_grouped_gemm_w13_nvfp4.argtypes = [_DP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
                                                  _P]
         L.moe_grouped_gemm_w2_nvfp4.argtypes = [_DP, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]
+        L.moe_forward_ex.argtypes = [_DP, _P, _P, ctypes.POINTER(moe_weights),
+                                     ctypes.POINTER(moe_options), _P,
+                                     ctypes.POINTER(moe_debug_out), ctypes.POINTER(_P), _P, _SZ,
+                                     _P]
         L.moe_route_static.argtypes = [_DP, _P, _P, _P, _P, _P, _P, _P, _P]
         L.moe_route_static_status.argtypes = [_P, ctypes.POINTER(ctypes.c_uint32)]
         L.moe_check_status.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_uint32)]
@@ -115,7 +123,7 @@ def lib():
                    "moe_grouped_gemm_w2", "moe_combine", "moe_forward", "moe_forward_timed",
                    "moe_check_status", "moe_forward_nvfp4", "moe_forward_nvfp4_timed",
                    "moe_grouped_gemm_w13_nvfp4", "moe_grouped_gemm_w2_nvfp4",
-                   "moe_route_static", "moe_route_static_status"):
+                   "moe_route_static", "moe_route_static_status", "moe_forward_ex"):
             getattr(L, fn).restype = ctypes.c_int
         _LIB = L
     return _LIB
@@ -296,6 +304,22 @@ def moe_route_static_status(stream=None) -> int:
     return bits.value
 
 
+def moe_forward_ex(d, x, logits, w13, w13_s, w2, w2_s, out, ws, fuse_combine=False, debug=None,
+                   events=None, stream=None):
+    """moe_forward with options (fuse_combine: the W2 GEMM's epilogue performs the
+    weighted top-k combine + shared add) and optional stage events."""
+    W = moe_weights(_p(w13), _p(w13_s), _p(w2), _p(w2_s))
+    opt = moe_options(1 if fuse_combine else 0)
+    dbg = None
+    if debug:
+        dbg = moe_debug_out(*[_p(debug.get(n)) for n in DEBUG_FIELDS])
+    ev = (_P * 8)(*[e.cuda_event for e in events]) if events else None
+    _check("moe_forward_ex", lib().moe_forward_ex(
+        _d(d), _p(x), _p(logits), ctypes.byref(W), ctypes.byref(opt), _p(out),
+        ctypes.byref(dbg) if dbg is not None else None, ev, _p(ws), ws.numel(),
+        _stream(stream)))
+
+
 def _host_p(t):
     if t.device.type != "cpu":
         raise ValueError("tensor must live in host memory")
@@ -442,9 +466,12 @@ class MoELayer:
     bf16 output [T, H]."""
 
     def __init__(self, H, I, E, k, has_shared, w13, w13_s, w2, w2_s, fmt="mxfp4", w13_gs=None,
-                 w2_gs=None):
+                 w2_gs=None, fuse_combine=False):
         if fmt not in ("mxfp4", "nvfp4"):
             raise ValueError(f"unknown weight format {fmt!r}")
+        if fuse_combine and fmt != "mxfp4":
+            raise ValueError("the combine fused into the W2 epilogue takes MXFP4 weights")
+        self.fuse_combine = bool(fuse_combine)
         self.H, self.I, self.E, self.k, self.has_shared = H, I, E, k, has_shared
         self.w13, self.w13_s, self.w2, self.w2_s = w13, w13_s, w2, w2_s
         self.fmt, self.w13_gs, self.w2_gs = fmt, w13_gs, w2_gs
@@ -497,8 +524,9 @@ class MoELayer:
         if out is None:
             out = torch.empty(T, self.H, dtype=torch.bfloat16, device=x.device)
         if self.fmt == "mxfp4":
-            moe_forward(self.dims(T), x, logits, self.w13, self.w13_s, self.w2, self.w2_s, out,
-                        self.workspace(T), debug=debug, stream=stream)
+            moe_forward_ex(self.dims(T), x, logits, self.w13, self.w13_s, self.w2, self.w2_s, out,
+                           self.workspace(T), fuse_combine=self.fuse_combine, debug=debug,
+                           stream=stream)
         else:
             moe_forward_nvfp4(self.dims(T), x, logits, self.w13, self.w13_s, self.w13_gs,
                               self.w2, self.w2_s, self.w2_gs, out, self.workspace(T),
@@ -509,8 +537,9 @@ class MoELayer:
         """forward recording the 8 stage events of moe_forward_timed (see STAGES)."""
         T = x.shape[0]
         if self.fmt == "mxfp4":
-            moe_forward_timed(self.dims(T), x, logits, self.w13, self.w13_s, self.w2, self.w2_s,
-                              out, self.workspace(T), events, stream=stream)
+            moe_forward_ex(self.dims(T), x, logits, self.w13, self.w13_s, self.w2, self.w2_s, out,
+                           self.workspace(T), fuse_combine=self.fuse_combine, events=events,
+                           stream=stream)
         else:
             moe_forward_nvfp4_timed(self.dims(T), x, logits, self.w13, self.w13_s, self.w13_gs,
                                     self.w2, self.w2_s, self.w2_gs, out, self.workspace(T),

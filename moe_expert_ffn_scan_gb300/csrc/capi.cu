@@ -152,6 +152,7 @@ struct ForwardWs {
   uint8_t *xq, *xs, *hq, *hs;
   uint16_t *y13, *y2;
   uint16_t* he;  // NVFP4: W2's operand as bf16 rows [Rs][I]
+  int32_t* cnt;  // f2: (token, 128-column block) arrival counters [T][H/128]
 };
 
 ForwardWs carve_forward(Carver& c, const moe_dims* d, WeightFormat fmt = kMxfp4) {
@@ -176,6 +177,7 @@ ForwardWs carve_forward(Carver& c, const moe_dims* d, WeightFormat fmt = kMxfp4)
     f.he = c.take<uint16_t>(Rs * I);
   }
   f.y2 = c.take<uint16_t>(Rs * H);
+  f.cnt = c.take<int32_t>(T * (H / 128));
   return f;
 }
 
@@ -201,10 +203,28 @@ HostStagingWs carve_host_staging(Carver& c, const moe_dims* d) {
 
 // early_plan: the plan's producer ran at least two launches before this GEMM (see
 // GemmLaunch).
+// f2: the combine performed by the W2 GEMM's epilogue (see GemmLaunch).
+struct FusedCombine {
+  uint16_t* out = nullptr;
+  const int32_t* perm_src = nullptr;
+  const int32_t* inv = nullptr;
+  const float* w = nullptr;
+  int32_t* cnt = nullptr;
+};
+
 int run_gemm(const moe_dims* d, const uint8_t* act, const uint8_t* act_s, const int32_t* offsets,
              const uint8_t* w, const uint8_t* w_s, int N, int K, uint16_t* y, const PlanWs& plan,
-             int max_group_rows, uint32_t* status, cudaStream_t st, int early_plan) {
+             int max_group_rows, uint32_t* status, cudaStream_t st, int early_plan,
+             const FusedCombine& fc = FusedCombine{}) {
   GemmLaunch a{};
+  a.out = fc.out;
+  a.perm_src = fc.perm_src;
+  a.inv = fc.inv;
+  a.cw = fc.w;
+  a.cnt = fc.cnt;
+  a.T = d->T;
+  a.k = d->k;
+  a.has_shared = d->has_shared;
   a.w_codes = w;
   a.w_scales = w_s;
   a.act = act;
@@ -582,9 +602,14 @@ namespace {
 // The layer a1..a7 on one stream for either weight format (see moe_forward_timed).
 int forward_impl(const moe_dims* d, const uint16_t* x, const float* logits,
                  const LayerWeights& W, uint16_t* out, const moe_debug_out* dbg,
-                 void* const* events, void* ws, size_t ws_bytes, cudaStream_t st) {
+                 void* const* events, void* ws, size_t ws_bytes, cudaStream_t st,
+                 const moe_options* opt = nullptr) {
   if (!(W.fmt == kMxfp4 ? dims_ok(d) : nv_dims_ok(d))) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (!x || !logits || !out || !ws) return MOE_ERR_INVALID_ARG;
+  const bool fuse_combine = opt && opt->fuse_combine;
+  if (opt && ((opt->fuse_combine != 0 && opt->fuse_combine != 1) ||
+              (fuse_combine && W.fmt != kMxfp4)))
+    return MOE_ERR_INVALID_ARG;
   if (!weights_ok(W.w13, W.w13_s) || !weights_ok(W.w2, W.w2_s)) return MOE_ERR_INVALID_ARG;
   if (!aligned(W.w13_gs, 4) || !aligned(W.w2_gs, 4)) return MOE_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(out, 16) || !aligned(ws, kAlign) || !aligned(logits, 4))
@@ -639,7 +664,7 @@ int forward_impl(const moe_dims* d, const uint16_t* x, const float* logits,
   uint8_t* xs_out = dbg && dbg->xs ? f.xs : nullptr;
   if (W.fmt == kMxfp4) {
     MOE_TRY(launch_quant_scatter(x, T, H, k, d->has_shared, f.inv, xq_out, xs_out, f.gemm.xg,
-                                 f.gemm.xsg, status, st))
+                                 f.gemm.xsg, fuse_combine ? f.cnt : nullptr, status, st))
   } else {
     MOE_TRY(launch_quant_scatter_bf16(x, T, H, k, d->has_shared, f.inv, xq_out, xs_out,
                                       f.gemm.xe, status, st))
@@ -665,14 +690,23 @@ int forward_impl(const moe_dims* d, const uint16_t* x, const float* logits,
   }
   MOE_MARK(5)
   if (W.fmt == kMxfp4) {
+    FusedCombine fc;
+    if (fuse_combine) {
+      fc.out = out;
+      fc.perm_src = f.perm_src;
+      fc.inv = f.inv;
+      fc.w = f.w;
+      fc.cnt = f.cnt;
+    }
     rc = run_gemm(d, f.hq, f.hs, f.offsets, W.w2, W.w2_s, H, I, f.y2, f.gemm.plan, T, status,
-                  st, /*early_plan=*/1);  // follows SwiGLU; the plan preceded W13
+                  st, /*early_plan=*/1, fc);  // follows SwiGLU; the plan preceded W13
   } else {
     rc = run_gemm_nv(d, f.he, W.w2, W.w2_s, W.w2_gs, 1, H, I, f.y2, f.gemm.plan, T, status, st);
   }
   if (rc != MOE_OK) return rc;
   MOE_MARK(6)
-  MOE_TRY(launch_combine(f.y2, f.inv, f.w, T, k, H, d->has_shared, out, status, st))
+  if (!fuse_combine)
+    MOE_TRY(launch_combine(f.y2, f.inv, f.w, T, k, H, d->has_shared, out, status, st))
   MOE_MARK(7)
 #undef MOE_TRY
 #undef MOE_MARK
@@ -715,6 +749,15 @@ int moe_forward_timed(const moe_dims* d, const uint16_t* x, const float* logits,
   if (!W) return dims_ok(d) ? MOE_ERR_INVALID_ARG : MOE_ERR_UNSUPPORTED_SHAPE;
   return forward_impl(d, x, logits, mx_weights(W), out, dbg, events, ws, ws_bytes,
                       static_cast<cudaStream_t>(stream));
+}
+
+int moe_forward_ex(const moe_dims* d, const uint16_t* x, const float* logits,
+                   const moe_weights* W, const moe_options* opt, uint16_t* out,
+                   const moe_debug_out* dbg, void* const* events, void* ws, size_t ws_bytes,
+                   void* stream) {
+  if (!W) return dims_ok(d) ? MOE_ERR_INVALID_ARG : MOE_ERR_UNSUPPORTED_SHAPE;
+  return forward_impl(d, x, logits, mx_weights(W), out, dbg, events, ws, ws_bytes,
+                      static_cast<cudaStream_t>(stream), opt);
 }
 
 size_t moe_workspace_size_nvfp4(const moe_dims* d) {

@@ -136,11 +136,15 @@ __global__ void __launch_bounds__(256) k_quant_scatter(const uint16_t* __restric
                                                        uint8_t* __restrict__ xs,
                                                        uint8_t* __restrict__ xg,
                                                        uint8_t* __restrict__ xsg,
+                                                       int32_t* __restrict__ cnt,
                                                        uint32_t* status) {
   pdl_wait();
   pdl_trigger();
   const int nblk = H / 128;
   const BlockLane<Idx> L(T, nblk);
+  // the (token, 128-column block) arrival counters of a W2 GEMM that performs the
+  // combine in its epilogue start at zero
+  if (cnt && L.live && L.sub == 0) cnt[static_cast<size_t>(L.r) * nblk + L.b] = 0;
   float f[16];
   if (L.live) {
     load_bf16x16(x + static_cast<size_t>(L.r) * H + L.b * 128 + L.sub * 16, f);
@@ -437,10 +441,10 @@ cudaError_t launch_quant_act(const uint16_t* x, int rows, int cols, uint8_t* q, 
 
 cudaError_t launch_quant_scatter(const uint16_t* x, int T, int H, int k, int has_shared,
                                  const int32_t* inv, uint8_t* xq, uint8_t* xs, uint8_t* xg,
-                                 uint8_t* xsg, uint32_t* status, cudaStream_t st) {
+                                 uint8_t* xsg, int32_t* cnt, uint32_t* status, cudaStream_t st) {
   return launch_blocks(k_quant_scatter<uint32_t>, k_quant_scatter<unsigned long long>,
                        static_cast<long long>(T) * (H / 128), st, x, T, H, k, has_shared, inv, xq,
-                       xs, xg, xsg, status);
+                       xs, xg, xsg, cnt, status);
 }
 
 cudaError_t launch_quant_scatter_bf16(const uint16_t* x, int T, int H, int k, int has_shared,

@@ -41,6 +41,16 @@ struct GemmParams {
   int N, K, G, rows_total;
   uint32_t* status;
   int early;  // the plan may be read, and weights loaded, before griddepcontrol.wait
+  // f2 (W2 only; null out = off): the epilogue also performs a7.  After a tile's y2
+  // rows are stored, each row bumps its (token, 128-column block) arrival counter; the
+  // tile that completes a block (k + has_shared arrivals) sums that token's rows for
+  // the block's 128 columns exactly as k_combine does and writes out.
+  uint16_t* out;            // [T][N] bf16
+  const int32_t* perm_src;  // [R] packed row -> routed row t*k+j
+  const int32_t* inv;       // [R] routed row -> packed row
+  const float* cw;          // [T][k] routing weights
+  int32_t* cnt;             // [T][N/128] arrival counters, zero before the launch
+  int T, k, has_shared;
 };
 
 // Quads (4 sub-tiles = 512 K elements) of scale bytes the scale-factor warp keeps in
@@ -93,7 +103,9 @@ struct GemmCfg {
   // drain[issuer] (the abort path's wait for MMAs already issued)
   static constexpr int kNumBars = (kIssuers + 2) * STAGES + 4 + kIssuers;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kSmemBytes = kOffMisc + 16;
+  // f2's list of the tokens a tile completed: [count, tokens...]
+  static constexpr int kOffFc = kOffMisc + 16;
+  static constexpr int kSmemBytes = kOffFc + 4 * (BN_MAX + 1);
   static constexpr int kSfCols = 4 * (KO + kSfbAtoms);      // TMEM columns per stage
   static constexpr int kTmemNeed = 2 * kAccCols + STAGES * kSfCols;
   static constexpr int kTmemCols =
@@ -119,6 +131,60 @@ __device__ __forceinline__ uint32_t idesc_mxf4_e4m3(int n) {
   d |= 1u << 23;                              // scale factor type: E8M0
   d |= static_cast<uint32_t>(128 >> 4) << 24; // M >> 4
   return d;
+}
+
+__device__ __forceinline__ void epilogue_bar_sync() {
+  asm volatile("bar.sync 1, 128;" ::: "memory");  // warps 4-7 only
+}
+
+// f2: the combine for the tokens whose (token, block nt) this tile completed.  et:
+// the epilogue thread (0..127) = column nt*128 + et.  Called by all 128 epilogue
+// threads after their y2 stores of the tile.
+__device__ __forceinline__ void fused_combine_tile(const GemmParams& p, int row0, int rows,
+                                                   int nt, int et, int* fc) {
+  const int R = p.T * p.k;
+  const int Rs = R + (p.has_shared ? p.T : 0);
+  const int need = p.k + (p.has_shared ? 1 : 0);
+  const int nblk = p.N / 128;
+  if (et == 0) fc[0] = 0;
+  __threadfence();  // release: this thread's y2 stores of the tile, device-wide
+  epilogue_bar_sync();
+  for (int rl = et; rl < rows; rl += 128) {
+    const int r = row0 + rl;
+    const int t = r < R ? p.perm_src[r] / p.k : r - R;
+    if (t < 0 || t >= p.T) {
+      set_status(p.status, STATUS_BAD_INDEX);
+      continue;
+    }
+    if (atomicAdd(&p.cnt[static_cast<size_t>(t) * nblk + nt], 1) == need - 1)
+      fc[1 + atomicAdd(&fc[0], 1)] = t;
+  }
+  epilogue_bar_sync();
+  const int nc = fc[0];
+  if (nc > 0) __threadfence();  // acquire: the other tiles' rows of the completed tokens
+  const int col = nt * 128 + et;
+  for (int i = 0; i < nc; ++i) {
+    const int t = fc[1 + i];
+    float acc = 0.f;  // k_combine's order: fp32 fma in j order, then the shared row
+    for (int j = 0; j < p.k; ++j) {
+      const int r = p.inv[static_cast<size_t>(t) * p.k + j];
+      if (r < 0 || r >= Rs) {
+        set_status(p.status, STATUS_BAD_INDEX);
+        continue;
+      }
+      const float yv = __uint_as_float(static_cast<uint32_t>(
+                                           __ldcg(p.y + static_cast<size_t>(r) * p.N + col))
+                                       << 16);
+      acc = fmaf(p.cw[static_cast<size_t>(t) * p.k + j], yv, acc);
+    }
+    if (p.has_shared)
+      acc += __uint_as_float(static_cast<uint32_t>(
+                                 __ldcg(p.y + static_cast<size_t>(R + t) * p.N + col))
+                             << 16);
+    const __nv_bfloat16 o = __float2bfloat16_rn(acc);
+    p.out[static_cast<size_t>(t) * p.N + col] = *reinterpret_cast<const uint16_t*>(&o);
+  }
+  epilogue_bar_sync();  // the list is reused by the next tile
 }
 
 __device__ __forceinline__ uint32_t u4_comp(const uint4& v, int t) {
@@ -580,6 +646,8 @@ __global__ void __launch_bounds__(256, OCC)
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[b]);
       ++tc;
+      if (p.out) fused_combine_tile(p, row0, rows, nt, q * 32 + lane,
+                                    reinterpret_cast<int*>(smem + C::kOffFc));
     }
   }
 
@@ -730,6 +798,14 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& a, cudaStream_t st) {
   p.G = a.G;
   p.rows_total = a.rows_total;
   p.status = a.status;
+  p.out = a.out;
+  p.perm_src = a.perm_src;
+  p.inv = a.inv;
+  p.cw = a.cw;
+  p.cnt = a.cnt;
+  p.T = a.T;
+  p.k = a.k;
+  p.has_shared = a.has_shared;
   // A list whose groups cannot exist (no group has more than max_group_rows rows) is
   // provably empty and not launched.
   // The first launch inherits the caller's word on the plan; each later variant

@@ -20,19 +20,23 @@
 // kind::f16 MMAs accumulate those exact products in fp32, as the MXFP4 path does; the
 // tensor scale multiplies the fp32 sum in the epilogue before the bf16 rounding.
 //
-// Design (per CTA, one per SM, 16 warps):
+// Design (per CTA, one per SM, 8 + 4 NG warps):
 //   * warp 0: TMA of the packed codes (0.5 B / weight, 128B- or 64B-swizzled so the
 //     converters read them without bank conflicts) and the E4M3 scales of a K stage
 //     -- the weights cross HBM in their 0.5625 B / weight NVFP4 form;
 //   * warp 2: TMA of the bf16 token rows of the stage (their own ring);
-//   * warps 4-11: converters.  Warp w owns TMEM lanes 32 (w % 4) .. +31 (one weight
-//     row per thread) and half (w - 4) / 4 of the stage's K; it decodes its codes to
-//     bf16 with byte-permute table lookups, multiplies by the block scale (exact) and
-//     writes them into TMEM with tcgen05.st: the MMA's A operand lives in tensor
-//     memory, so the dequantised weights never pass through shared memory;
+//   * warps 4 .. 4 + 4 NG - 1: NG converter groups of four warps.  Group g converts the
+//     K stages it with it % NG == g, so NG stages are decoded at once; warp w of a group
+//     owns TMEM lanes 32 (w % 4) .. +31 (one weight row per thread).  A thread decodes
+//     its row's KS codes to bf16 -- two codes (one byte) per lookup in a 256-entry
+//     shared-memory table of bf16 pairs, replicated per lane so the lookups never
+//     conflict (or, where shared memory is short, with byte-permute lookups of two
+//     8-entry byte tables) -- multiplies them by the block scale (exact) and writes
+//     them into TMEM with tcgen05.st: the MMA's A operand lives in tensor memory, so
+//     the dequantised weights never pass through shared memory;
 //   * warp 1 (and warp 3 in the small variant): MMA issue, tcgen05.mma kind::f16 with
 //     A from TMEM and B (tokens) from shared memory, fp32 accumulators in TMEM;
-//   * warps 12-15: epilogue (TMEM -> registers, x tensor scale, -> bf16 rows).
+//   * the last four warps: epilogue (TMEM -> registers, x tensor scale, -> bf16 rows).
 // Every wait is bounded; an expired wait sets a status bit and the CTA unwinds.
 #include "kernels.cuh"
 
@@ -53,8 +57,9 @@ struct NvParams {
 
 // BN: token tile; KS: K elements per stage; CS: code/scale ring slots; NA: token ring
 // slots = TMEM A buffers; ACC: accumulator buffers; ISS: MMA-issuing threads (each
-// takes every ISS-th stage of a tile into its own accumulator).
-template <int BN, int KS, int CS, int NA, int ACC, int ISS>
+// takes every ISS-th stage of a tile into its own accumulator); NG: converter groups;
+// LUT: decode through the shared-memory table (else byte permutes).
+template <int BN, int KS, int CS, int NA, int ACC, int ISS, int NG, bool LUT>
 struct NvCfg {
   static constexpr int kCodeBytes = 128 * (KS / 2);  // [128 rows][KS/2 B], swizzled
   static constexpr int kScaleBytes = 128 * 16;       // [128 rows][16 B] (256 K of scales)
@@ -67,20 +72,27 @@ struct NvCfg {
   // acc_full[ACC], acc_empty[ACC], drain[ISS]
   static constexpr int kNumBars = 2 * CS + NA + ISS * NA + NA + 2 * ACC + ISS;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kSmemBytes = kOffMisc + 16;
+  // decode table: 256 code bytes x 32 lanes x one bf16 pair (entry b of lane l at word
+  // b * 32 + l: every lane reads its own bank)
+  static constexpr int kOffLut = (kOffMisc + 16 + 127) / 128 * 128;
+  static constexpr int kLutBytes = LUT ? 256 * 32 * 4 : 0;
+  static constexpr int kSmemBytes = kOffLut + kLutBytes;
   static constexpr int kAccCols = ISS * BN;          // one accumulator buffer
   static constexpr int kACols = KS / 2;              // bf16 pairs per A buffer row
   static constexpr int kTmemNeed = ACC * kAccCols + NA * kACols;
   static constexpr int kTmemCols = kTmemNeed <= 256 ? 256 : 512;
-  static constexpr int kConvWarps = 8;
-  static constexpr int kHalfK = KS / 2;              // K elements per converter thread
-  static constexpr int kBlocks = kHalfK / 16;        // E4M3 scale blocks per thread
+  static constexpr int kWarps = 8 + 4 * NG;          // 4 control, 4 NG converters, 4 epilogue
+  static constexpr int kThreads = 32 * kWarps;
+  static constexpr int kEpiWarp0 = 4 + 4 * NG;
+  static constexpr int kBlocks = KS / 16;            // E4M3 scale blocks per thread per stage
   static_assert(BN % 16 == 0 && BN <= 256, "token tile");
   static_assert(KS == 128 || KS == 256, "stage K");
   static_assert(kTmemNeed <= 512, "TMEM");
   static_assert(kSmemBytes + 1024 <= 232448, "shared memory");
   static_assert(kCodeBytes % 1024 == 0 && kTokBytes % 1024 == 0, "tile alignment");
   static_assert(ISS == 1 || ISS == 2, "issuers");
+  static_assert(KS == 128 || !LUT, "the table-decoding converter takes 128-K stages");
+  static_assert(kThreads <= 1024, "threads");
 };
 
 // Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, M = 128.
@@ -128,11 +140,11 @@ __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, __nv_bfloat162 s) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-template <int BN, int KS, int CS, int NA, int ACC, int ISS>
-__global__ void __launch_bounds__(512, 1)
+template <int BN, int KS, int CS, int NA, int ACC, int ISS, int NG, bool LUT>
+__global__ void __launch_bounds__(NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>::kThreads, 1)
     k_gemm_nv(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmS,
               const __grid_constant__ CUtensorMap tmX, const NvParams p) {
-  using C = NvCfg<BN, KS, CS, NA, ACC, ISS>;
+  using C = NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>;
   extern __shared__ __align__(1024) uint8_t smem[];
   if ((smem_u32(smem) & 1023u) != 0) {
     if (threadIdx.x == 0) set_status(p.status, STATUS_BAD_PLAN);
@@ -154,12 +166,12 @@ __global__ void __launch_bounds__(512, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < CS; ++s) {
       mbar_init(&code_full[s], 1);                 // TMA (+tx)
-      mbar_init(&code_empty[s], C::kConvWarps);    // every converter warp read its part
+      mbar_init(&code_empty[s], 4);                // the converting group's four warps
     }
     for (int s = 0; s < NA; ++s) {
       mbar_init(&tok_full[s], 1);                  // TMA (+tx)
       mbar_init(&mma_done[s], 1);                  // tcgen05.commit
-      for (int i = 0; i < ISS; ++i) mbar_init(&conv_full[i * NA + s], C::kConvWarps);
+      for (int i = 0; i < ISS; ++i) mbar_init(&conv_full[i * NA + s], 4);
     }
     for (int b = 0; b < ACC; ++b) {
       mbar_init(&acc_full[b], ISS);
@@ -171,6 +183,15 @@ __global__ void __launch_bounds__(512, 1)
     tma_prefetch_desc(&tmC);
     tma_prefetch_desc(&tmS);
     tma_prefetch_desc(&tmX);
+  }
+  if constexpr (LUT) {
+    // the decode table: entry b = the bf16 pair of code byte b (low nibble first)
+    uint32_t* lut = reinterpret_cast<uint32_t*>(smem + C::kOffLut);
+    for (int i = threadIdx.x; i < 256 * 32; i += C::kThreads) {
+      uint32_t o[4];
+      e2m1x8_to_bf16(static_cast<uint32_t>(i >> 5), o);
+      lut[i] = o[0];
+    }
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
   tc_fence_before();
@@ -289,18 +310,22 @@ __global__ void __launch_bounds__(512, 1)
         ++tc;
       }
     }
-  } else if (warp >= 4 && warp < 4 + C::kConvWarps) {
+  } else if (warp >= 4 && warp < C::kEpiWarp0) {
     // ------------------------------------------------------------ converters
     const int q = warp & 3;            // TMEM lane quarter = weight rows 32q .. 32q+31
-    const int h = (warp - 4) >> 2;     // half of the stage's K
+    const int cg = (warp - 4) >> 2;    // converter group: stages it with it % NG == cg
     const int r = q * 32 + lane;       // weight row within the tile
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    const uint32_t* lut = reinterpret_cast<const uint32_t*>(smem + C::kOffLut) + lane;
     uint32_t it = 0;
     bool ok = true;
     for (long long L = blockIdx.x; L < total && ok && !*abort_flag; L += gridDim.x) {
       int g, row0, rows, nt;
-      if (!load_item(L, g, row0, rows, nt)) continue;
+      if (!load_item(L, g, row0, rows, nt)) {
+        continue;
+      }
       for (int kb = 0; kb < nk; ++kb, ++it) {
+        if (static_cast<int>(it % NG) != cg) continue;
         const int cs = it % CS, s = it % NA;
         // the TMEM A buffer of this stage is free once the MMAs of stage it - NA are
         // done (their commit); the code slot once its TMA has landed
@@ -316,23 +341,22 @@ __global__ void __launch_bounds__(512, 1)
         }
         tc_fence_after();
         const uint8_t* cbase = smem + C::kOffCode + cs * C::kCodeStage;
-        // this thread's codes: row r, bytes [h * KS/4, (h+1) * KS/4) of its KS/2-byte
-        // row, in 16-byte chunks stored at chunk ^ swizzle(r)
-        constexpr int kChunks = KS / 64;  // 16-byte chunks per thread
+        // this thread's codes: row r of KS/2 bytes, in 16-byte chunks stored at
+        // chunk ^ swizzle(r)
+        constexpr int kChunks = KS / 32;
         uint4 cw[kChunks];
 #pragma unroll
         for (int j = 0; j < kChunks; ++j) {
-          const int chunk = h * kChunks + j;
-          const int phys = KS == 256 ? (chunk ^ (r & 7)) : (chunk ^ ((r >> 1) & 3));
+          const int phys = KS == 256 ? (j ^ (r & 7)) : (j ^ ((r >> 1) & 3));
           cw[j] = *reinterpret_cast<const uint4*>(cbase + r * (KS / 2) + phys * 16);
         }
         // this thread's scale bytes: row r of the 16-byte scale row; a 128-K stage uses
-        // half of the 256 K it covers
+        // the half of the 256 K it covers
         const uint4 sv = *reinterpret_cast<const uint4*>(cbase + C::kCodeBytes + r * 16);
-        const int sbyte0 = (KS == 128 ? (kb & 1) * 8 : 0) + h * C::kBlocks;
+        const int sbyte0 = KS == 128 ? (kb & 1) * 8 : 0;
         __syncwarp();
         if (lane == 0) mbar_arrive(&code_empty[cs]);
-        const uint32_t col0 = a_base + s * C::kACols + h * (C::kHalfK / 2);
+        const uint32_t col0 = a_base + s * C::kACols;
 #pragma unroll
         for (int blk = 0; blk < C::kBlocks; ++blk) {
           const int sb = sbyte0 + blk;
@@ -342,13 +366,22 @@ __global__ void __launch_bounds__(512, 1)
           const uint4 cv = cw[blk >> 1];
           const uint32_t w0 = (blk & 1) ? cv.z : cv.x;
           const uint32_t w1 = (blk & 1) ? cv.w : cv.y;
-          uint32_t o[8], t[4];
-          e2m1x8_to_bf16(w0, t);
+          uint32_t o[8];
+          if constexpr (LUT) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) o[i] = bf16x2_mul(t[i], sc);
-          e2m1x8_to_bf16(w1, t);
+            for (int i = 0; i < 4; ++i) {
+              o[i] = bf16x2_mul(lut[__byte_perm(w0, 0u, 0x4440u | i) << 5], sc);
+              o[4 + i] = bf16x2_mul(lut[__byte_perm(w1, 0u, 0x4440u | i) << 5], sc);
+            }
+          } else {
+            uint32_t t[4];
+            e2m1x8_to_bf16(w0, t);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) o[4 + i] = bf16x2_mul(t[i], sc);
+            for (int i = 0; i < 4; ++i) o[i] = bf16x2_mul(t[i], sc);
+            e2m1x8_to_bf16(w1, t);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) o[4 + i] = bf16x2_mul(t[i], sc);
+          }
           tmem_st_32x32b_x8(lane_base + col0 + blk * 8, o);
         }
         tmem_st_wait();
@@ -364,7 +397,7 @@ __global__ void __launch_bounds__(512, 1)
         if (lane == 0) mbar_arrive(&conv_full[(ISS == 2 ? (kb & 1) : 0) * NA + s]);
       }
     }
-  } else if (warp >= 12) {
+  } else if (warp >= C::kEpiWarp0) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
     uint32_t tc = 0;
@@ -430,10 +463,10 @@ __global__ void __launch_bounds__(512, 1)
 
 // ---------------------------------------------------------------- host side -------
 
-template <int BN, int KS, int CS, int NA, int ACC, int ISS>
+template <int BN, int KS, int CS, int NA, int ACC, int ISS, int NG, bool LUT>
 cudaError_t launch_nv_one(const NvGemmLaunch& a, int v, cudaStream_t st) {
-  using C = NvCfg<BN, KS, CS, NA, ACC, ISS>;
-  auto kern = k_gemm_nv<BN, KS, CS, NA, ACC, ISS>;
+  using C = NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>;
+  auto kern = k_gemm_nv<BN, KS, CS, NA, ACC, ISS, NG, LUT>;
   const int max_items = a.max_items[v];
   const long long tiles = static_cast<long long>(max_items) * (a.N / 128);
   if (tiles == 0) return cudaSuccess;
@@ -466,7 +499,7 @@ cudaError_t launch_nv_one(const NvGemmLaunch& a, int v, cudaStream_t st) {
   p.rows_total = a.rows_total;
   p.status = a.status;
   const int grid = static_cast<int>(tiles < sms ? tiles : sms);
-  return launch_k(kern, grid, 512, C::kSmemBytes, st, tmC, tmS, tmX, p);
+  return launch_k(kern, grid, C::kThreads, C::kSmemBytes, st, tmC, tmS, tmX, p);
 }
 
 }  // namespace
@@ -518,20 +551,22 @@ int nv_encode_maps(const NvGemmLaunch& a, int ks, int bn, CUtensorMap* tmC, CUte
   return MOE_OK;
 }
 
-// Variants by the tile plan's lists (same row bounds as the MXFP4 GEMM's):
-//   small  rows <= 16:  256-K stages, 6 code slots, 3 token/TMEM slots, 2 issuers;
-//   medium rows <= 64:  256-K stages, 4 code slots, 3 token/TMEM slots;
-//   mid    rows <= 128: 256-K stages, 3 code slots, 2 token/TMEM slots;
-//   large  rows <= 240: 128-K stages (a 240-row bf16 token tile is 60 KB per 128 K),
-//          3 slots, one accumulator (240 of TMEM's 512 columns).
+// Variants by the tile plan's lists (same row bounds as the MXFP4 GEMM's); 128-K
+// stages, four converter groups (three in the large variant):
+//   small  rows <= 16:  8 code slots, 7 token/TMEM slots, 2 issuers, table decoding;
+//   medium rows <= 64:  6 code slots, 5 token/TMEM slots, table decoding;
+//   mid    rows <= 128: 4 code slots, 4 token/TMEM slots, table decoding;
+//   large  rows <= 240: 3 slots (a 240-row bf16 token tile is 60 KB per 128 K), one
+//          accumulator (240 of TMEM's 512 columns), byte-permute decoding (no shared
+//          memory left for the table).
 cudaError_t launch_grouped_gemm_nv(const NvGemmLaunch& a, cudaStream_t st) {
-  cudaError_t e = launch_nv_one<kSmallBN, 256, 6, 3, 2, 2>(a, 0, st);
+  cudaError_t e = launch_nv_one<kSmallBN, 128, 8, 7, 2, 2, 4, true>(a, 0, st);
   if (e != cudaSuccess || a.max_group_rows <= kSmallBN) return e;
-  e = launch_nv_one<kMediumBN, 256, 4, 3, 2, 1>(a, 1, st);
+  e = launch_nv_one<kMediumBN, 128, 6, 5, 2, 1, 4, true>(a, 1, st);
   if (e != cudaSuccess || a.max_group_rows <= kMediumBN) return e;
-  e = launch_nv_one<kMidBN, 256, 3, 2, 2, 1>(a, 2, st);
+  e = launch_nv_one<kMidBN, 128, 4, 4, 2, 1, 4, true>(a, 2, st);
   if (e != cudaSuccess || a.max_group_rows <= kMidBN) return e;
-  return launch_nv_one<kLargeBN, 128, 3, 3, 1, 1>(a, 3, st);
+  return launch_nv_one<kLargeBN, 128, 3, 3, 1, 1, 3, false>(a, 3, st);
 }
 
 }  // namespace moe

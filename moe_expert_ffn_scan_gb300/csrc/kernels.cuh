@@ -68,9 +68,10 @@ cudaError_t launch_prep_small(const float* logits, int T, int E, int k, int has_
                               int32_t* idx, float* w, int32_t* counts, int32_t* offsets,
                               int32_t* perm_src, int32_t* inv, PlanOut plan, uint32_t* status,
                               cudaStream_t st);
+// cnt (nullable): [T][H/128] arrival counters of a combine-fused W2 GEMM, zeroed here.
 cudaError_t launch_quant_scatter(const uint16_t* x, int T, int H, int k, int has_shared,
                                  const int32_t* inv, uint8_t* xq, uint8_t* xs, uint8_t* xg,
-                                 uint8_t* xsg, uint32_t* status, cudaStream_t st);
+                                 uint8_t* xsg, int32_t* cnt, uint32_t* status, cudaStream_t st);
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* idx, float* w,
                          uint32_t* clear_status, cudaStream_t st);
 int perm_blocks(int T);
@@ -115,6 +116,14 @@ struct GemmLaunch {
   // (its producer ran two or more launches earlier): the weight loads of each CTA's
   // first stages then go out before the wait for the preceding kernel.
   int early_plan;
+  // f2 (the W2 GEMM only): with out non-null the epilogue also performs the weighted
+  // top-k combine + shared add into out [T][N]; cnt [T][N/128] must be zero.
+  uint16_t* out = nullptr;
+  const int32_t* perm_src = nullptr;
+  const int32_t* inv = nullptr;
+  const float* cw = nullptr;
+  int32_t* cnt = nullptr;
+  int T = 0, k = 0, has_shared = 0;
 };
 cudaError_t launch_grouped_gemm(const GemmLaunch& a, cudaStream_t st);
 
