@@ -671,6 +671,368 @@ __global__ void __launch_bounds__(256, OCC)
   }
 }
 
+// ---------------------------------------------------------------- SM pairs ---------
+// The mid and large tiles on SM pairs (a cluster of two CTAs, cta_group::2 MMAs): one
+// MMA covers 256 weight rows, CTA r of the pair holding rows 128 r .. 128 r + 127 of
+// the pair's weight tile, the accumulator of those rows in its TMEM, and half of the
+// token tile (tokens r * bn/2 .. of the item's bn); the even-ranked CTA issues the
+// MMAs.  Against one CTA per tile this halves the MMA instructions per flop and the
+// token bytes each SM stages per stage, which leaves shared memory for a third stage.
+//   * both CTAs load their weight and token halves by TMA, completing on the leader's
+//     full barrier (the leader expects the bytes of all four loads);
+//   * both stage their scale factors (own weight rows; SFB_FULL: the item's whole token
+//     range in each CTA, else each CTA its own token half) and arrive on the leader's
+//     scale barrier; the leader copies both CTAs' scales to their TMEM (tcgen05.cp for
+//     the pair), then issues the MMAs;
+//   * MMA completion is multicast to both CTAs' empty / accumulator-full barriers; both
+//     epilogues arrive on the leader's accumulator-empty barrier.
+template <int BN2, int STAGES, bool SFB_FULL>
+struct GemmCfg2 {
+  static constexpr int KO = 2;
+  static constexpr int BH = BN2 / 2;              // token rows per CTA
+  static constexpr int kASub = 128 * 128;
+  static constexpr int kBSub = BH * 128;
+  static constexpr int kABytes = KO * kASub;
+  static constexpr int kBBytes = KO * kBSub;
+  static constexpr int kSfbAtoms = SFB_FULL ? (BN2 + 127) / 128 : (BH + 127) / 128;
+  // wide scale staging (every 32-row atom written four times, one tcgen05.cp.128xNb per
+  // operand and stage; see GemmCfg)
+  static constexpr int kSfaStage = KO * 2048;
+  static constexpr int kSfbStage = kSfbAtoms * 2048;
+  static constexpr int kSfTotal = STAGES * (kSfaStage + kSfbStage);
+  static constexpr int kOffSfa = 0;
+  static constexpr int kOffSfb = STAGES * kSfaStage;
+  static constexpr int kOffA = (kSfTotal + 1023) / 1024 * 1024;
+  static constexpr int kOffB = kOffA + STAGES * kABytes;
+  static constexpr int kOffBar = kOffB + STAGES * kBBytes;
+  // full[S] (leader: 1 + tx), empty[S] (1: multicast commit), sf_full[S] (leader: 2),
+  // acc_full[2] (1: multicast commit), acc_empty[2] (leader: 8 epilogue warps), drain
+  static constexpr int kNumBars = 3 * STAGES + 5;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmemBytes = kOffMisc + 16;
+  static constexpr int kSfCols = 4 * (KO + kSfbAtoms);
+  static constexpr int kTmemNeed = 2 * BN2 + STAGES * kSfCols;
+  static constexpr int kTmemCols = kTmemNeed <= 256 ? 256 : 512;
+  static constexpr uint32_t kTxBytes = 2u * (KO * kWeightTileTxBytes + kBBytes);
+  static_assert(BN2 % 32 == 0 && BN2 <= 256, "token tile: two halves of multiples of 16");
+  static_assert(kSfbAtoms <= 2, "wide scale copies move <= 256 bits");
+  static_assert(kTmemNeed <= 512, "TMEM");
+  static_assert(kSmemBytes <= 232448, "dynamic shared memory of one CTA");
+};
+
+// Instruction descriptor of the pair MMA: as idesc_mxf4_e4m3 with M = 256.
+__device__ __forceinline__ uint32_t idesc_mxf4_e4m3_m256(int n) {
+  uint32_t d = 0;
+  d |= 5u << 7;
+  d |= 0u << 10;
+  d |= static_cast<uint32_t>(n >> 3) << 17;
+  d |= 1u << 23;
+  d |= static_cast<uint32_t>(256 >> 4) << 24;
+  return d;
+}
+
+template <int BN2, int STAGES, bool SFB_FULL>
+__global__ void __launch_bounds__(256, 1)
+    k_gemm_mx2(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+               const GemmParams p) {
+  using C = GemmCfg2<BN2, STAGES, SFB_FULL>;
+  constexpr int KO = C::KO;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* full = bars;
+  uint64_t* empty = full + STAGES;
+  uint64_t* sf_full = empty + STAGES;
+  uint64_t* acc_full = sf_full + STAGES;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+      mbar_init(&sf_full[s], 2);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 8);
+    }
+    mbar_init(drain, 1);
+    // the 128B-swizzled tiles need 1024-byte alignment: checked, and a misaligned base
+    // turns every role into a no-op (the CTA still takes part in the pair's set-up and
+    // teardown, which its peer waits for)
+    const bool bad = (smem_u32(smem) & 1023u) != 0;
+    *abort_flag = bad ? 1 : 0;
+    if (bad) set_status(p.status, STATUS_BAD_PLAN);
+    fence_mbar_init();
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmX);
+  }
+  if (warp == 1) tmem_alloc_pair(tmem_slot, C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the peer's barriers exist before any remote arrive or multicast
+  tc_fence_after();
+  pdl_wait();
+  const uint32_t tmem = *tmem_slot;
+
+  const int n_tiles2 = p.N / 256;
+  const int nk = p.K / (128 * KO);
+  int count = *p.item_count;
+  if (count > p.max_items) {
+    if (threadIdx.x == 0) set_status(p.status, STATUS_BAD_PLAN);
+    count = p.max_items;
+  }
+  const long long total = static_cast<long long>(count) * n_tiles2;
+  const long long cl = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+  auto load_item = [&](long long L, int& g, int& row0, int& rows, int& nt2) -> bool {
+    const int4 it = p.items[L / n_tiles2];
+    nt2 = static_cast<int>(L % n_tiles2);
+    g = it.x;
+    row0 = it.y;
+    rows = it.z;
+    if (rows <= 0) return false;
+    if (g < 0 || g >= p.G || row0 < 0 || rows > BN2 || row0 + rows > p.rows_total) {
+      if (threadIdx.x == 0) set_status(p.status, STATUS_BAD_PLAN);
+      return false;
+    }
+    return true;
+  };
+  // the leader's copies of the barriers the peer completes
+  auto leader_addr = [&](const uint64_t* b) -> uint32_t { return mapa_shared(smem_u32(b), 0); };
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- weight TMA
+    if (lane == 0) {
+      uint32_t it = 0;
+      for (long long L = cl; L < total && !*abort_flag; L += ncl) {
+        int g, row0, rows, nt2;
+        if (!load_item(L, g, row0, rows, nt2)) continue;
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % STAGES;
+          if (it >= STAGES &&
+              !mbar_wait(&empty[s], ((it / STAGES) & 1u) ^ 1u, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (leader) mbar_arrive_expect_tx(&full[s], C::kTxBytes);
+          tma_load_4d_pair(smem + C::kOffA + s * C::kABytes, &tmW, leader_addr(&full[s]), 0,
+                           (nt2 * 2 + static_cast<int>(rank)) * 128, kb * KO, g);
+        }
+        if (!ok) break;
+      }
+    }
+  } else if (warp == 3) {
+    // ---------------------------------------------------------------- token TMA
+    if (lane == 0) {
+      uint32_t it = 0;
+      for (long long L = cl; L < total && !*abort_flag; L += ncl) {
+        int g, row0, rows, nt2;
+        if (!load_item(L, g, row0, rows, nt2)) continue;
+        const int half = ((rows + 15) & ~15) >> 1;
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % STAGES;
+          if (it >= STAGES &&
+              !mbar_wait(&empty[s], ((it / STAGES) & 1u) ^ 1u, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tma_load_3d_pair(smem + C::kOffB + s * C::kBBytes, &tmX, leader_addr(&full[s]), 0,
+                           row0 + static_cast<int>(rank) * half, kb * KO);
+        }
+        if (!ok) break;
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (leader && lane == 0) {
+      uint32_t it = 0, tc = 0;
+      for (long long L = cl; L < total && !*abort_flag; L += ncl) {
+        int g, row0, rows, nt2;
+        if (!load_item(L, g, row0, rows, nt2)) continue;
+        const int bn = (rows + 15) & ~15;
+        const uint32_t b = tc & 1u, use = tc >> 1;
+        if (tc >= 2 && !mbar_wait(&acc_empty[b], (use - 1) & 1u, p.status, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + b * BN2;
+        const uint32_t idesc = idesc_mxf4_e4m3_m256(bn);
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1u;
+          if (!mbar_wait(&sf_full[s], ph, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sf_t = tmem + 2 * BN2 + s * C::kSfCols;
+          const uint32_t sfb_t = sf_t + 4 * KO;
+          const uint64_t da = smem_desc(smem_u32(smem + C::kOffSfa + s * C::kSfaStage), 2048, 128,
+                                        kLayoutNone);
+          const uint64_t db = smem_desc(smem_u32(smem + C::kOffSfb + s * C::kSfbStage), 2048, 128,
+                                        kLayoutNone);
+          tc_cp_128x256b_pair(sf_t, da);
+          if (C::kSfbAtoms == 2) tc_cp_128x256b_pair(sfb_t, db);
+          else tc_cp_128x128b_pair(sfb_t, db);
+          if (!mbar_wait(&full[s], ph, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smem + C::kOffA + s * C::kABytes);
+          const uint32_t b0 = smem_u32(smem + C::kOffB + s * C::kBBytes);
+#pragma unroll
+          for (int ko = 0; ko < KO; ++ko) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = smem_desc(a0 + ko * C::kASub + kk * 32, 0, 1024, kLayoutSw128);
+              const uint64_t bd = smem_desc(b0 + ko * C::kBSub + kk * 32, 0, 1024, kLayoutSw128);
+              const uint32_t id = idesc | (static_cast<uint32_t>(kk) << 29) |
+                                  (static_cast<uint32_t>(ko) << 4);
+              mma_mxf8f6f4_pair(d_tmem, ad, bd, id, sf_t + 4 * ko, sfb_t,
+                                kb > 0 || ko != 0 || kk != 0);
+            }
+          }
+          tc_commit_pair_mc(&empty[s], 3);
+        }
+        if (!ok) break;
+        tc_commit_pair_mc(&acc_full[b], 3);
+        ++tc;
+      }
+    }
+  } else if (warp == 2) {
+    // ---------------------------------------------------------------- scale factors
+    // Weight atoms: this CTA's 128 rows (row r at byte (r % 32) * 16 + (r / 32) * 4 +
+    // kblock); token atoms: the item's tokens (SFB_FULL) or this CTA's half, token c of
+    // atom a at byte (c % 32) * 16 + ((c / 32) % 4) * 4 + ko.  Each 32-row atom is
+    // written four times (the wide layout: one 128-lane copy per operand).
+    constexpr int NA = C::kSfbAtoms;
+    const int kw = p.K / 32, kx = p.K / 128;
+    uint32_t it = 0;
+    for (long long L = cl; L < total && !*abort_flag; L += ncl) {
+      int g, row0, rows, nt2;
+      if (!load_item(L, g, row0, rows, nt2)) continue;
+      const int half = ((rows + 15) & ~15) >> 1;
+      const int t0 = SFB_FULL ? row0 : row0 + static_cast<int>(rank) * half;
+      const int tn = SFB_FULL ? rows : (rank == 0 ? (rows < half ? rows : half)
+                                                  : (rows - half > 0 ? rows - half : 0));
+      const uint8_t* wsp =
+          p.w_scales + (static_cast<size_t>(g) * p.N + (nt2 * 2 + static_cast<int>(rank)) * 128) *
+                           kw;
+      bool ok = true;
+      for (int kb = 0; kb < nk; ++kb, ++it) {
+        const int s = it % STAGES;
+        if (it >= STAGES) {
+          int w_ok = 1;
+          if (lane == 0)
+            w_ok = mbar_wait(&empty[s], ((it / STAGES) & 1u) ^ 1u, p.status, abort_flag);
+          if (!__shfl_sync(0xFFFFFFFFu, w_ok, 0)) {
+            ok = false;
+            break;
+          }
+        }
+#pragma unroll
+        for (int ko = 0; ko < KO; ++ko) {
+          uint32_t wa[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            wa[j] = __ldg(reinterpret_cast<const uint32_t*>(
+                wsp + static_cast<size_t>(j * 32 + lane) * kw + (kb * KO + ko) * 4));
+          const uint4 v = make_uint4(wa[0], wa[1], wa[2], wa[3]);
+#pragma unroll
+          for (int rep = 0; rep < 4; ++rep)
+            *reinterpret_cast<uint4*>(smem + C::kOffSfa + s * C::kSfaStage + ko * 2048 +
+                                      (rep * 32 + lane) * 16) = v;
+        }
+#pragma unroll
+        for (int a = 0; a < NA; ++a) {
+          uint32_t xb[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int c = a * 128 + j * 32 + lane;  // token index within the staged range
+            uint32_t packed = 0;
+#pragma unroll
+            for (int ko = 0; ko < KO; ++ko) {
+              uint32_t sb = 127u;
+              if (c < tn) sb = __ldg(p.x_scales + static_cast<size_t>(t0 + c) * kx + kb * KO + ko);
+              packed |= sb << (8 * ko);
+            }
+            xb[j] = packed;
+          }
+          const uint4 v = make_uint4(xb[0], xb[1], xb[2], xb[3]);
+#pragma unroll
+          for (int rep = 0; rep < 4; ++rep)
+            *reinterpret_cast<uint4*>(smem + C::kOffSfb + s * C::kSfbStage + a * 2048 +
+                                      (rep * 32 + lane) * 16) = v;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (leader) mbar_arrive(&sf_full[s]);
+          else mbar_arrive_cluster(leader_addr(&sf_full[s]));
+        }
+      }
+      if (!ok) break;
+    }
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------------- epilogue
+    const int q = warp - 4;
+    uint32_t tc = 0;
+    for (long long L = cl; L < total && !*abort_flag; L += ncl) {
+      int g, row0, rows, nt2;
+      if (!load_item(L, g, row0, rows, nt2)) continue;
+      const uint32_t b = tc & 1u, use = tc >> 1;
+      int w_ok = 1;
+      if (lane == 0) w_ok = mbar_wait(&acc_full[b], use & 1u, p.status, abort_flag);
+      if (!__shfl_sync(0xFFFFFFFFu, w_ok, 0)) break;
+      tc_fence_after();
+      const int n = (nt2 * 2 + static_cast<int>(rank)) * 128 + q * 32 + lane;
+      uint16_t* ycol = p.y + static_cast<size_t>(row0) * p.N + n;
+      const uint32_t acc = tmem + (static_cast<uint32_t>(q * 32) << 16) + b * BN2;
+      for (int c0 = 0; c0 < rows; c0 += 16) {
+        uint32_t r[16];
+        tmem_ld_32x32b_x16(acc + c0, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          if (c0 + i < rows) {
+            const __nv_bfloat16 h = __float2bfloat16_rn(__uint_as_float(r[i]));
+            ycol[static_cast<size_t>(c0 + i) * p.N] = *reinterpret_cast<const uint16_t*>(&h);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (leader) mbar_arrive(&acc_empty[b]);
+        else mbar_arrive_cluster(leader_addr(&acc_empty[b]));
+      }
+      ++tc;
+    }
+  }
+
+  // After an abort the leader's MMA thread waits (bounded) for the MMAs it issued.
+  if (warp == 1 && lane == 0 && leader && *abort_flag) {
+    tc_commit_pair_mc(drain, 1);
+    mbar_wait_drain(drain, 0);
+  }
+  pdl_trigger();
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // neither CTA releases TMEM or shared memory the pair still uses
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, C::kTmemCols);
+  }
+}
+
 // ---------------------------------------------------------------- host side -------
 
 EncodeTiledFn get_encode_tiled_fn() {
@@ -729,6 +1091,50 @@ cudaError_t launch_one(const CUtensorMap& tmW, const CUtensorMap& tmX, const Gem
   // variants wait for their predecessor the plain way.  The two-CTA-per-SM small and
   // medium variants keep the overlap.
   return launch_k_pdl(OCC > 1, kern, grid, 256, C::kSmemBytes, st, tmW, tmX, q);
+}
+
+// The pair kernel for one list: clusters of two CTAs, as many clusters as fit at once.
+template <int BN2, int STAGES, bool SFB_FULL>
+cudaError_t launch_pair(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmParams& p,
+                        int max_items, cudaStream_t st) {
+  using C = GemmCfg2<BN2, STAGES, SFB_FULL>;
+  auto kern = k_gemm_mx2<BN2, STAGES, SFB_FULL>;
+  static unsigned long long attr_ctx[64] = {};
+  static int max_clusters[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  const long long pairs = static_cast<long long>(max_items) * (p.N / 256);
+  if (pairs == 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const unsigned long long ctx = current_context_id();
+  if (ctx == 0 || attr_ctx[dev] != ctx) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(2 * (dev_info().sms / 2));
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    if (n < 1) return cudaErrorInvalidConfiguration;
+    max_clusters[dev] = n;
+    attr_ctx[dev] = current_context_id();
+  }
+  const long long clusters = pairs < max_clusters[dev] ? pairs : max_clusters[dev];
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
+  GemmParams q = p;
+  q.max_items = max_items;
+  return cudaLaunchKernelEx(&cfg, kern, tmW, tmX, q);
 }
 
 }  // namespace
@@ -818,6 +1224,22 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& a, cudaStream_t st) {
   e = launch_variant<kMediumBN, kMediumStages, kMediumStagesKO1, kMediumOcc>(
       a, p, a.items[1], a.item_counts + 1, a.max_items[1], st);
   if (e != cudaSuccess || a.max_group_rows <= kMediumBN) return e;
+  if (a.N % 256 == 0 && a.K % 256 == 0 && a.out == nullptr) {
+    // mid and large tiles on SM pairs (same kernel for both lists; the combine-fused
+    // W2 epilogue stays on the one-SM kernels)
+    CUtensorMap tmW, tmX;
+    if (gemm_encode_maps(a.w_codes, a.G, a.N, a.K, a.act, a.rows_total, 2, kPairBN / 2, &tmW,
+                         &tmX) != MOE_OK)
+      return cudaErrorInvalidValue;
+    GemmParams q = p;
+    q.items = a.items[2];
+    q.item_count = a.item_counts + 2;
+    e = launch_pair<kPairBN, kPairStages, kPairSfbFull>(tmW, tmX, q, a.max_items[2], st);
+    if (e != cudaSuccess || a.max_group_rows <= kMidBN) return e;
+    q.items = a.items[3];
+    q.item_count = a.item_counts + 3;
+    return launch_pair<kPairBN, kPairStages, kPairSfbFull>(tmW, tmX, q, a.max_items[3], st);
+  }
   e = launch_variant<kMidBN, kMidStages, kMidStagesKO1, 1>(a, p, a.items[2],
                                                            a.item_counts + 2, a.max_items[2], st);
   if (e != cudaSuccess || a.max_group_rows <= kMidBN) return e;

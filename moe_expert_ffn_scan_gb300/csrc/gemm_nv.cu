@@ -556,8 +556,8 @@ int nv_encode_maps(const NvGemmLaunch& a, int ks, int bn, CUtensorMap* tmC, CUte
 //   small  rows <= 16:  8 code slots, 7 token/TMEM slots, 2 issuers, table decoding;
 //   medium rows <= 64:  6 code slots, 5 token/TMEM slots, table decoding;
 //   mid    rows <= 128: 4 code slots, 4 token/TMEM slots, table decoding;
-//   large  rows <= 240: 3 slots (a 240-row bf16 token tile is 60 KB per 128 K), one
-//          accumulator (240 of TMEM's 512 columns), byte-permute decoding (no shared
+//   large  rows <= 224: 3 slots (a 224-row bf16 token tile is 56 KB per 128 K), one
+//          accumulator (224 of TMEM's 512 columns), byte-permute decoding (no shared
 //          memory left for the table).
 cudaError_t launch_grouped_gemm_nv(const NvGemmLaunch& a, cudaStream_t st) {
   cudaError_t e = launch_nv_one<kSmallBN, 128, 8, 7, 2, 2, 4, true>(a, 0, st);

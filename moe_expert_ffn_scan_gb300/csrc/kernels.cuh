@@ -32,10 +32,10 @@ cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
 // GEMM variants, chosen per group by its row count M (the tile plan):
 //   small  M <= 16: N = 16 tokens, 2 CTAs per SM, 3 stages of two 128-K sub-tiles;
 //   medium M <= 64: N <= 64, 2 CTAs per SM, 2 stages;
-//   larger M is cut into ceil(M / 240) near-equal chunks (multiples of 16 rows):
+//   larger M is cut into ceil(M / 224) near-equal chunks (multiples of 16 rows):
 //   mid    chunks of <= 128 rows: N <= 128, 1 CTA per SM, 3 stages;
-//   large  chunks of 129..240 rows: N <= 240 (an N = 240 MMA carries more tensor work
-//          than its issue cost), 1 CTA per SM, 2 stages (all the shared memory).
+//   large  chunks of 129..224 rows: N <= 224, 1 CTA per SM, 2 stages (all the shared
+//          memory).
 // With K/128 odd the stages hold one sub-tile (the *KO1 stage counts).
 constexpr int kSmallBN = 16;
 constexpr int kSmallStages = 3;
@@ -48,9 +48,15 @@ constexpr int kMediumOcc = 2;
 constexpr int kMidBN = 128;
 constexpr int kMidStages = 3;
 constexpr int kMidStagesKO1 = 5;
-constexpr int kLargeBN = 240;
+constexpr int kLargeBN = 224;
 constexpr int kLargeStages = 2;
 constexpr int kLargeStagesKO1 = 2;
+// Mid and large tiles on SM pairs (when N and K are multiples of 256): 224-token tiles
+// (112 per SM), three stages of two 128-K sub-tiles.  kPairSfbFull: each CTA's token
+// scale factors cover the item's whole token range (else only the CTA's half).
+constexpr int kPairBN = 224;
+constexpr int kPairStages = 3;
+constexpr bool kPairSfbFull = true;
 
 // The tile plan's work lists, one per variant (0 small, 1 medium, 2 mid, 3 large),
 // each {group, row0, rows, 0} in group order, and their lengths.
