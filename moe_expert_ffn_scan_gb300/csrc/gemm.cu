@@ -165,22 +165,28 @@ __device__ __forceinline__ void fused_combine_tile(const GemmParams& p, int row0
   const int col = nt * 128 + et;
   for (int i = 0; i < nc; ++i) {
     const int t = fc[1 + i];
-    float acc = 0.f;  // k_combine's order: fp32 fma in j order, then the shared row
-    for (int j = 0; j < p.k; ++j) {
-      const int r = p.inv[static_cast<size_t>(t) * p.k + j];
-      if (r < 0 || r >= Rs) {
-        set_status(p.status, STATUS_BAD_INDEX);
-        continue;
+    // every row's value is loaded before any is summed (their latencies overlap)
+    uint16_t v[17];
+    bool okr[17];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      okr[j] = false;
+      v[j] = 0;
+      if (j < p.k) {
+        const int r = p.inv[static_cast<size_t>(t) * p.k + j];
+        okr[j] = r >= 0 && r < Rs;
+        if (okr[j]) v[j] = __ldcg(p.y + static_cast<size_t>(r) * p.N + col);
+        else set_status(p.status, STATUS_BAD_INDEX);
       }
-      const float yv = __uint_as_float(static_cast<uint32_t>(
-                                           __ldcg(p.y + static_cast<size_t>(r) * p.N + col))
-                                       << 16);
-      acc = fmaf(p.cw[static_cast<size_t>(t) * p.k + j], yv, acc);
     }
-    if (p.has_shared)
-      acc += __uint_as_float(static_cast<uint32_t>(
-                                 __ldcg(p.y + static_cast<size_t>(R + t) * p.N + col))
-                             << 16);
+    v[16] = p.has_shared ? __ldcg(p.y + static_cast<size_t>(R + t) * p.N + col) : 0;
+    float acc = 0.f;  // k_combine's order: fp32 fma in j order, then the shared row
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (j < p.k && okr[j])
+        acc = fmaf(p.cw[static_cast<size_t>(t) * p.k + j],
+                   __uint_as_float(static_cast<uint32_t>(v[j]) << 16), acc);
+    if (p.has_shared) acc += __uint_as_float(static_cast<uint32_t>(v[16]) << 16);
     const __nv_bfloat16 o = __float2bfloat16_rn(acc);
     p.out[static_cast<size_t>(t) * p.N + col] = *reinterpret_cast<const uint16_t*>(&o);
   }
@@ -680,13 +686,13 @@ __global__ void __launch_bounds__(256, OCC)
 // token bytes each SM stages per stage, which leaves shared memory for a third stage.
 //   * both CTAs load their weight and token halves by TMA, completing on the leader's
 //     full barrier (the leader expects the bytes of all four loads);
-//   * both stage their scale factors (own weight rows; SFB_FULL: the item's whole token
-//     range in each CTA, else each CTA its own token half) and arrive on the leader's
-//     scale barrier; the leader copies both CTAs' scales to their TMEM (tcgen05.cp for
+//   * both stage their scale factors (own weight rows; the item's whole token range --
+//     each SM's MMA scales every token column from its own TMEM) and arrive on the
+//     leader's scale barrier; the leader copies both CTAs' scales to their TMEM (tcgen05.cp for
 //     the pair), then issues the MMAs;
 //   * MMA completion is multicast to both CTAs' empty / accumulator-full barriers; both
 //     epilogues arrive on the leader's accumulator-empty barrier.
-template <int BN2, int STAGES, bool SFB_FULL>
+template <int BN2, int STAGES>
 struct GemmCfg2 {
   static constexpr int KO = 2;
   static constexpr int BH = BN2 / 2;              // token rows per CTA
@@ -694,7 +700,7 @@ struct GemmCfg2 {
   static constexpr int kBSub = BH * 128;
   static constexpr int kABytes = KO * kASub;
   static constexpr int kBBytes = KO * kBSub;
-  static constexpr int kSfbAtoms = SFB_FULL ? (BN2 + 127) / 128 : (BH + 127) / 128;
+  static constexpr int kSfbAtoms = (BN2 + 127) / 128;  // the item's whole token range
   // wide scale staging (every 32-row atom written four times, one tcgen05.cp.128xNb per
   // operand and stage; see GemmCfg)
   static constexpr int kSfaStage = KO * 2048;
@@ -731,11 +737,11 @@ __device__ __forceinline__ uint32_t idesc_mxf4_e4m3_m256(int n) {
   return d;
 }
 
-template <int BN2, int STAGES, bool SFB_FULL>
+template <int BN2, int STAGES>
 __global__ void __launch_bounds__(256, 1)
     k_gemm_mx2(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                const GemmParams p) {
-  using C = GemmCfg2<BN2, STAGES, SFB_FULL>;
+  using C = GemmCfg2<BN2, STAGES>;
   constexpr int KO = C::KO;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t rank = cluster_ctarank();
@@ -909,76 +915,119 @@ __global__ void __launch_bounds__(256, 1)
   } else if (warp == 2) {
     // ---------------------------------------------------------------- scale factors
     // Weight atoms: this CTA's 128 rows (row r at byte (r % 32) * 16 + (r / 32) * 4 +
-    // kblock); token atoms: the item's tokens (SFB_FULL) or this CTA's half, token c of
-    // atom a at byte (c % 32) * 16 + ((c / 32) % 4) * 4 + ko.  Each 32-row atom is
-    // written four times (the wide layout: one 128-lane copy per operand).
+    // kblock); token atoms: the item's whole token range in both CTAs (the MMA scales
+    // every token column on both SMs from their own TMEM), token c of atom a at byte
+    // (c % 32) * 16 + ((c / 32) % 4) * 4 + ko.  Each 32-row atom is written four times
+    // (the wide layout: one 128-lane copy per operand).  Scale bytes are fetched a quad
+    // of 128-K sub-tiles (two stages) at a time, kSfQuads quads ahead of the stage
+    // being staged, so their latency overlaps the MMAs.
     constexpr int NA = C::kSfbAtoms;
+    constexpr int J = (BN2 + 31) / 32;
+    constexpr int Q = kSfQuads;
+    constexpr int SPQ = 4 / KO;  // stages per quad
     const int kw = p.K / 32, kx = p.K / 128;
-    uint32_t it = 0;
-    for (long long L = cl; L < total && !*abort_flag; L += ncl) {
-      int g, row0, rows, nt2;
-      if (!load_item(L, g, row0, rows, nt2)) continue;
-      const int half = ((rows + 15) & ~15) >> 1;
-      const int t0 = SFB_FULL ? row0 : row0 + static_cast<int>(rank) * half;
-      const int tn = SFB_FULL ? rows : (rank == 0 ? (rows < half ? rows : half)
-                                                  : (rows - half > 0 ? rows - half : 0));
-      const uint8_t* wsp =
-          p.w_scales + (static_cast<size_t>(g) * p.N + (nt2 * 2 + static_cast<int>(rank)) * 128) *
-                           kw;
-      bool ok = true;
-      for (int kb = 0; kb < nk; ++kb, ++it) {
-        const int s = it % STAGES;
-        if (it >= STAGES) {
-          int w_ok = 1;
-          if (lane == 0)
-            w_ok = mbar_wait(&empty[s], ((it / STAGES) & 1u) ^ 1u, p.status, abort_flag);
-          if (!__shfl_sync(0xFFFFFFFFu, w_ok, 0)) {
-            ok = false;
-            break;
-          }
-        }
-#pragma unroll
-        for (int ko = 0; ko < KO; ++ko) {
-          uint32_t wa[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            wa[j] = __ldg(reinterpret_cast<const uint32_t*>(
-                wsp + static_cast<size_t>(j * 32 + lane) * kw + (kb * KO + ko) * 4));
-          const uint4 v = make_uint4(wa[0], wa[1], wa[2], wa[3]);
-#pragma unroll
-          for (int rep = 0; rep < 4; ++rep)
-            *reinterpret_cast<uint4*>(smem + C::kOffSfa + s * C::kSfaStage + ko * 2048 +
-                                      (rep * 32 + lane) * 16) = v;
-        }
-#pragma unroll
-        for (int a = 0; a < NA; ++a) {
-          uint32_t xb[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int c = a * 128 + j * 32 + lane;  // token index within the staged range
-            uint32_t packed = 0;
-#pragma unroll
-            for (int ko = 0; ko < KO; ++ko) {
-              uint32_t sb = 127u;
-              if (c < tn) sb = __ldg(p.x_scales + static_cast<size_t>(t0 + c) * kx + kb * KO + ko);
-              packed |= sb << (8 * ko);
-            }
-            xb[j] = packed;
-          }
-          const uint4 v = make_uint4(xb[0], xb[1], xb[2], xb[3]);
-#pragma unroll
-          for (int rep = 0; rep < 4; ++rep)
-            *reinterpret_cast<uint4*>(smem + C::kOffSfb + s * C::kSfbStage + a * 2048 +
-                                      (rep * 32 + lane) * 16) = v;
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          if (leader) mbar_arrive(&sf_full[s]);
-          else mbar_arrive_cluster(leader_addr(&sf_full[s]));
+    const int nq = p.K / 512;
+    struct Pos {
+      long long L;
+      int kq, g, row0, rows, nt2;
+    };
+    auto seek = [&](long long L, Pos& P) -> bool {
+      for (; L < total; L += ncl) {
+        if (load_item(L, P.g, P.row0, P.rows, P.nt2)) {
+          P.L = L;
+          P.kq = 0;
+          return true;
         }
       }
-      if (!ok) break;
+      return false;
+    };
+    auto step = [&](Pos& P) -> bool {
+      if (++P.kq < nq) return true;
+      return seek(P.L + ncl, P);
+    };
+    auto fetch = [&](const Pos& P, uint4 (&w4)[4], uint32_t (&a)[J]) {
+      const uint8_t* wsp =
+          p.w_scales +
+          (static_cast<size_t>(P.g) * p.N + (P.nt2 * 2 + static_cast<int>(rank)) * 128) * kw +
+          P.kq * 16;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        w4[j] = __ldg(reinterpret_cast<const uint4*>(wsp + static_cast<size_t>(j * 32 + lane) * kw));
+#pragma unroll
+      for (int j = 0; j < J; ++j) {
+        const int c = j * 32 + lane;
+        a[j] = c < P.rows ? __ldg(reinterpret_cast<const uint32_t*>(
+                                p.x_scales + static_cast<size_t>(P.row0 + c) * kx + P.kq * 4))
+                          : 0x7F7F7F7Fu;
+      }
+    };
+    uint4 wv[Q][4];
+    uint32_t av[Q][J];
+    Pos ld{}, cs{};
+    bool ld_ok = seek(cl, ld);
+    bool cs_ok = seek(cl, cs);
+#pragma unroll
+    for (int i = 0; i < Q; ++i)
+      if (ld_ok) {
+        fetch(ld, wv[i], av[i]);
+        ld_ok = step(ld);
+      }
+    uint32_t it = 0;
+    bool ok = nq > 0;
+    while (cs_ok && ok && !*abort_flag) {
+#pragma unroll
+      for (int i = 0; i < Q; ++i) {
+        if (!cs_ok || !ok) break;
+#pragma unroll
+        for (int b = 0; b < SPQ; ++b) {
+          const int s = it % STAGES;
+          if (it >= STAGES) {
+            int w_ok = 1;
+            if (lane == 0)
+              w_ok = mbar_wait(&empty[s], ((it / STAGES) & 1u) ^ 1u, p.status, abort_flag);
+            if (!__shfl_sync(0xFFFFFFFFu, w_ok, 0)) {
+              ok = false;
+              break;
+            }
+          }
+#pragma unroll
+          for (int ko = 0; ko < KO; ++ko) {
+            const uint4 v = make_uint4(u4_comp(wv[i][0], b * KO + ko), u4_comp(wv[i][1], b * KO + ko),
+                                       u4_comp(wv[i][2], b * KO + ko), u4_comp(wv[i][3], b * KO + ko));
+#pragma unroll
+            for (int rep = 0; rep < 4; ++rep)
+              *reinterpret_cast<uint4*>(smem + C::kOffSfa + s * C::kSfaStage + ko * 2048 +
+                                        (rep * 32 + lane) * 16) = v;
+          }
+#pragma unroll
+          for (int a = 0; a < NA; ++a) {
+            uint32_t xb[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int jj = a * 4 + j;
+              xb[j] = jj < J ? (av[i][jj < J ? jj : 0] >> (8 * b * KO)) & 0xFFFFu : 0x7F7Fu;
+            }
+            const uint4 v = make_uint4(xb[0], xb[1], xb[2], xb[3]);
+#pragma unroll
+            for (int rep = 0; rep < 4; ++rep)
+              *reinterpret_cast<uint4*>(smem + C::kOffSfb + s * C::kSfbStage + a * 2048 +
+                                        (rep * 32 + lane) * 16) = v;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (leader) mbar_arrive(&sf_full[s]);
+            else mbar_arrive_cluster(leader_addr(&sf_full[s]));
+          }
+          ++it;
+        }
+        if (!ok) break;
+        cs_ok = step(cs);
+        if (ld_ok) {  // refill slot i with the quad Q ahead
+          fetch(ld, wv[i], av[i]);
+          ld_ok = step(ld);
+        }
+      }
     }
   } else if (warp >= 4) {
     // ---------------------------------------------------------------- epilogue
@@ -1094,11 +1143,11 @@ cudaError_t launch_one(const CUtensorMap& tmW, const CUtensorMap& tmX, const Gem
 }
 
 // The pair kernel for one list: clusters of two CTAs, as many clusters as fit at once.
-template <int BN2, int STAGES, bool SFB_FULL>
+template <int BN2, int STAGES>
 cudaError_t launch_pair(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmParams& p,
                         int max_items, cudaStream_t st) {
-  using C = GemmCfg2<BN2, STAGES, SFB_FULL>;
-  auto kern = k_gemm_mx2<BN2, STAGES, SFB_FULL>;
+  using C = GemmCfg2<BN2, STAGES>;
+  auto kern = k_gemm_mx2<BN2, STAGES>;
   static unsigned long long attr_ctx[64] = {};
   static int max_clusters[64] = {};
   int dev = 0;
@@ -1224,7 +1273,7 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& a, cudaStream_t st) {
   e = launch_variant<kMediumBN, kMediumStages, kMediumStagesKO1, kMediumOcc>(
       a, p, a.items[1], a.item_counts + 1, a.max_items[1], st);
   if (e != cudaSuccess || a.max_group_rows <= kMediumBN) return e;
-  if (a.N % 256 == 0 && a.K % 256 == 0 && a.out == nullptr) {
+  if (a.N % 256 == 0 && a.K % 512 == 0 && a.out == nullptr) {
     // mid and large tiles on SM pairs (same kernel for both lists; the combine-fused
     // W2 epilogue stays on the one-SM kernels)
     CUtensorMap tmW, tmX;
@@ -1234,11 +1283,11 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& a, cudaStream_t st) {
     GemmParams q = p;
     q.items = a.items[2];
     q.item_count = a.item_counts + 2;
-    e = launch_pair<kPairBN, kPairStages, kPairSfbFull>(tmW, tmX, q, a.max_items[2], st);
+    e = launch_pair<kPairBN, kPairStages>(tmW, tmX, q, a.max_items[2], st);
     if (e != cudaSuccess || a.max_group_rows <= kMidBN) return e;
     q.items = a.items[3];
     q.item_count = a.item_counts + 3;
-    return launch_pair<kPairBN, kPairStages, kPairSfbFull>(tmW, tmX, q, a.max_items[3], st);
+    return launch_pair<kPairBN, kPairStages>(tmW, tmX, q, a.max_items[3], st);
   }
   e = launch_variant<kMidBN, kMidStages, kMidStagesKO1, 1>(a, p, a.items[2],
                                                            a.item_counts + 2, a.max_items[2], st);

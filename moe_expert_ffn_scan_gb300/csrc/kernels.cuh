@@ -51,12 +51,10 @@ constexpr int kMidStagesKO1 = 5;
 constexpr int kLargeBN = 224;
 constexpr int kLargeStages = 2;
 constexpr int kLargeStagesKO1 = 2;
-// Mid and large tiles on SM pairs (when N and K are multiples of 256): 224-token tiles
-// (112 per SM), three stages of two 128-K sub-tiles.  kPairSfbFull: each CTA's token
-// scale factors cover the item's whole token range (else only the CTA's half).
+// Mid and large tiles on SM pairs (when N % 256 == 0 and K % 512 == 0): 224-token tiles
+// (112 per SM), three stages of two 128-K sub-tiles.
 constexpr int kPairBN = 224;
 constexpr int kPairStages = 3;
-constexpr bool kPairSfbFull = true;
 
 // The tile plan's work lists, one per variant (0 small, 1 medium, 2 mid, 3 large),
 // each {group, row0, rows, 0} in group order, and their lengths.
