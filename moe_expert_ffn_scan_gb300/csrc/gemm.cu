@@ -692,7 +692,7 @@ __global__ void __launch_bounds__(256, OCC)
 //     the pair), then issues the MMAs;
 //   * MMA completion is multicast to both CTAs' empty / accumulator-full barriers; both
 //     epilogues arrive on the leader's accumulator-empty barrier.
-template <int BN2, int STAGES>
+template <int BN2, int STAGES, int SFS>
 struct GemmCfg2 {
   static constexpr int KO = 2;
   static constexpr int BH = BN2 / 2;              // token rows per CTA
@@ -705,15 +705,19 @@ struct GemmCfg2 {
   // operand and stage; see GemmCfg)
   static constexpr int kSfaStage = KO * 2048;
   static constexpr int kSfbStage = kSfbAtoms * 2048;
-  static constexpr int kSfTotal = STAGES * (kSfaStage + kSfbStage);
+  // The scale factors have a ring of their own (SFS slots, deeper than the data ring),
+  // so that their staging runs ahead of the stage the MMAs wait for instead of starting
+  // only when the data stage's slot frees up.
+  static constexpr int kSfTotal = SFS * (kSfaStage + kSfbStage);
   static constexpr int kOffSfa = 0;
-  static constexpr int kOffSfb = STAGES * kSfaStage;
+  static constexpr int kOffSfb = SFS * kSfaStage;
   static constexpr int kOffA = (kSfTotal + 1023) / 1024 * 1024;
   static constexpr int kOffB = kOffA + STAGES * kABytes;
   static constexpr int kOffBar = kOffB + STAGES * kBBytes;
-  // full[S] (leader: 1 + tx), empty[S] (1: multicast commit), sf_full[S] (leader: 2),
-  // acc_full[2] (1: multicast commit), acc_empty[2] (leader: 8 epilogue warps), drain
-  static constexpr int kNumBars = 3 * STAGES + 5;
+  // full[S] (leader: 1 + tx), empty[S] (1: multicast commit), sf_full[SFS] (leader: 2),
+  // sf_empty[SFS] (1: multicast commit after the copies), acc_full[2] (1: multicast
+  // commit), acc_empty[2] (leader: 8 epilogue warps), drain
+  static constexpr int kNumBars = 2 * STAGES + 2 * SFS + 5;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16;
   static constexpr int kSfCols = 4 * (KO + kSfbAtoms);
@@ -737,11 +741,11 @@ __device__ __forceinline__ uint32_t idesc_mxf4_e4m3_m256(int n) {
   return d;
 }
 
-template <int BN2, int STAGES>
+template <int BN2, int STAGES, int SFS>
 __global__ void __launch_bounds__(256, 1)
     k_gemm_mx2(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                const GemmParams p) {
-  using C = GemmCfg2<BN2, STAGES>;
+  using C = GemmCfg2<BN2, STAGES, SFS>;
   constexpr int KO = C::KO;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t rank = cluster_ctarank();
@@ -750,7 +754,8 @@ __global__ void __launch_bounds__(256, 1)
   uint64_t* full = bars;
   uint64_t* empty = full + STAGES;
   uint64_t* sf_full = empty + STAGES;
-  uint64_t* acc_full = sf_full + STAGES;
+  uint64_t* sf_empty = sf_full + SFS;
+  uint64_t* acc_full = sf_empty + SFS;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
@@ -761,7 +766,10 @@ __global__ void __launch_bounds__(256, 1)
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
-      mbar_init(&sf_full[s], 2);
+    }
+    for (int j = 0; j < SFS; ++j) {
+      mbar_init(&sf_full[j], 2);
+      mbar_init(&sf_empty[j], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -872,20 +880,27 @@ __global__ void __launch_bounds__(256, 1)
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1u;
-          if (!mbar_wait(&sf_full[s], ph, p.status, abort_flag)) {
+          const int j = it % SFS;
+          if (!mbar_wait(&sf_full[j], (it / SFS) & 1u, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          // TMEM scale slot s is free once the MMAs of stage it - STAGES completed
+          if (it >= STAGES && !mbar_wait(&empty[s], ph ^ 1u, p.status, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t sf_t = tmem + 2 * BN2 + s * C::kSfCols;
           const uint32_t sfb_t = sf_t + 4 * KO;
-          const uint64_t da = smem_desc(smem_u32(smem + C::kOffSfa + s * C::kSfaStage), 2048, 128,
+          const uint64_t da = smem_desc(smem_u32(smem + C::kOffSfa + j * C::kSfaStage), 2048, 128,
                                         kLayoutNone);
-          const uint64_t db = smem_desc(smem_u32(smem + C::kOffSfb + s * C::kSfbStage), 2048, 128,
+          const uint64_t db = smem_desc(smem_u32(smem + C::kOffSfb + j * C::kSfbStage), 2048, 128,
                                         kLayoutNone);
           tc_cp_128x256b_pair(sf_t, da);
           if (C::kSfbAtoms == 2) tc_cp_128x256b_pair(sfb_t, db);
           else tc_cp_128x128b_pair(sfb_t, db);
+          tc_commit_pair_mc(&sf_empty[j], 3);  // both CTAs' scale slot j, once copied
           if (!mbar_wait(&full[s], ph, p.status, abort_flag)) {
             ok = false;
             break;
@@ -980,11 +995,11 @@ __global__ void __launch_bounds__(256, 1)
         if (!cs_ok || !ok) break;
 #pragma unroll
         for (int b = 0; b < SPQ; ++b) {
-          const int s = it % STAGES;
-          if (it >= STAGES) {
+          const int s = it % SFS;  // scale ring slot
+          if (it >= SFS) {
             int w_ok = 1;
             if (lane == 0)
-              w_ok = mbar_wait(&empty[s], ((it / STAGES) & 1u) ^ 1u, p.status, abort_flag);
+              w_ok = mbar_wait(&sf_empty[s], ((it / SFS) & 1u) ^ 1u, p.status, abort_flag);
             if (!__shfl_sync(0xFFFFFFFFu, w_ok, 0)) {
               ok = false;
               break;
@@ -1143,11 +1158,11 @@ cudaError_t launch_one(const CUtensorMap& tmW, const CUtensorMap& tmX, const Gem
 }
 
 // The pair kernel for one list: clusters of two CTAs, as many clusters as fit at once.
-template <int BN2, int STAGES>
+template <int BN2, int STAGES, int SFS>
 cudaError_t launch_pair(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmParams& p,
                         int max_items, cudaStream_t st) {
-  using C = GemmCfg2<BN2, STAGES>;
-  auto kern = k_gemm_mx2<BN2, STAGES>;
+  using C = GemmCfg2<BN2, STAGES, SFS>;
+  auto kern = k_gemm_mx2<BN2, STAGES, SFS>;
   static unsigned long long attr_ctx[64] = {};
   static int max_clusters[64] = {};
   int dev = 0;
@@ -1283,11 +1298,11 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& a, cudaStream_t st) {
     GemmParams q = p;
     q.items = a.items[2];
     q.item_count = a.item_counts + 2;
-    e = launch_pair<kPairBN, kPairStages>(tmW, tmX, q, a.max_items[2], st);
+    e = launch_pair<kPairBN, kPairStages, kPairSfSlots>(tmW, tmX, q, a.max_items[2], st);
     if (e != cudaSuccess || a.max_group_rows <= kMidBN) return e;
     q.items = a.items[3];
     q.item_count = a.item_counts + 3;
-    return launch_pair<kPairBN, kPairStages>(tmW, tmX, q, a.max_items[3], st);
+    return launch_pair<kPairBN, kPairStages, kPairSfSlots>(tmW, tmX, q, a.max_items[3], st);
   }
   e = launch_variant<kMidBN, kMidStages, kMidStagesKO1, 1>(a, p, a.items[2],
                                                            a.item_counts + 2, a.max_items[2], st);

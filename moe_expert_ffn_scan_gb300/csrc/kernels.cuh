@@ -55,6 +55,7 @@ constexpr int kLargeStagesKO1 = 2;
 // (112 per SM), three stages of two 128-K sub-tiles.
 constexpr int kPairBN = 224;
 constexpr int kPairStages = 3;
+constexpr int kPairSfSlots = 5;  // scale-factor ring (its own barriers)
 
 // The tile plan's work lists, one per variant (0 small, 1 medium, 2 mid, 3 large),
 // each {group, row0, rows, 0} in group order, and their lengths.
