@@ -715,9 +715,10 @@ struct GemmCfg2 {
   static constexpr int kOffB = kOffA + STAGES * kABytes;
   static constexpr int kOffBar = kOffB + STAGES * kBBytes;
   // full[S] (leader: 1 + tx), empty[S] (1: multicast commit), sf_full[SFS] (leader: 2),
-  // sf_empty[SFS] (1: multicast commit after the copies), acc_full[2] (1: multicast
-  // commit), acc_empty[2] (leader: 8 epilogue warps), drain
-  static constexpr int kNumBars = 2 * STAGES + 2 * SFS + 5;
+  // sf_empty[SFS] (1: multicast commit after the copies), sf_ready[SFS] (peer: its
+  // scale warp, relayed to the leader's sf_full by the peer's warp 1), acc_full[2] (1:
+  // multicast commit), acc_empty[2] (leader: 8 epilogue warps), drain
+  static constexpr int kNumBars = 2 * STAGES + 3 * SFS + 5;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16;
   static constexpr int kSfCols = 4 * (KO + kSfbAtoms);
@@ -755,7 +756,8 @@ __global__ void __launch_bounds__(256, 1)
   uint64_t* empty = full + STAGES;
   uint64_t* sf_full = empty + STAGES;
   uint64_t* sf_empty = sf_full + SFS;
-  uint64_t* acc_full = sf_empty + SFS;
+  uint64_t* sf_ready = sf_empty + SFS;
+  uint64_t* acc_full = sf_ready + SFS;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
@@ -770,6 +772,7 @@ __global__ void __launch_bounds__(256, 1)
     for (int j = 0; j < SFS; ++j) {
       mbar_init(&sf_full[j], 2);
       mbar_init(&sf_empty[j], 1);
+      mbar_init(&sf_ready[j], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -863,9 +866,31 @@ __global__ void __launch_bounds__(256, 1)
         if (!ok) break;
       }
     }
+  } else if (warp == 1 && !leader) {
+    // ---------------------------------------------------------------- scale relay
+    // The peer's scale warp arrives on its own sf_ready; this thread, which has no
+    // memory operations in flight, forwards each arrival to the leader's sf_full.  (A
+    // cluster-scope release by the scale warp itself would wait for the scale loads
+    // it keeps in flight several stages ahead.)
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (long long L = cl; L < total && ok && !*abort_flag; L += ncl) {
+        int g, row0, rows, nt2;
+        if (!load_item(L, g, row0, rows, nt2)) continue;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int j = it % SFS;
+          if (!mbar_wait(&sf_ready[j], (it / SFS) & 1u, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_cluster(leader_addr(&sf_full[j]));
+        }
+      }
+    }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
-    if (leader && lane == 0) {
+    if (lane == 0) {
       uint32_t it = 0, tc = 0;
       for (long long L = cl; L < total && !*abort_flag; L += ncl) {
         int g, row0, rows, nt2;
@@ -1030,10 +1055,7 @@ __global__ void __launch_bounds__(256, 1)
           }
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) {
-            if (leader) mbar_arrive(&sf_full[s]);
-            else mbar_arrive_cluster(leader_addr(&sf_full[s]));
-          }
+          if (lane == 0) mbar_arrive(leader ? &sf_full[s] : &sf_ready[s]);
           ++it;
         }
         if (!ok) break;
