@@ -324,15 +324,29 @@ int moe_forward_timed(const moe_dims* d, const uint16_t* x, const float* logits,
                       void* const* events, void* ws, size_t ws_bytes, void* stream);
 
 /* Options of moe_forward_ex (zero-initialise; every field 0 = moe_forward).
+ *   fuse_swiglu (f1): 1 = the W13 grouped GEMM's epilogue performs a5 (LMSYS-H20 §4.3,
+ *     SwiGLU fused with the quantisation that emits W2's data and scales): each tile
+ *     of an SM pair (a cluster of two CTAs sharing each cta_group::2 MMA) holds 64
+ *     gate + the same 64 up rows per CTA, i.e. one 128-feature quantisation block per
+ *     pair; h = silu(gate) * up is formed from the bf16-rounded accumulators, the two
+ *     CTAs swap per-token amaxes, and the FP8 codes and scales are written directly --
+ *     the same hq / hs bit for bit as the stand-alone SwiGLU kernel, without y13 (the
+ *     dbg->y13 buffer is not written) and without that kernel.  Needs H % 512 == 0.
+ *   pair_tiles: 1 = the mid and large tile lists (groups of more than 64 rows) run on
+ *     SM pairs (one cta_group::2 MMA per 256 weight rows, half the token tile per SM)
+ *     instead of one SM per tile (when N % 256 == 0 and K % 512 == 0).
  *   fuse_combine (f2): 1 = the W2 grouped GEMM's epilogue performs a7 (LMSYS-H20 §3.2,
  *     the TopK reduction merged with the shared-expert add): once a tile has stored its
  *     y2 rows, each row bumps its (token, 128-column block) arrival counter, and the
  *     tile that brings a block to k + has_shared arrivals sums that token's rows for
  *     those 128 columns in the stand-alone combine's order (fp32, j order, shared row
  *     last) -- the same out bit for bit, deterministic, no float atomics -- and the
- *     separate combine kernel is not launched.  MXFP4 weights only. */
+ *     separate combine kernel is not launched.
+ * All options take MXFP4 weights (MOE_ERR_INVALID_ARG otherwise). */
 typedef struct moe_options {
   int32_t fuse_combine;
+  int32_t fuse_swiglu;
+  int32_t pair_tiles;
 } moe_options;
 
 /* moe_forward_timed with options (opt may be NULL: all zero; events may be NULL).

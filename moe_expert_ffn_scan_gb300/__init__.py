@@ -41,7 +41,7 @@ class moe_weights(ctypes.Structure):
 
 
 class moe_options(ctypes.Structure):
-    _fields_ = [("fuse_combine", ctypes.c_int32)]
+    _fields_ = [(n, ctypes.c_int32) for n in ("fuse_combine", "fuse_swiglu", "pair_tiles")]
 
 
 class moe_weights_nvfp4(ctypes.Structure):
@@ -304,12 +304,14 @@ def moe_route_static_status(stream=None) -> int:
     return bits.value
 
 
-def moe_forward_ex(d, x, logits, w13, w13_s, w2, w2_s, out, ws, fuse_combine=False, debug=None,
-                   events=None, stream=None):
+def moe_forward_ex(d, x, logits, w13, w13_s, w2, w2_s, out, ws, fuse_combine=False,
+                   fuse_swiglu=False, pair_tiles=False, debug=None, events=None, stream=None):
     """moe_forward with options (fuse_combine: the W2 GEMM's epilogue performs the
-    weighted top-k combine + shared add) and optional stage events."""
+    weighted top-k combine + shared add; fuse_swiglu: the W13 GEMM's epilogue performs
+    SwiGLU + FP8 quantisation; pair_tiles: groups above 64 rows on SM pairs) and
+    optional stage events."""
     W = moe_weights(_p(w13), _p(w13_s), _p(w2), _p(w2_s))
-    opt = moe_options(1 if fuse_combine else 0)
+    opt = moe_options(int(bool(fuse_combine)), int(bool(fuse_swiglu)), int(bool(pair_tiles)))
     dbg = None
     if debug:
         dbg = moe_debug_out(*[_p(debug.get(n)) for n in DEBUG_FIELDS])
@@ -466,12 +468,14 @@ class MoELayer:
     bf16 output [T, H]."""
 
     def __init__(self, H, I, E, k, has_shared, w13, w13_s, w2, w2_s, fmt="mxfp4", w13_gs=None,
-                 w2_gs=None, fuse_combine=False):
+                 w2_gs=None, fuse_combine=False, fuse_swiglu=False, pair_tiles=False):
         if fmt not in ("mxfp4", "nvfp4"):
             raise ValueError(f"unknown weight format {fmt!r}")
-        if fuse_combine and fmt != "mxfp4":
-            raise ValueError("the combine fused into the W2 epilogue takes MXFP4 weights")
+        if (fuse_combine or fuse_swiglu or pair_tiles) and fmt != "mxfp4":
+            raise ValueError("the fusion and tile options take MXFP4 weights")
         self.fuse_combine = bool(fuse_combine)
+        self.fuse_swiglu = bool(fuse_swiglu)
+        self.pair_tiles = bool(pair_tiles)
         self.H, self.I, self.E, self.k, self.has_shared = H, I, E, k, has_shared
         self.w13, self.w13_s, self.w2, self.w2_s = w13, w13_s, w2, w2_s
         self.fmt, self.w13_gs, self.w2_gs = fmt, w13_gs, w2_gs
@@ -525,8 +529,9 @@ class MoELayer:
             out = torch.empty(T, self.H, dtype=torch.bfloat16, device=x.device)
         if self.fmt == "mxfp4":
             moe_forward_ex(self.dims(T), x, logits, self.w13, self.w13_s, self.w2, self.w2_s, out,
-                           self.workspace(T), fuse_combine=self.fuse_combine, debug=debug,
-                           stream=stream)
+                           self.workspace(T), fuse_combine=self.fuse_combine,
+                           fuse_swiglu=self.fuse_swiglu, pair_tiles=self.pair_tiles,
+                           debug=debug, stream=stream)
         else:
             moe_forward_nvfp4(self.dims(T), x, logits, self.w13, self.w13_s, self.w13_gs,
                               self.w2, self.w2_s, self.w2_gs, out, self.workspace(T),
@@ -538,8 +543,9 @@ class MoELayer:
         T = x.shape[0]
         if self.fmt == "mxfp4":
             moe_forward_ex(self.dims(T), x, logits, self.w13, self.w13_s, self.w2, self.w2_s, out,
-                           self.workspace(T), fuse_combine=self.fuse_combine, events=events,
-                           stream=stream)
+                           self.workspace(T), fuse_combine=self.fuse_combine,
+                           fuse_swiglu=self.fuse_swiglu, pair_tiles=self.pair_tiles,
+                           events=events, stream=stream)
         else:
             moe_forward_nvfp4_timed(self.dims(T), x, logits, self.w13, self.w13_s, self.w13_gs,
                                     self.w2, self.w2_s, self.w2_gs, out, self.workspace(T),

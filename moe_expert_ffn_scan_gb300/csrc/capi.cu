@@ -203,13 +203,17 @@ HostStagingWs carve_host_staging(Carver& c, const moe_dims* d) {
 
 // early_plan: the plan's producer ran at least two launches before this GEMM (see
 // GemmLaunch).
-// f2: the combine performed by the W2 GEMM's epilogue (see GemmLaunch).
+// Fusions and tile choices of one GEMM launch (see GemmLaunch): f2, the combine in the
+// W2 epilogue; f1, SwiGLU + quantisation in the W13 epilogue; SM-pair tiles.
 struct FusedCombine {
   uint16_t* out = nullptr;
   const int32_t* perm_src = nullptr;
   const int32_t* inv = nullptr;
   const float* w = nullptr;
   int32_t* cnt = nullptr;
+  uint8_t* hq = nullptr;
+  uint8_t* hs = nullptr;
+  int pair_tiles = 0;
 };
 
 int run_gemm(const moe_dims* d, const uint8_t* act, const uint8_t* act_s, const int32_t* offsets,
@@ -222,6 +226,9 @@ int run_gemm(const moe_dims* d, const uint8_t* act, const uint8_t* act_s, const 
   a.inv = fc.inv;
   a.cw = fc.w;
   a.cnt = fc.cnt;
+  a.hq = fc.hq;
+  a.hs = fc.hs;
+  a.pair_tiles = fc.pair_tiles;
   a.T = d->T;
   a.k = d->k;
   a.has_shared = d->has_shared;
@@ -607,9 +614,15 @@ int forward_impl(const moe_dims* d, const uint16_t* x, const float* logits,
   if (!(W.fmt == kMxfp4 ? dims_ok(d) : nv_dims_ok(d))) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (!x || !logits || !out || !ws) return MOE_ERR_INVALID_ARG;
   const bool fuse_combine = opt && opt->fuse_combine;
+  const bool fuse_swiglu = opt && opt->fuse_swiglu;
+  const int pair_tiles = opt ? opt->pair_tiles : 0;
   if (opt && ((opt->fuse_combine != 0 && opt->fuse_combine != 1) ||
-              (fuse_combine && W.fmt != kMxfp4)))
+              (opt->fuse_swiglu != 0 && opt->fuse_swiglu != 1) ||
+              (opt->pair_tiles != 0 && opt->pair_tiles != 1) ||
+              ((fuse_combine || fuse_swiglu || pair_tiles) && W.fmt != kMxfp4)))
     return MOE_ERR_INVALID_ARG;
+  // the fused W13 epilogue runs on SM pairs: 2I % 256 == 0 always, H % 512 needed
+  if (fuse_swiglu && d->H % 512 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (!weights_ok(W.w13, W.w13_s) || !weights_ok(W.w2, W.w2_s)) return MOE_ERR_INVALID_ARG;
   if (!aligned(W.w13_gs, 4) || !aligned(W.w2_gs, 4)) return MOE_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(out, 16) || !aligned(ws, kAlign) || !aligned(logits, 4))
@@ -675,8 +688,14 @@ int forward_impl(const moe_dims* d, const uint16_t* x, const float* logits,
   // follows the quant-scatter, and the plan was written before it
   int rc;
   if (W.fmt == kMxfp4) {
+    FusedCombine fs;
+    fs.pair_tiles = pair_tiles;
+    if (fuse_swiglu) {
+      fs.hq = f.hq;
+      fs.hs = f.hs;
+    }
     rc = run_gemm(d, f.gemm.xg, f.gemm.xsg, f.offsets, W.w13, W.w13_s, 2 * I, H, f.y13,
-                  f.gemm.plan, T, status, st, /*early_plan=*/1);
+                  f.gemm.plan, T, status, st, /*early_plan=*/1, fs);
   } else {
     rc = run_gemm_nv(d, f.gemm.xe, W.w13, W.w13_s, W.w13_gs, 2, 2 * I, H, f.y13, f.gemm.plan, T,
                      status, st);
@@ -684,13 +703,14 @@ int forward_impl(const moe_dims* d, const uint16_t* x, const float* logits,
   if (rc != MOE_OK) return rc;
   MOE_MARK(4)
   if (W.fmt == kMxfp4) {
-    MOE_TRY(launch_swiglu_quant(f.y13, Rs, I, f.hq, f.hs, st))
+    if (!fuse_swiglu) MOE_TRY(launch_swiglu_quant(f.y13, Rs, I, f.hq, f.hs, st))
   } else {
     MOE_TRY(launch_swiglu_quant_bf16(f.y13, Rs, I, dbg_hq, dbg_hs, f.he, st))
   }
   MOE_MARK(5)
   if (W.fmt == kMxfp4) {
     FusedCombine fc;
+    fc.pair_tiles = pair_tiles;
     if (fuse_combine) {
       fc.out = out;
       fc.perm_src = f.perm_src;

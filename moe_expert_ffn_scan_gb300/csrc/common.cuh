@@ -74,21 +74,28 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
       : "memory");
 }
 
+// Test a phase; while it is incomplete the thread is suspended until it completes or
+// kTryWaitSuspendNs elapse (then the caller's loop checks its bounds).  A suspended
+// thread takes no issue slots, which matters for the many warps that wait most of the
+// time (epilogue warps, converter groups between their stages): a short hardware default
+// turns their waits into spin loops that compete with the producer and MMA threads.
+constexpr uint32_t kTryWaitSuspendNs = 20000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kTryWaitSuspendNs)
       : "memory");
   return ok != 0;
 }
 
 // Wait for the phase with the given parity to complete.  Returns false (and sets
 // STATUS_WAIT_TIMEOUT) if it did not complete within kWaitLimitNs, or if another
-// thread of the CTA already flagged an abort.
+// thread of the CTA already flagged an abort (both checked every few suspensions).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status,
                                           volatile int* abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -96,7 +103,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
   uint32_t n = 0;
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((++n & 255u) == 0) {
+    if ((++n & 7u) == 0) {
       if (*abort_flag) return false;
       if (globaltimer_ns() - t0 > kWaitLimitNs) {
         set_status(status, STATUS_WAIT_TIMEOUT);

@@ -51,6 +51,12 @@ struct GemmParams {
   const float* cw;          // [T][k] routing weights
   int32_t* cnt;             // [T][N/128] arrival counters, zero before the launch
   int T, k, has_shared;
+  // f1 (W13 on SM pairs only; null hq = off): the epilogue performs a5 -- h = silu(gate)
+  // * up from the bf16-rounded accumulators, quantised per row per 128 features -- and
+  // writes W2's operand hq [rows_total][N/2] and scales hs [rows_total][N/256] instead
+  // of y13.
+  uint8_t* hq;
+  uint8_t* hs;
 };
 
 // Quads (4 sub-tiles = 512 K elements) of scale bytes the scale-factor warp keeps in
@@ -692,7 +698,7 @@ __global__ void __launch_bounds__(256, OCC)
 //     the pair), then issues the MMAs;
 //   * MMA completion is multicast to both CTAs' empty / accumulator-full barriers; both
 //     epilogues arrive on the leader's accumulator-empty barrier.
-template <int BN2, int STAGES, int SFS>
+template <int BN2, int STAGES, int SFS, bool F1>
 struct GemmCfg2 {
   static constexpr int KO = 2;
   static constexpr int BH = BN2 / 2;              // token rows per CTA
@@ -718,9 +724,19 @@ struct GemmCfg2 {
   // sf_empty[SFS] (1: multicast commit after the copies), sf_ready[SFS] (peer: its
   // scale warp, relayed to the leader's sf_full by the peer's warp 1), acc_full[2] (1:
   // multicast commit), acc_empty[2] (leader: 8 epilogue warps), drain
-  static constexpr int kNumBars = 2 * STAGES + 3 * SFS + 5;
+  // (+ xchg_full[2] with F1: the peer's per-token amax arrived)
+  static constexpr int kNumBars = 2 * STAGES + 3 * SFS + 5 + (F1 ? 2 : 0);
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kSmemBytes = kOffMisc + 16;
+  // F1 epilogue scratch: up values of a 16-token chunk [64 features][16] fp32, the two
+  // gate warps' per-token amax [2][16], this CTA's amax per token [BN2], the peer's
+  // [2 slots][BN2], a chunk's codes [16 tokens][64 B], its scale bytes [16]
+  static constexpr int kOffUp = (kOffMisc + 16 + 15) / 16 * 16;
+  static constexpr int kOffAm32 = kOffUp + 64 * 16 * 4;
+  static constexpr int kOffAmMine = kOffAm32 + 2 * 16 * 4;
+  static constexpr int kOffAmPeer = kOffAmMine + BN2 * 4;
+  static constexpr int kOffCodes = kOffAmPeer + 2 * BN2 * 4;
+  static constexpr int kOffEs = kOffCodes + 16 * 64;
+  static constexpr int kSmemBytes = F1 ? kOffEs + 16 * 4 : kOffMisc + 16;
   static constexpr int kSfCols = 4 * (KO + kSfbAtoms);
   static constexpr int kTmemNeed = 2 * BN2 + STAGES * kSfCols;
   static constexpr int kTmemCols = kTmemNeed <= 256 ? 256 : 512;
@@ -730,6 +746,132 @@ struct GemmCfg2 {
   static_assert(kTmemNeed <= 512, "TMEM");
   static_assert(kSmemBytes <= 232448, "dynamic shared memory of one CTA");
 };
+
+// F1 epilogue of the W13 pair kernel (warps 4-7 of each CTA).  TMEM lanes 0-63 hold
+// this CTA's 64 gate features, lanes 64-127 the same 64 up features; columns are the
+// item's tokens.  Per tile: pass 1 computes h = silu(g) * u (g, u the accumulators
+// rounded to bf16, as y13 would be) per 16-token chunk, the up warps handing their
+// values to the gate warps through shared memory, and each token's amax over the 64
+// features; the two CTAs swap those amaxes (distributed shared memory, one remote
+// arrive); pass 2 recomputes h, takes the scale exponent of the 128-feature block from
+// the larger of the two amaxes and writes the FP8 codes (rows of 64 bytes) and, in the
+// leader, the scale bytes.  The arithmetic is k_swiglu_quant's, value for value.
+template <int BN2, typename LoadItem, typename LeaderAddr>
+__device__ __forceinline__ void f1_epilogue(const GemmParams& p, uint32_t tmem, uint8_t* smem,
+                                            int off_up, int off_am32, int off_am_mine,
+                                            int off_am_peer, int off_codes, int off_es,
+                                            uint64_t* acc_full, uint64_t* acc_empty,
+                                            uint64_t* xchg_full, volatile int* abort_flag,
+                                            uint32_t rank, bool leader, long long cl,
+                                            long long ncl, long long total, LoadItem load_item,
+                                            LeaderAddr leader_addr) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q = warp - 4;  // 0, 1: gate warps; 2, 3: up warps
+  const int et = q * 32 + lane;
+  float* upbuf = reinterpret_cast<float*>(smem + off_up);           // [64][16]
+  float* am32 = reinterpret_cast<float*>(smem + off_am32);          // [2][16]
+  float* am_mine = reinterpret_cast<float*>(smem + off_am_mine);    // [BN2]
+  float* am_peer = reinterpret_cast<float*>(smem + off_am_peer);    // [2][BN2]
+  uint8_t* codes = smem + off_codes;                                // [16][64]
+  int* es = reinterpret_cast<int*>(smem + off_es);                  // [16]
+  const int I = p.N / 2;
+  const int nblk = I / 128;
+  const uint32_t peer = rank ^ 1u;
+  uint32_t tc = 0;
+  for (long long L = cl; L < total && !*abort_flag; L += ncl) {
+    int g, row0, rows, nt2;
+    if (!load_item(L, g, row0, rows, nt2)) continue;
+    const uint32_t b = tc & 1u, use = tc >> 1;
+    int w_ok = 1;
+    if (lane == 0) w_ok = mbar_wait(&acc_full[b], use & 1u, p.status, abort_flag);
+    if (!__shfl_sync(0xFFFFFFFFu, w_ok, 0)) break;
+    tc_fence_after();
+    const uint32_t acc = tmem + (static_cast<uint32_t>(q * 32) << 16) + b * BN2;
+    // h of this thread's feature for tokens c0 .. c0 + 15 (gate warps only)
+    auto chunk_h = [&](int c0, float (&h)[16]) {
+      uint32_t r[16];
+      tmem_ld_32x32b_x16(acc + c0, r);
+      tmem_ld_wait();
+      if (q >= 2) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          upbuf[(et - 64) * 16 + i] = __bfloat162float(__float2bfloat16_rn(__uint_as_float(r[i])));
+      }
+      epilogue_bar_sync();
+      if (q < 2) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float gv = __bfloat162float(__float2bfloat16_rn(__uint_as_float(r[i])));
+          const float uv = upbuf[et * 16 + i];
+          h[i] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
+        }
+      }
+    };
+    // pass 1: this CTA's per-token amax over its 64 features
+    for (int c0 = 0; c0 < rows; c0 += 16) {
+      float h[16];
+      chunk_h(c0, h);
+      if (q < 2) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float m = fabsf(h[i]);
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+          if (lane == 0) am32[q * 16 + i] = m;
+        }
+      }
+      epilogue_bar_sync();
+      if (q == 0 && lane < 16 && c0 + lane < BN2) am_mine[c0 + lane] = fmaxf(am32[lane], am32[16 + lane]);
+    }
+    epilogue_bar_sync();
+    // swap with the peer: my amaxes into its am_peer[b], then its arrival on mine
+    if (q == 0 && lane == 0) {
+      const uint32_t dst = mapa_shared(smem_u32(am_peer + b * BN2), peer);
+      for (int c = 0; c < rows; ++c)
+        asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dst + 4u * c), "f"(am_mine[c])
+                     : "memory");
+      mbar_arrive_cluster(mapa_shared(smem_u32(&xchg_full[b]), peer));
+      w_ok = mbar_wait(&xchg_full[b], use & 1u, p.status, abort_flag);
+      es[0] = w_ok;
+    }
+    epilogue_bar_sync();
+    if (!es[0]) break;
+    epilogue_bar_sync();
+    // pass 2: codes and scales
+    for (int c0 = 0; c0 < rows; c0 += 16) {
+      float h[16];
+      chunk_h(c0, h);
+      if (q < 2) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int c = c0 + i < BN2 ? c0 + i : BN2 - 1;
+          const int e = fp8_scale_exponent(fmaxf(am_mine[c], am_peer[b * BN2 + c]));
+          codes[i * 64 + et] = static_cast<uint8_t>(
+              __nv_cvt_float_to_fp8(h[i] * pow2_neg(e), __NV_SATFINITE, __NV_E4M3));
+          if (q == 0 && lane == 0) es[i] = e;
+        }
+      }
+      epilogue_bar_sync();
+      if (et < 64) {
+        const int i = et >> 2, part = et & 3;
+        if (c0 + i < rows) {
+          const size_t row = static_cast<size_t>(row0 + c0 + i);
+          *reinterpret_cast<uint4*>(p.hq + row * I + nt2 * 128 + rank * 64 + part * 16) =
+              *reinterpret_cast<const uint4*>(codes + i * 64 + part * 16);
+          if (leader && part == 0) p.hs[row * nblk + nt2] = static_cast<uint8_t>(es[i] + 127);
+        }
+      }
+      epilogue_bar_sync();
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) {
+      if (leader) mbar_arrive(&acc_empty[b]);
+      else mbar_arrive_cluster(leader_addr(&acc_empty[b]));
+    }
+    ++tc;
+  }
+}
 
 // Instruction descriptor of the pair MMA: as idesc_mxf4_e4m3 with M = 256.
 __device__ __forceinline__ uint32_t idesc_mxf4_e4m3_m256(int n) {
@@ -742,11 +884,11 @@ __device__ __forceinline__ uint32_t idesc_mxf4_e4m3_m256(int n) {
   return d;
 }
 
-template <int BN2, int STAGES, int SFS>
+template <int BN2, int STAGES, int SFS, bool F1>
 __global__ void __launch_bounds__(256, 1)
     k_gemm_mx2(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                const GemmParams p) {
-  using C = GemmCfg2<BN2, STAGES, SFS>;
+  using C = GemmCfg2<BN2, STAGES, SFS, F1>;
   constexpr int KO = C::KO;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t rank = cluster_ctarank();
@@ -760,6 +902,7 @@ __global__ void __launch_bounds__(256, 1)
   uint64_t* acc_full = sf_ready + SFS;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
+  uint64_t* xchg_full = drain + 1;  // F1 only
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -779,6 +922,10 @@ __global__ void __launch_bounds__(256, 1)
       mbar_init(&acc_empty[b], 8);
     }
     mbar_init(drain, 1);
+    if constexpr (F1) {
+      mbar_init(&xchg_full[0], 1);
+      mbar_init(&xchg_full[1], 1);
+    }
     // the 128B-swizzled tiles need 1024-byte alignment: checked, and a misaligned base
     // turns every role into a no-op (the CTA still takes part in the pair's set-up and
     // teardown, which its peer waits for)
@@ -838,8 +985,20 @@ __global__ void __launch_bounds__(256, 1)
             break;
           }
           if (leader) mbar_arrive_expect_tx(&full[s], C::kTxBytes);
-          tma_load_4d_pair(smem + C::kOffA + s * C::kABytes, &tmW, leader_addr(&full[s]), 0,
-                           (nt2 * 2 + static_cast<int>(rank)) * 128, kb * KO, g);
+          if constexpr (F1) {
+            // rows 0-63: gate rows 128 nt2 + 64 r ..; rows 64-127: the same up rows
+            const int gate0 = nt2 * 128 + static_cast<int>(rank) * 64;
+            const uint32_t fb = leader_addr(&full[s]);
+#pragma unroll
+            for (int ko = 0; ko < KO; ++ko) {
+              uint8_t* dst = smem + C::kOffA + s * C::kABytes + ko * C::kASub;
+              tma_load_4d_pair(dst, &tmW, fb, 0, gate0, kb * KO + ko, g);
+              tma_load_4d_pair(dst + 64 * 128, &tmW, fb, 0, p.N / 2 + gate0, kb * KO + ko, g);
+            }
+          } else {
+            tma_load_4d_pair(smem + C::kOffA + s * C::kABytes, &tmW, leader_addr(&full[s]), 0,
+                             (nt2 * 2 + static_cast<int>(rank)) * 128, kb * KO, g);
+          }
         }
         if (!ok) break;
       }
@@ -986,13 +1145,15 @@ __global__ void __launch_bounds__(256, 1)
       return seek(P.L + ncl, P);
     };
     auto fetch = [&](const Pos& P, uint4 (&w4)[4], uint32_t (&a)[J]) {
-      const uint8_t* wsp =
-          p.w_scales +
-          (static_cast<size_t>(P.g) * p.N + (P.nt2 * 2 + static_cast<int>(rank)) * 128) * kw +
-          P.kq * 16;
+      const uint8_t* wsp = p.w_scales + static_cast<size_t>(P.g) * p.N * kw + P.kq * 16;
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        w4[j] = __ldg(reinterpret_cast<const uint4*>(wsp + static_cast<size_t>(j * 32 + lane) * kw));
+      for (int j = 0; j < 4; ++j) {
+        // this CTA's weight row j * 32 + lane (F1: gate rows, then the same up rows)
+        const int row = F1 ? (j < 2 ? 0 : p.N / 2) + P.nt2 * 128 + static_cast<int>(rank) * 64 +
+                                 (j & 1) * 32 + lane
+                           : (P.nt2 * 2 + static_cast<int>(rank)) * 128 + j * 32 + lane;
+        w4[j] = __ldg(reinterpret_cast<const uint4*>(wsp + static_cast<size_t>(row) * kw));
+      }
 #pragma unroll
       for (int j = 0; j < J; ++j) {
         const int c = j * 32 + lane;
@@ -1066,6 +1227,11 @@ __global__ void __launch_bounds__(256, 1)
         }
       }
     }
+  } else if (warp >= 4 && F1) {
+    // ---------------------------------------------------------------- F1 epilogue
+    f1_epilogue<BN2>(p, tmem, smem, C::kOffUp, C::kOffAm32, C::kOffAmMine, C::kOffAmPeer,
+                     C::kOffCodes, C::kOffEs, acc_full, acc_empty, xchg_full, abort_flag, rank,
+                     leader, cl, ncl, total, load_item, leader_addr);
   } else if (warp >= 4) {
     // ---------------------------------------------------------------- epilogue
     const int q = warp - 4;
@@ -1180,11 +1346,11 @@ cudaError_t launch_one(const CUtensorMap& tmW, const CUtensorMap& tmX, const Gem
 }
 
 // The pair kernel for one list: clusters of two CTAs, as many clusters as fit at once.
-template <int BN2, int STAGES, int SFS>
+template <int BN2, int STAGES, int SFS, bool F1>
 cudaError_t launch_pair(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmParams& p,
                         int max_items, cudaStream_t st) {
-  using C = GemmCfg2<BN2, STAGES, SFS>;
-  auto kern = k_gemm_mx2<BN2, STAGES, SFS>;
+  using C = GemmCfg2<BN2, STAGES, SFS, F1>;
+  auto kern = k_gemm_mx2<BN2, STAGES, SFS, F1>;
   static unsigned long long attr_ctx[64] = {};
   static int max_clusters[64] = {};
   int dev = 0;
@@ -1229,7 +1395,8 @@ cudaError_t launch_pair(const CUtensorMap& tmW, const CUtensorMap& tmX, const Ge
 // sub-tiles, G} (box {128, 128, ko, 1}, FP4 unpacked to the 16-byte-aligned form),
 // packed activation rows as a 3D view {128 bytes, rows, K/128} (box {128, xr, ko}).
 int gemm_encode_maps(const uint8_t* w_codes, int G, int N, int K, const uint8_t* act,
-                     int rows_total, int ko, int xr, CUtensorMap* tmW, CUtensorMap* tmX) {
+                     int rows_total, int ko, int xr, CUtensorMap* tmW, CUtensorMap* tmX,
+                     int wr = 128) {
   EncodeTiledFn enc = get_encode_tiled_fn();
   if (!enc) return MOE_ERR_CUDA;
   {
@@ -1237,7 +1404,7 @@ int gemm_encode_maps(const uint8_t* w_codes, int G, int N, int K, const uint8_t*
                           static_cast<cuuint64_t>(G)};
     cuuint64_t strides[3] = {static_cast<cuuint64_t>(K / 2), 64,
                              static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(K / 2)};
-    cuuint32_t box[4] = {128, 128, static_cast<cuuint32_t>(ko), 1};
+    cuuint32_t box[4] = {128, static_cast<cuuint32_t>(wr), static_cast<cuuint32_t>(ko), 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
     if (enc(tmW, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 4, const_cast<uint8_t*>(w_codes), dims,
             strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -1280,6 +1447,31 @@ cudaError_t launch_variant(const GemmLaunch& a, GemmParams p, const int4* items,
 
 }  // namespace
 
+// f1: W13 with SwiGLU + quantisation in the epilogue: every list on the SM-pair kernel
+// (its tile of 2 x (64 gate + 64 up) weight rows is one 128-feature quantisation block).
+static cudaError_t launch_w13_fused_swiglu(const GemmLaunch& a, GemmParams p, cudaStream_t st) {
+  if (a.N % 256 != 0 || a.K % 512 != 0) return cudaErrorInvalidValue;
+  CUtensorMap tmW, tmX;
+  if (gemm_encode_maps(a.w_codes, a.G, a.N, a.K, a.act, a.rows_total, 1, kPairBN / 2, &tmW,
+                       &tmX, 64) != MOE_OK)
+    return cudaErrorInvalidValue;
+  // the token map moves two 128-K sub-tiles per load, the weight map one 64-row box
+  CUtensorMap tmW2, tmX2;
+  if (gemm_encode_maps(a.w_codes, a.G, a.N, a.K, a.act, a.rows_total, 2, kPairBN / 2, &tmW2,
+                       &tmX2) != MOE_OK)
+    return cudaErrorInvalidValue;
+  const int bounds[kNumVariants] = {kSmallBN, kMediumBN, kMidBN, kLargeBN};
+  for (int v = 0; v < kNumVariants; ++v) {
+    GemmParams q = p;
+    q.items = a.items[v];
+    q.item_count = a.item_counts + v;
+    const cudaError_t e =
+        launch_pair<kPairBN, kPairStages, kPairSfSlotsF1, true>(tmW, tmX2, q, a.max_items[v], st);
+    if (e != cudaSuccess || a.max_group_rows <= bounds[v]) return e;
+  }
+  return cudaSuccess;
+}
+
 cudaError_t launch_grouped_gemm(const GemmLaunch& a, cudaStream_t st) {
   GemmParams p{};
   p.w_scales = a.w_scales;
@@ -1298,6 +1490,9 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& a, cudaStream_t st) {
   p.T = a.T;
   p.k = a.k;
   p.has_shared = a.has_shared;
+  p.hq = a.hq;
+  p.hs = a.hs;
+  if (a.hq) return launch_w13_fused_swiglu(a, p, st);
   // A list whose groups cannot exist (no group has more than max_group_rows rows) is
   // provably empty and not launched.
   // The first launch inherits the caller's word on the plan; each later variant
@@ -1310,7 +1505,7 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& a, cudaStream_t st) {
   e = launch_variant<kMediumBN, kMediumStages, kMediumStagesKO1, kMediumOcc>(
       a, p, a.items[1], a.item_counts + 1, a.max_items[1], st);
   if (e != cudaSuccess || a.max_group_rows <= kMediumBN) return e;
-  if (a.N % 256 == 0 && a.K % 512 == 0 && a.out == nullptr) {
+  if (a.pair_tiles && a.N % 256 == 0 && a.K % 512 == 0 && a.out == nullptr) {
     // mid and large tiles on SM pairs (same kernel for both lists; the combine-fused
     // W2 epilogue stays on the one-SM kernels)
     CUtensorMap tmW, tmX;
@@ -1320,11 +1515,12 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& a, cudaStream_t st) {
     GemmParams q = p;
     q.items = a.items[2];
     q.item_count = a.item_counts + 2;
-    e = launch_pair<kPairBN, kPairStages, kPairSfSlots>(tmW, tmX, q, a.max_items[2], st);
+    e = launch_pair<kPairBN, kPairStages, kPairSfSlots, false>(tmW, tmX, q, a.max_items[2], st);
     if (e != cudaSuccess || a.max_group_rows <= kMidBN) return e;
     q.items = a.items[3];
     q.item_count = a.item_counts + 3;
-    return launch_pair<kPairBN, kPairStages, kPairSfSlots>(tmW, tmX, q, a.max_items[3], st);
+    return launch_pair<kPairBN, kPairStages, kPairSfSlots, false>(tmW, tmX, q, a.max_items[3],
+                                                                   st);
   }
   e = launch_variant<kMidBN, kMidStages, kMidStagesKO1, 1>(a, p, a.items[2],
                                                            a.item_counts + 2, a.max_items[2], st);

@@ -55,7 +55,9 @@ constexpr int kLargeStagesKO1 = 2;
 // (112 per SM), three stages of two 128-K sub-tiles.
 constexpr int kPairBN = 224;
 constexpr int kPairStages = 3;
-constexpr int kPairSfSlots = 5;  // scale-factor ring (its own barriers)
+constexpr int kPairSfSlots = 5;    // scale-factor ring (its own barriers)
+constexpr int kPairSfSlotsF1 = 4;  // with the fused SwiGLU epilogue's scratch
+
 
 // The tile plan's work lists, one per variant (0 small, 1 medium, 2 mid, 3 large),
 // each {group, row0, rows, 0} in group order, and their lengths.
@@ -129,6 +131,13 @@ struct GemmLaunch {
   const float* cw = nullptr;
   int32_t* cnt = nullptr;
   int T = 0, k = 0, has_shared = 0;
+  // f1 (the W13 GEMM only): with hq non-null the epilogue performs SwiGLU + FP8
+  // quantisation into hq [rows_total][N/2] and hs [rows_total][N/256] (y is not written).
+  uint8_t* hq = nullptr;
+  uint8_t* hs = nullptr;
+  // 1: the mid and large lists on the SM-pair kernel (when N % 256 == 0 and K % 512 ==
+  // 0), else on the one-SM mid and large variants
+  int pair_tiles = 0;
 };
 cudaError_t launch_grouped_gemm(const GemmLaunch& a, cudaStream_t st);
 
