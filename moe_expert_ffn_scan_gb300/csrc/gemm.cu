@@ -626,9 +626,20 @@ __global__ void __launch_bounds__(256, OCC)
       int g, row0, rows, nt;
       if (!load_item(L, g, row0, rows, nt)) continue;
       const uint32_t b = tc & 1u, use = tc >> 1;
-      int w_ok = 1;
-      if (lane == 0) w_ok = mbar_wait(&acc_full[b], use & 1u, p.status, abort_flag);
-      if (!__shfl_sync(0xFFFFFFFFu, w_ok, 0)) break;
+      if (p.out) {
+        // the fused combine meets at named barriers: one thread waits for the four warps,
+        // so that none leaves the loop alone
+        volatile int* go = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 8);
+        if (q == 0 && lane == 0) *go = mbar_wait(&acc_full[b], use & 1u, p.status, abort_flag);
+        epilogue_bar_sync();
+        const int ok_all = *go;
+        epilogue_bar_sync();
+        if (!ok_all) break;
+      } else {
+        int w_ok = 1;
+        if (lane == 0) w_ok = mbar_wait(&acc_full[b], use & 1u, p.status, abort_flag);
+        if (!__shfl_sync(0xFFFFFFFFu, w_ok, 0)) break;
+      }
       tc_fence_after();
       const int n = nt * 128 + q * 32 + lane;
       uint16_t* ycol = p.y + static_cast<size_t>(row0) * p.N + n;
@@ -736,7 +747,7 @@ struct GemmCfg2 {
   static constexpr int kOffAmPeer = kOffAmMine + BN2 * 4;
   static constexpr int kOffCodes = kOffAmPeer + 2 * BN2 * 4;
   static constexpr int kOffEs = kOffCodes + 16 * 64;
-  static constexpr int kSmemBytes = F1 ? kOffEs + 16 * 4 : kOffMisc + 16;
+  static constexpr int kSmemBytes = F1 ? kOffEs + 16 * 4 + 16 : kOffMisc + 16;
   static constexpr int kSfCols = 4 * (KO + kSfbAtoms);
   static constexpr int kTmemNeed = 2 * BN2 + STAGES * kSfCols;
   static constexpr int kTmemCols = kTmemNeed <= 256 ? 256 : 512;
@@ -774,6 +785,7 @@ __device__ __forceinline__ void f1_epilogue(const GemmParams& p, uint32_t tmem, 
   float* am_peer = reinterpret_cast<float*>(smem + off_am_peer);    // [2][BN2]
   uint8_t* codes = smem + off_codes;                                // [16][64]
   int* es = reinterpret_cast<int*>(smem + off_es);                  // [16]
+  volatile int* go = reinterpret_cast<volatile int*>(smem + off_es + 16 * 4);  // shared answer
   const int I = p.N / 2;
   const int nblk = I / 128;
   const uint32_t peer = rank ^ 1u;
@@ -782,9 +794,12 @@ __device__ __forceinline__ void f1_epilogue(const GemmParams& p, uint32_t tmem, 
     int g, row0, rows, nt2;
     if (!load_item(L, g, row0, rows, nt2)) continue;
     const uint32_t b = tc & 1u, use = tc >> 1;
+    // one thread waits and the four warps take its answer together: they meet at named
+    // barriers below, which a warp that left the loop alone would never reach
     int w_ok = 1;
-    if (lane == 0) w_ok = mbar_wait(&acc_full[b], use & 1u, p.status, abort_flag);
-    if (!__shfl_sync(0xFFFFFFFFu, w_ok, 0)) break;
+    if (q == 0 && lane == 0) *go = mbar_wait(&acc_full[b], use & 1u, p.status, abort_flag);
+    epilogue_bar_sync();
+    if (!*go) break;
     tc_fence_after();
     const uint32_t acc = tmem + (static_cast<uint32_t>(q * 32) << 16) + b * BN2;
     // h of this thread's feature for tokens c0 .. c0 + 15 (gate warps only)
@@ -832,11 +847,10 @@ __device__ __forceinline__ void f1_epilogue(const GemmParams& p, uint32_t tmem, 
                      : "memory");
       mbar_arrive_cluster(mapa_shared(smem_u32(&xchg_full[b]), peer));
       w_ok = mbar_wait(&xchg_full[b], use & 1u, p.status, abort_flag);
-      es[0] = w_ok;
+      *go = w_ok;
     }
     epilogue_bar_sync();
-    if (!es[0]) break;
-    epilogue_bar_sync();
+    if (!*go) break;
     // pass 2: codes and scales
     for (int c0 = 0; c0 < rows; c0 += 16) {
       float h[16];
