@@ -159,6 +159,23 @@ int moe_route_static_status(void* stream, uint32_t* bits_out);
 int moe_router_logits(int32_t T, int32_t H, int32_t E, const uint16_t* x, const float* wg,
                       float* logits, void* stream);
 
+/* f4 on the tensor cores.  The gate weight is split once (weight preprocessing, like
+ * loading a checkpoint) into three bf16 matrices with wg == hi + mid + lo exactly
+ * (8 + 8 + 8 significant bits; exact unless a piece falls below bf16's normal range,
+ * i.e. for weights under about 2^-110 in magnitude): moe_router_split writes them to
+ * wg3 [3][E][H] (moe_router_split_bytes(E, H) bytes, 16-byte aligned, caller-owned).
+ * moe_router_logits_split then computes the same logits as moe_router_logits with
+ * tcgen05 MMAs: each product x * piece is exact in fp32 and the three pieces' products
+ * of every 16-column step are accumulated in fp32 (a fixed order: run-to-run
+ * identical; within the same fp32 accumulation bound).  The pages' TopK step
+ * (LMSYS-H20 §3.2) ranks these scores.  Shapes and alignment as moe_router_logits; no
+ * workspace; device-side wait failures of this call are not reported (it has no status
+ * word). */
+size_t moe_router_split_bytes(int32_t E, int32_t H);
+int moe_router_split(int32_t E, int32_t H, const float* wg, uint16_t* wg3, void* stream);
+int moe_router_logits_split(int32_t T, int32_t H, int32_t E, const uint16_t* x,
+                            const uint16_t* wg3, float* logits, void* stream);
+
 /* a3: online FP8 E4M3 quantisation of bf16 x [rows][cols] with one power-of-two
  * scale per row per 128 columns (rule above) -> q [rows][cols], s [rows][cols/128].
  * Pages: LMSYS-H20 §2.2 (online FP8 activations), §3.2 (fused FP8 quantisation).

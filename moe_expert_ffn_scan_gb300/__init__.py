@@ -80,6 +80,12 @@ def lib():
             getattr(L, fn).restype = _SZ
         L.moe_route.argtypes = [_DP, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]
         L.moe_quant_act.argtypes = [_I, _I, _P, _P, _P, _P]
+        L.moe_router_split_bytes.argtypes = [_I, _I]
+        L.moe_router_split_bytes.restype = _SZ
+        L.moe_router_split.argtypes = [_I, _I, _P, _P, _P]
+        L.moe_router_split.restype = ctypes.c_int
+        L.moe_router_logits_split.argtypes = [_I, _I, _I, _P, _P, _P, _P]
+        L.moe_router_logits_split.restype = ctypes.c_int
         L.moe_router_logits.argtypes = [_I, _I, _I, _P, _P, _P, _P]
         L.moe_grouped_gemm_w13.argtypes = [_DP, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]
         L.moe_swiglu_quant.argtypes = [_I, _I, _P, _P, _P, _P]
@@ -206,6 +212,25 @@ def moe_router_logits(x, wg, logits, stream=None):
     E = wg.shape[0]
     _check("moe_router_logits", lib().moe_router_logits(T, H, E, _p(x), _p(wg), _p(logits),
                                                         _stream(stream)))
+
+
+def moe_router_split(wg, wg3=None, stream=None):
+    """Splits the fp32 gate weight [E, H] into the three bf16 pieces [3, E, H] the
+    tensor-core router projection reads (hi + mid + lo == wg).  Returns wg3."""
+    E, H = wg.shape
+    if wg3 is None:
+        wg3 = torch.empty(3, E, H, dtype=torch.bfloat16, device=wg.device)
+    _check("moe_router_split", lib().moe_router_split(E, H, _p(wg), _p(wg3), _stream(stream)))
+    return wg3
+
+
+def moe_router_logits_split(x, wg3, logits, stream=None):
+    """logits [T, E] fp32 = x [T, H] bf16 . wg^T on the tensor cores, from the pieces of
+    moe_router_split."""
+    T, H = x.shape
+    E = wg3.shape[1]
+    _check("moe_router_logits_split", lib().moe_router_logits_split(
+        T, H, E, _p(x), _p(wg3), _p(logits), _stream(stream)))
 
 
 def moe_quant_act(x, q, s, stream=None):

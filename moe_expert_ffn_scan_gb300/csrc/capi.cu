@@ -365,6 +365,26 @@ int moe_router_logits(int32_t T, int32_t H, int32_t E, const uint16_t* x, const 
       launch_router_logits(x, wg, logits, T, H, E, static_cast<cudaStream_t>(stream)));
 }
 
+size_t moe_router_split_bytes(int32_t E, int32_t H) {
+  if (E < 1 || H < 16 || H % 16) return 0;
+  return static_cast<size_t>(3) * E * H * sizeof(uint16_t);
+}
+
+int moe_router_split(int32_t E, int32_t H, const float* wg, uint16_t* wg3, void* stream) {
+  if (E < 1 || H < 16 || H % 16) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!wg || !wg3 || !aligned(wg, 4) || !aligned(wg3, 16)) return MOE_ERR_INVALID_ARG;
+  return cuda_rc(launch_router_split(wg, E, H, wg3, static_cast<cudaStream_t>(stream)));
+}
+
+int moe_router_logits_split(int32_t T, int32_t H, int32_t E, const uint16_t* x,
+                            const uint16_t* wg3, float* logits, void* stream) {
+  if (T < 1 || E < 1 || H < 16 || H % 16) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!x || !wg3 || !logits || !aligned(x, 16) || !aligned(wg3, 16) || !aligned(logits, 4))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_rc(launch_router_logits_split(x, wg3, logits, T, H, E, nullptr,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
 int moe_quant_act(int32_t rows, int32_t cols, const uint16_t* x, uint8_t* q, uint8_t* s,
                   void* stream) {
   if (rows < 0 || cols <= 0 || cols % 128) return MOE_ERR_UNSUPPORTED_SHAPE;

@@ -98,6 +98,11 @@ cudaError_t launch_quant_act(const uint16_t* x, int rows, int cols, uint8_t* q, 
 constexpr int kRouterGemvMaxT = 1024;
 cudaError_t launch_router_logits(const uint16_t* x, const float* wg, float* logits, int T, int H,
                                  int E, cudaStream_t st);
+// The router projection on the tensor cores: W_g split into three bf16 pieces
+// [3][E][H] (hi, mid, lo; hi + mid + lo == W_g), then logits from x and the pieces.
+cudaError_t launch_router_split(const float* wg, int E, int H, uint16_t* wg3, cudaStream_t st);
+cudaError_t launch_router_logits_split(const uint16_t* x, const uint16_t* wg3, float* logits,
+                                       int T, int H, int E, uint32_t* status, cudaStream_t st);
 cudaError_t launch_swiglu_quant(const uint16_t* y13, int rows, int I, uint8_t* hq, uint8_t* hs,
                                 cudaStream_t st);
 cudaError_t launch_gather_rows(const uint8_t* xq, const uint8_t* xs, const int32_t* perm_src,

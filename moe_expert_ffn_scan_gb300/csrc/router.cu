@@ -206,4 +206,243 @@ cudaError_t launch_router_logits(const uint16_t* x, const float* wg, float* logi
   return launch_k(k_router_tiled, grid, 256, 0, st, x, wg, logits, T, H, E);
 }
 
+
+// ---------------------------------------------------------------- tensor cores ------
+// The same projection on the tcgen05 tensor cores, for prefill-sized T.  W_g is split
+// once into three bf16 matrices with W_g = hi + mid + lo exactly (hi = bf16(W_g), mid =
+// bf16(W_g - hi), lo = W_g - hi - mid: 8 + 8 + 8 significant bits, the fp32 weight's 24;
+// exact unless a piece falls below bf16's normal range, i.e. for weights under about
+// 2^-110).  x is bf16, so every product x * piece is exact in fp32, and kind::f16 MMAs
+// with fp32 accumulation sum x . hi, x . mid and x . lo of each 16-column step into one
+// accumulator: the fp32 contraction, on the tensor cores.
+//
+// k_router_tc: a CTA owns tiles of 128 tokens x 128 experts (persistent), K staged 64
+// columns at a time (one 128-byte swizzle row) by TMA -- x's tile and the three
+// pieces' tiles -- three stages; warp 0 issues the TMA, warp 1 the MMAs (12 per stage:
+// 4 K-steps x 3 pieces, into a double-buffered TMEM accumulator), warps 4-7 store the
+// fp32 logits.  Every wait is bounded.
+
+namespace {
+
+constexpr int kRtStages = 3;
+constexpr int kRtTile = 128;                     // tokens and experts per tile
+constexpr int kRtXBytes = kRtTile * 128;          // [128 rows][64 bf16]
+constexpr int kRtStageBytes = 4 * kRtXBytes;      // x + three pieces
+constexpr int kRtOffBar = kRtStages * kRtStageBytes;
+constexpr int kRtSmem = kRtOffBar + (2 * kRtStages + 4) * 8 + 16;
+
+__global__ void __launch_bounds__(256) k_router_split(const float* __restrict__ wg, size_t n,
+                                                      uint16_t* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
+  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const float w = wg[i];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+    const float r1 = w - __bfloat162float(hi);  // exact
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));  // exact
+    out[i] = *reinterpret_cast<const uint16_t*>(&hi);
+    out[n + i] = *reinterpret_cast<const uint16_t*>(&mid);
+    out[2 * n + i] = *reinterpret_cast<const uint16_t*>(&lo);
+  }
+}
+
+__device__ __forceinline__ uint32_t idesc_bf16_m128(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(128 >> 4) << 24);
+}
+
+__global__ void __launch_bounds__(256, 1)
+    k_router_tc(const __grid_constant__ CUtensorMap tmXr, const __grid_constant__ CUtensorMap tmWr,
+                float* __restrict__ logits, int T, int H, int E, uint32_t* status) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kRtOffBar);
+  uint64_t* full = bars;
+  uint64_t* empty = full + kRtStages;
+  uint64_t* acc_full = empty + kRtStages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kRtOffBar + (2 * kRtStages + 4) * 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool misaligned = (smem_u32(smem) & 1023u) != 0;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kRtStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);
+    }
+    *abort_flag = misaligned ? 1 : 0;
+    if (misaligned) set_status(status, STATUS_BAD_PLAN);
+    fence_mbar_init();
+    tma_prefetch_desc(&tmXr);
+    tma_prefetch_desc(&tmWr);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, 256);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  pdl_wait();
+  const uint32_t tmem = *tmem_slot;
+  const int ttiles = (T + kRtTile - 1) / kRtTile, etiles = (E + kRtTile - 1) / kRtTile;
+  const long long total = static_cast<long long>(ttiles) * etiles;
+  const int nk = (H + 63) / 64;
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t it = 0;
+      for (long long L = blockIdx.x; L < total && !*abort_flag; L += gridDim.x) {
+        const int t0 = static_cast<int>(L / etiles) * kRtTile;
+        const int e0 = static_cast<int>(L % etiles) * kRtTile;
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % kRtStages;
+          if (it >= kRtStages &&
+              !mbar_wait(&empty[s], ((it / kRtStages) & 1u) ^ 1u, status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + s * kRtStageBytes;
+          mbar_arrive_expect_tx(&full[s], kRtStageBytes);
+          tma_load_2d(st, &tmXr, &full[s], kb * 64, t0);
+#pragma unroll
+          for (int pc = 0; pc < 3; ++pc)
+            tma_load_3d(st + (1 + pc) * kRtXBytes, &tmWr, &full[s], kb * 64, e0, pc);
+        }
+        if (!ok) break;
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      uint32_t it = 0, tc = 0;
+      const uint32_t idesc = idesc_bf16_m128(kRtTile);
+      for (long long L = blockIdx.x; L < total && !*abort_flag; L += gridDim.x) {
+        const uint32_t b = tc & 1u, use = tc >> 1;
+        if (tc >= 2 && !mbar_wait(&acc_empty[b], (use - 1) & 1u, status, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + b * kRtTile;
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % kRtStages;
+          if (!mbar_wait(&full[s], (it / kRtStages) & 1u, status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t base = smem_u32(smem + s * kRtStageBytes);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = smem_desc(base + kk * 32, 0, 1024, kLayoutSw128);
+#pragma unroll
+            for (int pc = 0; pc < 3; ++pc) {
+              const uint64_t bd =
+                  smem_desc(base + (1 + pc) * kRtXBytes + kk * 32, 0, 1024, kLayoutSw128);
+              mma_bf16_ss(d, ad, bd, idesc, kb > 0 || kk > 0 || pc > 0);
+            }
+          }
+          tc_commit(&empty[s]);
+        }
+        if (!ok) break;
+        tc_commit(&acc_full[b]);
+        ++tc;
+      }
+    }
+  } else if (warp >= 4) {
+    const int q = warp - 4;
+    uint32_t tc = 0;
+    for (long long L = blockIdx.x; L < total && !*abort_flag; L += gridDim.x) {
+      const int t0 = static_cast<int>(L / etiles) * kRtTile;
+      const int e0 = static_cast<int>(L % etiles) * kRtTile;
+      const uint32_t b = tc & 1u, use = tc >> 1;
+      int w_ok = 1;
+      if (lane == 0) w_ok = mbar_wait(&acc_full[b], use & 1u, status, abort_flag);
+      if (!__shfl_sync(0xFFFFFFFFu, w_ok, 0)) break;
+      tc_fence_after();
+      const int t = t0 + q * 32 + lane;  // this thread's token row (TMEM lane)
+      const uint32_t acc = tmem + (static_cast<uint32_t>(q * 32) << 16) + b * kRtTile;
+      float* out = logits + static_cast<size_t>(t < T ? t : 0) * E;
+      for (int c0 = 0; c0 < kRtTile && e0 + c0 < E; c0 += 16) {
+        uint32_t r[16];
+        tmem_ld_32x32b_x16(acc + c0, r);
+        tmem_ld_wait();
+        if (t < T) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (e0 + c0 + i < E) out[e0 + c0 + i] = __uint_as_float(r[i]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[b]);
+      ++tc;
+    }
+  }
+  pdl_trigger();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_router_split(const float* wg, int E, int H, uint16_t* wg3, cudaStream_t st) {
+  const size_t n = static_cast<size_t>(E) * H;
+  if (n == 0) return cudaSuccess;
+  const long long blocks = static_cast<long long>((n + 255) / 256);
+  const unsigned grid = static_cast<unsigned>(blocks < 4096 ? blocks : 4096);
+  return launch_k(k_router_split, grid, 256, 0, st, wg, n, wg3);
+}
+
+cudaError_t launch_router_logits_split(const uint16_t* x, const uint16_t* wg3, float* logits,
+                                       int T, int H, int E, uint32_t* status, cudaStream_t st) {
+  EncodeTiledFn enc = get_encode_tiled_fn();
+  if (!enc) return cudaErrorNotSupported;
+  CUtensorMap tmX, tmW;
+  {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(H) * 2};
+    cuuint32_t box[2] = {64, kRtTile};
+    cuuint32_t es[2] = {1, 1};
+    if (enc(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides,
+            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(E), 3};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(H) * 2,
+                             static_cast<cuuint64_t>(E) * static_cast<cuuint64_t>(H) * 2};
+    cuuint32_t box[3] = {64, kRtTile, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (enc(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(wg3), dims, strides,
+            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  static unsigned long long attr_ctx[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  const unsigned long long ctx = current_context_id();
+  if (ctx == 0 || attr_ctx[dev] != ctx) {
+    e = cudaFuncSetAttribute(k_router_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kRtSmem);
+    if (e != cudaSuccess) return e;
+    attr_ctx[dev] = current_context_id();
+  }
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const long long tiles = static_cast<long long>((T + kRtTile - 1) / kRtTile) *
+                          ((E + kRtTile - 1) / kRtTile);
+  const int grid = static_cast<int>(tiles < sms ? tiles : sms);
+  return launch_k(k_router_tc, grid, 256, kRtSmem, st, tmX, tmW, logits, T, H, E, status);
+}
+
 }  // namespace moe

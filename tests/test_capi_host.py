@@ -164,6 +164,17 @@ def test_nvfp4_validation_before_any_launch(lib):
                                          None) == 3
 
 
+def test_router_split_validation(lib):
+    P = ctypes.c_void_p
+    assert moe.lib().moe_router_split_bytes(384, 7168) == 3 * 384 * 7168 * 2
+    assert moe.lib().moe_router_split_bytes(8, 100) == 0
+    assert lib.moe_router_split(8, 100, P(0x1000), P(0x1000), None) == 2
+    assert lib.moe_router_split(8, 128, P(0x1000), P(0x1008), None) == 1
+    assert lib.moe_router_logits_split(0, 128, 8, P(0x1000), P(0x1000), P(0x1000), None) == 2
+    assert lib.moe_router_logits_split(4, 128, 8, P(0x1008), P(0x1000), P(0x1000), None) == 1
+    assert lib.moe_router_logits_split(4, 128, 8, P(0x1000), None, P(0x1000), None) == 1
+
+
 def test_python_binding_rejects_host_tensors(lib):
     import torch
     x = torch.zeros(4, 128, dtype=torch.bfloat16)

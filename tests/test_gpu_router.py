@@ -122,3 +122,69 @@ def test_router_logits_prefill_size_sampled():
     got = lg[torch.from_numpy(toks).to(DEV)].cpu().numpy().astype(np.float64)
     assert np.all(np.abs(got - ref) <= _bound(xb, wn))
     assert torch.isfinite(lg).all()
+
+
+# ---------------------------------------------------------------- tensor cores ------
+
+def _run_split(x, wg):
+    wg3 = moe.moe_router_split(wg)
+    lg = torch.full((x.shape[0], wg.shape[0]), float("nan"), dtype=torch.float32, device=DEV)
+    moe.moe_router_logits_split(x, wg3, lg)
+    torch.cuda.synchronize()
+    return lg, wg3
+
+
+def test_router_split_is_exact():
+    """hi + mid + lo reproduces every fp32 gate weight exactly (checked in float64)."""
+    for E, H, seed in ((384, 7168, 1), (8, 512, 2)):
+        wg = gi.gate_weight(E, H, seed, DEV)
+        wg3 = moe.moe_router_split(wg)
+        torch.cuda.synchronize()
+        pieces = wg3.float().cpu().numpy().astype(np.float64)
+        assert np.array_equal(pieces.sum(axis=0), wg.cpu().numpy().astype(np.float64))
+    # and on values that need all three pieces: 24 significant bits
+    w = torch.tensor([[1.0 + 2.0 ** -23, -3.0 - 2.0 ** -20, 0.02 + 2.0 ** -30, 1e-20] * 4],
+                     dtype=torch.float32, device=DEV)
+    p = moe.moe_router_split(w).float().cpu().numpy().astype(np.float64)
+    assert np.array_equal(p.sum(axis=0), w.cpu().numpy().astype(np.float64))
+
+
+@pytest.mark.parametrize("T,H,E", [
+    (64, 512, 8),       # the tiny layer's dims: one tile, 8 of 128 expert columns
+    (130, 1024, 40),    # ragged token tile
+    (1300, 256, 1000),  # ragged token and expert tiles, many tiles per CTA
+    (300, 7168, 384),   # the model's H and E
+    (17, 16, 7),        # H below one 64-column stage
+    (200, 80, 130),     # H not a multiple of 64: a zero-filled stage tail
+])
+def test_router_logits_split_matches_oracle(T, H, E):
+    x, wg = _inputs(T, H, E, seed=T + E + 1)
+    lg, _ = _run_split(x, wg)
+    lg = lg.cpu().numpy().astype(np.float64)
+    xb = bits_np(x)
+    wn = wg.cpu().numpy()
+    ref = o.router_logits(xb, wn)
+    err = np.abs(lg - ref)
+    bound = _bound(xb, wn)
+    assert np.all(np.isfinite(lg)), "unwritten or non-finite logits"
+    bad = np.argwhere(err > bound)
+    assert bad.size == 0, f"{len(bad)} logits out of bound, first {bad[:3].tolist()}"
+    assert float(np.median(err / np.maximum(bound, 1e-300))) < 0.05
+
+
+def test_router_logits_split_deterministic_and_prefill_sampled():
+    T, H, E = 32768, 7168, 384
+    x, wg = _inputs(T, H, E, seed=3)
+    a, wg3 = _run_split(x, wg)
+    b = torch.empty_like(a)
+    moe.moe_router_logits_split(x, wg3, b)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    rng = np.random.default_rng(3)
+    toks = np.sort(rng.choice(T, size=64, replace=False))
+    xb = bits_np(x[torch.from_numpy(toks).to(DEV)])
+    wn = wg.cpu().numpy()
+    ref = o.router_logits(xb, wn)
+    got = a[torch.from_numpy(toks).to(DEV)].cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(got - ref) <= _bound(xb, wn))
+    assert torch.isfinite(a).all()
