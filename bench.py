@@ -533,8 +533,19 @@ def measure_layer(args, workload, steps, warmup, rank, world, local, clocks, *, 
         # layer's boundary takes logits); W_g synthetic fp32 [E, H]
         wg = t["wg"] if t.get("wg") is not None else gi.gate_weight(d.E, d.H, args.seed, dev)
         rlg = torch.empty(d.T, d.E, dtype=torch.float32, device=dev)
+        # above ROUTER_TC_MIN_T tokens the tensor-core form (W_g split once per weight
+        # into three bf16 pieces, outside the timed region); below, the fp32 GEMV
+        use_tc = d.T >= ROUTER_TC_MIN_T
+        if use_tc:
+            wg3 = moe.moe_router_split(wg)
+
+            def router_call():
+                moe.moe_router_logits_split(x, wg3, rlg)
+        else:
+            def router_call():
+                moe.moe_router_logits(x, wg, rlg)
         for _ in range(3):
-            moe.moe_router_logits(x, wg, rlg)
+            router_call()
         n_r = min(steps, 20)
         r_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                 for _ in range(n_r)]
@@ -542,14 +553,21 @@ def measure_layer(args, workload, steps, warmup, rank, world, local, clocks, *, 
             if do_flush:
                 flush.fill_(i & 0xFF)
             r_ev[i][0].record(stream)
-            moe.moe_router_logits(x, wg, rlg)
+            router_call()
             r_ev[i][1].record(stream)
         torch.cuda.synchronize()
         r_ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in r_ev)
-        r_bytes = d.E * d.H * 4 + d.T * d.H * 2 + d.T * d.E * 4
+        r_bytes = d.E * d.H * (6 if use_tc else 4) + d.T * d.H * 2 + d.T * d.E * 4
+        r_flop = 2.0 * d.T * d.E * d.H
         router_rec = {"ms": r_ms, "gbs": r_bytes / (r_ms * 1e-3) / 1e9,
-                      "tflops": 2.0 * d.T * d.E * d.H / (r_ms * 1e-3) / 1e12,
-                      "kernel": "k_router_gemv" if d.T <= 1024 else "k_router_tiled"}
+                      "tflops": r_flop / (r_ms * 1e-3) / 1e12,
+                      "kernel": "k_router_tc" if use_tc else
+                      ("k_router_gemv" if d.T <= 1024 else "k_router_tiled")}
+        if use_tc:
+            # three bf16 MMAs per product: the tensor pipe's work is 3x the projection's
+            bpk, bpk_src = bf16_tensor_peak_tflops()
+            router_rec["tensor_frac"] = 3.0 * r_flop / (r_ms * 1e-3) / 1e12 / bpk
+            router_rec["tensor_peak"] = {"tflops": bpk, "source": bpk_src}
 
     cpu_rec = None
     if cpu and rank == 0:
@@ -673,6 +691,9 @@ def sub_record(rec):
 # Steps of the extra workloads the default run measures beside the headline line:
 # enough that each timed region lasts >= 2 s (>= 10 clock samples at 200 ms).
 EXTRA_STEPS = {"decode256": 600, "prefill": 60, "decode_nvfp4": 3000}
+# token count from which the router timing uses the tensor-core projection (measured
+# faster from ~256 tokens; the fp32 GEMV wins for decode-sized batches)
+ROUTER_TC_MIN_T = 256
 EXTRA_E2E_STEPS = {"decode256": 50, "prefill": 20}
 
 

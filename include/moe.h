@@ -170,7 +170,9 @@ int moe_router_logits(int32_t T, int32_t H, int32_t E, const uint16_t* x, const 
  * identical; within the same fp32 accumulation bound).  The pages' TopK step
  * (LMSYS-H20 §3.2) ranks these scores.  Shapes and alignment as moe_router_logits; no
  * workspace; device-side wait failures of this call are not reported (it has no status
- * word). */
+ * word).  Its tiles are 128 tokens x 128 experts, so it pays off from a few hundred
+ * tokens (on GB300 at H = 7168, E = 384: 0.40 ms vs 4.2 ms at 32K tokens, 0.08 vs 0.10
+ * ms at 256); decode-sized batches are faster through moe_router_logits. */
 size_t moe_router_split_bytes(int32_t E, int32_t H);
 int moe_router_split(int32_t E, int32_t H, const float* wg, uint16_t* wg3, void* stream);
 int moe_router_logits_split(int32_t T, int32_t H, int32_t E, const uint16_t* x,

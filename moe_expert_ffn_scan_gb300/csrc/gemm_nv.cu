@@ -134,6 +134,44 @@ __device__ __forceinline__ __nv_bfloat162 e4m3_to_bf16x2(uint32_t b) {
   return __float2bfloat162_rn(f);
 }
 
+// Two E4M3 scale bytes (the low byte is the first block's) -> each as a pair of equal
+// bf16 values (exact: 4 significant bits), for the table-decoding converter.
+__device__ __forceinline__ void e4m3x2_to_bf16x2_dup(uint32_t two, uint32_t& s0, uint32_t& s1) {
+  const __half2_raw h2 =
+      __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two & 0xFFFFu), __NV_E4M3);
+  const __half2 h(h2);
+  const __nv_bfloat162 b0 = __float2bfloat162_rn(__low2float(h));
+  const __nv_bfloat162 b1 = __float2bfloat162_rn(__high2float(h));
+  s0 = *reinterpret_cast<const uint32_t*>(&b0);
+  s1 = *reinterpret_cast<const uint32_t*>(&b1);
+}
+
+// Eight E2M1 codes (one 32-bit word) -> four bf16 pairs times the block scale `sc`
+// (a bf16 pair): byte i of the word indexes the decode table (shared-memory address
+// `lut_lane` + 128 * byte: this lane's copy of the entry), the pair is multiplied by
+// the scale (exact).
+__device__ __forceinline__ void decode8_lut(uint32_t w, uint32_t lut_lane, uint32_t sc,
+                                            uint32_t* o) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t addr = lut_lane + (__byte_perm(w, 0u, 0x4440u | i) << 7);
+    uint32_t v;
+    asm("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[i]) : "r"(v), "r"(sc));
+  }
+}
+
+// tcgen05.st of 16 columns; no "memory" clobber: it reads only registers, and its
+// order against the other tcgen05 / mbarrier instructions (all volatile asm) is kept.
+__device__ __forceinline__ void tmem_st_x16_regs(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, "
+      "%10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]));
+}
+
 __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, __nv_bfloat162 s) {
   __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&a);
   v = __hmul2(v, s);
@@ -316,7 +354,7 @@ __global__ void __launch_bounds__(NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>::kThr
     const int cg = (warp - 4) >> 2;    // converter group: stages it with it % NG == cg
     const int r = q * 32 + lane;       // weight row within the tile
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-    const uint32_t* lut = reinterpret_cast<const uint32_t*>(smem + C::kOffLut) + lane;
+    const uint32_t lut_lane = smem_u32(smem + C::kOffLut) + 4u * lane;
     uint32_t it = 0;
     bool ok = true;
     for (long long L = blockIdx.x; L < total && ok && !*abort_flag; L += gridDim.x) {
@@ -357,23 +395,33 @@ __global__ void __launch_bounds__(NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>::kThr
         __syncwarp();
         if (lane == 0) mbar_arrive(&code_empty[cs]);
         const uint32_t col0 = a_base + s * C::kACols;
+        if constexpr (LUT) {
+          // a 128-K stage: scale bytes 0-7 (even 128-K step) or 8-15 (odd) of the row
+          const uint32_t s_lo = (kb & 1) ? sv.z : sv.x;
+          const uint32_t s_hi = (kb & 1) ? sv.w : sv.y;
 #pragma unroll
-        for (int blk = 0; blk < C::kBlocks; ++blk) {
-          const int sb = sbyte0 + blk;
-          const uint32_t sw = sb < 4 ? sv.x : sb < 8 ? sv.y : sb < 12 ? sv.z : sv.w;
-          const __nv_bfloat162 sc = e4m3_to_bf16x2((sw >> (8 * (sb & 3))) & 0xFFu);
-          // 16 elements = 8 code bytes = two 32-bit words of chunk blk / 2
-          const uint4 cv = cw[blk >> 1];
-          const uint32_t w0 = (blk & 1) ? cv.z : cv.x;
-          const uint32_t w1 = (blk & 1) ? cv.w : cv.y;
-          uint32_t o[8];
-          if constexpr (LUT) {
+          for (int bp = 0; bp < C::kBlocks / 2; ++bp) {  // two 16-element blocks = chunk bp
+            uint32_t sc0, sc1;
+            e4m3x2_to_bf16x2_dup((bp < 2 ? s_lo : s_hi) >> (16 * (bp & 1)), sc0, sc1);
+            const uint4 cv = cw[bp];
+            uint32_t o[16];
+            decode8_lut(cv.x, lut_lane, sc0, o);
+            decode8_lut(cv.y, lut_lane, sc0, o + 4);
+            decode8_lut(cv.z, lut_lane, sc1, o + 8);
+            decode8_lut(cv.w, lut_lane, sc1, o + 12);
+            tmem_st_x16_regs(lane_base + col0 + bp * 16, o);
+          }
+        } else {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              o[i] = bf16x2_mul(lut[__byte_perm(w0, 0u, 0x4440u | i) << 5], sc);
-              o[4 + i] = bf16x2_mul(lut[__byte_perm(w1, 0u, 0x4440u | i) << 5], sc);
-            }
-          } else {
+          for (int blk = 0; blk < C::kBlocks; ++blk) {
+            const int sb = sbyte0 + blk;
+            const uint32_t sw = sb < 4 ? sv.x : sb < 8 ? sv.y : sb < 12 ? sv.z : sv.w;
+            const __nv_bfloat162 sc = e4m3_to_bf16x2((sw >> (8 * (sb & 3))) & 0xFFu);
+            // 16 elements = 8 code bytes = two 32-bit words of chunk blk / 2
+            const uint4 cv = cw[blk >> 1];
+            const uint32_t w0 = (blk & 1) ? cv.z : cv.x;
+            const uint32_t w1 = (blk & 1) ? cv.w : cv.y;
+            uint32_t o[8];
             uint32_t t[4];
             e2m1x8_to_bf16(w0, t);
 #pragma unroll
@@ -381,8 +429,8 @@ __global__ void __launch_bounds__(NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>::kThr
             e2m1x8_to_bf16(w1, t);
 #pragma unroll
             for (int i = 0; i < 4; ++i) o[4 + i] = bf16x2_mul(t[i], sc);
+            tmem_st_32x32b_x8(lane_base + col0 + blk * 8, o);
           }
-          tmem_st_32x32b_x8(lane_base + col0 + blk * 8, o);
         }
         tmem_st_wait();
         // the tokens of this stage must have landed before the MMAs read them
