@@ -91,6 +91,7 @@ struct NvCfg {
   static_assert(kSmemBytes + 1024 <= 232448, "shared memory");
   static_assert(kCodeBytes % 1024 == 0 && kTokBytes % 1024 == 0, "tile alignment");
   static_assert(ISS == 1 || ISS == 2, "issuers");
+  static_assert(NG <= NA && NG <= CS && ISS <= NA, "ring slots advance by at most one lap a step");
   static_assert(KS == 128 || !LUT, "the table-decoding converter takes 128-K stages");
   static_assert(kThreads <= 1024, "threads");
 };
@@ -264,15 +265,15 @@ __global__ void __launch_bounds__(NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>::kThr
   if (warp == 0) {
     // ------------------------------------------------------------ codes + scales TMA
     if (lane == 0) {
-      uint32_t it = 0;
+      uint32_t s = 0, ph = 0;  // code ring slot and lap parity of the next stage
       for (long long L = blockIdx.x; L < total && !*abort_flag; L += gridDim.x) {
         int g, row0, rows, nt;
         if (!load_item(L, g, row0, rows, nt)) continue;
         bool ok = true;
-        for (int kb = 0; kb < nk; ++kb, ++it) {
-          const int s = it % CS;
-          if (it >= CS && !mbar_wait(&code_empty[s], ((it / CS) & 1u) ^ 1u, p.status,
-                                     abort_flag)) {
+        for (int kb = 0; kb < nk; ++kb) {
+          // the slot is free once its converters released it (a fresh barrier's
+          // parity-1 phase counts as complete on the first lap)
+          if (!mbar_wait(&code_empty[s], ph ^ 1u, p.status, abort_flag)) {
             ok = false;
             break;
           }
@@ -281,6 +282,10 @@ __global__ void __launch_bounds__(NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>::kThr
           tma_load_3d(dst, &tmC, &code_full[s], kb * (KS / 2), nt * 128, g);
           tma_load_3d(dst + C::kCodeBytes, &tmS, &code_full[s], ((kb * KS) / 256) * 16,
                       nt * 128, g);
+          if (++s == CS) {
+            s = 0;
+            ph ^= 1u;
+          }
         }
         if (!ok) break;
       }
@@ -288,21 +293,23 @@ __global__ void __launch_bounds__(NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>::kThr
   } else if (warp == 2) {
     // ------------------------------------------------------------ token TMA
     if (lane == 0) {
-      uint32_t it = 0;
+      uint32_t s = 0, ph = 0;  // token ring slot and lap parity of the next stage
       for (long long L = blockIdx.x; L < total && !*abort_flag; L += gridDim.x) {
         int g, row0, rows, nt;
         if (!load_item(L, g, row0, rows, nt)) continue;
         bool ok = true;
-        for (int kb = 0; kb < nk; ++kb, ++it) {
-          const int s = it % NA;
-          if (it >= NA && !mbar_wait(&mma_done[s], ((it / NA) & 1u) ^ 1u, p.status,
-                                     abort_flag)) {
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&mma_done[s], ph ^ 1u, p.status, abort_flag)) {
             ok = false;
             break;
           }
           mbar_arrive_expect_tx(&tok_full[s], C::kTokBytes);
           tma_load_3d(smem + C::kOffTok + s * C::kTokBytes, &tmX, &tok_full[s], 0, row0,
                       kb * (KS / 64));
+          if (++s == NA) {
+            s = 0;
+            ph ^= 1u;
+          }
         }
         if (!ok) break;
       }
@@ -311,7 +318,7 @@ __global__ void __launch_bounds__(NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>::kThr
     // ------------------------------------------------------------ MMA issuer(s)
     const int par = warp == 1 ? 0 : 1;
     if (lane == 0) {
-      uint32_t it = 0, tc = 0;
+      uint32_t it0 = 0, tc = 0;  // it0: global index of the tile's first stage
       uint32_t phases = 0;  // bit s: parity of the next phase of conv_full[par][s]
       for (long long L = blockIdx.x; L < total && !*abort_flag; L += gridDim.x) {
         int g, row0, rows, nt;
@@ -323,29 +330,46 @@ __global__ void __launch_bounds__(NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>::kThr
         const uint32_t d_tmem = tmem + b * C::kAccCols + par * BN;
         const uint32_t idesc = idesc_bf16(bn);
         bool ok = true;
-        for (int kb = 0; kb < nk; ++kb, ++it) {
-          if (ISS == 2 && (kb & 1) != par) continue;
-          const int s = it % NA;
+        const int kb_first = ISS == 2 ? par : 0;
+        // ring slot of the stage (global index it0 + kb) and the parity of its token
+        // phase, advanced by ISS stages per step (one division per tile)
+        uint32_t s = (it0 + kb_first) % NA, tph = ((it0 + kb_first) / NA) & 1u;
+        for (int kb = kb_first; kb < nk; kb += ISS) {  // this issuer's stages
           const uint32_t ph = (phases >> s) & 1u;
           phases ^= 1u << s;
-          if (!mbar_wait(&conv_full[par * NA + s], ph, p.status, abort_flag)) {
+          // the stage's weights are in TMEM (its converters) and its tokens have landed
+          if (!mbar_wait(&conv_full[par * NA + s], ph, p.status, abort_flag) ||
+              !mbar_wait(&tok_full[s], tph, p.status, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t a_t = a_base + s * C::kACols;
-          const uint32_t b0 = smem_u32(smem + C::kOffTok + s * C::kTokBytes);
+          // the 16-K steps of the token tile are fixed offsets from its descriptor (the
+          // start-address field holds address / 16; the tile lies below 256 KB, so
+          // adding to the low word never carries out of the field)
+          const uint64_t bd0 =
+              smem_desc(smem_u32(smem + C::kOffTok + s * C::kTokBytes), 0, 1024, kLayoutSw128);
+          const uint32_t bd_lo = static_cast<uint32_t>(bd0);
+          const uint64_t bd_hi = bd0 & 0xFFFFFFFF00000000ull;
 #pragma unroll
           for (int kk = 0; kk < KS / 16; ++kk) {
-            const uint64_t bd = smem_desc(b0 + (kk >> 2) * (BN * 128) + (kk & 3) * 32, 0, 1024,
-                                          kLayoutSw128);
-            mma_bf16_ts(d_tmem, a_t + kk * 8, bd, idesc, kb > par || kk != 0);
+            const uint32_t off =
+                static_cast<uint32_t>(((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4);
+            mma_bf16_ts(d_tmem, a_t + kk * 8, bd_hi | (bd_lo + off), idesc,
+                        kb > par || kk != 0);
           }
           tc_commit(&mma_done[s]);
+          s += ISS;
+          if (s >= NA) {
+            s -= NA;
+            tph ^= 1u;
+          }
         }
         if (!ok) break;
         tc_commit(&acc_full[b]);
         ++tc;
+        it0 += nk;
       }
     }
   } else if (warp >= 4 && warp < C::kEpiWarp0) {
@@ -355,25 +379,24 @@ __global__ void __launch_bounds__(NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>::kThr
     const int r = q * 32 + lane;       // weight row within the tile
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     const uint32_t lut_lane = smem_u32(smem + C::kOffLut) + 4u * lane;
-    uint32_t it = 0;
+    // This group's stages have global indices cg, cg + NG, cg + 2 NG, ... across all
+    // tiles, so their ring slots and phase parities advance by NG per stage.
+    uint32_t s = cg, ps = 0;    // TMEM A buffer / token ring (NA slots)
+    uint32_t cs = cg, pc = 0;   // code ring (CS slots)
+    uint32_t it0 = 0;           // global index of the tile's first stage
     bool ok = true;
     for (long long L = blockIdx.x; L < total && ok && !*abort_flag; L += gridDim.x) {
       int g, row0, rows, nt;
       if (!load_item(L, g, row0, rows, nt)) {
         continue;
       }
-      for (int kb = 0; kb < nk; ++kb, ++it) {
-        if (static_cast<int>(it % NG) != cg) continue;
-        const int cs = it % CS, s = it % NA;
+      for (int kb = static_cast<int>((cg + NG - it0 % NG) % NG); kb < nk; kb += NG) {
         // the TMEM A buffer of this stage is free once the MMAs of stage it - NA are
-        // done (their commit); the code slot once its TMA has landed
-        int w_ok = 1;
-        if (lane == 0) {
-          if (it >= NA)
-            w_ok = mbar_wait(&mma_done[s], ((it / NA) & 1u) ^ 1u, p.status, abort_flag);
-          if (w_ok) w_ok = mbar_wait(&code_full[cs], (it / CS) & 1u, p.status, abort_flag);
-        }
-        if (!__shfl_sync(0xFFFFFFFFu, w_ok, 0)) {
+        // done (their commit; the first pass finds the fresh barrier's parity-1 phase
+        // complete); the code slot once its TMA has landed.  The whole warp waits.
+        const bool w_ok = mbar_wait(&mma_done[s], ps ^ 1u, p.status, abort_flag) &&
+                          mbar_wait(&code_full[cs], pc, p.status, abort_flag);
+        if (!__all_sync(0xFFFFFFFFu, w_ok)) {
           ok = false;
           break;
         }
@@ -433,17 +456,21 @@ __global__ void __launch_bounds__(NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>::kThr
           }
         }
         tmem_st_wait();
-        // the tokens of this stage must have landed before the MMAs read them
-        if (lane == 0)
-          w_ok = mbar_wait(&tok_full[s], (it / NA) & 1u, p.status, abort_flag);
-        if (!__shfl_sync(0xFFFFFFFFu, w_ok, 0)) {
-          ok = false;
-          break;
-        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&conv_full[(ISS == 2 ? (kb & 1) : 0) * NA + s]);
+        s += NG;
+        if (s >= NA) {
+          s -= NA;
+          ps ^= 1u;
+        }
+        cs += NG;
+        if (cs >= CS) {
+          cs -= CS;
+          pc ^= 1u;
+        }
       }
+      it0 += nk;
     }
   } else if (warp >= C::kEpiWarp0) {
     // ------------------------------------------------------------ epilogue
