@@ -397,7 +397,7 @@ def gemm_roofline(d, groups, t_ms, which, hbm, hbm_src, tpk, tpk_src, fmt="mxfp4
 
 
 def measure_layer(args, workload, steps, warmup, rank, world, local, clocks, *, soak_s=0.0,
-                  e2e_steps=None, router=False, cpu=False, fmt="mxfp4", tag=None):
+                  e2e_steps=None, router=False, cpu=False, fmt="mxfp4", tag=None, options=()):
     """One workload: the layer step captured as a CUDA graph, timed over `steps` replays
     (each followed by an event-instrumented forward for the stage times), inside a
     clock-sampling window tagged `tag` (the workload's name).  fmt: the expert weight
@@ -527,6 +527,45 @@ def measure_layer(args, workload, steps, warmup, rank, world, local, clocks, *, 
     if e2e_steps and fmt == "mxfp4":
         e2e = measure_e2e(layer, d, x, lg, out, e2e_steps, do_flush, flush, world)
 
+    # the layer again with each option of moe_forward_ex (f1 SwiGLU in the W13 epilogue,
+    # f2 combine in the W2 epilogue, SM-pair tiles), same inputs and weights: its step
+    # time beside the default's, and whether its output equals the default's bit for bit
+    opt_rec = {}
+    if options and fmt == "mxfp4":
+        out.zero_()
+        layer.forward(x, lg, out=out)
+        torch.cuda.synchronize()
+        ref_out = out.clone()
+        n_o = min(steps, 30)
+        for opt in options:
+            lo = moe.MoELayer(d.H, d.I, d.E, d.k, d.has_shared, t["w13"], t["w13_s"], t["w2"],
+                              t["w2_s"], **{opt: True})
+            o_out = torch.zeros_like(out)
+            lo.forward(x, lg, out=o_out)
+            torch.cuda.synchronize()
+            o_bits = moe.moe_check_status(lo.workspace(d.T))
+            same = bool(torch.equal(o_out, ref_out)) and o_bits == 0
+            og = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(og):
+                lo.forward(x, lg, out=o_out)
+            for _ in range(warmup):
+                og.replay()
+            oe = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(n_o)]
+            for i in range(n_o):
+                if do_flush:
+                    flush.fill_(i & 0xFF)
+                oe[i][0].record(stream)
+                og.replay()
+                oe[i][1].record(stream)
+            torch.cuda.synchronize()
+            o_ms = max_over_ranks(statistics.mean(a_.elapsed_time(b_) for a_, b_ in oe), world)
+            opt_rec[opt] = {"ms_per_step": o_ms, "vs_default": o_ms / ms_max,
+                            "output_identical_to_default": same, "steps": n_o}
+            del og, lo, o_out
+            torch.cuda.synchronize()
+            torch.cuda.empty_cache()
+
     router_rec = None
     if router:
         # the router gate projection for this workload's T (outside the layer step: the
@@ -606,6 +645,7 @@ def measure_layer(args, workload, steps, warmup, rank, world, local, clocks, *, 
         "router_gate": router_rec, "cpu_baseline": cpu_rec, "e2e": e2e,
         "gpu_launches": 2 * launches_per_step * steps,
         "clocks": clocks.summary(tag),
+        "options": opt_rec or None,
     }
     del graph, layer, t, x, lg, out, ws, flush
     torch.cuda.synchronize()
@@ -682,7 +722,7 @@ def sub_record(rec):
     """The compact form of a workload's measurement carried inside the headline line."""
     keep = ("value", "ms_per_step", "steps", "config", "roofline", "roofline_w2", "stage_ms",
             "ms_per_step_l2_write_flushed", "ms_per_step_percentiles", "weight_gbs",
-            "gemm_tflops", "router_gate", "e2e", "clocks")
+            "gemm_tflops", "router_gate", "e2e", "clocks", "options")
     out = {k: rec[k] for k in keep}
     out["unit"] = "tokens/s"
     return out
@@ -695,6 +735,8 @@ EXTRA_STEPS = {"decode256": 600, "prefill": 60, "decode_nvfp4": 3000}
 # faster from ~256 tokens; the fp32 GEMV wins for decode-sized batches)
 ROUTER_TC_MIN_T = 256
 EXTRA_E2E_STEPS = {"decode256": 50, "prefill": 20}
+# moe_forward_ex options timed beside the default layer (decode, decode256, prefill)
+OPTIONS = ("fuse_swiglu", "fuse_combine", "pair_tiles")
 
 
 def run_ours(args, rank, world, local):
@@ -704,7 +746,8 @@ def run_ours(args, rank, world, local):
     with clocks:
         head = measure_layer(args, args.workload, args.steps, args.warmup, rank, world, local,
                              clocks, soak_s=2.5, e2e_steps=None if args.no_e2e else args.steps,
-                             router=True, cpu=not args.no_cpu_baseline, fmt=args.weights)
+                             router=True, cpu=not args.no_cpu_baseline, fmt=args.weights,
+                             options=() if args.no_extra else OPTIONS)
         extras = {}
         sweep = None
         if args.workload == "decode" and args.weights == "mxfp4" and not args.no_extra \
@@ -713,7 +756,7 @@ def run_ours(args, rank, world, local):
                 extras[wl] = sub_record(measure_layer(
                     args, wl, EXTRA_STEPS[wl], args.warmup, rank, world, local, clocks,
                     e2e_steps=None if args.no_e2e else EXTRA_E2E_STEPS[wl],
-                    router=(wl == "prefill")))
+                    router=(wl == "prefill"), options=OPTIONS))
             # the decode layer again with NVFP4 expert weights (f3)
             extras["decode_nvfp4"] = sub_record(measure_layer(
                 args, "decode", EXTRA_STEPS["decode_nvfp4"], args.warmup, rank, world, local,
@@ -750,6 +793,7 @@ def run_ours(args, rank, world, local):
             "e2e": head["e2e"],
             "gpu_launches": head["gpu_launches"],
             "clocks": clk,
+            "options": head["options"],
         }
         if extras:
             line["workloads"] = extras

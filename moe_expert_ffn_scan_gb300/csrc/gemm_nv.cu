@@ -30,10 +30,13 @@
 //     owns TMEM lanes 32 (w % 4) .. +31 (one weight row per thread).  A thread decodes
 //     its row's KS codes to bf16 -- two codes (one byte) per lookup in a 256-entry
 //     shared-memory table of bf16 pairs, replicated per lane so the lookups never
-//     conflict (or, where shared memory is short, with byte-permute lookups of two
-//     8-entry byte tables) -- multiplies them by the block scale (exact) and writes
-//     them into TMEM with tcgen05.st: the MMA's A operand lives in tensor memory, so
-//     the dequantised weights never pass through shared memory;
+//     conflict; with 256-byte entries (whose second half is the E4M3 scale table) one
+//     byte permute forms a lookup's whole offset and the table address rides in the
+//     load's immediate, so a lookup costs a permute and a load (where shared memory is
+//     short: 128-byte entries, or byte-permute lookups of two 8-entry byte tables) --
+//     multiplies them by the block scale (exact) and writes them into TMEM with
+//     tcgen05.st: the MMA's A operand lives in tensor memory, so the dequantised
+//     weights never pass through shared memory;
 //   * warp 1 (and warp 3 in the small variant): MMA issue, tcgen05.mma kind::f16 with
 //     A from TMEM and B (tokens) from shared memory, fp32 accumulators in TMEM;
 //   * the last four warps: epilogue (TMEM -> registers, x tensor scale, -> bf16 rows).
@@ -43,6 +46,12 @@
 namespace moe {
 
 namespace {
+
+// Shared-window address at which a kernel's dynamic shared memory starts when it has no
+// static shared memory: right after the per-block reserved shared memory (1 KB on
+// sm_100-class GPUs; the launcher checks the device attribute, the kernel its own
+// base).  The LUT-2 decode addresses its table as an immediate from it.
+constexpr uint32_t kDynSmemBase = 1024;
 
 struct NvParams {
   const int4* items;          // {group, row0, rows, 0}
@@ -58,8 +67,9 @@ struct NvParams {
 // BN: token tile; KS: K elements per stage; CS: code/scale ring slots; NA: token ring
 // slots = TMEM A buffers; ACC: accumulator buffers; ISS: MMA-issuing threads (each
 // takes every ISS-th stage of a tile into its own accumulator); NG: converter groups;
-// LUT: decode through the shared-memory table (else byte permutes).
-template <int BN, int KS, int CS, int NA, int ACC, int ISS, int NG, bool LUT>
+// LUT: how codes are decoded: 0 = byte permutes, 1 = a shared-memory table of 128-byte
+// entries, 2 = a table of 256-byte entries whose free half holds the E4M3 scale table.
+template <int BN, int KS, int CS, int NA, int ACC, int ISS, int NG, int LUT>
 struct NvCfg {
   static constexpr int kCodeBytes = 128 * (KS / 2);  // [128 rows][KS/2 B], swizzled
   static constexpr int kScaleBytes = 128 * 16;       // [128 rows][16 B] (256 K of scales)
@@ -72,10 +82,11 @@ struct NvCfg {
   // acc_full[ACC], acc_empty[ACC], drain[ISS]
   static constexpr int kNumBars = 2 * CS + NA + ISS * NA + NA + 2 * ACC + ISS;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  // decode table: 256 code bytes x 32 lanes x one bf16 pair (entry b of lane l at word
-  // b * 32 + l: every lane reads its own bank)
-  static constexpr int kOffLut = (kOffMisc + 16 + 127) / 128 * 128;
-  static constexpr int kLutBytes = LUT ? 256 * 32 * 4 : 0;
+  // decode table: 256 code bytes x 32 lanes x one bf16 pair, entry b of lane l at byte
+  // b * 128 + 4 l (LUT 1) or b * 256 + 4 l (LUT 2, whose bytes b * 256 + 128 + 4 l hold
+  // the bf16 pair of E4M3 scale byte b): every lane reads its own bank
+  static constexpr int kOffLut = (kOffMisc + 16 + 255) / 256 * 256;
+  static constexpr int kLutBytes = LUT == 2 ? 256 * 256 : LUT == 1 ? 256 * 128 : 0;
   static constexpr int kSmemBytes = kOffLut + kLutBytes;
   static constexpr int kAccCols = ISS * BN;          // one accumulator buffer
   static constexpr int kACols = KS / 2;              // bf16 pairs per A buffer row
@@ -92,7 +103,8 @@ struct NvCfg {
   static_assert(kCodeBytes % 1024 == 0 && kTokBytes % 1024 == 0, "tile alignment");
   static_assert(ISS == 1 || ISS == 2, "issuers");
   static_assert(NG <= NA && NG <= CS && ISS <= NA, "ring slots advance by at most one lap a step");
-  static_assert(KS == 128 || !LUT, "the table-decoding converter takes 128-K stages");
+  static_assert(KS == 128 || LUT == 0, "the table-decoding converter takes 128-K stages");
+  static_assert(LUT >= 0 && LUT <= 2, "decode form");
   static_assert(kThreads <= 1024, "threads");
 };
 
@@ -162,6 +174,37 @@ __device__ __forceinline__ void decode8_lut(uint32_t w, uint32_t lut_lane, uint3
   }
 }
 
+// LUT 2: eight codes -> four bf16 pairs times the scale pair.  One byte permute forms
+// the table offset of code byte i (byte i of the word as the offset's second byte, this
+// lane's 4 l as its first), so the lookup needs no address arithmetic beyond the add
+// of the table base.
+// The table's shared-window address TAB is a compile-time constant (the dynamic shared
+// memory starts right after the per-block reserved shared memory, kDynSmemBase; the
+// kernel checks that on entry), so it rides in the load's immediate offset and a lookup
+// is one byte permute + one load.
+template <uint32_t TAB>
+__device__ __forceinline__ void decode8_lut2(uint32_t w, uint32_t lane4, uint32_t sc,
+                                             uint32_t* o) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t v;
+    asm("ld.shared.b32 %0, [%1+%2];"
+        : "=r"(v)
+        : "r"(__byte_perm(w, lane4, 0x5504u | (i << 4))), "n"(TAB));
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[i]) : "r"(v), "r"(sc));
+  }
+}
+
+// LUT 2: the bf16 pair of E4M3 scale byte j of `word` (the table's second half).
+template <uint32_t TAB>
+__device__ __forceinline__ uint32_t scale_lut2(uint32_t word, int j, uint32_t lane4) {
+  uint32_t v;
+  asm("ld.shared.b32 %0, [%1+%2];"
+      : "=r"(v)
+      : "r"(__byte_perm(word, lane4, 0x5504u | (j << 4))), "n"(TAB + 128));
+  return v;
+}
+
 // tcgen05.st of 16 columns; no "memory" clobber: it reads only registers, and its
 // order against the other tcgen05 / mbarrier instructions (all volatile asm) is kept.
 __device__ __forceinline__ void tmem_st_x16_regs(uint32_t taddr, const uint32_t (&r)[16]) {
@@ -179,13 +222,13 @@ __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, __nv_bfloat162 s) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-template <int BN, int KS, int CS, int NA, int ACC, int ISS, int NG, bool LUT>
+template <int BN, int KS, int CS, int NA, int ACC, int ISS, int NG, int LUT>
 __global__ void __launch_bounds__(NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>::kThreads, 1)
     k_gemm_nv(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmS,
               const __grid_constant__ CUtensorMap tmX, const NvParams p) {
   using C = NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>;
   extern __shared__ __align__(1024) uint8_t smem[];
-  if ((smem_u32(smem) & 1023u) != 0) {
+  if ((smem_u32(smem) & 1023u) != 0 || (LUT == 2 && smem_u32(smem) != kDynSmemBase)) {
     if (threadIdx.x == 0) set_status(p.status, STATUS_BAD_PLAN);
     return;
   }
@@ -223,13 +266,28 @@ __global__ void __launch_bounds__(NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>::kThr
     tma_prefetch_desc(&tmS);
     tma_prefetch_desc(&tmX);
   }
-  if constexpr (LUT) {
+  if constexpr (LUT == 1) {
     // the decode table: entry b = the bf16 pair of code byte b (low nibble first)
     uint32_t* lut = reinterpret_cast<uint32_t*>(smem + C::kOffLut);
     for (int i = threadIdx.x; i < 256 * 32; i += C::kThreads) {
       uint32_t o[4];
       e2m1x8_to_bf16(static_cast<uint32_t>(i >> 5), o);
       lut[i] = o[0];
+    }
+  } else if constexpr (LUT == 2) {
+    // 256-byte entries: words 0-31 the bf16 pair of code byte b, words 32-63 the
+    // value of E4M3 byte b as a pair of equal bf16 (one copy per lane each)
+    uint32_t* lut = reinterpret_cast<uint32_t*>(smem + C::kOffLut);
+    for (int i = threadIdx.x; i < 256 * 64; i += C::kThreads) {
+      const uint32_t b = static_cast<uint32_t>(i >> 6);
+      if ((i & 63) < 32) {
+        uint32_t o[4];
+        e2m1x8_to_bf16(b, o);
+        lut[i] = o[0];
+      } else {
+        const __nv_bfloat162 sc = e4m3_to_bf16x2(b);
+        lut[i] = *reinterpret_cast<const uint32_t*>(&sc);
+      }
     }
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
@@ -379,6 +437,8 @@ __global__ void __launch_bounds__(NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>::kThr
     const int r = q * 32 + lane;       // weight row within the tile
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     const uint32_t lut_lane = smem_u32(smem + C::kOffLut) + 4u * lane;
+    const uint32_t lane4 = 4u * lane;
+    constexpr uint32_t kTab = kDynSmemBase + C::kOffLut;  // the table's shared address
     // This group's stages have global indices cg, cg + NG, cg + 2 NG, ... across all
     // tiles, so their ring slots and phase parities advance by NG per stage.
     uint32_t s = cg, ps = 0;    // TMEM A buffer / token ring (NA slots)
@@ -418,7 +478,24 @@ __global__ void __launch_bounds__(NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>::kThr
         __syncwarp();
         if (lane == 0) mbar_arrive(&code_empty[cs]);
         const uint32_t col0 = a_base + s * C::kACols;
-        if constexpr (LUT) {
+        if constexpr (LUT == 2) {
+          // a 128-K stage: scale bytes 0-7 (even 128-K step) or 8-15 (odd) of the row
+          const uint32_t s_lo = (kb & 1) ? sv.z : sv.x;
+          const uint32_t s_hi = (kb & 1) ? sv.w : sv.y;
+#pragma unroll
+          for (int bp = 0; bp < C::kBlocks / 2; ++bp) {  // two 16-element blocks = chunk bp
+            const uint32_t sw = bp < 2 ? s_lo : s_hi;
+            const uint32_t sc0 = scale_lut2<kTab>(sw, 2 * (bp & 1), lane4);
+            const uint32_t sc1 = scale_lut2<kTab>(sw, 2 * (bp & 1) + 1, lane4);
+            const uint4 cv = cw[bp];
+            uint32_t o[16];
+            decode8_lut2<kTab>(cv.x, lane4, sc0, o);
+            decode8_lut2<kTab>(cv.y, lane4, sc0, o + 4);
+            decode8_lut2<kTab>(cv.z, lane4, sc1, o + 8);
+            decode8_lut2<kTab>(cv.w, lane4, sc1, o + 12);
+            tmem_st_x16_regs(lane_base + col0 + bp * 16, o);
+          }
+        } else if constexpr (LUT == 1) {
           // a 128-K stage: scale bytes 0-7 (even 128-K step) or 8-15 (odd) of the row
           const uint32_t s_lo = (kb & 1) ? sv.z : sv.x;
           const uint32_t s_hi = (kb & 1) ? sv.w : sv.y;
@@ -538,7 +615,7 @@ __global__ void __launch_bounds__(NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>::kThr
 
 // ---------------------------------------------------------------- host side -------
 
-template <int BN, int KS, int CS, int NA, int ACC, int ISS, int NG, bool LUT>
+template <int BN, int KS, int CS, int NA, int ACC, int ISS, int NG, int LUT>
 cudaError_t launch_nv_one(const NvGemmLaunch& a, int v, cudaStream_t st) {
   using C = NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>;
   auto kern = k_gemm_nv<BN, KS, CS, NA, ACC, ISS, NG, LUT>;
@@ -552,6 +629,12 @@ cudaError_t launch_nv_one(const NvGemmLaunch& a, int v, cudaStream_t st) {
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   const unsigned long long ctx = current_context_id();
   if (ctx == 0 || attr_ctx[dev] != ctx) {
+    if (LUT == 2) {  // the table-address immediate assumes this reserved size
+      int reserved = -1;
+      e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+      if (e != cudaSuccess) return e;
+      if (reserved != static_cast<int>(kDynSmemBase)) return cudaErrorNotSupported;
+    }
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_ctx[dev] = current_context_id();
@@ -635,13 +718,13 @@ int nv_encode_maps(const NvGemmLaunch& a, int ks, int bn, CUtensorMap* tmC, CUte
 //          accumulator (224 of TMEM's 512 columns), byte-permute decoding (no shared
 //          memory left for the table).
 cudaError_t launch_grouped_gemm_nv(const NvGemmLaunch& a, cudaStream_t st) {
-  cudaError_t e = launch_nv_one<kSmallBN, 128, 8, 7, 2, 2, 4, true>(a, 0, st);
+  cudaError_t e = launch_nv_one<kSmallBN, 128, 8, 7, 2, 2, 4, 2>(a, 0, st);
   if (e != cudaSuccess || a.max_group_rows <= kSmallBN) return e;
-  e = launch_nv_one<kMediumBN, 128, 6, 5, 2, 1, 4, true>(a, 1, st);
+  e = launch_nv_one<kMediumBN, 128, 6, 5, 2, 1, 4, 2>(a, 1, st);
   if (e != cudaSuccess || a.max_group_rows <= kMediumBN) return e;
-  e = launch_nv_one<kMidBN, 128, 4, 4, 2, 1, 4, true>(a, 2, st);
+  e = launch_nv_one<kMidBN, 128, 4, 4, 2, 1, 4, 1>(a, 2, st);
   if (e != cudaSuccess || a.max_group_rows <= kMidBN) return e;
-  return launch_nv_one<kLargeBN, 128, 3, 3, 1, 1, 3, false>(a, 3, st);
+  return launch_nv_one<kLargeBN, 128, 3, 3, 1, 1, 3, 0>(a, 3, st);
 }
 
 }  // namespace moe
