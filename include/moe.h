@@ -348,12 +348,16 @@ int moe_forward_timed(const moe_dims* d, const uint16_t* x, const float* logits,
  *     of an SM pair (a cluster of two CTAs sharing each cta_group::2 MMA) holds 64
  *     gate + the same 64 up rows per CTA, i.e. one 128-feature quantisation block per
  *     pair; h = silu(gate) * up is formed from the bf16-rounded accumulators, the two
- *     CTAs swap per-token amaxes, and the FP8 codes and scales are written directly --
- *     the same hq / hs bit for bit as the stand-alone SwiGLU kernel, without y13 (the
- *     dbg->y13 buffer is not written) and without that kernel.  Needs H % 512 == 0.
+ *     CTAs swap per-token amaxes, and the FP8 codes and scales are written directly
+ *     with the stand-alone SwiGLU kernel's arithmetic, without y13 (the dbg->y13
+ *     buffer is not written) and without that kernel.  The pair tile sums K in one
+ *     accumulator where the stand-alone small tiles use two (even / odd stages), so a
+ *     rare y13 element -- and so an FP8 code -- can differ from the stand-alone path
+ *     at large K; within the float contract.  Needs H % 512 == 0.
  *   pair_tiles: 1 = the mid and large tile lists (groups of more than 64 rows) run on
  *     SM pairs (one cta_group::2 MMA per 256 weight rows, half the token tile per SM)
- *     instead of one SM per tile (when N % 256 == 0 and K % 512 == 0).
+ *     instead of one SM per tile (when N % 256 == 0 and K % 512 == 0); the same
+ *     accumulation order as the one-SM tiles of those lists.
  *   fuse_combine (f2): 1 = the W2 grouped GEMM's epilogue performs a7 (LMSYS-H20 §3.2,
  *     the TopK reduction merged with the shared-expert add): once a tile has stored its
  *     y2 rows, each row bumps its (token, 128-column block) arrival counter, and the

@@ -125,6 +125,50 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) 
   return true;
 }
 
+// ------------------------------------------------------------------ tile walk -----
+
+// A persistent CTA's walk over the tiles blockIdx.x, blockIdx.x + gridDim.x, ... below
+// `total`, tile L being n-tile L % n_tiles of work item L / n_tiles.  The walk divides
+// once (at the start) and then steps by adding; each tile's work item (an int4 the plan
+// kernel wrote) is loaded one tile ahead, so that load's latency overlaps the previous
+// tile.  Every role of a CTA walks the same sequence.
+struct TileWalk {
+  const int4* items;
+  long long L, total;
+  int step, n_tiles, dq, dr;  // step = dq * n_tiles + dr
+  int item, nt, item_n, nt_n;
+  int4 cur, nxt;
+  __device__ __forceinline__ TileWalk(const int4* it, long long tot, int ntiles)
+      : items(it), L(blockIdx.x), total(tot), step(static_cast<int>(gridDim.x)),
+        n_tiles(ntiles) {
+    dq = step / ntiles;
+    dr = step % ntiles;
+    item = static_cast<int>(blockIdx.x) / ntiles;
+    nt = static_cast<int>(blockIdx.x) % ntiles;
+    cur = make_int4(0, 0, 0, 0);
+    nxt = cur;
+    if (L < total) cur = __ldg(items + item);
+    fetch_next();
+  }
+  __device__ __forceinline__ void fetch_next() {
+    item_n = item + dq;
+    nt_n = nt + dr;
+    if (nt_n >= n_tiles) {
+      nt_n -= n_tiles;
+      ++item_n;
+    }
+    if (L + step < total) nxt = __ldg(items + item_n);
+  }
+  __device__ __forceinline__ bool valid() const { return L < total; }
+  __device__ __forceinline__ void next() {
+    L += step;
+    item = item_n;
+    nt = nt_n;
+    cur = nxt;
+    fetch_next();
+  }
+};
+
 // ------------------------------------------------------------------ TMA -----------
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {

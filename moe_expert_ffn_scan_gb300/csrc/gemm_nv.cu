@@ -305,9 +305,11 @@ __global__ void __launch_bounds__(NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>::kThr
     count = p.max_items;
   }
   const long long total = static_cast<long long>(count) * n_tiles;
-  auto load_item = [&](long long L, int& g, int& row0, int& rows, int& nt) -> bool {
-    const int4 it = p.items[L / n_tiles];
-    nt = static_cast<int>(L % n_tiles);
+  // the current tile of a walk: its group, first packed row and rows; false for an
+  // empty item (skipped by every role alike) or an inconsistent one (flagged)
+  auto load_item = [&](const TileWalk& w, int& g, int& row0, int& rows, int& nt) -> bool {
+    const int4 it = w.cur;
+    nt = w.nt;
     g = it.x;
     row0 = it.y;
     rows = it.z;
@@ -324,9 +326,9 @@ __global__ void __launch_bounds__(NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>::kThr
     // ------------------------------------------------------------ codes + scales TMA
     if (lane == 0) {
       uint32_t s = 0, ph = 0;  // code ring slot and lap parity of the next stage
-      for (long long L = blockIdx.x; L < total && !*abort_flag; L += gridDim.x) {
+      for (TileWalk tw(p.items, total, n_tiles); tw.valid() && !*abort_flag; tw.next()) {
         int g, row0, rows, nt;
-        if (!load_item(L, g, row0, rows, nt)) continue;
+        if (!load_item(tw, g, row0, rows, nt)) continue;
         bool ok = true;
         for (int kb = 0; kb < nk; ++kb) {
           // the slot is free once its converters released it (a fresh barrier's
@@ -352,9 +354,9 @@ __global__ void __launch_bounds__(NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>::kThr
     // ------------------------------------------------------------ token TMA
     if (lane == 0) {
       uint32_t s = 0, ph = 0;  // token ring slot and lap parity of the next stage
-      for (long long L = blockIdx.x; L < total && !*abort_flag; L += gridDim.x) {
+      for (TileWalk tw(p.items, total, n_tiles); tw.valid() && !*abort_flag; tw.next()) {
         int g, row0, rows, nt;
-        if (!load_item(L, g, row0, rows, nt)) continue;
+        if (!load_item(tw, g, row0, rows, nt)) continue;
         bool ok = true;
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait(&mma_done[s], ph ^ 1u, p.status, abort_flag)) {
@@ -378,9 +380,9 @@ __global__ void __launch_bounds__(NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>::kThr
     if (lane == 0) {
       uint32_t it0 = 0, tc = 0;  // it0: global index of the tile's first stage
       uint32_t phases = 0;  // bit s: parity of the next phase of conv_full[par][s]
-      for (long long L = blockIdx.x; L < total && !*abort_flag; L += gridDim.x) {
+      for (TileWalk tw(p.items, total, n_tiles); tw.valid() && !*abort_flag; tw.next()) {
         int g, row0, rows, nt;
-        if (!load_item(L, g, row0, rows, nt)) continue;
+        if (!load_item(tw, g, row0, rows, nt)) continue;
         const int bn = (rows + 15) & ~15;
         const uint32_t b = tc % ACC, use = tc / ACC;
         if (tc >= ACC && !mbar_wait(&acc_empty[b], (use - 1) & 1u, p.status, abort_flag)) break;
@@ -445,9 +447,9 @@ __global__ void __launch_bounds__(NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>::kThr
     uint32_t cs = cg, pc = 0;   // code ring (CS slots)
     uint32_t it0 = 0;           // global index of the tile's first stage
     bool ok = true;
-    for (long long L = blockIdx.x; L < total && ok && !*abort_flag; L += gridDim.x) {
+    for (TileWalk tw(p.items, total, n_tiles); tw.valid() && ok && !*abort_flag; tw.next()) {
       int g, row0, rows, nt;
-      if (!load_item(L, g, row0, rows, nt)) {
+      if (!load_item(tw, g, row0, rows, nt)) {
         continue;
       }
       for (int kb = static_cast<int>((cg + NG - it0 % NG) % NG); kb < nk; kb += NG) {
@@ -553,9 +555,9 @@ __global__ void __launch_bounds__(NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>::kThr
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
     uint32_t tc = 0;
-    for (long long L = blockIdx.x; L < total && !*abort_flag; L += gridDim.x) {
+    for (TileWalk tw(p.items, total, n_tiles); tw.valid() && !*abort_flag; tw.next()) {
       int g, row0, rows, nt;
-      if (!load_item(L, g, row0, rows, nt)) continue;
+      if (!load_item(tw, g, row0, rows, nt)) continue;
       const uint32_t b = tc % ACC, use = tc / ACC;
       int w_ok = 1;
       if (lane == 0) w_ok = mbar_wait(&acc_full[b], use & 1u, p.status, abort_flag);
