@@ -127,11 +127,12 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) 
 
 // ------------------------------------------------------------------ tile walk -----
 
-// A persistent CTA's walk over the tiles blockIdx.x, blockIdx.x + gridDim.x, ... below
-// `total`, tile L being n-tile L % n_tiles of work item L / n_tiles.  The walk divides
-// once (at the start) and then steps by adding; each tile's work item (an int4 the plan
-// kernel wrote) is loaded one tile ahead, so that load's latency overlaps the previous
-// tile.  Every role of a CTA walks the same sequence.
+// A persistent CTA's walk over the tiles start, start + step, ... below `total` (by
+// default start = blockIdx.x, step = gridDim.x), tile L being n-tile L % n_tiles of
+// work item L / n_tiles.  The walk divides once (at the start) and then steps by
+// adding; each tile's work item (an int4 the plan kernel wrote) is loaded one tile
+// ahead, so that load's latency overlaps the previous tile.  Every role of a CTA walks
+// the same sequence.
 struct TileWalk {
   const int4* items;
   long long L, total;
@@ -139,12 +140,14 @@ struct TileWalk {
   int item, nt, item_n, nt_n;
   int4 cur, nxt;
   __device__ __forceinline__ TileWalk(const int4* it, long long tot, int ntiles)
-      : items(it), L(blockIdx.x), total(tot), step(static_cast<int>(gridDim.x)),
-        n_tiles(ntiles) {
+      : TileWalk(it, tot, ntiles, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x)) {}
+  __device__ __forceinline__ TileWalk(const int4* it, long long tot, int ntiles, int start,
+                                      int stride)
+      : items(it), L(start), total(tot), step(stride), n_tiles(ntiles) {
     dq = step / ntiles;
     dr = step % ntiles;
-    item = static_cast<int>(blockIdx.x) / ntiles;
-    nt = static_cast<int>(blockIdx.x) % ntiles;
+    item = start / ntiles;
+    nt = start % ntiles;
     cur = make_int4(0, 0, 0, 0);
     nxt = cur;
     if (L < total) cur = __ldg(items + item);

@@ -265,12 +265,14 @@ __global__ void __launch_bounds__(256, OCC)
     if (threadIdx.x == 0) set_status(p.status, STATUS_BAD_PLAN);
     count = p.max_items;
   }
-  const long long total = static_cast<long long>(count) * n_tiles;
+  long long total = static_cast<long long>(count) * n_tiles;
+  if (total > 0x7FFFFFFFll) {
+    if (threadIdx.x == 0) set_status(p.status, STATUS_BAD_PLAN);
+    total = 0;
+  }
 
-  // Reads and validates one work item; every role sees the same result.
-  auto load_item = [&](long long L, int& g, int& row0, int& rows, int& nt) -> bool {
-    int4 it = p.items[L / n_tiles];
-    nt = static_cast<int>(L % n_tiles);
+  // Validates one work item; every role sees the same result.
+  auto check_item = [&](const int4 it, int& g, int& row0, int& rows) -> bool {
     g = it.x;
     row0 = it.y;
     rows = it.z;
@@ -280,6 +282,12 @@ __global__ void __launch_bounds__(256, OCC)
       return false;
     }
     return true;
+  };
+  // Tile L directly (the scale stager's look-ahead): item L / n_tiles, n-tile L % n_tiles.
+  auto load_item = [&](long long L, int& g, int& row0, int& rows, int& nt) -> bool {
+    const int Li = static_cast<int>(L);  // total < 2^31 (checked above)
+    nt = Li % n_tiles;
+    return check_item(__ldg(p.items + Li / n_tiles), g, row0, rows);
   };
 
   if (warp == 0) {
@@ -313,11 +321,12 @@ __global__ void __launch_bounds__(256, OCC)
         }
       }
       uint32_t it = 0;
-      for (long long L = blockIdx.x; L < total && !*abort_flag; L += gridDim.x) {
-        int g, row0, rows, nt;
-        if (!load_item(L, g, row0, rows, nt)) continue;
+      for (TileWalk tw(p.items, total, n_tiles); tw.valid() && !*abort_flag; tw.next()) {
+        int g, row0, rows;
+        const int nt = tw.nt;
+        if (!check_item(tw.cur, g, row0, rows)) continue;
         for (int kb = 0; kb < nk; ++kb, ++it) {
-          if (L == L0 && kb < pre) continue;  // issued above
+          if (tw.L == L0 && kb < pre) continue;  // issued above
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1u;
           if (it >= STAGES && !mbar_wait(&empty[s], ph ^ 1u, p.status, abort_flag)) break;
@@ -339,9 +348,10 @@ __global__ void __launch_bounds__(256, OCC)
     if (lane == 0) {
       if (p.early) pdl_wait();
       uint32_t it = 0;
-      for (long long L = blockIdx.x; L < total && !*abort_flag; L += gridDim.x) {
-        int g, row0, rows, nt;
-        if (!load_item(L, g, row0, rows, nt)) continue;
+      for (TileWalk tw(p.items, total, n_tiles); tw.valid() && !*abort_flag; tw.next()) {
+        int g, row0, rows;
+        const int nt = tw.nt;
+        if (!check_item(tw.cur, g, row0, rows)) continue;
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1u;
@@ -359,9 +369,10 @@ __global__ void __launch_bounds__(256, OCC)
     if (lane == 0) {
       uint32_t it = 0, tc = 0;
       uint32_t phases = 0;  // bit s: parity of the next phase of full[par][s] to wait for
-      for (long long L = blockIdx.x; L < total && !*abort_flag; L += gridDim.x) {
-        int g, row0, rows, nt;
-        if (!load_item(L, g, row0, rows, nt)) continue;
+      for (TileWalk tw(p.items, total, n_tiles); tw.valid() && !*abort_flag; tw.next()) {
+        int g, row0, rows;
+        const int nt = tw.nt;
+        if (!check_item(tw.cur, g, row0, rows)) continue;
         const int bn = (rows + 15) & ~15;
         const uint32_t b = tc & 1u, use = tc >> 1;
         if (tc >= 2 && !mbar_wait(&acc_empty[b], (use - 1) & 1u, p.status, abort_flag)) break;
@@ -581,9 +592,10 @@ __global__ void __launch_bounds__(256, OCC)
       // General path (K not a multiple of 512): one stage at a time.
       if (p.early) pdl_wait();  // token scales come from the preceding kernel
       uint32_t it = 0;
-      for (long long L = blockIdx.x; L < total && !*abort_flag; L += gridDim.x) {
-        int g, row0, rows, nt;
-        if (!load_item(L, g, row0, rows, nt)) continue;
+      for (TileWalk tw(p.items, total, n_tiles); tw.valid() && !*abort_flag; tw.next()) {
+        int g, row0, rows;
+        const int nt = tw.nt;
+        if (!check_item(tw.cur, g, row0, rows)) continue;
         const uint8_t* wsp = p.w_scales + (static_cast<size_t>(g) * p.N + nt * 128) * kw;
         bool ok = true;
         for (int kb = 0; kb < nk; ++kb, ++it) {
@@ -622,9 +634,10 @@ __global__ void __launch_bounds__(256, OCC)
     // ---------------------------------------------------------------- epilogue
     const int q = warp - 4;
     uint32_t tc = 0;
-    for (long long L = blockIdx.x; L < total && !*abort_flag; L += gridDim.x) {
-      int g, row0, rows, nt;
-      if (!load_item(L, g, row0, rows, nt)) continue;
+    for (TileWalk tw(p.items, total, n_tiles); tw.valid() && !*abort_flag; tw.next()) {
+      int g, row0, rows;
+      const int nt = tw.nt;
+      if (!check_item(tw.cur, g, row0, rows)) continue;
       const uint32_t b = tc & 1u, use = tc >> 1;
       if (p.out) {
         // the fused combine meets at named barriers: one thread waits for the four warps,
@@ -965,11 +978,14 @@ __global__ void __launch_bounds__(256, 1)
     if (threadIdx.x == 0) set_status(p.status, STATUS_BAD_PLAN);
     count = p.max_items;
   }
-  const long long total = static_cast<long long>(count) * n_tiles2;
+  long long total = static_cast<long long>(count) * n_tiles2;
+  if (total > 0x7FFFFFFFll) {
+    if (threadIdx.x == 0) set_status(p.status, STATUS_BAD_PLAN);
+    total = 0;
+  }
   const long long cl = blockIdx.x >> 1, ncl = gridDim.x >> 1;
-  auto load_item = [&](long long L, int& g, int& row0, int& rows, int& nt2) -> bool {
-    const int4 it = p.items[L / n_tiles2];
-    nt2 = static_cast<int>(L % n_tiles2);
+  // validates one work item; every role sees the same result
+  auto check_item = [&](const int4 it, int& g, int& row0, int& rows) -> bool {
     g = it.x;
     row0 = it.y;
     rows = it.z;
@@ -980,6 +996,12 @@ __global__ void __launch_bounds__(256, 1)
     }
     return true;
   };
+  // tile L directly (the scale stager's look-ahead, the fused epilogue)
+  auto load_item = [&](long long L, int& g, int& row0, int& rows, int& nt2) -> bool {
+    const int Li = static_cast<int>(L);  // total < 2^31 (checked above)
+    nt2 = Li % n_tiles2;
+    return check_item(__ldg(p.items + Li / n_tiles2), g, row0, rows);
+  };
   // the leader's copies of the barriers the peer completes
   auto leader_addr = [&](const uint64_t* b) -> uint32_t { return mapa_shared(smem_u32(b), 0); };
 
@@ -987,9 +1009,11 @@ __global__ void __launch_bounds__(256, 1)
     // ---------------------------------------------------------------- weight TMA
     if (lane == 0) {
       uint32_t it = 0;
-      for (long long L = cl; L < total && !*abort_flag; L += ncl) {
-        int g, row0, rows, nt2;
-        if (!load_item(L, g, row0, rows, nt2)) continue;
+      for (TileWalk tw(p.items, total, n_tiles2, static_cast<int>(cl), static_cast<int>(ncl));
+           tw.valid() && !*abort_flag; tw.next()) {
+        int g, row0, rows;
+        const int nt2 = tw.nt;
+        if (!check_item(tw.cur, g, row0, rows)) continue;
         bool ok = true;
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = it % STAGES;
@@ -1021,9 +1045,11 @@ __global__ void __launch_bounds__(256, 1)
     // ---------------------------------------------------------------- token TMA
     if (lane == 0) {
       uint32_t it = 0;
-      for (long long L = cl; L < total && !*abort_flag; L += ncl) {
-        int g, row0, rows, nt2;
-        if (!load_item(L, g, row0, rows, nt2)) continue;
+      for (TileWalk tw(p.items, total, n_tiles2, static_cast<int>(cl), static_cast<int>(ncl));
+           tw.valid() && !*abort_flag; tw.next()) {
+        int g, row0, rows;
+        const int nt2 = tw.nt;
+        if (!check_item(tw.cur, g, row0, rows)) continue;
         const int half = ((rows + 15) & ~15) >> 1;
         bool ok = true;
         for (int kb = 0; kb < nk; ++kb, ++it) {
@@ -1048,9 +1074,11 @@ __global__ void __launch_bounds__(256, 1)
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      for (long long L = cl; L < total && ok && !*abort_flag; L += ncl) {
-        int g, row0, rows, nt2;
-        if (!load_item(L, g, row0, rows, nt2)) continue;
+      for (TileWalk tw(p.items, total, n_tiles2, static_cast<int>(cl), static_cast<int>(ncl));
+           tw.valid() && ok && !*abort_flag; tw.next()) {
+        int g, row0, rows;
+        const int nt2 = tw.nt;
+        if (!check_item(tw.cur, g, row0, rows)) continue;
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int j = it % SFS;
           if (!mbar_wait(&sf_ready[j], (it / SFS) & 1u, p.status, abort_flag)) {
@@ -1065,9 +1093,11 @@ __global__ void __launch_bounds__(256, 1)
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       uint32_t it = 0, tc = 0;
-      for (long long L = cl; L < total && !*abort_flag; L += ncl) {
-        int g, row0, rows, nt2;
-        if (!load_item(L, g, row0, rows, nt2)) continue;
+      for (TileWalk tw(p.items, total, n_tiles2, static_cast<int>(cl), static_cast<int>(ncl));
+           tw.valid() && !*abort_flag; tw.next()) {
+        int g, row0, rows;
+        const int nt2 = tw.nt;
+        if (!check_item(tw.cur, g, row0, rows)) continue;
         const int bn = (rows + 15) & ~15;
         const uint32_t b = tc & 1u, use = tc >> 1;
         if (tc >= 2 && !mbar_wait(&acc_empty[b], (use - 1) & 1u, p.status, abort_flag)) break;
@@ -1250,9 +1280,11 @@ __global__ void __launch_bounds__(256, 1)
     // ---------------------------------------------------------------- epilogue
     const int q = warp - 4;
     uint32_t tc = 0;
-    for (long long L = cl; L < total && !*abort_flag; L += ncl) {
-      int g, row0, rows, nt2;
-      if (!load_item(L, g, row0, rows, nt2)) continue;
+    for (TileWalk tw(p.items, total, n_tiles2, static_cast<int>(cl), static_cast<int>(ncl));
+         tw.valid() && !*abort_flag; tw.next()) {
+      int g, row0, rows;
+      const int nt2 = tw.nt;
+      if (!check_item(tw.cur, g, row0, rows)) continue;
       const uint32_t b = tc & 1u, use = tc >> 1;
       int w_ok = 1;
       if (lane == 0) w_ok = mbar_wait(&acc_full[b], use & 1u, p.status, abort_flag);
