@@ -20,6 +20,9 @@ line (--no-extra skips them).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|decode256|prefill|tiny]
   python bench.py --workload sweep       (the grouped-GEMM sweep alone, every point)
+  python bench.py --workload gemm --gemm w13|w2 --groups G --rows M [--weights nvfp4]
+                                         (one grouped GEMM, e.g. for an ncu capture)
+  python bench.py --workload prefill --options pair_tiles,...   (moe_forward_ex options)
   python bench.py --impl reference ...   (the CPU oracle on a bounded sample)
 
 Multi-GPU: one independent replica per GPU (the layer is not sharded; no
@@ -57,7 +60,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode", choices=list(gi.WORKLOADS) + ["sweep"])
+    ap.add_argument("--workload", default="decode",
+                    choices=list(gi.WORKLOADS) + ["sweep", "gemm"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -70,6 +74,13 @@ def parse():
                     help="expert weight format of the measured layer")
     ap.add_argument("--no-extra", action="store_true",
                     help="decode only: skip the decode256 / prefill / sweep records")
+    ap.add_argument("--options", default="",
+                    help="comma list of moe_forward_ex options for the measured layer "
+                         "(fuse_swiglu, fuse_combine, pair_tiles)")
+    ap.add_argument("--gemm", default="w13", choices=["w13", "w2"],
+                    help="--workload gemm: which grouped GEMM (sweep shapes)")
+    ap.add_argument("--groups", type=int, default=64, help="--workload gemm: groups")
+    ap.add_argument("--rows", type=int, default=2, help="--workload gemm: rows per group")
     return ap.parse_args()
 
 
@@ -130,17 +141,23 @@ def hbm_peak_gbs():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def fp8_tensor_peak_tflops():
+def fp8_tensor_peak_tflops(sustained=False):
     """Dense FP8 tensor peak: the measured bf16 cuBLAS peak x the nominal 2x FP8/bf16
-    ratio, else the fallback bf16 figure x 2."""
+    ratio (the burst figure, or with sustained=True the seconds-long loop's figure, for
+    a kernel timed inside a long run of steps), else the fallback bf16 figure x 2."""
     peaks, _ = measured_peaks()
     if peaks:
-        for key in ("bf16_tflops", "bf16"):
+        keys = ("bf16_tflops_sustained",) if sustained else ("bf16_tflops", "bf16")
+        for key in keys:
             if key in peaks:
                 try:
-                    return 2.0 * float(peaks[key]), "measured bf16 x2 (nominal fp8/bf16 ratio)"
+                    return 2.0 * float(peaks[key]), (
+                        f"measured bf16 {'sustained' if sustained else 'burst'} x2 "
+                        "(nominal fp8/bf16 ratio)")
                 except (TypeError, ValueError):
                     pass
+        if sustained:
+            return fp8_tensor_peak_tflops(False)
     return 2.0 * FALLBACK_BF16_TFLOPS, "fallback bf16 x2 (nominal fp8/bf16 ratio)"
 
 
@@ -313,7 +330,7 @@ def blas_threads():
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    if args.workload == "sweep":
+    if args.workload in ("sweep", "gemm"):
         print(json.dumps({"impl": "reference", "unavailable": "the GEMM sweep has no CPU arm; "
                           "run a layer workload"}), flush=True)
         return
@@ -354,22 +371,26 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def bf16_tensor_peak_tflops():
+def bf16_tensor_peak_tflops(sustained=False):
     """Dense bf16 tensor peak (the NVFP4 path's kind::f16 MMAs): the measured cuBLAS
-    bf16 burst figure, else the fallback."""
+    bf16 burst figure (sustained=True: the seconds-long loop's), else the fallback."""
     peaks, _ = measured_peaks()
-    if peaks and "bf16_tflops" in peaks:
+    key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
+    if peaks and key in peaks:
         try:
-            return float(peaks["bf16_tflops"]), "measured bf16 (cuBLAS burst)"
+            return float(peaks[key]), f"measured bf16 (cuBLAS {'sustained' if sustained else 'burst'})"
         except (TypeError, ValueError):
             pass
+    if sustained:
+        return bf16_tensor_peak_tflops(False)
     return FALLBACK_BF16_TFLOPS, "fallback bf16"
 
 
 WEIGHT_BYTES = {"mxfp4": 0.5 + 1.0 / 32.0, "nvfp4": 0.5 + 1.0 / 16.0}
 
 
-def gemm_roofline(d, groups, t_ms, which, hbm, hbm_src, tpk, tpk_src, fmt="mxfp4"):
+def gemm_roofline(d, groups, t_ms, which, hbm, hbm_src, tpk, tpk_src, fmt="mxfp4",
+                  tpk_burst=None):
     """Roofline of one grouped GEMM launch sequence (W13 or W2) of a layer step.
     Algorithmic bytes: the active groups' weight bytes (codes + scales) plus the packed
     FP8 rows and scales read and the bf16 rows written; flops: 2 x rows x N x K.  The
@@ -391,9 +412,13 @@ def gemm_roofline(d, groups, t_ms, which, hbm, hbm_src, tpk, tpk_src, fmt="mxfp4
                 "frac": ach / hbm, "traffic": None, "peak_source": f"{hbm_src} HBM copy bandwidth",
                 "algorithmic_bytes": wbytes + abytes}
     ach = flops / t / 1e12
-    return {"bound": "tensor", "achieved": ach, "peak": tpk, "unit": "TFLOP/s",
-            "frac": ach / tpk, "traffic": None, "peak_source": tpk_src,
-            "algorithmic_flops": flops}
+    rec = {"bound": "tensor", "achieved": ach, "peak": tpk, "unit": "TFLOP/s",
+           "frac": ach / tpk, "traffic": None, "peak_source": tpk_src,
+           "algorithmic_flops": flops}
+    if tpk_burst is not None and tpk_burst != tpk:
+        rec["frac_of_burst_peak"] = ach / tpk_burst
+        rec["burst_peak"] = tpk_burst
+    return rec
 
 
 def measure_layer(args, workload, steps, warmup, rank, world, local, clocks, *, soak_s=0.0,
@@ -414,8 +439,12 @@ def measure_layer(args, workload, steps, warmup, rank, world, local, clocks, *, 
         for n in ("w13", "w13_s", "w2", "w2_s"):
             del t[n]
         t.update(gi.nvfp4_layer_weights(d, seed=args.seed + rank, device=dev))
+    # --options applies to the headline layer only
+    layer_opts = ({o_: True for o_ in args.options.split(",") if o_}
+                  if tag == workload == args.workload else {})
     layer = moe.MoELayer(d.H, d.I, d.E, d.k, d.has_shared, t["w13"], t["w13_s"], t["w2"],
-                         t["w2_s"], fmt=fmt, w13_gs=t.get("w13_gs"), w2_gs=t.get("w2_gs"))
+                         t["w2_s"], fmt=fmt, w13_gs=t.get("w13_gs"), w2_gs=t.get("w2_gs"),
+                         **layer_opts)
     x, lg = t["x"], t["logits"]
     out = torch.empty(d.T, d.H, dtype=torch.bfloat16, device=dev)
     ws = layer.workspace(d.T)
@@ -510,11 +539,16 @@ def measure_layer(args, workload, steps, warmup, rank, world, local, clocks, *, 
     stage_mean = {s_: statistics.mean(v) for s_, v in stage_ms.items()}
 
     hbm, hbm_src = hbm_peak_gbs()
-    tpk, tpk_src = fp8_tensor_peak_tflops() if fmt == "mxfp4" else bf16_tensor_peak_tflops()
+    # a timed region of a second or more of back-to-back steps is a long run: the
+    # tensor peak is then the measured sustained figure (the burst one is reported too)
+    long_run = sum(step_ms) >= 1000.0
+    peak_fn = fp8_tensor_peak_tflops if fmt == "mxfp4" else bf16_tensor_peak_tflops
+    tpk_burst, _ = peak_fn(False)
+    tpk, tpk_src = peak_fn(long_run)
     roof13 = gemm_roofline(d, groups, stage_mean["gemm_w13"], "w13", hbm, hbm_src, tpk, tpk_src,
-                           fmt)
+                           fmt, tpk_burst)
     roof2 = gemm_roofline(d, groups, stage_mean["gemm_w2"], "w2", hbm, hbm_src, tpk, tpk_src,
-                          fmt)
+                          fmt, tpk_burst)
     kname = "k_gemm_mx" if fmt == "mxfp4" else "k_gemm_nv"
     roof13["kernel"] = f"{kname} (W13 grouped GEMM)"
     roof2["kernel"] = f"{kname} (W2 grouped GEMM)"
@@ -634,7 +668,8 @@ def measure_layer(args, workload, steps, warmup, rank, world, local, clocks, *, 
         "ms_per_step": ms_max, "steps": steps, "warmup": warmup,
         "config": {"workload": workload, "T": d.T, "H": d.H, "I": d.I, "E": d.E, "k": d.k,
                    "shared_experts": d.has_shared, "weights": fmt, "active_groups": groups,
-                   "routed_rows": d.R, "l2": l2_note, "parallelism": f"replicas x{world}"},
+                   "routed_rows": d.R, "l2": l2_note, "parallelism": f"replicas x{world}",
+                   "options": sorted(layer_opts) or None},
         "roofline": roof13, "roofline_w2": roof2, "stage_ms": stage_mean,
         "stream_ms_per_step": stream_step_ms, "ms_per_step_l2_write_flushed": flushed_ms,
         "ms_per_step_percentiles": pct,
@@ -747,11 +782,11 @@ def run_ours(args, rank, world, local):
         head = measure_layer(args, args.workload, args.steps, args.warmup, rank, world, local,
                              clocks, soak_s=2.5, e2e_steps=None if args.no_e2e else args.steps,
                              router=True, cpu=not args.no_cpu_baseline, fmt=args.weights,
-                             options=() if args.no_extra else OPTIONS)
+                             options=() if (args.no_extra or args.options) else OPTIONS)
         extras = {}
         sweep = None
         if args.workload == "decode" and args.weights == "mxfp4" and not args.no_extra \
-                and args.experts is None and args.tokens is None:
+                and args.experts is None and args.tokens is None and not args.options:
             for wl in ("decode256", "prefill"):
                 extras[wl] = sub_record(measure_layer(
                     args, wl, EXTRA_STEPS[wl], args.warmup, rank, world, local, clocks,
@@ -862,6 +897,71 @@ def sweep_points(args, local, steps, warmup, ms=None):
     return points
 
 
+def run_gemm_point(args, rank, world, local):
+    """One grouped GEMM of the sweep shapes (--gemm, --groups G, --rows M, --weights):
+    the W13 or W2 call alone, L2 flushed before each call; for ncu captures of one
+    kernel variant."""
+    import moe_expert_ffn_scan_gb300 as moe
+    moe.lib()
+    dev = torch.device("cuda", local)
+    which, G, M, fmt = args.gemm, args.groups, args.rows, args.weights
+    N, K = gi.SWEEP_SHAPES[which]
+    x, offsets, w, ws_ = gi.sweep_point(which, M, seed=args.seed, device=dev, G=G)
+    rows = x.shape[0]
+    q = torch.empty(rows, K, dtype=torch.uint8, device=dev)
+    qs = torch.empty(rows, K // 128, dtype=torch.uint8, device=dev)
+    moe.moe_quant_act(x, q, qs)
+    y = torch.empty(rows, N, dtype=torch.bfloat16, device=dev)
+    d = moe.dims(rows, K, N // 2, G, 1, 0) if which == "w13" else moe.dims(rows, N, K, G, 1, 0)
+    if fmt == "nvfp4":
+        w, wsn, gs = gi.nvfp4_weights(G, N, K, args.seed, dev,
+                                      segments=2 if which == "w13" else 1)
+        wsp = moe.alloc_workspace(moe.gemm_workspace_size_nvfp4(d), dev)
+
+        def call():
+            if which == "w13":
+                moe.moe_grouped_gemm_w13_nvfp4(d, q, qs, None, offsets, w, wsn, gs, y, wsp)
+            else:
+                moe.moe_grouped_gemm_w2_nvfp4(d, q, qs, offsets, w, wsn, gs.reshape(-1), y, wsp)
+    else:
+        wsp = moe.alloc_workspace(moe.gemm_workspace_size(d), dev)
+
+        def call():
+            if which == "w13":
+                moe.moe_grouped_gemm_w13(d, q, qs, None, offsets, w, ws_, y, wsp)
+            else:
+                moe.moe_grouped_gemm_w2(d, q, qs, offsets, w, ws_, y, wsp)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        evs[i][0].record()
+        call()
+        evs[i][1].record()
+    torch.cuda.synchronize()
+    bits = moe.moe_check_status(wsp)
+    if bits:
+        raise RuntimeError(f"device status bits {bits:#x}")
+    ms_ = statistics.median(a.elapsed_time(b) for a, b in evs) if evs else 0.0
+    wbytes = G * N * K * WEIGHT_BYTES[fmt]
+    if rank == 0:
+        hbm, hbm_src = hbm_peak_gbs()
+        print(json.dumps({
+            "metric": "grouped-GEMM weight GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms": ms_, "unit": "GB/s",
+            "value": wbytes / (ms_ * 1e-3) / 1e9 if ms_ else None,
+            "hbm_frac": wbytes / (ms_ * 1e-3) / 1e9 / hbm if ms_ else None,
+            "hbm_peak_source": hbm_src, "tflops": 2.0 * rows * N * K / (ms_ * 1e-3) / 1e12
+            if ms_ else None, "data": "synthetic",
+            "config": {"workload": "gemm", "gemm": which, "groups": G, "rows_per_group": M,
+                       "N": N, "K": K, "weights": fmt, "l2": "flushed before each call"}}),
+            flush=True)
+
+
 def run_sweep(args, rank, world, local):
     """The grouped-GEMM sweep on its own: one JSON line with every point."""
     import moe_expert_ffn_scan_gb300 as moe
@@ -890,6 +990,8 @@ def main():
             run_reference(args, rank, world)
         elif args.workload == "sweep":
             run_sweep(args, rank, world, local)
+        elif args.workload == "gemm":
+            run_gemm_point(args, rank, world, local)
         else:
             run_ours(args, rank, world, local)
     finally:

@@ -1384,10 +1384,11 @@ cudaError_t launch_one(const CUtensorMap& tmW, const CUtensorMap& tmX, const Gem
   const int grid = static_cast<int>(tiles < slots ? tiles : slots);
   GemmParams q = p;
   q.max_items = max_items;
-  // The large variant (one CTA per SM) runs ~8% slower at 32K tokens when launched as a
-  // programmatic dependent (measured; cause not identified), so the one-CTA-per-SM
-  // variants wait for their predecessor the plain way.  The two-CTA-per-SM small and
-  // medium variants keep the overlap.
+  // The large variant (one CTA per SM) runs slower at 32K tokens when launched as a
+  // programmatic dependent (measured: 17.4 vs 17.05 ms per layer, ~8% before the tile
+  // walk; cause not identified), so the one-CTA-per-SM variants wait for their
+  // predecessor the plain way.  The two-CTA-per-SM small and medium variants keep the
+  // overlap.
   return launch_k_pdl(OCC > 1, kern, grid, 256, C::kSmemBytes, st, tmW, tmX, q);
 }
 
