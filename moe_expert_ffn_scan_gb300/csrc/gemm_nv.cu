@@ -447,6 +447,13 @@ __global__ void __launch_bounds__(NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>::kThr
     uint32_t cs = cg, pc = 0;   // code ring (CS slots)
     uint32_t it0 = 0;           // global index of the tile's first stage
     bool ok = true;
+    // With two or more spare TMEM buffers (NA >= NG + 2) a group waits for a stage's
+    // TMEM stores, and releases the stage to the MMA, only after its next stage's codes
+    // are in registers, so the store latency overlaps those loads.  (With NA == NG the
+    // next stage reuses the deferred stage's own buffer -- a deadlock; with one spare
+    // buffer the deferral serialises the groups behind the MMAs: measured slower.)
+    constexpr bool kDefer = NA >= NG + 2;
+    int pend = -1;  // conv_full barrier of the stage whose TMEM stores are in flight
     for (TileWalk tw(p.items, total, n_tiles); tw.valid() && ok && !*abort_flag; tw.next()) {
       int g, row0, rows, nt;
       if (!load_item(tw, g, row0, rows, nt)) {
@@ -479,6 +486,13 @@ __global__ void __launch_bounds__(NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>::kThr
         const int sbyte0 = KS == 128 ? (kb & 1) * 8 : 0;
         __syncwarp();
         if (lane == 0) mbar_arrive(&code_empty[cs]);
+        if (kDefer && pend >= 0) {
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&conv_full[pend]);
+          pend = -1;
+        }
         const uint32_t col0 = a_base + s * C::kACols;
         if constexpr (LUT == 2) {
           // a 128-K stage: scale bytes 0-7 (even 128-K step) or 8-15 (odd) of the row
@@ -534,10 +548,14 @@ __global__ void __launch_bounds__(NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>::kThr
             tmem_st_32x32b_x8(lane_base + col0 + blk * 8, o);
           }
         }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&conv_full[(ISS == 2 ? (kb & 1) : 0) * NA + s]);
+        if constexpr (kDefer) {
+          pend = (ISS == 2 ? (kb & 1) : 0) * NA + s;
+        } else {
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&conv_full[(ISS == 2 ? (kb & 1) : 0) * NA + s]);
+        }
         s += NG;
         if (s >= NA) {
           s -= NA;
@@ -550,6 +568,12 @@ __global__ void __launch_bounds__(NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>::kThr
         }
       }
       it0 += nk;
+    }
+    tmem_st_wait();  // (also on the abort path: no TMEM store outlives the role)
+    if (kDefer && pend >= 0 && ok && !*abort_flag) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&conv_full[pend]);
     }
   } else if (warp >= C::kEpiWarp0) {
     // ------------------------------------------------------------ epilogue
