@@ -422,7 +422,8 @@ def gemm_roofline(d, groups, t_ms, which, hbm, hbm_src, tpk, tpk_src, fmt="mxfp4
 
 
 def measure_layer(args, workload, steps, warmup, rank, world, local, clocks, *, soak_s=0.0,
-                  e2e_steps=None, router=False, cpu=False, fmt="mxfp4", tag=None, options=()):
+                  e2e_steps=None, router=False, cpu=False, fmt="mxfp4", tag=None, options=(),
+                  tune=False):
     """One workload: the layer step captured as a CUDA graph, timed over `steps` replays
     (each followed by an event-instrumented forward for the stage times), inside a
     clock-sampling window tagged `tag` (the workload's name).  fmt: the expert weight
@@ -600,6 +601,17 @@ def measure_layer(args, workload, steps, warmup, rank, world, local, clocks, *, 
             torch.cuda.synchronize()
             torch.cuda.empty_cache()
 
+    # exact-shape tuning of the tile plan on this batch's routing histogram: the chunk
+    # size for groups above 64 rows (every candidate gives the same output bit for bit)
+    tune_rec = None
+    if tune and fmt == "mxfp4":
+        best, times = layer.tune_chunk_rows(x, lg, steps=10, warmup=3)
+        layer.large_chunk_rows = 0
+        tune_rec = {"best_chunk_rows": best, "ms_per_candidate": times,
+                    "default_chunk_rows": 224,
+                    "gain_vs_default": times[224] / times[best] if 224 in times else None,
+                    "how": "median of 10 forwards per candidate (CUDA events, not graphs)"}
+
     router_rec = None
     if router:
         # the router gate projection for this workload's T (outside the layer step: the
@@ -681,6 +693,7 @@ def measure_layer(args, workload, steps, warmup, rank, world, local, clocks, *, 
         "gpu_launches": 2 * launches_per_step * steps,
         "clocks": clocks.summary(tag),
         "options": opt_rec or None,
+        "plan_tuning": tune_rec,
     }
     del graph, layer, t, x, lg, out, ws, flush
     torch.cuda.synchronize()
@@ -757,7 +770,7 @@ def sub_record(rec):
     """The compact form of a workload's measurement carried inside the headline line."""
     keep = ("value", "ms_per_step", "steps", "config", "roofline", "roofline_w2", "stage_ms",
             "ms_per_step_l2_write_flushed", "ms_per_step_percentiles", "weight_gbs",
-            "gemm_tflops", "router_gate", "e2e", "clocks", "options")
+            "gemm_tflops", "router_gate", "e2e", "clocks", "options", "plan_tuning")
     out = {k: rec[k] for k in keep}
     out["unit"] = "tokens/s"
     return out
@@ -791,7 +804,7 @@ def run_ours(args, rank, world, local):
                 extras[wl] = sub_record(measure_layer(
                     args, wl, EXTRA_STEPS[wl], args.warmup, rank, world, local, clocks,
                     e2e_steps=None if args.no_e2e else EXTRA_E2E_STEPS[wl],
-                    router=(wl == "prefill"), options=OPTIONS))
+                    router=(wl == "prefill"), options=OPTIONS, tune=True))
             # the decode layer again with NVFP4 expert weights (f3)
             extras["decode_nvfp4"] = sub_record(measure_layer(
                 args, "decode", EXTRA_STEPS["decode_nvfp4"], args.warmup, rank, world, local,

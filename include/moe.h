@@ -365,11 +365,20 @@ int moe_forward_timed(const moe_dims* d, const uint16_t* x, const float* logits,
  *     those 128 columns in the stand-alone combine's order (fp32, j order, shared row
  *     last) -- the same out bit for bit, deterministic, no float atomics -- and the
  *     separate combine kernel is not launched.
- * All options take MXFP4 weights (MOE_ERR_INVALID_ARG otherwise). */
+ *   large_chunk_rows: the tile plan (a8) cuts every group of more than 64 rows into
+ *     ceil(M / C) near-equal chunks of at most C rows, C = large_chunk_rows (0: 224;
+ *     else a multiple of 16 in [144, 224], MOE_ERR_INVALID_ARG otherwise); chunks of
+ *     <= 128 rows run on the mid tiles, larger ones on the large tiles.  The knob of
+ *     LMSYS-H20 §3.3's exact-shape tuning: the best C depends on the routing histogram
+ *     (the binding's tune_chunk_rows times candidates on a recorded batch).  Results
+ *     are the same bit for bit for every C (each output element's K sum runs in the
+ *     same order on the mid and large tiles).
+ * The fusion and pair options take MXFP4 weights (MOE_ERR_INVALID_ARG otherwise). */
 typedef struct moe_options {
   int32_t fuse_combine;
   int32_t fuse_swiglu;
   int32_t pair_tiles;
+  int32_t large_chunk_rows;
 } moe_options;
 
 /* moe_forward_timed with options (opt may be NULL: all zero; events may be NULL).

@@ -41,7 +41,8 @@ class moe_weights(ctypes.Structure):
 
 
 class moe_options(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_int32) for n in ("fuse_combine", "fuse_swiglu", "pair_tiles")]
+    _fields_ = [(n, ctypes.c_int32) for n in ("fuse_combine", "fuse_swiglu", "pair_tiles",
+                                              "large_chunk_rows")]
 
 
 class moe_weights_nvfp4(ctypes.Structure):
@@ -330,13 +331,16 @@ def moe_route_static_status(stream=None) -> int:
 
 
 def moe_forward_ex(d, x, logits, w13, w13_s, w2, w2_s, out, ws, fuse_combine=False,
-                   fuse_swiglu=False, pair_tiles=False, debug=None, events=None, stream=None):
+                   fuse_swiglu=False, pair_tiles=False, large_chunk_rows=0, debug=None,
+                   events=None, stream=None):
     """moe_forward with options (fuse_combine: the W2 GEMM's epilogue performs the
     weighted top-k combine + shared add; fuse_swiglu: the W13 GEMM's epilogue performs
-    SwiGLU + FP8 quantisation; pair_tiles: groups above 64 rows on SM pairs) and
+    SwiGLU + FP8 quantisation; pair_tiles: groups above 64 rows on SM pairs;
+    large_chunk_rows: the tile plan's chunk size for groups above 64 rows, 0 = 224) and
     optional stage events."""
     W = moe_weights(_p(w13), _p(w13_s), _p(w2), _p(w2_s))
-    opt = moe_options(int(bool(fuse_combine)), int(bool(fuse_swiglu)), int(bool(pair_tiles)))
+    opt = moe_options(int(bool(fuse_combine)), int(bool(fuse_swiglu)), int(bool(pair_tiles)),
+                      int(large_chunk_rows))
     dbg = None
     if debug:
         dbg = moe_debug_out(*[_p(debug.get(n)) for n in DEBUG_FIELDS])
@@ -493,14 +497,16 @@ class MoELayer:
     bf16 output [T, H]."""
 
     def __init__(self, H, I, E, k, has_shared, w13, w13_s, w2, w2_s, fmt="mxfp4", w13_gs=None,
-                 w2_gs=None, fuse_combine=False, fuse_swiglu=False, pair_tiles=False):
+                 w2_gs=None, fuse_combine=False, fuse_swiglu=False, pair_tiles=False,
+                 large_chunk_rows=0):
         if fmt not in ("mxfp4", "nvfp4"):
             raise ValueError(f"unknown weight format {fmt!r}")
-        if (fuse_combine or fuse_swiglu or pair_tiles) and fmt != "mxfp4":
+        if (fuse_combine or fuse_swiglu or pair_tiles or large_chunk_rows) and fmt != "mxfp4":
             raise ValueError("the fusion and tile options take MXFP4 weights")
         self.fuse_combine = bool(fuse_combine)
         self.fuse_swiglu = bool(fuse_swiglu)
         self.pair_tiles = bool(pair_tiles)
+        self.large_chunk_rows = int(large_chunk_rows)
         self.H, self.I, self.E, self.k, self.has_shared = H, I, E, k, has_shared
         self.w13, self.w13_s, self.w2, self.w2_s = w13, w13_s, w2, w2_s
         self.fmt, self.w13_gs, self.w2_gs = fmt, w13_gs, w2_gs
@@ -556,12 +562,45 @@ class MoELayer:
             moe_forward_ex(self.dims(T), x, logits, self.w13, self.w13_s, self.w2, self.w2_s, out,
                            self.workspace(T), fuse_combine=self.fuse_combine,
                            fuse_swiglu=self.fuse_swiglu, pair_tiles=self.pair_tiles,
-                           debug=debug, stream=stream)
+                           large_chunk_rows=self.large_chunk_rows, debug=debug, stream=stream)
         else:
             moe_forward_nvfp4(self.dims(T), x, logits, self.w13, self.w13_s, self.w13_gs,
                               self.w2, self.w2_s, self.w2_gs, out, self.workspace(T),
                               debug=debug, stream=stream)
         return out
+
+    CHUNK_CANDIDATES = (224, 208, 192, 176, 160, 144)
+
+    def tune_chunk_rows(self, x, logits, candidates=CHUNK_CANDIDATES, steps=10, warmup=3):
+        """Exact-shape tuning of the tile plan on a recorded batch (its routing histogram
+        decides the group sizes): times the layer with each candidate chunk size for
+        groups above 64 rows (CUDA events, median of `steps` forwards after `warmup`),
+        keeps the fastest in self.large_chunk_rows and returns (best, {candidate: ms}).
+        Every candidate gives the same output bit for bit; only the tiling changes."""
+        self._mxfp4_only("chunk-size tuning")
+        out = torch.empty(x.shape[0], self.H, dtype=torch.bfloat16, device=x.device)
+        times = {}
+        keep = self.large_chunk_rows
+        try:
+            for c in candidates:
+                self.large_chunk_rows = int(c)
+                for _ in range(warmup):
+                    self.forward(x, logits, out=out)
+                ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                      for _ in range(steps)]
+                for a, b in ev:
+                    a.record()
+                    self.forward(x, logits, out=out)
+                    b.record()
+                torch.cuda.synchronize()
+                ts = sorted(a.elapsed_time(b) for a, b in ev)
+                times[int(c)] = ts[len(ts) // 2]
+        except Exception:
+            self.large_chunk_rows = keep
+            raise
+        best = min(times, key=times.get)
+        self.large_chunk_rows = best
+        return best, times
 
     def forward_timed(self, x, logits, out, events, stream=None):
         """forward recording the 8 stage events of moe_forward_timed (see STAGES)."""
@@ -570,7 +609,8 @@ class MoELayer:
             moe_forward_ex(self.dims(T), x, logits, self.w13, self.w13_s, self.w2, self.w2_s, out,
                            self.workspace(T), fuse_combine=self.fuse_combine,
                            fuse_swiglu=self.fuse_swiglu, pair_tiles=self.pair_tiles,
-                           events=events, stream=stream)
+                           large_chunk_rows=self.large_chunk_rows, events=events,
+                           stream=stream)
         else:
             moe_forward_nvfp4_timed(self.dims(T), x, logits, self.w13, self.w13_s, self.w13_gs,
                                     self.w2, self.w2_s, self.w2_gs, out, self.workspace(T),

@@ -109,6 +109,7 @@ PlanWs carve_plan(Carver& c, const moe_dims* d) {
     p.out.capacity[v] = p.max_items[v];
   }
   p.out.counts = c.take<int32_t>(kNumVariants);
+  p.out.chunk_rows = 0;  // kLargeBN
   return p;
 }
 
@@ -636,10 +637,14 @@ int forward_impl(const moe_dims* d, const uint16_t* x, const float* logits,
   const bool fuse_combine = opt && opt->fuse_combine;
   const bool fuse_swiglu = opt && opt->fuse_swiglu;
   const int pair_tiles = opt ? opt->pair_tiles : 0;
+  const int chunk_rows = opt ? opt->large_chunk_rows : 0;
   if (opt && ((opt->fuse_combine != 0 && opt->fuse_combine != 1) ||
               (opt->fuse_swiglu != 0 && opt->fuse_swiglu != 1) ||
               (opt->pair_tiles != 0 && opt->pair_tiles != 1) ||
               ((fuse_combine || fuse_swiglu || pair_tiles) && W.fmt != kMxfp4)))
+    return MOE_ERR_INVALID_ARG;
+  if (chunk_rows != 0 &&
+      (chunk_rows < kMinChunkRows || chunk_rows > kLargeBN || chunk_rows % 16 != 0))
     return MOE_ERR_INVALID_ARG;
   // the fused W13 epilogue runs on SM pairs: 2I % 256 == 0 always, H % 512 needed
   if (fuse_swiglu && d->H % 512 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -650,6 +655,7 @@ int forward_impl(const moe_dims* d, const uint16_t* x, const float* logits,
   Carver c(ws);
   ForwardWs f = carve_forward(c, d, W.fmt);
   if (ws_bytes < c.used) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  f.gemm.plan.out.chunk_rows = chunk_rows;
   // caller-visible intermediates replace the workspace buffers
   uint8_t* dbg_hq = nullptr;
   uint8_t* dbg_hs = nullptr;

@@ -66,7 +66,13 @@ struct PlanOut {
   int4* items[kNumVariants];
   int32_t* counts;                 // [kNumVariants]
   int32_t capacity[kNumVariants];  // list lengths; items past them are not written
+  int32_t chunk_rows;              // groups above kMediumBN rows are cut into chunks of at
+                                   // most this many rows (0: kLargeBN; else a multiple of
+                                   // 16 in [kMinChunkRows, kLargeBN])
 };
+// Smallest chunk size the plan accepts: every chunk but a group's last then has more
+// than kMediumBN rows, which the mid list's capacity assumes.
+constexpr int kMinChunkRows = 144;
 
 // Token count up to which route + histogram + permute + plan run as one CTA.
 constexpr int kPrepMaxT = 128;

@@ -231,9 +231,10 @@ __global__ void __launch_bounds__(kPermTokens) k_permute_block(
 // Per group g with M = offsets[g+1] - offsets[g] rows (the effective M the pages tune
 // for): M <= kSmallBN -> one small-M item (padded only to 16 tokens, never to a large
 // tile); M <= kMediumBN -> one medium item; larger groups are split into
-// ceil(M / kLargeBN) near-equal chunks (multiples of 16 rows except the last), which go
-// to the mid kernel when they are at most kMidBN rows and to the large kernel
-// otherwise.  Items are {group, row0, rows, 0}.  One CTA of 1024 threads; each
+// ceil(M / C) near-equal chunks (multiples of 16 rows except the last; C = the plan's
+// chunk_rows, kLargeBN by default, a tunable of the exact-shape tuning of LMSYS-H20
+// §3.3), which go to the mid kernel when they are at most kMidBN rows and to the large
+// kernel otherwise.  Items are {group, row0, rows, 0}.  One CTA of 1024 threads; each
 // thread owns a contiguous run of groups; positions come from block-wide scans, so
 // the lists are in group order and deterministic.
 __device__ __forceinline__ int32_t block_exclusive_scan(int32_t v, int32_t* s_warp,
@@ -263,13 +264,15 @@ __device__ __forceinline__ int32_t block_exclusive_scan(int32_t v, int32_t* s_wa
   return excl;
 }
 
-// Variant of a group with m > 0 rows and the chunking of the two chunked variants.
-__device__ __forceinline__ int plan_variant(int32_t m, int32_t& nch, int32_t& base) {
+// Variant of a group with m > 0 rows and the chunking of the two chunked variants
+// (chunks of at most `chunk` rows).
+__device__ __forceinline__ int plan_variant(int32_t m, int32_t chunk, int32_t& nch,
+                                            int32_t& base) {
   nch = 1;
   base = m;
   if (m <= kSmallBN) return 0;
   if (m <= kMediumBN) return 1;
-  nch = (m + kLargeBN - 1) / kLargeBN;
+  nch = (m + chunk - 1) / chunk;
   base = ((m + nch - 1) / nch + 15) / 16 * 16;
   return base <= kMidBN ? 2 : 3;
 }
@@ -279,6 +282,11 @@ __device__ __forceinline__ int plan_variant(int32_t m, int32_t& nch, int32_t& ba
 __device__ void plan_groups(const int32_t* offsets, int G, const PlanOut& plan,
                             uint32_t* status, int32_t* s_warp) {
   const int tid = threadIdx.x;
+  int32_t chunk = plan.chunk_rows == 0 ? kLargeBN : plan.chunk_rows;
+  if (chunk < kMinChunkRows || chunk > kLargeBN || chunk % 16 != 0) {  // host-checked
+    if (tid == 0) set_status(status, STATUS_BAD_PLAN);
+    chunk = kLargeBN;
+  }
   const int per = (G + 1023) / 1024;
   const int g0 = tid * per, g1 = min(G, g0 + per);
   int32_t n[kNumVariants] = {0, 0, 0, 0};
@@ -287,7 +295,7 @@ __device__ void plan_groups(const int32_t* offsets, int G, const PlanOut& plan,
     if (m < 0) set_status(status, STATUS_BAD_PLAN);
     if (m <= 0) continue;
     int32_t nch, base;
-    const int v = plan_variant(m, nch, base);  // (not folded into n[...] += nch: the
+    const int v = plan_variant(m, chunk, nch, base);  // (not folded into n[...] += nch: the
     n[v] += nch;                               // right operand would be read first)
   }
   int32_t pos[kNumVariants], tot[kNumVariants];
@@ -297,7 +305,7 @@ __device__ void plan_groups(const int32_t* offsets, int G, const PlanOut& plan,
     int32_t r0 = offsets[g], m = offsets[g + 1] - r0;
     if (m <= 0) continue;
     int32_t nch, base;
-    const int v = plan_variant(m, nch, base);
+    const int v = plan_variant(m, chunk, nch, base);
     for (int c = 0; c < nch; ++c) {
       int32_t a = c * base, b = min(m, a + base);
       const int32_t p = pos[v]++;

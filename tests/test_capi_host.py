@@ -138,6 +138,25 @@ def test_validation_happens_before_any_launch(lib):
                            P(0x1000), None, P(0x10000), 1 << 30, None) == 1
 
 
+def test_forward_options_validated_before_any_launch(lib):
+    """moe_forward_ex: option values outside {0, 1}, and chunk sizes that are not a
+    multiple of 16 in [144, 224], are rejected before anything launches; a valid option
+    set gets as far as the workspace-size check."""
+    d = moe.dims(7, 512, 256, 8, 2, 0)
+    W = moe.moe_weights(0x10000, 0x10000, 0x10000, 0x10000)
+    P = ctypes.c_void_p
+
+    def call(opt, ws_bytes=1 << 30):
+        return lib.moe_forward_ex(ctypes.byref(d), P(0x1000), P(0x1000), ctypes.byref(W),
+                                  ctypes.byref(opt), P(0x1000), None, None, P(0x10000),
+                                  ws_bytes, None)
+    for bad in ((2, 0, 0, 0), (0, 2, 0, 0), (0, 0, 2, 0), (0, 0, 0, 100), (0, 0, 0, 150),
+                (0, 0, 0, 240), (0, 0, 0, 128), (0, 0, 0, -16)):
+        assert call(moe.moe_options(*bad)) == 1, bad
+    for ok in ((0, 0, 0, 0), (0, 0, 0, 144), (0, 0, 0, 176), (0, 0, 0, 224), (1, 0, 1, 160)):
+        assert call(moe.moe_options(*ok), ws_bytes=16) == 3, ok
+
+
 def test_nvfp4_validation_before_any_launch(lib):
     P = ctypes.c_void_p
     ok = moe.dims(7, 7168, 3072, 384, 8, 1)

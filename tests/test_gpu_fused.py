@@ -21,7 +21,8 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def _run(d, t, fuse_combine=False, fuse_swiglu=False, pair_tiles=False, more=False):
+def _run(d, t, fuse_combine=False, fuse_swiglu=False, pair_tiles=False, more=False,
+         large_chunk_rows=0):
     md = moe.dims(d.T, d.H, d.I, d.E, d.k, d.has_shared)
     out = torch.full((d.T, d.H), float("nan"), dtype=torch.bfloat16, device=DEV)
     ws = moe.alloc_workspace(moe.workspace_size(md))
@@ -32,7 +33,7 @@ def _run(d, t, fuse_combine=False, fuse_swiglu=False, pair_tiles=False, more=Fal
                    y13=torch.empty(d.Rs, 2 * d.I, dtype=torch.bfloat16, device=DEV))
     moe.moe_forward_ex(md, t["x"], t["logits"], t["w13"], t["w13_s"], t["w2"], t["w2_s"], out, ws,
                        fuse_combine=fuse_combine, fuse_swiglu=fuse_swiglu, pair_tiles=pair_tiles,
-                       debug=dbg)
+                       large_chunk_rows=large_chunk_rows, debug=dbg)
     bits = moe.moe_check_status(ws)
     assert bits == 0, f"device status {bits:#x}"
     return (out, dbg["y2"]) if not more else (out, dbg)
@@ -123,6 +124,38 @@ def test_pair_tiles_forward_matches_oracle(T, kind):
     ref_out, ref = _run(d, t, more=True)
     assert_float_close(bf16_np(got["y13"]), bf16_np(ref["y13"]), "y13 (pair vs one SM)")
     assert_float_close(bf16_np(out), bf16_np(ref_out), "out (pair vs one SM)")
+
+
+@pytest.mark.parametrize("pair", [False, True])
+def test_chunk_rows_give_identical_outputs(pair):
+    """The tile plan's chunk size (exact-shape tuning, LMSYS-H20 §3.3) changes only how
+    groups above 64 rows are tiled (mid vs large tiles, chunk boundaries): every output
+    element's K sum runs in the same order, so y13, hq/hs, y2 and out are equal bit for
+    bit to the default plan's.  Zipf groups of up to ~1000 rows."""
+    d = gi.Dims(T=2000, H=512, I=256, E=16, k=6, has_shared=1)
+    t = {n: (v.to(DEV) if v is not None else None)
+         for n, v in gi.custom_layer(d, seed=11, logits_kind="zipf").items()}
+    ref_out, ref = _run(d, t, pair_tiles=pair, more=True)
+    for c in (144, 160, 176, 208):
+        out, got = _run(d, t, pair_tiles=pair, more=True, large_chunk_rows=c)
+        for n in ("y13", "hq", "hs", "y2"):
+            assert torch.equal(got[n], ref[n]), (c, n)
+        assert torch.equal(out, ref_out), c
+
+
+def test_chunk_rows_tuner_returns_a_candidate():
+    d = gi.Dims(T=1024, H=512, I=256, E=8, k=4, has_shared=1)
+    t = {n: (v.to(DEV) if v is not None else None)
+         for n, v in gi.custom_layer(d, seed=12, logits_kind="zipf").items()}
+    layer = moe.MoELayer(d.H, d.I, d.E, d.k, d.has_shared, t["w13"], t["w13_s"], t["w2"],
+                         t["w2_s"])
+    ref = layer.forward(t["x"], t["logits"]).clone()
+    best, times = layer.tune_chunk_rows(t["x"], t["logits"], candidates=(224, 176, 144),
+                                        steps=3, warmup=1)
+    assert best in (224, 176, 144) and set(times) == {224, 176, 144}
+    assert layer.large_chunk_rows == best
+    assert torch.equal(layer.forward(t["x"], t["logits"]), ref)
+    assert moe.moe_check_status(layer.workspace(d.T)) == 0
 
 
 def test_options_are_validated():
