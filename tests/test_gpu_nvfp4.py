@@ -80,6 +80,7 @@ NV_SHAPES = [
     # decode-like: long K, 1-7 rows per group
     ("w13", 6, 1024, 7168, [1, 2, 7, 1, 0, 3]),
     ("w13", 3, 512, 1024, [256, 100, 250]),           # mid chunks
+    ("w13", 5, 512, 1024, [17, 32, 24, 33, 16]),      # medium tiles' lower range
     ("w2", 2, 1536, 1536, [200, 129]),
     ("w13", 3, 512, 7168, [224, 0, 190]),             # large, long K
     ("w2", 2, 512, 3072, [240, 241]),                 # 240-row chunk, then 2 of 121

@@ -151,6 +151,12 @@ GEMM_SHAPES = [
     ("w2", 24, 2048, 1536, [(i * 5) % 16 + 1 for i in range(24)]),
     # decode-like: long K (28 two-sub-tile stages), 1-7 rows per group
     ("w13", 6, 1024, 7168, [1, 2, 7, 1, 0, 3]),
+    # the medium tiles' lower range (17..33 rows, around the 32-row mark), many tiles,
+    # long and odd K
+    ("w13", 6, 1024, 1024, [17, 32, 16, 33, 24, 31]),
+    ("w2", 4, 512, 3072, [20, 32, 17, 29]),
+    ("w13", 3, 256, 640, [18, 25, 32]),
+    ("w13", 2, 512, 7168, [32, 21]),
     # mid variant: one chunk of 65..128 rows, or two of <= 128 (M = 241..256)
     ("w13", 3, 512, 1024, [256, 100, 250]),
     ("w2", 2, 1024, 640, [80, 128]),        # K/128 odd: one-sub-tile stages

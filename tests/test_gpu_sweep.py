@@ -16,8 +16,9 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-@pytest.mark.parametrize("which,M", [("w13", 1), ("w13", 7), ("w2", 16), ("w13", 64),
-                                     ("w2", 512), ("w13", 4096), ("w2", 2048)])
+@pytest.mark.parametrize("which,M", [("w13", 1), ("w13", 7), ("w2", 16), ("w13", 32),
+                                     ("w2", 32), ("w13", 64), ("w2", 512), ("w13", 4096),
+                                     ("w2", 2048)])
 def test_sweep_point_sampled(which, M):
     N, K = gi.SWEEP_SHAPES[which]
     G = min(gi.sweep_groups(M), 32)  # fewer groups than the bench sweep: same per-group work
