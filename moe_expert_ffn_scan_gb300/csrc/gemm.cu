@@ -208,6 +208,15 @@ __global__ void __launch_bounds__(256, OCC)
     k_gemm_mx(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
               const GemmParams p) {
   using C = GemmCfg<BN_MAX, STAGES, KO, OCC>;
+  // An empty work list (the plan found no group for this variant): with the plan
+  // complete two launches back, the CTA leaves before setting anything up -- after
+  // waiting for the preceding kernel, so that the launches after it stay ordered
+  // behind that kernel.
+  if (p.early && *p.item_count <= 0) {
+    pdl_wait();
+    pdl_trigger();
+    return;
+  }
   // The 128B-swizzled tiles need 1024-byte alignment; the dynamic shared memory of a
   // kernel without static shared memory starts at such a boundary.  Checked, not
   // assumed: a misaligned base reports STATUS_BAD_PLAN and the CTA returns.

@@ -62,6 +62,7 @@ struct NvParams {
   int gs_segments;            // S: equal row segments of N with their own tensor scale
   int N, K, G, rows_total;
   uint32_t* status;
+  int early;  // 1: the tile plan was written two or more launches back
 };
 
 // BN: token tile; KS: K elements per stage; CS: code/scale ring slots; NA: token ring
@@ -227,6 +228,13 @@ __global__ void __launch_bounds__(NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>::kThr
     k_gemm_nv(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmS,
               const __grid_constant__ CUtensorMap tmX, const NvParams p) {
   using C = NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>;
+  // An empty work list: leave before any setup (after the wait that keeps the launch
+  // chain ordered), when the plan is known to be complete.
+  if (p.early && *p.item_count <= 0) {
+    pdl_wait();
+    pdl_trigger();
+    return;
+  }
   extern __shared__ __align__(1024) uint8_t smem[];
   if ((smem_u32(smem) & 1023u) != 0 || (LUT == 2 && smem_u32(smem) != kDynSmemBase)) {
     if (threadIdx.x == 0) set_status(p.status, STATUS_BAD_PLAN);
@@ -682,6 +690,8 @@ cudaError_t launch_nv_one(const NvGemmLaunch& a, int v, cudaStream_t st) {
   p.G = a.G;
   p.rows_total = a.rows_total;
   p.status = a.status;
+  // every variant after the first follows the first's launch, which follows the plan
+  p.early = v > 0 ? 1 : 0;
   const int grid = static_cast<int>(tiles < sms ? tiles : sms);
   return launch_k(kern, grid, C::kThreads, C::kSmemBytes, st, tmC, tmS, tmX, p);
 }
