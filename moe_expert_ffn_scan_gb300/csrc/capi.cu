@@ -110,6 +110,7 @@ PlanWs carve_plan(Carver& c, const moe_dims* d) {
   }
   p.out.counts = c.take<int32_t>(kNumVariants);
   p.out.chunk_rows = 0;  // kLargeBN
+  p.out.share_cnt = c.take<int32_t>(kShareSlots);
   return p;
 }
 
@@ -129,6 +130,7 @@ struct GemmWs {
   uint8_t* xg;   // MXFP4: packed FP8 rows for W13 [Rs][H]
   uint8_t* xsg;  // their scales [Rs][H/128]
   uint16_t* xe;  // NVFP4: packed bf16 rows for W13 (or W2's operand) [Rs][max(H, I)]
+  float* share_part;  // NVFP4: partials of the tiles two CTAs share
 };
 
 GemmWs carve_gemm(Carver& c, const moe_dims* d, WeightFormat fmt) {
@@ -141,6 +143,7 @@ GemmWs carve_gemm(Carver& c, const moe_dims* d, WeightFormat fmt) {
     g.xsg = c.take<uint8_t>(Rs * (d->H / 128));
   } else {
     g.xe = c.take<uint16_t>(Rs * static_cast<size_t>(d->H > d->I ? d->H : d->I));
+    g.share_part = c.take<float>(static_cast<size_t>(kShareSlots) * 2 * kSmallBN * 128);
   }
   return g;
 }
@@ -255,7 +258,7 @@ int run_gemm(const moe_dims* d, const uint8_t* act, const uint8_t* act_s, const 
 
 int run_gemm_nv(const moe_dims* d, const uint16_t* act, const uint8_t* w, const uint8_t* w_s,
                 const float* gs, int gs_segments, int N, int K, uint16_t* y, const PlanWs& plan,
-                int max_group_rows, uint32_t* status, cudaStream_t st) {
+                int max_group_rows, uint32_t* status, float* share_part, cudaStream_t st) {
   NvGemmLaunch a{};
   a.w_codes = w;
   a.w_scales = w_s;
@@ -274,6 +277,8 @@ int run_gemm_nv(const moe_dims* d, const uint16_t* act, const uint8_t* w, const 
   a.item_counts = plan.out.counts;
   a.max_group_rows = max_group_rows;
   a.status = status;
+  a.share_cnt = plan.out.share_cnt;
+  a.share_part = share_part;
   return cuda_rc(launch_grouped_gemm_nv(a, st));
 }
 
@@ -724,7 +729,7 @@ int forward_impl(const moe_dims* d, const uint16_t* x, const float* logits,
                   f.gemm.plan, T, status, st, /*early_plan=*/1, fs);
   } else {
     rc = run_gemm_nv(d, f.gemm.xe, W.w13, W.w13_s, W.w13_gs, 2, 2 * I, H, f.y13, f.gemm.plan, T,
-                     status, st);
+                     status, f.gemm.share_part, st);
   }
   if (rc != MOE_OK) return rc;
   MOE_MARK(4)
@@ -747,7 +752,8 @@ int forward_impl(const moe_dims* d, const uint16_t* x, const float* logits,
     rc = run_gemm(d, f.hq, f.hs, f.offsets, W.w2, W.w2_s, H, I, f.y2, f.gemm.plan, T, status,
                   st, /*early_plan=*/1, fc);  // follows SwiGLU; the plan preceded W13
   } else {
-    rc = run_gemm_nv(d, f.he, W.w2, W.w2_s, W.w2_gs, 1, H, I, f.y2, f.gemm.plan, T, status, st);
+    rc = run_gemm_nv(d, f.he, W.w2, W.w2_s, W.w2_gs, 1, H, I, f.y2, f.gemm.plan, T, status,
+                     f.gemm.share_part, st);
   }
   if (rc != MOE_OK) return rc;
   MOE_MARK(6)
@@ -782,7 +788,8 @@ int gemm_nv_call(const moe_dims* d, const uint8_t* q, const uint8_t* qs, const i
   if (launch_expand_rows(q, qs, perm_src, d->T, d->k, static_cast<int>(rows_R(d)), Rs, K, g.xe,
                          g.status, st) != cudaSuccess)
     return MOE_ERR_CUDA;
-  return run_gemm_nv(d, g.xe, w, w_s, gs, gs_segments, N, K, y, g.plan, Rs, g.status, st);
+  return run_gemm_nv(d, g.xe, w, w_s, gs, gs_segments, N, K, y, g.plan, Rs, g.status,
+                     g.share_part, st);
 }
 
 }  // namespace

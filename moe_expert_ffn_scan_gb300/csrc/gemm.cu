@@ -643,7 +643,11 @@ __global__ void __launch_bounds__(256, OCC)
     // ---------------------------------------------------------------- epilogue
     const int q = warp - 4;
     uint32_t tc = 0;
-    for (TileWalk tw(p.items, total, n_tiles); tw.valid() && !*abort_flag; tw.next()) {
+    // with the fused combine the four warps meet at named barriers: they leave the loop
+    // together on the collective wait's verdict (an abort makes it fail), never one by
+    // one on the abort flag
+    for (TileWalk tw(p.items, total, n_tiles); tw.valid() && (p.out != nullptr || !*abort_flag);
+         tw.next()) {
       int g, row0, rows;
       const int nt = tw.nt;
       if (!check_item(tw.cur, g, row0, rows)) continue;
@@ -812,7 +816,9 @@ __device__ __forceinline__ void f1_epilogue(const GemmParams& p, uint32_t tmem, 
   const int nblk = I / 128;
   const uint32_t peer = rank ^ 1u;
   uint32_t tc = 0;
-  for (long long L = cl; L < total && !*abort_flag; L += ncl) {
+  // (no abort-flag test in the loop condition: the warps leave together, on the
+  // collective wait's verdict, which an abort makes fail)
+  for (long long L = cl; L < total; L += ncl) {
     int g, row0, rows, nt2;
     if (!load_item(L, g, row0, rows, nt2)) continue;
     const uint32_t b = tc & 1u, use = tc >> 1;

@@ -40,6 +40,9 @@
 //   * warp 1 (and warp 3 in the small variant): MMA issue, tcgen05.mma kind::f16 with
 //     A from TMEM and B (tokens) from shared memory, fp32 accumulators in TMEM;
 //   * the last four warps: epilogue (TMEM -> registers, x tensor scale, -> bf16 rows).
+// Persistent CTAs walk the tiles round robin; in the small tiles the last partial wave is
+// cut along K (SegWalk) so that no CTA decodes a whole tile alone while the others idle,
+// the part that completes a split tile adding the fp32 partials in part order.
 // Every wait is bounded; an expired wait sets a status bit and the CTA unwinds.
 #include "kernels.cuh"
 
@@ -63,7 +66,80 @@ struct NvParams {
   int N, K, G, rows_total;
   uint32_t* status;
   int early;  // 1: the tile plan was written two or more launches back
+  int32_t* share_cnt;   // [kShareSlots], zero between launches
+  float* share_part;    // [kShareSlots][2][BN][128]
 };
+
+// A CTA's sequence of segments: stage ranges [kb0, kb1) of tiles (tile L = n-tile
+// L % n_tiles of work item L / n_tiles).  The full waves -- W = total / P tiles per CTA,
+// P = gridDim.x -- go round robin (tiles c, c + P, ..., whole; TileWalk).  Without a
+// split tail the R = total - W P tiles left go one per CTA as well.  A CTA's rate is
+// bound by its own decoding, so a CTA left alone in that last partial wave does not
+// speed up; with the split tail each of those R tiles is cut into S = min(4, P / R, nk)
+// K parts, one per CTA (CTA c < R S takes part c % S of tile W P + c / S), and the
+// part that completes last adds the S fp32 partials in part order (the result does
+// not depend on the order the parts finish in).
+struct SegWalk {
+  TileWalk tw;
+  const int4* items;
+  long long main_total, total;
+  int nk, n_tiles, kb0, kb1, nt;
+  int parts, part, tail_tile;  // tail unit: S, its part, r (tile W P + r)
+  int phase;                   // 0 full waves, 1 the tail unit, 2 done
+  int4 cur;
+  __device__ __forceinline__ SegWalk(const int4* it, long long tot, int ntiles, int nk_,
+                                     bool split_tail)
+      : tw(it, split_tail ? tot / gridDim.x * gridDim.x : tot, ntiles), items(it),
+        main_total(split_tail ? tot / gridDim.x * gridDim.x : tot), total(tot), nk(nk_),
+        n_tiles(ntiles), kb0(0), kb1(nk_), nt(0), parts(1), part(0), tail_tile(0), phase(0),
+        cur(make_int4(0, 0, 0, 0)) {
+    if (tw.valid()) {
+      nt = tw.nt;
+      cur = tw.cur;
+    } else {
+      enter_tail();
+    }
+  }
+  __device__ __forceinline__ void enter_tail() {
+    phase = 2;
+    const long long R = total - main_total;
+    if (R <= 0) return;  // no split tail (or none left)
+    long long S = static_cast<long long>(gridDim.x) / R;
+    if (S > 4) S = 4;
+    if (S > nk) S = nk;
+    const long long c = blockIdx.x;
+    if (c >= R * S) return;
+    parts = static_cast<int>(S);
+    tail_tile = static_cast<int>(c / S);
+    part = static_cast<int>(c % S);
+    kb0 = part * nk / parts;
+    kb1 = (part + 1) * nk / parts;
+    const long long L = main_total + tail_tile;
+    cur = __ldg(items + L / n_tiles);
+    nt = static_cast<int>(L % n_tiles);
+    phase = 1;
+  }
+  __device__ __forceinline__ bool valid() const { return phase < 2; }
+  __device__ __forceinline__ void next() {
+    if (phase == 0) {
+      tw.next();
+      if (tw.valid()) {
+        nt = tw.nt;
+        cur = tw.cur;
+      } else {
+        enter_tail();
+      }
+    } else {
+      phase = 2;
+    }
+  }
+  // a part of a split tile (its partial goes through the slots)
+  __device__ __forceinline__ bool split() const { return phase == 1 && parts > 1; }
+};
+
+__device__ __forceinline__ void nv_epi_bar() {
+  asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps
+}
 
 // BN: token tile; KS: K elements per stage; CS: code/scale ring slots; NA: token ring
 // slots = TMEM A buffers; ACC: accumulator buffers; ISS: MMA-issuing threads (each
@@ -313,9 +389,13 @@ __global__ void __launch_bounds__(NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>::kThr
     count = p.max_items;
   }
   const long long total = static_cast<long long>(count) * n_tiles;
+  // The small tiles split their last partial wave (the slots hold up to kShareSlots
+  // parts of at most kShareSlots tiles).
+  const bool split_tail = BN == kSmallBN && p.share_cnt != nullptr &&
+                          p.share_part != nullptr && gridDim.x <= kShareSlots;
   // the current tile of a walk: its group, first packed row and rows; false for an
   // empty item (skipped by every role alike) or an inconsistent one (flagged)
-  auto load_item = [&](const TileWalk& w, int& g, int& row0, int& rows, int& nt) -> bool {
+  auto load_item = [&](const SegWalk& w, int& g, int& row0, int& rows, int& nt) -> bool {
     const int4 it = w.cur;
     nt = w.nt;
     g = it.x;
@@ -334,11 +414,11 @@ __global__ void __launch_bounds__(NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>::kThr
     // ------------------------------------------------------------ codes + scales TMA
     if (lane == 0) {
       uint32_t s = 0, ph = 0;  // code ring slot and lap parity of the next stage
-      for (TileWalk tw(p.items, total, n_tiles); tw.valid() && !*abort_flag; tw.next()) {
+      for (SegWalk tw(p.items, total, n_tiles, nk, split_tail); tw.valid() && !*abort_flag; tw.next()) {
         int g, row0, rows, nt;
         if (!load_item(tw, g, row0, rows, nt)) continue;
         bool ok = true;
-        for (int kb = 0; kb < nk; ++kb) {
+        for (int kb = tw.kb0; kb < tw.kb1; ++kb) {
           // the slot is free once its converters released it (a fresh barrier's
           // parity-1 phase counts as complete on the first lap)
           if (!mbar_wait(&code_empty[s], ph ^ 1u, p.status, abort_flag)) {
@@ -362,11 +442,11 @@ __global__ void __launch_bounds__(NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>::kThr
     // ------------------------------------------------------------ token TMA
     if (lane == 0) {
       uint32_t s = 0, ph = 0;  // token ring slot and lap parity of the next stage
-      for (TileWalk tw(p.items, total, n_tiles); tw.valid() && !*abort_flag; tw.next()) {
+      for (SegWalk tw(p.items, total, n_tiles, nk, split_tail); tw.valid() && !*abort_flag; tw.next()) {
         int g, row0, rows, nt;
         if (!load_item(tw, g, row0, rows, nt)) continue;
         bool ok = true;
-        for (int kb = 0; kb < nk; ++kb) {
+        for (int kb = tw.kb0; kb < tw.kb1; ++kb) {
           if (!mbar_wait(&mma_done[s], ph ^ 1u, p.status, abort_flag)) {
             ok = false;
             break;
@@ -386,9 +466,9 @@ __global__ void __launch_bounds__(NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>::kThr
     // ------------------------------------------------------------ MMA issuer(s)
     const int par = warp == 1 ? 0 : 1;
     if (lane == 0) {
-      uint32_t it0 = 0, tc = 0;  // it0: global index of the tile's first stage
+      uint32_t it0 = 0, tc = 0;  // it0: this CTA's index of the segment's first stage
       uint32_t phases = 0;  // bit s: parity of the next phase of conv_full[par][s]
-      for (TileWalk tw(p.items, total, n_tiles); tw.valid() && !*abort_flag; tw.next()) {
+      for (SegWalk tw(p.items, total, n_tiles, nk, split_tail); tw.valid() && !*abort_flag; tw.next()) {
         int g, row0, rows, nt;
         if (!load_item(tw, g, row0, rows, nt)) continue;
         const int bn = (rows + 15) & ~15;
@@ -398,11 +478,13 @@ __global__ void __launch_bounds__(NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>::kThr
         const uint32_t d_tmem = tmem + b * C::kAccCols + par * BN;
         const uint32_t idesc = idesc_bf16(bn);
         bool ok = true;
-        const int kb_first = ISS == 2 ? par : 0;
-        // ring slot of the stage (global index it0 + kb) and the parity of its token
-        // phase, advanced by ISS stages per step (one division per tile)
-        uint32_t s = (it0 + kb_first) % NA, tph = ((it0 + kb_first) / NA) & 1u;
-        for (int kb = kb_first; kb < nk; kb += ISS) {  // this issuer's stages
+        // this issuer's first stage of the segment (parity par of the tile's stage index)
+        const int kb_first = ISS == 2 ? tw.kb0 + ((par - tw.kb0) & 1) : tw.kb0;
+        // ring slot of the stage (index it0 + kb - kb0) and the parity of its token
+        // phase, advanced by ISS stages per step (one division per segment)
+        const uint32_t i0 = it0 + static_cast<uint32_t>(kb_first - tw.kb0);
+        uint32_t s = i0 % NA, tph = (i0 / NA) & 1u;
+        for (int kb = kb_first; kb < tw.kb1; kb += ISS) {  // this issuer's stages
           const uint32_t ph = (phases >> s) & 1u;
           phases ^= 1u << s;
           // the stage's weights are in TMEM (its converters) and its tokens have landed
@@ -425,7 +507,7 @@ __global__ void __launch_bounds__(NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>::kThr
             const uint32_t off =
                 static_cast<uint32_t>(((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4);
             mma_bf16_ts(d_tmem, a_t + kk * 8, bd_hi | (bd_lo + off), idesc,
-                        kb > par || kk != 0);
+                        kb != kb_first || kk != 0);
           }
           tc_commit(&mma_done[s]);
           s += ISS;
@@ -437,7 +519,7 @@ __global__ void __launch_bounds__(NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>::kThr
         if (!ok) break;
         tc_commit(&acc_full[b]);
         ++tc;
-        it0 += nk;
+        it0 += static_cast<uint32_t>(tw.kb1 - tw.kb0);
       }
     }
   } else if (warp >= 4 && warp < C::kEpiWarp0) {
@@ -453,7 +535,7 @@ __global__ void __launch_bounds__(NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>::kThr
     // tiles, so their ring slots and phase parities advance by NG per stage.
     uint32_t s = cg, ps = 0;    // TMEM A buffer / token ring (NA slots)
     uint32_t cs = cg, pc = 0;   // code ring (CS slots)
-    uint32_t it0 = 0;           // global index of the tile's first stage
+    uint32_t it0 = 0;           // this CTA's index of the segment's first stage
     bool ok = true;
     // With two or more spare TMEM buffers (NA >= NG + 2) a group waits for a stage's
     // TMEM stores, and releases the stage to the MMA, only after its next stage's codes
@@ -462,12 +544,14 @@ __global__ void __launch_bounds__(NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>::kThr
     // buffer the deferral serialises the groups behind the MMAs: measured slower.)
     constexpr bool kDefer = NA >= NG + 2;
     int pend = -1;  // conv_full barrier of the stage whose TMEM stores are in flight
-    for (TileWalk tw(p.items, total, n_tiles); tw.valid() && ok && !*abort_flag; tw.next()) {
+    for (SegWalk tw(p.items, total, n_tiles, nk, split_tail); tw.valid() && ok && !*abort_flag;
+         tw.next()) {
       int g, row0, rows, nt;
       if (!load_item(tw, g, row0, rows, nt)) {
         continue;
       }
-      for (int kb = static_cast<int>((cg + NG - it0 % NG) % NG); kb < nk; kb += NG) {
+      for (int kb = tw.kb0 + static_cast<int>((cg + NG - it0 % NG) % NG); kb < tw.kb1;
+           kb += NG) {
         // the TMEM A buffer of this stage is free once the MMAs of stage it - NA are
         // done (their commit; the first pass finds the fresh barrier's parity-1 phase
         // complete); the code slot once its TMA has landed.  The whole warp waits.
@@ -575,7 +659,7 @@ __global__ void __launch_bounds__(NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>::kThr
           pc ^= 1u;
         }
       }
-      it0 += nk;
+      it0 += static_cast<uint32_t>(tw.kb1 - tw.kb0);
     }
     tmem_st_wait();  // (also on the abort path: no TMEM store outlives the role)
     if (kDefer && pend >= 0 && ok && !*abort_flag) {
@@ -586,14 +670,29 @@ __global__ void __launch_bounds__(NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>::kThr
   } else if (warp >= C::kEpiWarp0) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
+    // per-CTA scratch of the split tail: the accumulator wait's verdict and a split
+    // tile's arrival count, each handed to all four epilogue warps at a named barrier
+    volatile int* go = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 8);
+    volatile int* arrived = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 12);
     uint32_t tc = 0;
-    for (TileWalk tw(p.items, total, n_tiles); tw.valid() && !*abort_flag; tw.next()) {
+    // (with a split tail the warps leave the loop only together, on the collective
+    // wait's verdict -- an abort makes that wait fail -- never one by one on the flag)
+    for (SegWalk tw(p.items, total, n_tiles, nk, split_tail); tw.valid() && (split_tail || !*abort_flag);
+         tw.next()) {
       int g, row0, rows, nt;
       if (!load_item(tw, g, row0, rows, nt)) continue;
       const uint32_t b = tc % ACC, use = tc / ACC;
       int w_ok = 1;
-      if (lane == 0) w_ok = mbar_wait(&acc_full[b], use & 1u, p.status, abort_flag);
-      if (!__shfl_sync(0xFFFFFFFFu, w_ok, 0)) break;
+      if (split_tail) {  // the four warps meet at named barriers: they decide together
+        if (q == 0 && lane == 0) *go = mbar_wait(&acc_full[b], use & 1u, p.status, abort_flag);
+        nv_epi_bar();
+        w_ok = *go;
+        nv_epi_bar();
+      } else {
+        if (lane == 0) w_ok = mbar_wait(&acc_full[b], use & 1u, p.status, abort_flag);
+        w_ok = __shfl_sync(0xFFFFFFFFu, w_ok, 0);
+      }
+      if (!w_ok) break;
       tc_fence_after();
       const int n = nt * 128 + q * 32 + lane;
       float gsc = 1.0f;
@@ -601,24 +700,42 @@ __global__ void __launch_bounds__(NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>::kThr
                             n / (p.N / p.gs_segments));
       uint16_t* ycol = p.y + static_cast<size_t>(row0) * p.N + n;
       const uint32_t acc = tmem + (static_cast<uint32_t>(q * 32) << 16) + b * C::kAccCols;
+      // with two issuers, which of the even-stage / odd-stage accumulators this
+      // segment wrote (a one-stage segment writes one)
+      const bool two = tw.kb1 - tw.kb0 > 1;
+      const bool has_even = ISS == 1 || two || (tw.kb0 & 1) == 0;
+      const bool has_odd = ISS == 2 && (two || (tw.kb0 & 1) == 1);
+      const bool shared = split_tail && tw.split();
+      // a split tile's part: slot r S + part of the partials, counter r
+      float* mine = shared ? p.share_part +
+                                 (static_cast<size_t>(tw.tail_tile * tw.parts + tw.part) * BN) *
+                                     128 + q * 32 + lane
+                           : nullptr;
       for (int c0 = 0; c0 < rows; c0 += 16) {
         uint32_t rr[16];
         float v[16];
-        tmem_ld_32x32b_x16(acc + c0, rr);
-        tmem_ld_wait();
+        if (has_even) {
+          tmem_ld_32x32b_x16(acc + c0, rr);
+          tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(rr[i]);
-        if (ISS == 2 && nk > 1) {  // even-stage + odd-stage sums, in that order
+          for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(rr[i]);
+        }
+        if (has_odd) {  // even-stage + odd-stage sums, in that order
           tmem_ld_32x32b_x16(acc + BN + c0, rr);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] += __uint_as_float(rr[i]);
+          for (int i = 0; i < 16; ++i) v[i] = has_even ? v[i] + __uint_as_float(rr[i])
+                                                       : __uint_as_float(rr[i]);
         }
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           if (c0 + i < rows) {
-            const __nv_bfloat16 hv = __float2bfloat16_rn(v[i] * gsc);
-            ycol[static_cast<size_t>(c0 + i) * p.N] = *reinterpret_cast<const uint16_t*>(&hv);
+            if (shared) {
+              mine[static_cast<size_t>(c0 + i) * 128] = v[i];
+            } else {
+              const __nv_bfloat16 hv = __float2bfloat16_rn(v[i] * gsc);
+              ycol[static_cast<size_t>(c0 + i) * p.N] = *reinterpret_cast<const uint16_t*>(&hv);
+            }
           }
         }
       }
@@ -626,6 +743,29 @@ __global__ void __launch_bounds__(NvCfg<BN, KS, CS, NA, ACC, ISS, NG, LUT>::kThr
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[b]);
       ++tc;
+      if (shared) {
+        // publish this part, count the arrival; the part that completes the tile adds
+        // all S partials, in part order
+        __threadfence();
+        nv_epi_bar();
+        if (q == 0 && lane == 0) *arrived = atomicAdd(&p.share_cnt[tw.tail_tile], 1);
+        nv_epi_bar();
+        if (*arrived == tw.parts - 1) {
+          __threadfence();
+          const float* first = p.share_part +
+                               (static_cast<size_t>(tw.tail_tile * tw.parts) * BN) * 128 +
+                               q * 32 + lane;
+          for (int r = 0; r < rows; ++r) {
+            float sum = __ldcg(first + static_cast<size_t>(r) * 128);
+            for (int j = 1; j < tw.parts; ++j)
+              sum += __ldcg(first + (static_cast<size_t>(j) * BN + r) * 128);
+            const __nv_bfloat16 hv = __float2bfloat16_rn(sum * gsc);
+            ycol[static_cast<size_t>(r) * p.N] = *reinterpret_cast<const uint16_t*>(&hv);
+          }
+          if (q == 0 && lane == 0) p.share_cnt[tw.tail_tile] = 0;  // for the next launch
+        }
+        nv_epi_bar();  // *arrived is read by all before a later part writes it
+      }
     }
   }
 
@@ -692,6 +832,8 @@ cudaError_t launch_nv_one(const NvGemmLaunch& a, int v, cudaStream_t st) {
   p.status = a.status;
   // every variant after the first follows the first's launch, which follows the plan
   p.early = v > 0 ? 1 : 0;
+  p.share_cnt = a.share_cnt;
+  p.share_part = a.share_part;
   const int grid = static_cast<int>(tiles < sms ? tiles : sms);
   return launch_k(kern, grid, C::kThreads, C::kSmemBytes, st, tmC, tmS, tmX, p);
 }

@@ -69,7 +69,14 @@ struct PlanOut {
   int32_t chunk_rows;              // groups above kMediumBN rows are cut into chunks of at
                                    // most this many rows (0: kLargeBN; else a multiple of
                                    // 16 in [kMinChunkRows, kLargeBN])
+  int32_t* share_cnt;              // [kShareSlots] arrival counters of the tiles whose K
+                                   // range the NVFP4 GEMM's last partial wave splits
+                                   // among CTAs; zeroed by the plan kernel, left zero by
+                                   // each GEMM
 };
+// Slots for the split tiles of the NVFP4 GEMM's last partial wave (at most one per CTA:
+// the split applies when the grid has at most kShareSlots CTAs).
+constexpr int kShareSlots = 256;
 // Smallest chunk size the plan accepts: every chunk but a group's last then has more
 // than kMediumBN rows, which the mid list's capacity assumes.
 constexpr int kMinChunkRows = 144;
@@ -167,6 +174,8 @@ struct NvGemmLaunch {
   int max_items[kNumVariants];
   int max_group_rows;
   uint32_t* status;
+  int32_t* share_cnt;  // the plan's counters (PlanOut::share_cnt)
+  float* share_part;   // [kShareSlots][2][kSmallBN][128]: fp32 partials of split tiles
 };
 cudaError_t launch_grouped_gemm_nv(const NvGemmLaunch& a, cudaStream_t st);
 int nv_encode_maps(const NvGemmLaunch& a, int ks, int bn, CUtensorMap* tmC, CUtensorMap* tmS,

@@ -282,6 +282,8 @@ __device__ __forceinline__ int plan_variant(int32_t m, int32_t chunk, int32_t& n
 __device__ void plan_groups(const int32_t* offsets, int G, const PlanOut& plan,
                             uint32_t* status, int32_t* s_warp) {
   const int tid = threadIdx.x;
+  if (plan.share_cnt)
+    for (int i = tid; i < kShareSlots; i += blockDim.x) plan.share_cnt[i] = 0;
   int32_t chunk = plan.chunk_rows == 0 ? kLargeBN : plan.chunk_rows;
   if (chunk < kMinChunkRows || chunk > kLargeBN || chunk % 16 != 0) {  // host-checked
     if (tid == 0) set_status(status, STATUS_BAD_PLAN);

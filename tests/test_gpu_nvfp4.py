@@ -81,6 +81,11 @@ NV_SHAPES = [
     ("w13", 6, 1024, 7168, [1, 2, 7, 1, 0, 3]),
     ("w13", 3, 512, 1024, [256, 100, 250]),           # mid chunks
     ("w13", 5, 512, 1024, [17, 32, 24, 33, 16]),      # medium tiles' lower range
+    # small tiles whose last partial wave is split into K parts (on 152 SMs: 160 tiles ->
+    # 8 tiles in 4 parts; 212 tiles -> 60 tiles in 2 parts; long K in 4 parts)
+    ("w13", 20, 1024, 1024, [(i % 16) + 1 for i in range(20)]),
+    ("w2", 53, 512, 3072, [(i * 3) % 16 + 1 for i in range(53)]),
+    ("w13", 40, 512, 7168, [1 + i % 7 for i in range(40)]),
     ("w2", 2, 1536, 1536, [200, 129]),
     ("w13", 3, 512, 7168, [224, 0, 190]),             # large, long K
     ("w2", 2, 512, 3072, [240, 241]),                 # 240-row chunk, then 2 of 121
