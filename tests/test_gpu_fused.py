@@ -115,6 +115,33 @@ def test_pair_tiles_exact_integer_y13():
     assert bad.size == 0, f"{len(bad)} mismatches, first {bad[:4].tolist()}"
 
 
+@pytest.mark.parametrize("pair", [True, False])
+def test_exact_integer_y13_at_chunk_boundaries(pair):
+    """Groups of exactly 128, 129, 240, 256, 480 and 512 rows (one-hot logits, top-1):
+    one mid chunk, one large chunk of 129 rows, two mid chunks of 120 / 128, three large
+    chunks of 160 and of 171 rows -- on SM pairs and on one SM, y13 equal to the
+    oracle's exact integers (integer activations, integer E2M1 codes, unit scales)."""
+    sizes = [128, 129, 240, 256, 480, 512]
+    E, T = len(sizes), sum(sizes)
+    d = gi.Dims(T=T, H=1024, I=256, E=E, k=1, has_shared=0)
+    t = gi.custom_layer(d, seed=21, logits_kind="normal")
+    expert = np.repeat(np.arange(E), sizes)
+    logits = torch.full((T, E), -8.0, dtype=torch.float32)
+    logits[torch.arange(T), torch.from_numpy(expert)] = 8.0
+    t["logits"] = logits
+    g = torch.Generator().manual_seed(21)
+    t["x"] = torch.randint(-8, 9, (d.T, d.H), generator=g).to(torch.bfloat16)
+    t["w13"] = gi.integer_fp4_bytes((d.G, 2 * d.I, d.H // 2), 21, "cpu", "w13")
+    t["w13_s"] = torch.full((d.G, 2 * d.I, d.H // 32), 127, dtype=torch.uint8)
+    td = {n: (v.to(DEV) if v is not None else None) for n, v in t.items()}
+    _, got = _run(d, td, pair_tiles=pair, more=True)
+    ref = o.moe_forward(bits_np(t["x"]), t["logits"].numpy(), d.k, t["w13"].numpy(),
+                        t["w13_s"].numpy(), t["w2"].numpy(), t["w2_s"].numpy(), d.has_shared)
+    y13 = bf16_np(got["y13"])
+    bad = np.argwhere(y13 != ref["y13"])
+    assert bad.size == 0, f"{len(bad)} mismatches, first {bad[:4].tolist()}"
+
+
 @pytest.mark.parametrize("T,kind", [(300, "zipf"), (2000, "zipf")])
 def test_pair_tiles_forward_matches_oracle(T, kind):
     d = gi.Dims(T=T, H=1024, I=512, E=8, k=4, has_shared=1)
