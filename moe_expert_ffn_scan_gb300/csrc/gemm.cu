@@ -143,9 +143,10 @@ __device__ __forceinline__ void epilogue_bar_sync() {
   asm volatile("bar.sync 1, 128;" ::: "memory");  // warps 4-7 only
 }
 
-// f2: the combine for the tokens whose (token, block nt) this tile completed.  et:
-// the epilogue thread (0..127) = column nt*128 + et.  Called by all 128 epilogue
+// f2: the combine for the tokens whose (token, block nt) this tile completed.  et: the
+// epilogue thread (0..127); U: tokens per thread per pass.  Called by all 128 epilogue
 // threads after their y2 stores of the tile.
+template <int U>
 __device__ __forceinline__ void fused_combine_tile(const GemmParams& p, int row0, int rows,
                                                    int nt, int et, int* fc) {
   const int R = p.T * p.k;
@@ -168,33 +169,83 @@ __device__ __forceinline__ void fused_combine_tile(const GemmParams& p, int row0
   epilogue_bar_sync();
   const int nc = fc[0];
   if (nc > 0) __threadfence();  // acquire: the other tiles' rows of the completed tokens
-  const int col = nt * 128 + et;
-  for (int i = 0; i < nc; ++i) {
-    const int t = fc[1 + i];
-    // every row's value is loaded before any is summed (their latencies overlap)
-    uint16_t v[17];
-    bool okr[17];
+  // 16 threads per token, each 8 columns (one 16-byte load per row); 8 token slots, U
+  // tokens per thread per pass, so a pass has up to U x 9 row loads of each thread in
+  // flight before any is summed
+  const int slot = et >> 4;
+  const int col = nt * 128 + (et & 15) * 8;
+  for (int i0 = 0; i0 < nc; i0 += 8 * U) {
+    int tk[U];
+    float acc[U][8];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      okr[j] = false;
-      v[j] = 0;
-      if (j < p.k) {
-        const int r = p.inv[static_cast<size_t>(t) * p.k + j];
-        okr[j] = r >= 0 && r < Rs;
-        if (okr[j]) v[j] = __ldcg(p.y + static_cast<size_t>(r) * p.N + col);
-        else set_status(p.status, STATUS_BAD_INDEX);
+    for (int u = 0; u < U; ++u) {
+      const int i = i0 + u * 8 + slot;
+      tk[u] = i < nc ? fc[1 + i] : -1;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) acc[u][c] = 0.f;
+    }
+    // k_combine's order: fp32 fma in j order, then the shared row
+    for (int j0 = 0; j0 < p.k; j0 += 8) {
+      uint4 v[U][8];
+      float w[U][8];
+      uint32_t okm[U];  // rows loaded (a bad index is skipped, as k_combine does)
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        okm[u] = 0u;
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          const int j = j0 + jj;
+          v[u][jj] = make_uint4(0, 0, 0, 0);
+          w[u][jj] = 0.f;
+          if (tk[u] >= 0 && j < p.k) {
+            const size_t tj = static_cast<size_t>(tk[u]) * p.k + j;
+            const int r = p.inv[tj];
+            if (r >= 0 && r < Rs) {
+              v[u][jj] = __ldcg(reinterpret_cast<const uint4*>(p.y + static_cast<size_t>(r) * p.N + col));
+              w[u][jj] = p.cw[tj];
+              okm[u] |= 1u << jj;
+            } else {
+              set_status(p.status, STATUS_BAD_INDEX);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          if (!((okm[u] >> jj) & 1u)) continue;
+          const uint32_t q[4] = {v[u][jj].x, v[u][jj].y, v[u][jj].z, v[u][jj].w};
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint32_t bits = (c & 1) ? (q[c >> 1] & 0xFFFF0000u) : (q[c >> 1] << 16);
+            acc[u][c] = fmaf(w[u][jj], __uint_as_float(bits), acc[u][c]);
+          }
+        }
       }
     }
-    v[16] = p.has_shared ? __ldcg(p.y + static_cast<size_t>(R + t) * p.N + col) : 0;
-    float acc = 0.f;  // k_combine's order: fp32 fma in j order, then the shared row
 #pragma unroll
-    for (int j = 0; j < 16; ++j)
-      if (j < p.k && okr[j])
-        acc = fmaf(p.cw[static_cast<size_t>(t) * p.k + j],
-                   __uint_as_float(static_cast<uint32_t>(v[j]) << 16), acc);
-    if (p.has_shared) acc += __uint_as_float(static_cast<uint32_t>(v[16]) << 16);
-    const __nv_bfloat16 o = __float2bfloat16_rn(acc);
-    p.out[static_cast<size_t>(t) * p.N + col] = *reinterpret_cast<const uint16_t*>(&o);
+    for (int u = 0; u < U; ++u) {
+      if (tk[u] < 0) continue;
+      if (p.has_shared) {
+        const uint4 sv = __ldcg(reinterpret_cast<const uint4*>(
+            p.y + static_cast<size_t>(R + tk[u]) * p.N + col));
+        const uint32_t q[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t bits = (c & 1) ? (q[c >> 1] & 0xFFFF0000u) : (q[c >> 1] << 16);
+          acc[u][c] += __uint_as_float(bits);
+        }
+      }
+      uint32_t o[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(acc[u][2 * c], acc[u][2 * c + 1]);
+        o[c] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      *reinterpret_cast<uint4*>(p.out + static_cast<size_t>(tk[u]) * p.N + col) =
+          make_uint4(o[0], o[1], o[2], o[3]);
+    }
   }
   epilogue_bar_sync();  // the list is reused by the next tile
 }
@@ -203,7 +254,20 @@ __device__ __forceinline__ uint32_t u4_comp(const uint4& v, int t) {
   return t == 0 ? v.x : t == 1 ? v.y : t == 2 ? v.z : v.w;
 }
 
-template <int BN_MAX, int STAGES, int KO, int OCC>
+// Tiles of a list of `count` items (n-tiles of 128 rows per item).
+__device__ __forceinline__ long long tiles_of(const GemmParams& p, int count) {
+  return static_cast<long long>(count < p.max_items ? count : p.max_items) * (p.N / 128);
+}
+
+// The walk's stride for `total` tiles: at most gridDim.x, and the fewest CTAs that
+// still take ceil(total / gridDim.x) tiles each.
+__device__ __forceinline__ int walk_stride(long long total) {
+  if (total <= 0) return static_cast<int>(gridDim.x);
+  const long long per = (total + gridDim.x - 1) / gridDim.x;
+  return static_cast<int>((total + per - 1) / per);
+}
+
+template <int BN_MAX, int STAGES, int KO, int OCC, bool F2>
 __global__ void __launch_bounds__(256, OCC)
     k_gemm_mx(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
               const GemmParams p) {
@@ -212,7 +276,10 @@ __global__ void __launch_bounds__(256, OCC)
   // complete two launches back, the CTA leaves before setting anything up -- after
   // waiting for the preceding kernel, so that the launches after it stay ordered
   // behind that kernel.
-  if (p.early && *p.item_count <= 0) {
+  // Likewise a CTA that the balanced walk leaves without tiles (below).
+  if (p.early &&
+      (*p.item_count <= 0 ||
+       static_cast<int>(blockIdx.x) >= walk_stride(tiles_of(p, *p.item_count)))) {
     pdl_wait();
     pdl_trigger();
     return;
@@ -274,11 +341,17 @@ __global__ void __launch_bounds__(256, OCC)
     if (threadIdx.x == 0) set_status(p.status, STATUS_BAD_PLAN);
     count = p.max_items;
   }
-  long long total = static_cast<long long>(count) * n_tiles;
+  long long total = tiles_of(p, count);
   if (total > 0x7FFFFFFFll) {
     if (threadIdx.x == 0) set_status(p.status, STATUS_BAD_PLAN);
     total = 0;
   }
+  // Balanced waves: the walk's stride is the number of CTAs that gives each the same
+  // number of tiles give or take one; the CTAs past it walk nothing.  (With the full
+  // grid, a last wave of a few CTAs streams its tiles at those CTAs' own rate, too few
+  // loads in flight to keep HBM busy.)
+  const int wstride = walk_stride(total);
+  if (static_cast<int>(blockIdx.x) >= wstride) total = 0;
 
   // Validates one work item; every role sees the same result.
   auto check_item = [&](const int4 it, int& g, int& row0, int& rows) -> bool {
@@ -308,7 +381,7 @@ __global__ void __launch_bounds__(256, OCC)
       int pre = 0;
       if (p.early) {
         int g, row0, rows, nt;
-        for (long long L = blockIdx.x; L < total; L += gridDim.x)
+        for (long long L = blockIdx.x; L < total; L += wstride)
           if (load_item(L, g, row0, rows, nt)) {
             L0 = L;
             break;
@@ -330,7 +403,7 @@ __global__ void __launch_bounds__(256, OCC)
         }
       }
       uint32_t it = 0;
-      for (TileWalk tw(p.items, total, n_tiles); tw.valid() && !*abort_flag; tw.next()) {
+      for (TileWalk tw(p.items, total, n_tiles, static_cast<int>(blockIdx.x), wstride); tw.valid() && !*abort_flag; tw.next()) {
         int g, row0, rows;
         const int nt = tw.nt;
         if (!check_item(tw.cur, g, row0, rows)) continue;
@@ -357,7 +430,7 @@ __global__ void __launch_bounds__(256, OCC)
     if (lane == 0) {
       if (p.early) pdl_wait();
       uint32_t it = 0;
-      for (TileWalk tw(p.items, total, n_tiles); tw.valid() && !*abort_flag; tw.next()) {
+      for (TileWalk tw(p.items, total, n_tiles, static_cast<int>(blockIdx.x), wstride); tw.valid() && !*abort_flag; tw.next()) {
         int g, row0, rows;
         const int nt = tw.nt;
         if (!check_item(tw.cur, g, row0, rows)) continue;
@@ -378,7 +451,7 @@ __global__ void __launch_bounds__(256, OCC)
     if (lane == 0) {
       uint32_t it = 0, tc = 0;
       uint32_t phases = 0;  // bit s: parity of the next phase of full[par][s] to wait for
-      for (TileWalk tw(p.items, total, n_tiles); tw.valid() && !*abort_flag; tw.next()) {
+      for (TileWalk tw(p.items, total, n_tiles, static_cast<int>(blockIdx.x), wstride); tw.valid() && !*abort_flag; tw.next()) {
         int g, row0, rows;
         const int nt = tw.nt;
         if (!check_item(tw.cur, g, row0, rows)) continue;
@@ -507,7 +580,7 @@ __global__ void __launch_bounds__(256, OCC)
         int kq, g, row0, rows, nt;
       };
       auto seek = [&](long long L, Pos& P) -> bool {
-        for (; L < total; L += gridDim.x) {
+        for (; L < total; L += wstride) {
           if (load_item(L, P.g, P.row0, P.rows, P.nt)) {
             P.L = L;
             P.kq = 0;
@@ -518,7 +591,7 @@ __global__ void __launch_bounds__(256, OCC)
       };
       auto step = [&](Pos& P) -> bool {
         if (++P.kq < nq) return true;
-        return seek(P.L + gridDim.x, P);
+        return seek(P.L + wstride, P);
       };
       uint4 wv[Q][4];
       uint32_t av[Q][J];
@@ -601,7 +674,7 @@ __global__ void __launch_bounds__(256, OCC)
       // General path (K not a multiple of 512): one stage at a time.
       if (p.early) pdl_wait();  // token scales come from the preceding kernel
       uint32_t it = 0;
-      for (TileWalk tw(p.items, total, n_tiles); tw.valid() && !*abort_flag; tw.next()) {
+      for (TileWalk tw(p.items, total, n_tiles, static_cast<int>(blockIdx.x), wstride); tw.valid() && !*abort_flag; tw.next()) {
         int g, row0, rows;
         const int nt = tw.nt;
         if (!check_item(tw.cur, g, row0, rows)) continue;
@@ -646,13 +719,13 @@ __global__ void __launch_bounds__(256, OCC)
     // with the fused combine the four warps meet at named barriers: they leave the loop
     // together on the collective wait's verdict (an abort makes it fail), never one by
     // one on the abort flag
-    for (TileWalk tw(p.items, total, n_tiles); tw.valid() && (p.out != nullptr || !*abort_flag);
+    for (TileWalk tw(p.items, total, n_tiles, static_cast<int>(blockIdx.x), wstride); tw.valid() && (F2 || !*abort_flag);
          tw.next()) {
       int g, row0, rows;
       const int nt = tw.nt;
       if (!check_item(tw.cur, g, row0, rows)) continue;
       const uint32_t b = tc & 1u, use = tc >> 1;
-      if (p.out) {
+      if constexpr (F2) {
         // the fused combine meets at named barriers: one thread waits for the four warps,
         // so that none leaves the loop alone
         volatile int* go = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 8);
@@ -695,8 +768,10 @@ __global__ void __launch_bounds__(256, OCC)
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[b]);
       ++tc;
-      if (p.out) fused_combine_tile(p, row0, rows, nt, q * 32 + lane,
-                                    reinterpret_cast<int*>(smem + C::kOffFc));
+      // four tokens per thread per pass where one CTA holds the SM's registers
+      if constexpr (F2)
+        fused_combine_tile<(OCC == 1 ? 4 : 2)>(p, row0, rows, nt, q * 32 + lane,
+                                                reinterpret_cast<int*>(smem + C::kOffFc));
     }
   }
 
@@ -1376,11 +1451,11 @@ DevInfo& dev_info() {
   return info[dev];
 }
 
-template <int BN_MAX, int STAGES, int KO, int OCC>
-cudaError_t launch_one(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmParams& p,
-                       int max_items, cudaStream_t st) {
+template <int BN_MAX, int STAGES, int KO, int OCC, bool F2>
+cudaError_t launch_one_f(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmParams& p,
+                         int max_items, cudaStream_t st) {
   using C = GemmCfg<BN_MAX, STAGES, KO, OCC>;
-  auto kern = k_gemm_mx<BN_MAX, STAGES, KO, OCC>;
+  auto kern = k_gemm_mx<BN_MAX, STAGES, KO, OCC, F2>;
   // the shared-memory attribute is set once per context (again after a reset)
   static unsigned long long attr_ctx[64] = {};
   int dev = 0;
@@ -1405,6 +1480,15 @@ cudaError_t launch_one(const CUtensorMap& tmW, const CUtensorMap& tmX, const Gem
   // predecessor the plain way.  The two-CTA-per-SM small and medium variants keep the
   // overlap.
   return launch_k_pdl(OCC > 1, kern, grid, 256, C::kSmemBytes, st, tmW, tmX, q);
+}
+
+// The combine-fused W2 epilogue (f2) is its own instantiation, so that its gather's
+// registers do not weigh on the plain epilogue's allocation.
+template <int BN_MAX, int STAGES, int KO, int OCC>
+cudaError_t launch_one(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmParams& p,
+                       int max_items, cudaStream_t st) {
+  if (p.out) return launch_one_f<BN_MAX, STAGES, KO, OCC, true>(tmW, tmX, p, max_items, st);
+  return launch_one_f<BN_MAX, STAGES, KO, OCC, false>(tmW, tmX, p, max_items, st);
 }
 
 // The pair kernel for one list: clusters of two CTAs, as many clusters as fit at once.

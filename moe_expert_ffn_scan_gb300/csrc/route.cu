@@ -278,9 +278,12 @@ __device__ __forceinline__ int plan_variant(int32_t m, int32_t chunk, int32_t& n
 }
 
 // Builds the per-variant item lists from group offsets (global or shared memory).
-// Called by all 1024 threads of one CTA.
+// Called by all 1024 threads of one CTA.  last_first: the last group's items lead
+// their list, the others following in group order (the decode path puts its shared
+// expert first: measured 1% faster with NVFP4 weights at 7 tokens, W2 0.148 vs 0.152
+// ms; no change with MXFP4); otherwise the lists follow the group order.
 __device__ void plan_groups(const int32_t* offsets, int G, const PlanOut& plan,
-                            uint32_t* status, int32_t* s_warp) {
+                            uint32_t* status, int32_t* s_warp, bool last_first) {
   const int tid = threadIdx.x;
   if (plan.share_cnt)
     for (int i = tid; i < kShareSlots; i += blockDim.x) plan.share_cnt[i] = 0;
@@ -292,7 +295,10 @@ __device__ void plan_groups(const int32_t* offsets, int G, const PlanOut& plan,
   const int per = (G + 1023) / 1024;
   const int g0 = tid * per, g1 = min(G, g0 + per);
   int32_t n[kNumVariants] = {0, 0, 0, 0};
-  for (int g = g0; g < g1; ++g) {
+  // list position j holds group gj(j): the identity, or the last group first
+  auto gj = [&](int j) { return last_first ? (j == 0 ? G - 1 : j - 1) : j; };
+  for (int j = g0; j < g1; ++j) {
+    const int g = gj(j);
     int32_t m = offsets[g + 1] - offsets[g];
     if (m < 0) set_status(status, STATUS_BAD_PLAN);
     if (m <= 0) continue;
@@ -303,7 +309,8 @@ __device__ void plan_groups(const int32_t* offsets, int G, const PlanOut& plan,
   int32_t pos[kNumVariants], tot[kNumVariants];
 #pragma unroll
   for (int v = 0; v < kNumVariants; ++v) pos[v] = block_exclusive_scan(n[v], s_warp, &tot[v]);
-  for (int g = g0; g < g1; ++g) {
+  for (int j = g0; j < g1; ++j) {
+    const int g = gj(j);
     int32_t r0 = offsets[g], m = offsets[g + 1] - r0;
     if (m <= 0) continue;
     int32_t nch, base;
@@ -329,7 +336,7 @@ __global__ void __launch_bounds__(1024) k_plan(const int32_t* __restrict__ offse
   pdl_wait();
   pdl_trigger();
   __shared__ int32_t s_warp[32];
-  plan_groups(offsets, G, plan, status, s_warp);
+  plan_groups(offsets, G, plan, status, s_warp, false);
 }
 
 // ------------------------------------------------ a1 + a2 + a8 in one CTA (small T) ---
@@ -412,7 +419,7 @@ __global__ void __launch_bounds__(1024) k_prep_small(
     perm_src[p] = i;
     inv[i] = p;
   }
-  plan_groups(s_off, G, plan, status, s_warp);
+  plan_groups(s_off, G, plan, status, s_warp, has_shared != 0);
 }
 
 // ---------------------------------------------------------------- launchers -------

@@ -45,6 +45,8 @@ def _run(d, t, fuse_combine=False, fuse_swiglu=False, pair_tiles=False, more=Fal
     (7, 1024, 256, 64, 8, 1, "normal"),   # decode-like: 1-2 rows per group, small tiles
     (300, 256, 256, 5, 2, 1, "zipf"),     # groups past 128 rows: mid and large tiles
     (1000, 512, 256, 16, 6, 1, "zipf"),   # many tiles per token, every variant
+    (96, 256, 256, 24, 12, 1, "normal"),  # top-k past 8: the gather's second row batch
+    (40, 512, 256, 16, 16, 0, "normal"),  # top-16 of 16: every token in every group
 ])
 def test_fused_combine_equals_standalone(T, H, I, E, k, sh, kind):
     d = gi.Dims(T=T, H=H, I=I, E=E, k=k, has_shared=sh)
