@@ -201,7 +201,8 @@ __device__ __forceinline__ void fused_combine_tile(const GemmParams& p, int row0
             const size_t tj = static_cast<size_t>(tk[u]) * p.k + j;
             const int r = p.inv[tj];
             if (r >= 0 && r < Rs) {
-              v[u][jj] = __ldcg(reinterpret_cast<const uint4*>(p.y + static_cast<size_t>(r) * p.N + col));
+              v[u][jj] = __ldcg(
+                  reinterpret_cast<const uint4*>(p.y + static_cast<size_t>(r) * p.N + col));
               w[u][jj] = p.cw[tj];
               okm[u] |= 1u << jj;
             } else {
@@ -351,7 +352,8 @@ __global__ void __launch_bounds__(256, OCC)
   // grid, a last wave of a few CTAs streams its tiles at those CTAs' own rate, too few
   // loads in flight to keep HBM busy.)
   const int wstride = walk_stride(total);
-  if (static_cast<int>(blockIdx.x) >= wstride) total = 0;
+  const int wstart = static_cast<int>(blockIdx.x);
+  if (wstart >= wstride) total = 0;
 
   // Validates one work item; every role sees the same result.
   auto check_item = [&](const int4 it, int& g, int& row0, int& rows) -> bool {
@@ -403,7 +405,8 @@ __global__ void __launch_bounds__(256, OCC)
         }
       }
       uint32_t it = 0;
-      for (TileWalk tw(p.items, total, n_tiles, static_cast<int>(blockIdx.x), wstride); tw.valid() && !*abort_flag; tw.next()) {
+      for (TileWalk tw(p.items, total, n_tiles, wstart, wstride); tw.valid() && !*abort_flag;
+           tw.next()) {
         int g, row0, rows;
         const int nt = tw.nt;
         if (!check_item(tw.cur, g, row0, rows)) continue;
@@ -430,7 +433,8 @@ __global__ void __launch_bounds__(256, OCC)
     if (lane == 0) {
       if (p.early) pdl_wait();
       uint32_t it = 0;
-      for (TileWalk tw(p.items, total, n_tiles, static_cast<int>(blockIdx.x), wstride); tw.valid() && !*abort_flag; tw.next()) {
+      for (TileWalk tw(p.items, total, n_tiles, wstart, wstride); tw.valid() && !*abort_flag;
+           tw.next()) {
         int g, row0, rows;
         const int nt = tw.nt;
         if (!check_item(tw.cur, g, row0, rows)) continue;
@@ -451,7 +455,8 @@ __global__ void __launch_bounds__(256, OCC)
     if (lane == 0) {
       uint32_t it = 0, tc = 0;
       uint32_t phases = 0;  // bit s: parity of the next phase of full[par][s] to wait for
-      for (TileWalk tw(p.items, total, n_tiles, static_cast<int>(blockIdx.x), wstride); tw.valid() && !*abort_flag; tw.next()) {
+      for (TileWalk tw(p.items, total, n_tiles, wstart, wstride); tw.valid() && !*abort_flag;
+           tw.next()) {
         int g, row0, rows;
         const int nt = tw.nt;
         if (!check_item(tw.cur, g, row0, rows)) continue;
@@ -674,7 +679,8 @@ __global__ void __launch_bounds__(256, OCC)
       // General path (K not a multiple of 512): one stage at a time.
       if (p.early) pdl_wait();  // token scales come from the preceding kernel
       uint32_t it = 0;
-      for (TileWalk tw(p.items, total, n_tiles, static_cast<int>(blockIdx.x), wstride); tw.valid() && !*abort_flag; tw.next()) {
+      for (TileWalk tw(p.items, total, n_tiles, wstart, wstride); tw.valid() && !*abort_flag;
+           tw.next()) {
         int g, row0, rows;
         const int nt = tw.nt;
         if (!check_item(tw.cur, g, row0, rows)) continue;
@@ -719,7 +725,7 @@ __global__ void __launch_bounds__(256, OCC)
     // with the fused combine the four warps meet at named barriers: they leave the loop
     // together on the collective wait's verdict (an abort makes it fail), never one by
     // one on the abort flag
-    for (TileWalk tw(p.items, total, n_tiles, static_cast<int>(blockIdx.x), wstride); tw.valid() && (F2 || !*abort_flag);
+    for (TileWalk tw(p.items, total, n_tiles, wstart, wstride); tw.valid() && (F2 || !*abort_flag);
          tw.next()) {
       int g, row0, rows;
       const int nt = tw.nt;
