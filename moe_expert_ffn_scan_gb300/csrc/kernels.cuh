@@ -60,7 +60,8 @@ constexpr int kPairSfSlotsF1 = 4;  // with the fused SwiGLU epilogue's scratch
 
 
 // The tile plan's work lists, one per variant (0 small, 1 medium, 2 mid, 3 large),
-// each {group, row0, rows, 0} in group order, and their lengths.
+// each {group, row0, rows, 0} in group order (the decode path's one-CTA plan lists
+// the shared expert's items first), and their lengths.
 constexpr int kNumVariants = 4;
 struct PlanOut {
   int4* items[kNumVariants];

@@ -236,7 +236,8 @@ __global__ void __launch_bounds__(kPermTokens) k_permute_block(
 // §3.3), which go to the mid kernel when they are at most kMidBN rows and to the large
 // kernel otherwise.  Items are {group, row0, rows, 0}.  One CTA of 1024 threads; each
 // thread owns a contiguous run of groups; positions come from block-wide scans, so
-// the lists are in group order and deterministic.
+// the lists are in group order (or with the last group first, below) and
+// deterministic.
 __device__ __forceinline__ int32_t block_exclusive_scan(int32_t v, int32_t* s_warp,
                                                         int32_t* total) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
